@@ -1,0 +1,12 @@
+"""Float64 CPU oracle for paged decode attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; never by the library.  It shares no
+code with the CUDA path.  Its parity pins live in ``tests/test_oracle.py``.
+"""
+from .paged_attention import (PAGE_SIZE, attend, bf16_bits_to_float64, dequantize,
+                              e4m3fn_to_float64, gather_sequence, paged_decode_attention,
+                              run_workload)
+
+__all__ = ["PAGE_SIZE", "attend", "bf16_bits_to_float64", "dequantize", "e4m3fn_to_float64",
+           "gather_sequence", "paged_decode_attention", "run_workload"]

@@ -1,0 +1,227 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module only draws random numbers and lays them out in the paged-cache
+format; it holds none of the attention arithmetic.  Both the float64 oracle
+(test infrastructure) and the CUDA path take their inputs from here.
+
+Layout (ATOM model-operations guide, "Attention dispatch" / "KV cache
+operations"; configuration guide, ``kv_cache_block_size``):
+
+* ``q``            bf16  ``[T, Hq, D]``          T = number of query tokens
+* ``k_cache``      bf16 or fp8-e4m3 codes ``[NB, 16, Hkv, D]``  (flash layout)
+* ``v_cache``      same dtype and shape as ``k_cache``
+* ``block_tables`` int32 ``[B, max_blocks]``     logical page -> physical page,
+                   ``-1`` past a sequence's last page
+* ``seq_lens``     int32 ``[B]``  context length, *including* the sequence's
+                   query tokens (their K/V are already in the cache)
+* ``query_start_loc`` int32 ``[B+1]`` cumulative query-token offsets, or
+                   ``None`` when every sequence has exactly one query token.
+
+Every page of the pool is filled with random data (never NaN), including the
+tail slots of a sequence's last page and the pages no sequence uses.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+PAGE_SIZE = 16
+
+
+@dataclasses.dataclass
+class WorkloadSpec:
+    """Shape and distribution of one synthetic decode batch."""
+
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    kv_dtype: str                      # "bf16" or "fp8"
+    seq_len_kind: str                  # "fixed" | "uniform" | "loguniform"
+    seq_len_args: tuple
+    query_len_choices: tuple = (1,)    # each sequence draws its query length from these
+    pool_pages: Optional[int] = None   # physical pool size; default ceil(1.1 * used)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    fp8_source_scale: float = 1.0      # fp8 codes = e4m3(N(0,1) / fp8_source_scale)
+    seed: int = 0
+
+    @property
+    def group_size(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def max_query_len(self) -> int:
+        return max(self.query_len_choices)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+# The five decode regimes: a tiny parity case, a Llama-3-8B-shaped batch, a
+# single long-context user, an fp8-KV batch at batch 256 and an MTP
+# verification batch with ragged query runs.
+CONFIGS = {
+    "tiny": WorkloadSpec(
+        name="tiny", num_seqs=4, num_q_heads=8, num_kv_heads=2, head_dim=128,
+        kv_dtype="bf16", seq_len_kind="fixed", seq_len_args=(1, 17, 64, 200),
+        pool_pages=64, seed=1000),
+    "llama3_8b": WorkloadSpec(
+        name="llama3_8b", num_seqs=64, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        kv_dtype="bf16", seq_len_kind="uniform", seq_len_args=(512, 4096), seed=1001),
+    "batch1_32k": WorkloadSpec(
+        name="batch1_32k", num_seqs=1, num_q_heads=64, num_kv_heads=8, head_dim=64,
+        kv_dtype="bf16", seq_len_kind="fixed", seq_len_args=(32768,), seed=1002),
+    "fp8": WorkloadSpec(
+        name="fp8", num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        kv_dtype="fp8", seq_len_kind="loguniform", seq_len_args=(128, 8192),
+        k_scale=0.05, v_scale=0.05, fp8_source_scale=0.05, seed=1003),
+    "mtp": WorkloadSpec(
+        name="mtp", num_seqs=32, num_q_heads=64, num_kv_heads=8, head_dim=128,
+        kv_dtype="bf16", seq_len_kind="uniform", seq_len_args=(1024, 16384),
+        query_len_choices=(2, 3, 4), seed=1004),
+}
+
+CONFIG_ORDER = ["tiny", "llama3_8b", "batch1_32k", "fp8", "mtp"]
+
+
+@dataclasses.dataclass
+class Workload:
+    spec: WorkloadSpec
+    seq_lens: np.ndarray            # int32 [B]
+    query_lens: np.ndarray          # int32 [B]
+    query_start_loc: Optional[np.ndarray]   # int32 [B+1] or None
+    block_tables: np.ndarray        # int32 [B, max_blocks], -1 padded
+    num_pages: int                  # NB, physical pool size
+    q: torch.Tensor                 # bf16 [T, Hq, D]
+    k_cache: torch.Tensor           # bf16 or uint8 (e4m3 codes) [NB, 16, Hkv, D]
+    v_cache: torch.Tensor
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_lens.sum())
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.spec.kv_dtype == "fp8" else 2
+
+    def kv_bytes(self) -> int:
+        """Algorithmic KV bytes of one step: every cached token's K and V row
+        of every KV head, read once."""
+        s = self.spec
+        return int(self.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2 * self.kv_elem_bytes
+
+
+def draw_metadata(spec: WorkloadSpec, rng: np.random.Generator):
+    """Sequence lengths, query lengths and a randomly permuted page pool."""
+    B = spec.num_seqs
+    if spec.seq_len_kind == "fixed":
+        seq_lens = np.array(spec.seq_len_args, dtype=np.int64)
+        assert seq_lens.shape == (B,) or seq_lens.shape == (1,)
+        seq_lens = np.broadcast_to(seq_lens, (B,)).copy()
+    elif spec.seq_len_kind == "uniform":
+        lo, hi = spec.seq_len_args
+        seq_lens = rng.integers(lo, hi, size=B, endpoint=True)
+    elif spec.seq_len_kind == "loguniform":
+        lo, hi = spec.seq_len_args
+        seq_lens = np.floor(np.exp(rng.uniform(np.log(lo), np.log(hi + 1), size=B))).astype(np.int64)
+        seq_lens = np.clip(seq_lens, lo, hi)
+    else:
+        raise ValueError(spec.seq_len_kind)
+    query_lens = rng.choice(np.array(spec.query_len_choices, dtype=np.int64), size=B)
+    seq_lens = np.maximum(seq_lens, query_lens)
+    pages_per_seq = (seq_lens + PAGE_SIZE - 1) // PAGE_SIZE
+    used = int(pages_per_seq.sum())
+    pool = spec.pool_pages if spec.pool_pages is not None else int(math.ceil(1.1 * used))
+    assert pool >= used, (pool, used)
+    perm = rng.permutation(pool)
+    max_blocks = int(pages_per_seq.max())
+    block_tables = np.full((B, max_blocks), -1, dtype=np.int64)
+    cursor = 0
+    for i in range(B):
+        n = int(pages_per_seq[i])
+        block_tables[i, :n] = perm[cursor:cursor + n]
+        cursor += n
+    if spec.query_len_choices == (1,):
+        qsl = None
+    else:
+        qsl = np.zeros(B + 1, dtype=np.int64)
+        qsl[1:] = np.cumsum(query_lens)
+        qsl = qsl.astype(np.int32)
+    return (seq_lens.astype(np.int32), query_lens.astype(np.int32), qsl,
+            block_tables.astype(np.int32), pool)
+
+
+def _fill_normal(t: torch.Tensor, gen: torch.Generator, divisor: float, fp8: bool) -> None:
+    """Fill ``t`` (bf16 or uint8) chunk by chunk with N(0,1)/divisor, rounded
+    to nearest-even bf16 or encoded as e4m3fn codes."""
+    flat = t.view(-1)
+    n = flat.numel()
+    chunk = 1 << 26
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        x = torch.randn(e - s, generator=gen, device=t.device, dtype=torch.float32)
+        if divisor != 1.0:
+            x = x / divisor
+        if fp8:
+            flat[s:e] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        else:
+            flat[s:e] = x.to(torch.bfloat16)
+
+
+def make_workload(spec: WorkloadSpec, device: str = "cpu", seed: Optional[int] = None) -> Workload:
+    """Build one seeded batch.  Metadata comes from numpy's PCG64 with
+    ``seed``; tensor contents from torch's generator on ``device`` with the
+    same seed (so CPU and CUDA draws differ, but each is reproducible)."""
+    seed = spec.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    seq_lens, query_lens, qsl, block_tables, pool = draw_metadata(spec, rng)
+    T = int(query_lens.sum())
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    fp8 = spec.kv_dtype == "fp8"
+    q = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=device)
+    _fill_normal(q, gen, 1.0, False)
+    kv_shape = (pool, PAGE_SIZE, spec.num_kv_heads, spec.head_dim)
+    kv_torch_dtype = torch.uint8 if fp8 else torch.bfloat16
+    k_cache = torch.empty(kv_shape, dtype=kv_torch_dtype, device=device)
+    v_cache = torch.empty(kv_shape, dtype=kv_torch_dtype, device=device)
+    div = spec.fp8_source_scale if fp8 else 1.0
+    _fill_normal(k_cache, gen, div, fp8)
+    _fill_normal(v_cache, gen, div, fp8)
+    return Workload(spec=spec, seq_lens=seq_lens, query_lens=query_lens,
+                    query_start_loc=qsl, block_tables=block_tables, num_pages=pool,
+                    q=q, k_cache=k_cache, v_cache=v_cache)
+
+
+def custom_spec(name="custom", num_seqs=None, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                kv_dtype="bf16", seq_lens=(5, 16, 33), query_len_choices=(1,),
+                pool_pages=None, k_scale=1.0, v_scale=1.0, fp8_source_scale=1.0,
+                seed=7) -> WorkloadSpec:
+    """A small spec with explicit sequence lengths (for edge cases)."""
+    return WorkloadSpec(name=name, num_seqs=len(seq_lens) if num_seqs is None else num_seqs,
+                        num_q_heads=num_q_heads,
+                        num_kv_heads=num_kv_heads, head_dim=head_dim, kv_dtype=kv_dtype,
+                        seq_len_kind="fixed", seq_len_args=tuple(seq_lens),
+                        query_len_choices=tuple(query_len_choices), pool_pages=pool_pages,
+                        k_scale=k_scale, v_scale=v_scale, fp8_source_scale=fp8_source_scale,
+                        seed=seed)
+
+
+def host_arrays(w: Workload):
+    """Raw host copies for the CPU side: bf16 as uint16 bit patterns, fp8 as
+    uint8 codes."""
+    q_bits = w.q.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    if w.spec.kv_dtype == "fp8":
+        k = w.k_cache.detach().cpu().contiguous().numpy()
+        v = w.v_cache.detach().cpu().contiguous().numpy()
+    else:
+        k = w.k_cache.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        v = w.v_cache.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return q_bits, k, v

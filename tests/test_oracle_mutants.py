@@ -1,0 +1,87 @@
+"""The oracle's pins must catch plausible mistakes.  Each mutant below is the
+oracle's source with one planted error (a dropped term, a wrong sign, bias or
+index, a transposed mapping); the test asserts that at least one pin in
+``test_oracle.py`` fails on it.  Everything runs on the CPU."""
+import importlib.util
+import inspect
+import os
+import types
+
+import pytest
+
+import oracle.paged_attention as real
+
+HERE = os.path.dirname(__file__)
+
+MUTANTS = {
+    "slot_off_by_one": ("slots = j % PAGE_SIZE", "slots = (j + 1) % PAGE_SIZE"),
+    "page_index_rounding": ("[j // PAGE_SIZE]", "[(j + 1) // PAGE_SIZE]"),
+    "causal_off_by_one": ("limits = L - qn + np.arange(qn)", "limits = L - qn + np.arange(qn) - 1"),
+    "causal_reversed": ("limits = L - qn + np.arange(qn)", "limits = L - 1 - np.arange(qn)"),
+    "gqa_interleaved": ("heads = np.arange(hk * G, (hk + 1) * G)", "heads = np.arange(hk, Hq, Hkv)"),
+    "scale_dropped": ("s = scale * (q_rows @ keys.T)", "s = (q_rows @ keys.T)"),
+    "e4m3_bias": ("np.ldexp(1.0, (e - 7)", "np.ldexp(1.0, (e - 8)"),
+    "e4m3_subnormal": ("* np.ldexp(1.0, -6)", "* np.ldexp(1.0, -7)"),
+    "e4m3_mantissa": ("(1.0 + m / 8.0)", "(1.0 + m / 16.0)"),
+    "e4m3_sign": ("np.where(s == 1, -1.0, 1.0)", "np.where(s == 1, 1.0, 1.0)"),
+    "fp8_scale_dropped": ("return e4m3fn_to_float64(raw) * np.float64(np.float32(tensor_scale))",
+                          "return e4m3fn_to_float64(raw)"),
+    "lse_max_dropped": ("lse = m[:, 0] + np.log", "lse = np.log"),
+    "weights_unnormalised": ("w = np.exp(s - lse[:, None])", "w = np.exp(s - m)"),
+    "values_are_keys": ("out = w @ values", "out = w @ keys"),
+    "bf16_shift": ("<< np.uint32(16)", "<< np.uint32(15)"),
+}
+
+
+def _mutant_module(name, old, new):
+    src = inspect.getsource(real)
+    assert src.count(old) == 1, (name, old)
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+def _pins_module():
+    spec = importlib.util.spec_from_file_location("_pins_for_mutants", os.path.join(HERE, "test_oracle.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _pin_calls(pins):
+    yield pins.test_bf16_golden_points, ()
+    yield pins.test_e4m3_golden_points, ()
+    yield pins.test_e4m3_decode_matches_torch_all_codes, ()
+    yield pins.test_fp8_scale_is_fp32_rounded, ()
+    for kv in ("bf16", "fp8"):
+        for ql in ((1,), (2, 3, 4)):
+            yield pins.test_oracle_matches_sdpa_on_contiguous_kv, (kv, ql)
+    yield pins.test_length_one_returns_first_value_row, ()
+    yield pins.test_zero_query_gives_mean_value_and_log_length, ()
+    yield pins.test_two_keys_closed_form, ()
+    yield pins.test_gqa_mapping_consecutive_heads_share_kv_head, ()
+    yield pins.test_mtp_row_equals_prefix_attention, ()
+    yield pins.test_fp8_scale_folding_and_linearity, ()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    old, new = MUTANTS[name]
+    mutant = _mutant_module(name, old, new)
+    pins = _pins_module()
+    pins.oracle = types.SimpleNamespace(**{k: getattr(mutant, k) for k in (
+        "PAGE_SIZE", "attend", "bf16_bits_to_float64", "dequantize", "e4m3fn_to_float64",
+        "gather_sequence", "paged_decode_attention", "run_workload")})
+    caught = []
+    for fn, args in _pin_calls(pins):
+        try:
+            fn(*args)
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            caught.append(fn.__name__)
+    assert caught, f"no pin detects mutant {name}"
+
+
+def test_unmutated_oracle_passes_the_same_calls():
+    pins = _pins_module()
+    for fn, args in _pin_calls(pins):
+        fn(*args)
