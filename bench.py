@@ -1,0 +1,353 @@
+"""Benchmark of paged decode attention on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one paged_attn_decode call (split kernel + log-sum-exp merge) over
+one batch of the chosen seeded synthetic workload, inputs resident in HBM.
+``value`` is whole-job KV throughput (algorithmic KV bytes of every rank's
+step / max over ranks of the step time), in GB/s.  Between timed steps the L2
+is not flushed; instead the KV bytes a step reads exceed the L2 (129 MB), by
+rotating through several independent KV pools when one pool is smaller.
+``--impl reference`` times the float64 CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention µs/step and KV GB/s (% of GB300 HBM peak), 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def cpu_oracle_sample(config: str, budget_s: float = 15.0, threads: int = 1):
+    """Time the float64 oracle on a bounded sample of the workload (whole
+    sequences, added until ~budget_s of CPU work) in a child process with
+    single-threaded BLAS.  Returns (GB/s of KV processed, cores, sample text)."""
+    code = f"""
+import json, os, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import oracle
+from paged_kv_decode_06_gb300 import workloads as wl
+spec = wl.CONFIGS[{config!r}]
+rng = np.random.default_rng(spec.seed)
+sl, ql, qsl, bt, pool = wl.draw_metadata(spec, rng)
+order = np.random.default_rng(123).permutation(spec.num_seqs)
+# a private pool holding only the sampled sequences' pages (same shapes and values' distribution)
+import torch
+budget = {budget_s}
+done_bytes = 0; t_used = 0.0; nseq = 0; ntok = 0
+for i in order:
+    L = int(sl[i]); q = int(ql[i]); n = (L + 15) // 16
+    sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                         kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
+                         k_scale=spec.k_scale, v_scale=spec.v_scale, fp8_source_scale=spec.fp8_source_scale,
+                         seed=int(i))
+    w = wl.make_workload(sub)
+    t0 = time.perf_counter()
+    oracle.run_workload(w)
+    t_used += time.perf_counter() - t0
+    done_bytes += w.kv_bytes(); nseq += 1; ntok += L
+    if t_used >= budget:
+        break
+print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": ntok, "seconds": t_used}}))
+"""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    sample = (f"float64 numpy oracle, {d['seqs']} whole sequences ({d['tokens']} cached tokens) of the "
+              f"{config} workload, {d['seconds']:.1f} s, single-threaded BLAS")
+    return d["gbs"], threads, sample
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    vals = []
+    sample = ""
+    for _ in range(max(1, args.warmup)):
+        cpu_oracle_sample(args.config, budget_s=2.0)
+    for _ in range(args.steps):
+        gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.ref_budget)
+        vals.append(gbs)
+    from paged_kv_decode_06_gb300 import workloads as wl
+    import numpy as np
+    spec = wl.CONFIGS[args.config]
+    sl, *_ = wl.draw_metadata(spec, np.random.default_rng(spec.seed))
+    eb = 1 if spec.kv_dtype == "fp8" else 2
+    step_bytes = int(sl.astype(np.int64).sum()) * spec.num_kv_heads * spec.head_dim * 2 * eb
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_bytes / (v * 1e9) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.config, "kv_bytes_per_step": step_bytes},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_06_gb300 import binding
+    from paged_kv_decode_06_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    binding.load()
+    spec = wl.CONFIGS[args.config]
+    base = wl.make_workload(spec, device=str(dev))
+    step_bytes = base.kv_bytes()
+    pools = max(1, math.ceil(2 * L2_BYTES / step_bytes))
+    works = [base] + [wl.make_workload(spec, device=str(dev), seed=spec.seed + 100 * k) for k in range(1, pools)]
+    # every pool shares the metadata of the first (same lengths, same page ids)
+    bt = torch.from_numpy(base.block_tables).to(dev)
+    sl = torch.from_numpy(base.seq_lens).to(dev)
+    qsl = torch.from_numpy(base.query_start_loc).to(dev) if base.query_start_loc is not None else None
+    mq = spec.max_query_len if qsl is not None else 1
+    out = torch.empty_like(base.q)
+    lse = torch.empty(base.q.shape[:2], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(k, opts=None):
+        w = works[k % pools]
+        binding.paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
+                                  spec.v_scale, out=out, lse=lse, options=opts)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    opts = [binding.make_options(split_start_event=starts[k], split_stop_event=stops[k]) for k in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin.record(stream)
+        for k in range(args.steps):
+            step(k, opts[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t_begin.elapsed_time(t_end) / args.steps
+    split_ms = [starts[k].elapsed_time(stops[k]) for k in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end-to-end through the public API: pinned host inputs in, results out, every step
+    h_q = [w.q.cpu().pin_memory() for w in works]
+    h_bt = torch.from_numpy(base.block_tables).pin_memory()
+    h_sl = torch.from_numpy(base.seq_lens).pin_memory()
+    h_qsl = torch.from_numpy(base.query_start_loc).pin_memory() if qsl is not None else None
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q = torch.empty_like(base.q)
+
+    def e2e_step(k):
+        w = works[k % pools]
+        d_q.copy_(h_q[k % pools], non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        sl.copy_(h_sl, non_blocking=True)
+        if qsl is not None:
+            qsl.copy_(h_qsl, non_blocking=True)
+        binding.paged_attn_decode(d_q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
+                                  spec.v_scale, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for k in range(args.warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = d_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4 + (h_qsl.numel() * 4 if h_qsl is not None else 0)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    status = binding.paged_attn_device_status(clear=True)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    split_mean = statistics.mean(split_ms)
+    achieved = step_bytes / (split_mean * 1e-3) / 1e9
+    plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                   binding.kv_dtype_code(spec.kv_dtype), mq)
+    traffic = _traffic_from_profiles(args.config)
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
+        "frac_of_hbm_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f8e4m3" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
+                   "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_dtype": spec.kv_dtype,
+                   "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
+                   "l2": "no flush; each step reads >= 2x L2 of KV (pools rotated when one is smaller)",
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "pa_split_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
+                     "per_launch_bytes": step_bytes},
+        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _traffic_from_profiles(config):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    when it was taken on the current kernel source (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for name in ("pa_split.cuh", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    entry = d.get(config)
+    if not entry or entry.get("kernel_source_sha256") != h.hexdigest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="llama3_8b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0)
+    args = ap.parse_args()
+    world, rank, local = _dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

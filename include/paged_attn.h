@@ -1,0 +1,187 @@
+/*
+ * paged_attn.h - C ABI of the GB300 (sm_103a) paged-KV decode attention library.
+ *
+ * The operation (ATOM model-operations guide, "Multi-head attention": forward
+ * flow step 3 and the "Attention dispatch" table, decode rows; configuration
+ * guide, "Quick reference": kv_cache_block_size = 16, kv_cache_dtype bf16|fp8;
+ * high-interactivity blog, "Attention Decode: Split Memory Work to Fill the
+ * Device"): every query token of every sequence, for every query head hq,
+ * attends over the sequence's cached keys and values,
+ *
+ *     out[t, hq, :] = sum_j softmax_j(scale * <q[t, hq, :], K_j>) * V_j
+ *     lse[t, hq]    = ln sum_j exp(scale * <q[t, hq, :], K_j>)
+ *
+ * where K_j, V_j are the rows of KV head hk = hq / (Hq / Hkv) for logical
+ * token j, found at physical page block_tables[i][j / 16], slot j % 16.
+ * Sequence i has L_i = seq_lens[i] cached tokens, which include its own q_i
+ * query tokens; query token r (0 <= r < q_i) sees keys j <= L_i - q_i + r
+ * (causal inside a multi-token verification run, as in MTP speculative
+ * decoding; a single-token decode sees all L_i keys).  fp8 caches hold OCP
+ * e4m3fn codes; the value of a cached K element is code * k_scale and of a V
+ * element code * v_scale (one fp32 scale per tensor).  bf16 caches ignore
+ * k_scale and v_scale.
+ *
+ * Conventions for every entry point:
+ *   - All tensor data pointers are DEVICE pointers on the current CUDA device.
+ *   - Strides are in elements.  Shapes and strides are read on the host only;
+ *     the library never reads device memory on the host and never
+ *     synchronises the stream.  Work is enqueued asynchronously on `stream`.
+ *   - The caller owns every tensor and must keep it alive until the stream
+ *     work completes.  The library owns only a per-device split workspace
+ *     (grown on demand outside stream capture, see paged_attn_reserve) unless
+ *     the caller passes its own through pa_options_t.
+ *   - Functions return a pa_status (PA_OK = 0); nothing throws across the
+ *     ABI.  paged_attn_last_error_message() gives a human-readable detail of
+ *     the last failure on the calling thread.
+ */
+#ifndef PAGED_ATTN_H
+#define PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t / CUstream; NULL = legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+/* Element types of pa_tensor_t. */
+enum pa_dtype {
+  PA_BF16 = 1,      /* bfloat16                                  */
+  PA_FP8_E4M3 = 2,  /* OCP fp8 e4m3fn codes (1 byte per element) */
+  PA_F32 = 3,       /* float32                                   */
+  PA_I32 = 4        /* int32                                     */
+};
+
+/* Status codes. */
+enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* shape, dtype, stride or alignment mismatch; NULL required pointer */
+  PA_ERR_UNSUPPORTED = 2,  /* valid but outside the kernel's envelope (head_dim, group size, ...) */
+  PA_ERR_WORKSPACE = 3,    /* workspace too small while the stream is being captured, or caller
+                              workspace too small */
+  PA_ERR_CUDA = 4          /* a CUDA runtime/driver call or a kernel launch failed */
+};
+
+/* A strided view of device memory (DLPack-like, without the dependency).
+ * Dimensions beyond ndim are ignored. */
+typedef struct pa_tensor_t {
+  void* data;
+  int32_t dtype;      /* enum pa_dtype */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];  /* elements */
+} pa_tensor_t;
+
+/* Optional controls for paged_attn_decode_ex.  Zero-initialise for defaults. */
+typedef struct pa_options_t {
+  int32_t num_ctas;            /* >0: launch this many split CTAs instead of one per SM */
+  int32_t min_pages_per_cta;   /* >0: override the minimum pages of work per CTA (default 4) */
+  int32_t heads_per_cta;       /* >0: KV heads per CTA (must divide Hkv); 0 = planner's choice */
+  int32_t disable_pdl;         /* !=0: launch the merge kernel without programmatic dependent launch */
+  void* workspace;             /* optional caller-owned device workspace ...                   */
+  size_t workspace_bytes;      /* ... of this size (see paged_attn_workspace_size)            */
+  void* split_start_event;     /* optional cudaEvent_t recorded just before the split kernel  */
+  void* split_stop_event;      /* optional cudaEvent_t recorded just after the split kernel   */
+} pa_options_t;
+
+/* Launch plan the library picks for a problem shape (for tests, tuning and
+ * roofline accounting). */
+typedef struct pa_plan_t {
+  int32_t num_ctas;          /* split-kernel grid size                                  */
+  int32_t heads_per_cta;     /* KV heads a CTA processes per page (HC)                  */
+  int32_t row_tiles;         /* 16-row MMA tiles per KV head (ceil(G*max_query_len/16)) */
+  int32_t num_stages;        /* depth of the shared-memory page ring                    */
+  int32_t threads_per_cta;   /* 32 * (1 producer warp + heads_per_cta * row_tiles)      */
+  int32_t smem_bytes;        /* dynamic shared memory per CTA                           */
+  int32_t min_pages_per_cta; /* work below which fewer CTAs are used                    */
+  int32_t merge_rows;        /* rows per merge unit (heads_per_cta * G * max_query_len) */
+  int64_t workspace_bytes;   /* split workspace the call needs                          */
+} pa_plan_t;
+
+/*
+ * paged_attn_decode - decode attention over a paged KV cache (definition above).
+ *
+ *   q               bf16 [T, Hq, D]; stride[2] == 1, stride[1] == D, stride[0]*2 % 16 == 0,
+ *                   data 16-byte aligned.  T = total query tokens.
+ *   k_cache         bf16 or fp8e4m3 [NB, 16, Hkv, D]; stride[3] == 1; every other stride
+ *                   times the element size a multiple of 16 bytes; data 16-byte aligned.
+ *   v_cache         same dtype and shape as k_cache (strides may differ, same rules).
+ *   block_tables    int32 [B, max_blocks]; stride[1] == 1.  Entry [i][j] is the physical
+ *                   page of logical page j of sequence i; only j < ceil(L_i / 16) is read.
+ *   seq_lens        int32 [B], contiguous.  L_i >= q_i >= 1.
+ *   query_start_loc int32 [B+1] contiguous cumulative query-token offsets (ragged MTP
+ *                   runs), or data == NULL: one query token per sequence (T == B).
+ *   max_query_len   host-known upper bound of q_i (1 when query_start_loc is NULL);
+ *                   chooses the tile without a device read.  G * max_query_len <= 64.
+ *   scale           softmax scale applied to <q, k> (e.g. 1/sqrt(D)).
+ *   k_scale, v_scale per-tensor dequantisation scales of fp8 caches (ignored for bf16).
+ *   out             bf16 [T, Hq, D], stride[2] == 1; written.
+ *   lse             f32 [T, Hq] natural-log log-sum-exp of the scaled logits, or
+ *                   data == NULL (not written).
+ *   stream          stream the work is enqueued on.
+ *
+ * Supported: D in {64, 128}; page size 16; Hq % Hkv == 0; 1 <= B <= 8192.
+ * Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED are detected on the host before
+ * anything is enqueued.  Data errors that only the device can see (a page id
+ * outside [0, NB), L_i < q_i, q_i > max_query_len) set bits of the device status
+ * word (paged_attn_device_status); the affected rows are undefined.
+ */
+int paged_attn_decode(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa_tensor_t* v_cache,
+                      const pa_tensor_t* block_tables, const pa_tensor_t* seq_lens,
+                      const pa_tensor_t* query_start_loc, int32_t max_query_len, float scale,
+                      float k_scale, float v_scale, const pa_tensor_t* out, const pa_tensor_t* lse,
+                      pa_stream_t stream);
+
+/* paged_attn_decode with options (opts may be NULL = defaults).  Same operation,
+ * arguments and errors as paged_attn_decode. */
+int paged_attn_decode_ex(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa_tensor_t* v_cache,
+                         const pa_tensor_t* block_tables, const pa_tensor_t* seq_lens,
+                         const pa_tensor_t* query_start_loc, int32_t max_query_len, float scale,
+                         float k_scale, float v_scale, const pa_tensor_t* out, const pa_tensor_t* lse,
+                         const pa_options_t* opts, pa_stream_t stream);
+
+/* Plan for a shape on the current device (kv_dtype: PA_BF16 or PA_FP8_E4M3).
+ * opts may be NULL.  Reads device attributes only; enqueues nothing. */
+int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t kv_dtype, int32_t max_query_len, const pa_options_t* opts,
+                    pa_plan_t* plan);
+
+/* Bytes of split workspace a call with this shape needs (same as plan.workspace_bytes). */
+int paged_attn_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t kv_dtype, int32_t max_query_len,
+                              size_t* bytes);
+
+/* Grow the library-owned workspace of the current device to fit this shape.  Call it
+ * (or one ordinary decode call) before capturing paged_attn_decode in a CUDA graph:
+ * during capture the library never allocates and returns PA_ERR_WORKSPACE instead.
+ * Synchronises the device if it has to reallocate. */
+int paged_attn_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t kv_dtype, int32_t max_query_len);
+
+/* Release the library-owned workspace of the current device (synchronises the device). */
+int paged_attn_release(void);
+
+/* Read the device status word of the current device into *flags (bit 0: page id out of
+ * range; bit 1: seq_len < query length; bit 2: query length outside [1, max_query_len]
+ * or query_start_loc inconsistent; bit 3: a pipeline wait timed out; bit 4: a query value
+ * overflowed the f16 range on the fp8 path).  clear != 0 resets it to 0.  Synchronises
+ * the device: a debugging aid, not for the hot path. */
+int paged_attn_device_status(uint32_t* flags, int32_t clear);
+
+/* Static description of a status code. */
+const char* paged_attn_error_string(int status);
+
+/* Detail of the last failing call on this thread ("" if none). */
+const char* paged_attn_last_error_message(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t paged_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H */

@@ -1,0 +1,235 @@
+"""Thin ctypes binding over the C ABI of ``include/paged_attn.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  If the library has not been built, ``load()`` raises; there is no
+fallback implementation.  Function names mirror the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpagedattn.so")
+
+PA_BF16, PA_FP8_E4M3, PA_F32, PA_I32 = 1, 2, 3, 4
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
+
+STATUS_PAGE_RANGE, STATUS_SEQ_LEN, STATUS_QUERY_LEN, STATUS_TIMEOUT, STATUS_F16_RANGE = 1, 2, 4, 8, 16
+
+
+class PaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class PaOptions(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("min_pages_per_cta", ctypes.c_int32),
+                ("heads_per_cta", ctypes.c_int32), ("disable_pdl", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p)]
+
+
+class PaPlan(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("heads_per_cta", ctypes.c_int32), ("row_tiles", ctypes.c_int32),
+                ("num_stages", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("min_pages_per_cta", ctypes.c_int32), ("merge_rows", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+_P = ctypes.POINTER(PaTensor)
+_SIGNATURES = {
+    "paged_attn_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                         ctypes.c_float, _P, _P, ctypes.c_void_p]),
+    "paged_attn_decode_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                            ctypes.c_float, _P, _P, ctypes.POINTER(PaOptions), ctypes.c_void_p]),
+    "paged_attn_plan": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(PaOptions), ctypes.POINTER(PaPlan)]),
+    "paged_attn_workspace_size": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "paged_attn_reserve": (ctypes.c_int, [ctypes.c_int32] * 6),
+    "paged_attn_release": (ctypes.c_int, []),
+    "paged_attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]),
+    "paged_attn_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "paged_attn_last_error_message": (ctypes.c_char_p, []),
+    "paged_attn_version": (ctypes.c_int32, []),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load the built library (``build.build()`` makes it).  Raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing (run paged_kv_decode_06_gb300.build.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return PA_FP8_E4M3
+    if t.dtype == torch.float32:
+        return PA_F32
+    if t.dtype == torch.int32:
+        return PA_I32
+    return 0          # not a pa_dtype: the library rejects it with PA_ERR_INVALID_ARG
+
+
+def tensor_desc(t: Optional[torch.Tensor]) -> PaTensor:
+    d = PaTensor()
+    if t is None:
+        d.data = None
+        return d
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _check(lib, status: int):
+    if status != PA_OK:
+        raise PagedAttnError(status, lib.paged_attn_last_error_message().decode() or
+                             lib.paged_attn_error_string(status).decode())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=False, workspace=None,
+                 workspace_bytes=0, split_start_event=None, split_stop_event=None) -> PaOptions:
+    o = PaOptions()
+    o.num_ctas = num_ctas
+    o.min_pages_per_cta = min_pages_per_cta
+    o.heads_per_cta = heads_per_cta
+    o.disable_pdl = int(bool(disable_pdl))
+    o.workspace = workspace
+    o.workspace_bytes = workspace_bytes
+    o.split_start_event = int(split_start_event.cuda_event) if split_start_event is not None else None
+    o.split_stop_event = int(split_stop_event.cuda_event) if split_stop_event is not None else None
+    return o
+
+
+def paged_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc=None, max_query_len=1,
+                      scale=None, k_scale=1.0, v_scale=1.0, out=None, lse=None, stream=None, options=None,
+                      want_lse=True):
+    """Decode attention over a paged KV cache (see include/paged_attn.h).
+
+    Tensors are CUDA tensors: q bf16 [T, Hq, D]; k_cache / v_cache bf16 or
+    uint8 (e4m3fn codes) [NB, 16, Hkv, D]; block_tables int32 [B, max_blocks];
+    seq_lens int32 [B]; query_start_loc int32 [B+1] or None.  Returns
+    (out bf16 [T, Hq, D], lse f32 [T, Hq] or None)."""
+    lib = load()
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    args = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)]
+    o_desc, l_desc = tensor_desc(out), tensor_desc(lse)
+    refs = [ctypes.byref(a) for a in args]
+    if options is None:
+        st = lib.paged_attn_decode(*refs, int(max_query_len), float(scale), float(k_scale), float(v_scale),
+                                   ctypes.byref(o_desc), ctypes.byref(l_desc), _stream_handle(stream))
+    else:
+        st = lib.paged_attn_decode_ex(*refs, int(max_query_len), float(scale), float(k_scale), float(v_scale),
+                                      ctypes.byref(o_desc), ctypes.byref(l_desc), ctypes.byref(options),
+                                      _stream_handle(stream))
+    _check(lib, st)
+    return out, lse
+
+
+def paged_attn_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=PA_BF16, max_query_len=1,
+                    options=None) -> dict:
+    lib = load()
+    plan = PaPlan()
+    st = lib.paged_attn_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len,
+                             ctypes.byref(options) if options is not None else None, ctypes.byref(plan))
+    _check(lib, st)
+    return plan.as_dict()
+
+
+def paged_attn_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=PA_BF16, max_query_len=1):
+    lib = load()
+    n = ctypes.c_size_t(0)
+    _check(lib, lib.paged_attn_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype,
+                                              max_query_len, ctypes.byref(n)))
+    return n.value
+
+
+def paged_attn_reserve(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=PA_BF16, max_query_len=1):
+    lib = load()
+    _check(lib, lib.paged_attn_reserve(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len))
+
+
+def paged_attn_release():
+    lib = load()
+    _check(lib, lib.paged_attn_release())
+
+
+def paged_attn_device_status(clear: bool = True) -> int:
+    lib = load()
+    flags = ctypes.c_uint32(0)
+    _check(lib, lib.paged_attn_device_status(ctypes.byref(flags), int(clear)))
+    return flags.value
+
+
+def paged_attn_error_string(status: int) -> str:
+    return load().paged_attn_error_string(status).decode()
+
+
+def paged_attn_last_error_message() -> str:
+    return load().paged_attn_last_error_message().decode()
+
+
+def paged_attn_version() -> int:
+    return load().paged_attn_version()
+
+
+def kv_dtype_code(kv_dtype: str) -> int:
+    return PA_FP8_E4M3 if kv_dtype == "fp8" else PA_BF16
+
+
+def decode_workload(w, out=None, lse=None, stream=None, options=None, want_lse=True):
+    """Run the kernel on a ``workloads.Workload`` whose tensors live on the GPU.
+    Metadata (block tables, lengths) is copied to the device here."""
+    dev = w.q.device
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    qsl = torch.from_numpy(w.query_start_loc).to(dev) if w.query_start_loc is not None else None
+    s = w.spec
+    return paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, s.max_query_len if qsl is not None else 1,
+                             s.scale, s.k_scale, s.v_scale, out=out, lse=lse, stream=stream, options=options,
+                             want_lse=want_lse)

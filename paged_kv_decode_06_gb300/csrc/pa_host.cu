@@ -1,0 +1,537 @@
+// Host side of the C ABI declared in include/paged_attn.h: argument
+// validation, the launch planner (tile variant, heads per CTA, pipeline depth,
+// grid), the split workspace, TMA descriptor encoding and the two launches.
+// The host never reads device memory and never synchronises the stream on the
+// decode path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <initializer_list>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "paged_attn.h"
+#include "pa_kernels.h"
+
+namespace {
+
+// Device status word (one per device context); kernels get its address.
+__device__ uint32_t g_status_word;
+
+constexpr int kPageSize = 16;
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSeqs = 8192;
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kMaxStages = 8;
+constexpr int kDefaultMinPages = 4;
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int smem_optin = 0;
+  uint32_t* status = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up: attributes, kernel shared-memory limits, status word
+// address.  Caller holds g_mu.
+int device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    if ((e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+    if ((e = cudaDeviceGetAttribute(&s.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
+    s.smem_optin -= 1024;   // room for the kernels' static shared memory
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major * 10 + minor != 103)
+      return fail(PA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                  minor);
+    if ((e = pa::set_split_smem_limits_bf16(s.smem_optin)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(split bf16)");
+    if ((e = pa::set_split_smem_limits_fp8(s.smem_optin)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(split fp8)");
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_status_word)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    s.status = static_cast<uint32_t*>(ptr);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  if (dev_out) *dev_out = dev;
+  return PA_OK;
+}
+
+// ----------------------------------------------------------------- planning
+struct Plan {
+  int B, Hq, Hkv, D, esz, max_qlen;
+  int G, R_max, MT, HC, NC, nstage, threads, grid, min_pages;
+  uint32_t stage_bytes, kv_bytes, q_slot_bytes;
+  uint32_t off_stage, off_q, off_bar, off_prefix, smem;
+  size_t ws_meta, ws_prefix, ws_ml, ws_o, ws_bytes;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_shape_args(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen) {
+  if (B < 1 || B > kMaxSeqs) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d outside [1, %d]", B, kMaxSeqs);
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d must be a positive multiple of num_kv_heads %d", Hq, Hkv);
+  if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", D);
+  if (kv_dtype != PA_BF16 && kv_dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "kv dtype %d is neither PA_BF16 nor PA_FP8_E4M3", kv_dtype);
+  if (max_qlen < 1) return fail(PA_ERR_INVALID_ARG, "max_query_len %d < 1", max_qlen);
+  const int G = Hq / Hkv;
+  if (static_cast<int64_t>(G) * max_qlen > 64)
+    return fail(PA_ERR_UNSUPPORTED, "group size %d x max_query_len %d exceeds 64 query rows per KV head", G,
+                max_qlen);
+  return PA_OK;
+}
+
+int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const pa_options_t* opts, int num_sms,
+              int smem_optin, Plan* pl) {
+  int st = check_shape_args(B, Hq, Hkv, D, kv_dtype, max_qlen);
+  if (st != PA_OK) return st;
+  Plan p = {};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.max_qlen = max_qlen;
+  p.esz = (kv_dtype == PA_FP8_E4M3) ? 1 : 2;
+  p.G = Hq / Hkv;
+  p.R_max = p.G * max_qlen;
+  p.MT = (p.R_max + 15) / 16;
+  p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
+  const uint32_t bar_bytes = 8u * (2 * kMaxStages + 4);
+  const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (B + 1), 16));
+  const int forced_hc = opts ? opts->heads_per_cta : 0;
+  if (forced_hc < 0 || (forced_hc > 0 && Hkv % forced_hc != 0))
+    return fail(PA_ERR_INVALID_ARG, "heads_per_cta %d must divide num_kv_heads %d", forced_hc, Hkv);
+  bool found = false;
+  for (int pass = 0; pass < 2 && !found; ++pass) {
+    const int want_stages = pass == 0 ? 3 : 2;
+    for (int hc = (forced_hc > 0 ? forced_hc : std::min(Hkv, kMaxConsumerWarps)); hc >= 1; --hc) {
+      if (Hkv % hc != 0 || hc * p.MT > kMaxConsumerWarps) {
+        if (forced_hc > 0) break;
+        continue;
+      }
+      const uint32_t kv = static_cast<uint32_t>(hc) * kPageSize * D * p.esz;
+      const uint32_t stage = 2 * kv;
+      const uint32_t qslot = static_cast<uint32_t>(align_up(static_cast<size_t>(max_qlen) * hc * p.G * D * 2, 128));
+      const int64_t fixed = 1024 + 2 * qslot + bar_bytes + prefix_bytes;
+      const int64_t room = smem_optin - fixed;
+      const int nst = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / stage)) : 0;
+      if (nst >= want_stages) {
+        p.HC = hc;
+        p.kv_bytes = kv;
+        p.stage_bytes = stage;
+        p.q_slot_bytes = qslot;
+        p.nstage = nst;
+        found = true;
+        break;
+      }
+      if (forced_hc > 0) break;
+    }
+  }
+  if (!found) return fail(PA_ERR_UNSUPPORTED, "no launch configuration fits %d bytes of shared memory", smem_optin);
+  p.NC = Hkv / p.HC;
+  p.threads = 32 * (1 + p.HC * p.MT);
+  p.off_stage = 0;
+  p.off_q = p.off_stage + p.nstage * p.stage_bytes;
+  p.off_bar = p.off_q + 2 * p.q_slot_bytes;
+  p.off_prefix = p.off_bar + bar_bytes;
+  p.smem = 1024 + p.off_prefix + prefix_bytes;
+  p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
+  const size_t rows = static_cast<size_t>(2) * p.grid * p.HC * p.R_max;
+  p.ws_meta = 0;
+  p.ws_prefix = 256;
+  p.ws_ml = align_up(p.ws_prefix + 4u * (B + 1), 256);
+  p.ws_o = align_up(p.ws_ml + rows * 8, 256);
+  p.ws_bytes = align_up(p.ws_o + rows * D * 4, 256);
+  *pl = p;
+  return PA_OK;
+}
+
+// ---------------------------------------------------------------- validation
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int check_tensor(const pa_tensor_t* t, const char* name, int ndim, bool allow_null) {
+  if (t == nullptr) return fail(PA_ERR_INVALID_ARG, "%s: descriptor pointer is NULL", name);
+  if (t->data == nullptr) {
+    if (allow_null) return PA_OK;
+    return fail(PA_ERR_INVALID_ARG, "%s: data pointer is NULL", name);
+  }
+  if (t->ndim != ndim) return fail(PA_ERR_INVALID_ARG, "%s: ndim %d, expected %d", name, t->ndim, ndim);
+  for (int d = 0; d < ndim; ++d) {
+    if (t->shape[d] < 0) return fail(PA_ERR_INVALID_ARG, "%s: negative shape[%d]", name, d);
+    if (t->stride[d] < 0) return fail(PA_ERR_INVALID_ARG, "%s: negative stride[%d]", name, d);
+  }
+  return PA_OK;
+}
+
+int encode_cache_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int D, int Hkv, int64_t NB) {
+  const int rowb = D * esz;
+  const int rb = rowb >= 128 ? 128 : 64;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(kPageSize),
+                        static_cast<cuuint64_t>(NB)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->stride[2]) * esz, static_cast<cuuint64_t>(t->stride[1]) * esz,
+                           static_cast<cuuint64_t>(t->stride[0]) * esz};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(rb / esz), 1u, static_cast<cuuint32_t>(kPageSize), 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = g_encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                              t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for a KV cache", r);
+  return PA_OK;
+}
+
+int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* vc, const pa_tensor_t* bt,
+                const pa_tensor_t* sl, const pa_tensor_t* qsl, int32_t max_qlen, float scale, float k_scale,
+                float v_scale, const pa_tensor_t* out, const pa_tensor_t* lse, const pa_options_t* opts,
+                cudaStream_t stream) {
+  int st;
+  if ((st = check_tensor(q, "q", 3, false)) || (st = check_tensor(kc, "k_cache", 4, false)) ||
+      (st = check_tensor(vc, "v_cache", 4, false)) || (st = check_tensor(bt, "block_tables", 2, false)) ||
+      (st = check_tensor(sl, "seq_lens", 1, false)) || (st = check_tensor(qsl, "query_start_loc", 1, true)) ||
+      (st = check_tensor(out, "out", 3, false)) || (st = check_tensor(lse, "lse", 2, true)))
+    return st;
+  if (q->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "q must be bf16");
+  if (out->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "out must be bf16");
+  if (kc->dtype != PA_BF16 && kc->dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "k_cache must be bf16 or fp8 e4m3");
+  if (vc->dtype != kc->dtype) return fail(PA_ERR_INVALID_ARG, "v_cache dtype differs from k_cache");
+  if (bt->dtype != PA_I32 || sl->dtype != PA_I32) return fail(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32");
+  if (qsl->data && qsl->dtype != PA_I32) return fail(PA_ERR_INVALID_ARG, "query_start_loc must be int32");
+  if (lse->data && lse->dtype != PA_F32) return fail(PA_ERR_INVALID_ARG, "lse must be float32");
+  const int64_t T = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t NB = kc->shape[0], P = kc->shape[1], Hkv = kc->shape[2];
+  const int64_t B = bt->shape[0], MB = bt->shape[1];
+  if (P != kPageSize) return fail(PA_ERR_UNSUPPORTED, "page size %lld, only 16 is supported", (long long)P);
+  if (kc->shape[3] != D) return fail(PA_ERR_INVALID_ARG, "k_cache head_dim %lld != q head_dim %lld", (long long)kc->shape[3], (long long)D);
+  for (int d = 0; d < 4; ++d)
+    if (vc->shape[d] != kc->shape[d]) return fail(PA_ERR_INVALID_ARG, "v_cache shape differs from k_cache");
+  if (Hq > (1 << 20) || Hkv > (1 << 20) || T > (int64_t(1) << 30) || NB > (int64_t(1) << 31) - 1 || MB > (1 << 28))
+    return fail(PA_ERR_UNSUPPORTED, "tensor extents too large");
+  if (sl->shape[0] != B) return fail(PA_ERR_INVALID_ARG, "seq_lens has %lld entries, block_tables %lld rows", (long long)sl->shape[0], (long long)B);
+  if (B * MB > (int64_t(1) << 31)) return fail(PA_ERR_UNSUPPORTED, "block table too large");
+  if (out->shape[0] != T || out->shape[1] != Hq || out->shape[2] != D) return fail(PA_ERR_INVALID_ARG, "out shape differs from q");
+  if (lse->data && (lse->shape[0] != T || lse->shape[1] != Hq)) return fail(PA_ERR_INVALID_ARG, "lse shape must be [T, Hq]");
+  if (B == 0 || T == 0) return PA_OK;   // nothing to do
+  if (qsl->data) {
+    if (qsl->shape[0] != B + 1) return fail(PA_ERR_INVALID_ARG, "query_start_loc must have B+1 entries");
+    if (qsl->stride[0] != 1) return fail(PA_ERR_INVALID_ARG, "query_start_loc must be contiguous");
+    if (T < B || T > B * static_cast<int64_t>(max_qlen))
+      return fail(PA_ERR_INVALID_ARG, "T = %lld query tokens is outside [B, B * max_query_len]", (long long)T);
+  } else {
+    if (T != B) return fail(PA_ERR_INVALID_ARG, "without query_start_loc, q needs one token per sequence (T == B)");
+    if (max_qlen != 1) return fail(PA_ERR_INVALID_ARG, "max_query_len must be 1 without query_start_loc");
+  }
+  if (sl->stride[0] != 1) return fail(PA_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (bt->stride[1] != 1) return fail(PA_ERR_INVALID_ARG, "block_tables rows must be contiguous");
+  if (q->stride[2] != 1 || q->stride[1] != D) return fail(PA_ERR_INVALID_ARG, "q must have contiguous heads (stride[1] == D, stride[2] == 1)");
+  if ((q->stride[0] * 2) % 16 != 0 || !aligned(q->data, 16)) return fail(PA_ERR_INVALID_ARG, "q rows must be 16-byte aligned");
+  if (out->stride[2] != 1 || (out->stride[1] % 4) != 0 || (out->stride[0] % 4) != 0 || !aligned(out->data, 8))
+    return fail(PA_ERR_INVALID_ARG, "out must have a contiguous last dim, strides multiple of 4 elements, 8-byte alignment");
+  const int esz = kc->dtype == PA_FP8_E4M3 ? 1 : 2;
+  for (const pa_tensor_t* c : {kc, vc}) {
+    if (c->stride[3] != 1) return fail(PA_ERR_INVALID_ARG, "KV cache last dim must be contiguous");
+    for (int d = 0; d < 3; ++d)
+      if ((c->stride[d] * esz) % 16 != 0) return fail(PA_ERR_INVALID_ARG, "KV cache strides must be multiples of 16 bytes");
+    if (!aligned(c->data, 16)) return fail(PA_ERR_INVALID_ARG, "KV cache data must be 16-byte aligned");
+  }
+  if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return fail(PA_ERR_INVALID_ARG, "scale, k_scale and v_scale must be finite");
+  if ((st = check_shape_args(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq),
+                             static_cast<int>(Hkv), static_cast<int>(D), kc->dtype, max_qlen)) != PA_OK)
+    return st;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  Plan pl;
+  if ((st = make_plan(static_cast<int>(B), static_cast<int>(Hq), static_cast<int>(Hkv), static_cast<int>(D),
+                      kc->dtype, max_qlen, opts, ds->num_sms, ds->smem_optin, &pl)) != PA_OK)
+    return st;
+
+  // workspace
+  void* ws = nullptr;
+  if (opts && opts->workspace) {
+    if (opts->workspace_bytes < pl.ws_bytes)
+      return fail(PA_ERR_WORKSPACE, "caller workspace %zu bytes < %zu needed", opts->workspace_bytes, pl.ws_bytes);
+    if (!aligned(opts->workspace, 256)) return fail(PA_ERR_INVALID_ARG, "caller workspace must be 256-byte aligned");
+    ws = opts->workspace;
+  } else {
+    if (ds->ws_bytes < pl.ws_bytes) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+      if (cs != cudaStreamCaptureStatusNone)
+        return fail(PA_ERR_WORKSPACE, "workspace must grow to %zu bytes, which is not allowed during stream capture; "
+                    "call paged_attn_reserve first", pl.ws_bytes);
+      if (ds->ws) {
+        if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+        ds->ws = nullptr;
+        ds->ws_bytes = 0;
+      }
+      if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      ds->ws_bytes = pl.ws_bytes;
+    }
+    ws = ds->ws;
+  }
+
+  CUtensorMap tk, tv;
+  if ((st = encode_cache_map(&tk, kc, esz, static_cast<int>(D), static_cast<int>(Hkv), NB)) != PA_OK) return st;
+  if ((st = encode_cache_map(&tv, vc, esz, static_cast<int>(D), static_cast<int>(Hkv), NB)) != PA_OK) return st;
+
+  const float kLog2e = 1.4426950408889634f;
+  pa::SplitParams sp = {};
+  sp.q = static_cast<const uint16_t*>(q->data);
+  sp.q_stride_t = q->stride[0];
+  sp.out = static_cast<uint16_t*>(out->data);
+  sp.out_stride_t = out->stride[0];
+  sp.out_stride_h = out->stride[1];
+  sp.lse = static_cast<float*>(lse->data);
+  sp.lse_stride_t = lse->data ? lse->stride[0] : 0;
+  sp.lse_stride_h = lse->data ? lse->stride[1] : 0;
+  sp.block_tables = static_cast<const int32_t*>(bt->data);
+  sp.bt_stride = bt->stride[0];
+  sp.seq_lens = static_cast<const int32_t*>(sl->data);
+  sp.qsl = static_cast<const int32_t*>(qsl->data);
+  sp.num_seqs = static_cast<int32_t>(B);
+  sp.num_tokens = static_cast<int32_t>(T);
+  sp.Hq = static_cast<int32_t>(Hq);
+  sp.Hkv = static_cast<int32_t>(Hkv);
+  sp.G = pl.G;
+  sp.max_qlen = max_qlen;
+  sp.num_pages = static_cast<int32_t>(NB);
+  sp.max_blocks = static_cast<int32_t>(MB);
+  sp.HC = pl.HC;
+  sp.NC = pl.NC;
+  sp.MT = pl.MT;
+  sp.R_max = pl.R_max;
+  sp.nstage = pl.nstage;
+  sp.min_pages = pl.min_pages;
+  sp.scale_log2 = scale * (esz == 1 ? k_scale : 1.0f) * kLog2e;
+  sp.v_scale = esz == 1 ? v_scale : 1.0f;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  sp.ws_meta = reinterpret_cast<int64_t*>(wsb + pl.ws_meta);
+  sp.ws_prefix = reinterpret_cast<int32_t*>(wsb + pl.ws_prefix);
+  sp.ws_ml = reinterpret_cast<float2*>(wsb + pl.ws_ml);
+  sp.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
+  sp.err = ds->status;
+  sp.off_prefix = pl.off_prefix;
+  sp.off_bar = pl.off_bar;
+  sp.off_q = pl.off_q;
+  sp.q_slot_bytes = pl.q_slot_bytes;
+  sp.off_stage = pl.off_stage;
+  sp.stage_bytes = pl.stage_bytes;
+  sp.kv_bytes = pl.kv_bytes;
+
+  pa::MergeParams mp = {};
+  mp.out = sp.out;
+  mp.out_stride_t = sp.out_stride_t;
+  mp.out_stride_h = sp.out_stride_h;
+  mp.lse = sp.lse;
+  mp.lse_stride_t = sp.lse_stride_t;
+  mp.lse_stride_h = sp.lse_stride_h;
+  mp.seq_lens = sp.seq_lens;
+  mp.qsl = sp.qsl;
+  mp.num_seqs = sp.num_seqs;
+  mp.num_tokens = sp.num_tokens;
+  mp.G = pl.G;
+  mp.HC = pl.HC;
+  mp.NC = pl.NC;
+  mp.R_max = pl.R_max;
+  mp.max_qlen = max_qlen;
+  mp.v_scale = sp.v_scale;
+  mp.ws_meta = sp.ws_meta;
+  mp.ws_prefix = sp.ws_prefix;
+  mp.ws_ml = sp.ws_ml;
+  mp.ws_o = sp.ws_o;
+  mp.err = sp.err;
+
+  cudaEvent_t ev0 = opts ? static_cast<cudaEvent_t>(opts->split_start_event) : nullptr;
+  cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_stop_event) : nullptr;
+  cudaError_t e;
+  if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
+  e = (esz == 1) ? pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem), stream)
+                 : pa::launch_split_bf16(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+  if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stop)");
+  const bool pdl = !(opts && opts->disable_pdl) && !ev1;
+  const int merge_y = (pl.HC * pl.R_max + 7) / 8;
+  e = pa::launch_merge(static_cast<int>(D), mp, static_cast<int>(B) * pl.NC, merge_y, pdl, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_attn_decode_ex(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa_tensor_t* v_cache,
+                         const pa_tensor_t* block_tables, const pa_tensor_t* seq_lens,
+                         const pa_tensor_t* query_start_loc, int32_t max_query_len, float scale, float k_scale,
+                         float v_scale, const pa_tensor_t* out, const pa_tensor_t* lse, const pa_options_t* opts,
+                         pa_stream_t stream) {
+  t_last_error.clear();
+  return decode_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, max_query_len, scale, k_scale,
+                     v_scale, out, lse, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int paged_attn_decode(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa_tensor_t* v_cache,
+                      const pa_tensor_t* block_tables, const pa_tensor_t* seq_lens, const pa_tensor_t* query_start_loc,
+                      int32_t max_query_len, float scale, float k_scale, float v_scale, const pa_tensor_t* out,
+                      const pa_tensor_t* lse, pa_stream_t stream) {
+  return paged_attn_decode_ex(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, max_query_len, scale,
+                              k_scale, v_scale, out, lse, nullptr, stream);
+}
+
+int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype,
+                    int32_t max_query_len, const pa_options_t* opts, pa_plan_t* plan) {
+  t_last_error.clear();
+  if (plan == nullptr) return fail(PA_ERR_INVALID_ARG, "plan pointer is NULL");
+  int st = check_shape_args(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len);
+  if (st != PA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  Plan pl;
+  if ((st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, opts, ds->num_sms,
+                      ds->smem_optin, &pl)) != PA_OK)
+    return st;
+  plan->num_ctas = pl.grid;
+  plan->heads_per_cta = pl.HC;
+  plan->row_tiles = pl.MT;
+  plan->num_stages = pl.nstage;
+  plan->threads_per_cta = pl.threads;
+  plan->smem_bytes = static_cast<int32_t>(pl.smem);
+  plan->min_pages_per_cta = pl.min_pages;
+  plan->merge_rows = pl.HC * pl.R_max;
+  plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
+  return PA_OK;
+}
+
+int paged_attn_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t kv_dtype, int32_t max_query_len, size_t* bytes) {
+  if (bytes == nullptr) return fail(PA_ERR_INVALID_ARG, "bytes pointer is NULL");
+  pa_plan_t plan;
+  const int st = paged_attn_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, nullptr, &plan);
+  if (st == PA_OK) *bytes = static_cast<size_t>(plan.workspace_bytes);
+  return st;
+}
+
+int paged_attn_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t kv_dtype, int32_t max_query_len) {
+  t_last_error.clear();
+  int st = check_shape_args(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len);
+  if (st != PA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  Plan pl;
+  if ((st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, nullptr, ds->num_sms,
+                      ds->smem_optin, &pl)) != PA_OK)
+    return st;
+  if (ds->ws_bytes >= pl.ws_bytes) return PA_OK;
+  cudaError_t e;
+  if (ds->ws) {
+    if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    ds->ws = nullptr;
+    ds->ws_bytes = 0;
+  }
+  if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+  ds->ws_bytes = pl.ws_bytes;
+  return PA_OK;
+}
+
+int paged_attn_release(void) {
+  t_last_error.clear();
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds, nullptr);
+  if (st != PA_OK) return st;
+  if (ds->ws) {
+    cudaError_t e = cudaFree(ds->ws);
+    ds->ws = nullptr;
+    ds->ws_bytes = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+  }
+  return PA_OK;
+}
+
+int paged_attn_device_status(uint32_t* flags, int32_t clear) {
+  t_last_error.clear();
+  if (flags == nullptr) return fail(PA_ERR_INVALID_ARG, "flags pointer is NULL");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds, nullptr);
+  if (st != PA_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if ((e = cudaMemcpy(flags, ds->status, sizeof(uint32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "reading the status word");
+  if (clear && (e = cudaMemset(ds->status, 0, sizeof(uint32_t))) != cudaSuccess)
+    return cuda_fail(e, "clearing the status word");
+  if (clear && (e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  return PA_OK;
+}
+
+const char* paged_attn_error_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK: success";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument (shape, dtype, stride, alignment or NULL pointer)";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: outside the supported envelope";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: split workspace too small (or growth needed during capture)";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA call or kernel launch failed";
+    default: return "unknown paged_attn status";
+  }
+}
+
+const char* paged_attn_last_error_message(void) { return t_last_error.c_str(); }
+
+int32_t paged_attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Parameters shared by the host launcher and the split / merge kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct SplitParams {
+  // query / outputs
+  const uint16_t* q;        // bf16 [T, Hq, D], head stride D
+  int64_t q_stride_t;       // elements
+  uint16_t* out;            // bf16 [T, Hq, D]
+  int64_t out_stride_t, out_stride_h;
+  float* lse;               // f32 [T, Hq] or nullptr
+  int64_t lse_stride_t, lse_stride_h;
+  // paged metadata
+  const int32_t* block_tables;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* qsl;       // [B+1] or nullptr (one token per sequence)
+  int32_t num_seqs;         // B
+  int32_t num_tokens;       // T (rows of q / out)
+  int32_t Hq, Hkv, G;
+  int32_t max_qlen;
+  int32_t num_pages;        // NB
+  int32_t max_blocks;       // block-table columns
+  // plan
+  int32_t HC;               // KV heads per CTA
+  int32_t NC;               // head chunks = Hkv / HC
+  int32_t MT;               // 16-row tiles per head
+  int32_t R_max;            // G * max_qlen rows per head
+  int32_t nstage;
+  int32_t min_pages;        // minimum pages of work per CTA
+  // math
+  float scale_log2;         // scale * k_scale * log2(e)
+  float v_scale;            // applied to the output (1 for bf16 caches)
+  // workspace
+  int64_t* ws_meta;         // [0] = total pages X, [1] = CTAs used
+  int32_t* ws_prefix;       // [B+1] page prefix over sequences
+  float2* ws_ml;            // [2 * grid][HC][R_max] (running max in log2 units, sum)
+  float* ws_o;              // [2 * grid][HC][R_max][D] unnormalised partial outputs
+  uint32_t* err;            // device status word
+  // shared-memory layout (bytes from the 1024-aligned base)
+  uint32_t off_prefix;
+  uint32_t off_bar;
+  uint32_t off_q;
+  uint32_t q_slot_bytes;
+  uint32_t off_stage;
+  uint32_t stage_bytes;     // K tiles + V tiles of one page
+  uint32_t kv_bytes;        // K (or V) tiles of one page: HC * 16 * D * elem
+};
+
+struct MergeParams {
+  uint16_t* out;
+  int64_t out_stride_t, out_stride_h;
+  float* lse;
+  int64_t lse_stride_t, lse_stride_h;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int32_t num_seqs, num_tokens;
+  int32_t G, HC, NC, R_max, max_qlen;
+  float v_scale;
+  const int64_t* ws_meta;
+  const int32_t* ws_prefix;
+  const float2* ws_ml;
+  const float* ws_o;
+  uint32_t* err;
+};
+
+// Launchers (one translation unit per cache dtype).  `pdl` requests
+// programmatic dependent launch for the merge kernel.
+cudaError_t launch_split_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                              int grid, int threads, int smem, cudaStream_t stream);
+cudaError_t launch_split_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                             int grid, int threads, int smem, cudaStream_t stream);
+cudaError_t launch_merge(int head_dim, const MergeParams& p, int grid_x, int grid_y, bool pdl,
+                         cudaStream_t stream);
+cudaError_t set_split_smem_limits_bf16(int smem);
+cudaError_t set_split_smem_limits_fp8(int smem);
+
+}  // namespace pa

@@ -1,0 +1,129 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+that include/paged_attn.h declares, and rejects invalid arguments on the host
+with the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_kv_decode_06_gb300 import binding
+from paged_kv_decode_06_gb300 import build as builder
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paged_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    builder.build()
+    return binding.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(paged_attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("paged_attn_decode", "paged_attn_decode_ex", "paged_attn_plan", "paged_attn_reserve",
+              "paged_attn_device_status", "paged_attn_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) == set(binding.EXPORTED)
+
+
+def test_error_strings_and_version(lib):
+    for st in range(5):
+        assert binding.paged_attn_error_string(st).startswith("PA_")
+    assert "unknown" in binding.paged_attn_error_string(99)
+    assert binding.paged_attn_version() >= 100
+
+
+def _good_args(T=3, Hq=8, Hkv=2, D=128, NB=10, B=3, MB=4, kv=torch.bfloat16):
+    q = torch.zeros(T, Hq, D, dtype=torch.bfloat16)
+    k = torch.zeros(NB, 16, Hkv, D, dtype=kv)
+    v = torch.zeros(NB, 16, Hkv, D, dtype=kv)
+    bt = torch.zeros(B, MB, dtype=torch.int32)
+    sl = torch.ones(B, dtype=torch.int32)
+    out = torch.zeros_like(q)
+    lse = torch.zeros(T, Hq, dtype=torch.float32)
+    return dict(q=q, k=k, v=v, bt=bt, sl=sl, qsl=None, out=out, lse=lse, max_qlen=1)
+
+
+def _call(lib, a, scale=0.1):
+    descs = [binding.tensor_desc(a[n]) for n in ("q", "k", "v", "bt", "sl", "qsl", "out", "lse")]
+    refs = [ctypes.byref(d) for d in descs]
+    return lib.paged_attn_decode(*refs[:6], a["max_qlen"], scale, 1.0, 1.0, refs[6], refs[7], None)
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: a.update(q=a["q"].float()), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(out=a["out"].float()), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(bt=a["bt"].long()), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(v=torch.zeros(10, 16, 2, 128, dtype=torch.uint8)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(k=torch.zeros(10, 8, 2, 128, dtype=torch.bfloat16),
+                        v=torch.zeros(10, 8, 2, 128, dtype=torch.bfloat16)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(q=torch.zeros(3, 8, 96, dtype=torch.bfloat16), out=torch.zeros(3, 8, 96, dtype=torch.bfloat16),
+                        k=torch.zeros(10, 16, 2, 96, dtype=torch.bfloat16),
+                        v=torch.zeros(10, 16, 2, 96, dtype=torch.bfloat16)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(q=torch.zeros(3, 6, 128, dtype=torch.bfloat16), out=torch.zeros(3, 6, 128, dtype=torch.bfloat16),
+                        k=torch.zeros(10, 16, 4, 128, dtype=torch.bfloat16),
+                        v=torch.zeros(10, 16, 4, 128, dtype=torch.bfloat16), lse=None), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(sl=torch.ones(2, dtype=torch.int32)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(q=torch.zeros(4, 8, 128, dtype=torch.bfloat16), out=torch.zeros(4, 8, 128, dtype=torch.bfloat16),
+                        lse=None), binding.PA_ERR_INVALID_ARG),           # T != B without query_start_loc
+    (lambda a: a.update(max_qlen=2), binding.PA_ERR_INVALID_ARG),         # max_qlen > 1 without query_start_loc
+    (lambda a: a.update(q=torch.zeros(3, 8, 256, dtype=torch.bfloat16)[:, :, :128]), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(lse=torch.zeros(3, 4, dtype=torch.float32)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(bt=torch.zeros(4, 3, dtype=torch.int32).t()), binding.PA_ERR_INVALID_ARG),
+])
+def test_invalid_arguments_rejected_on_host(lib, mutate, expect):
+    a = _good_args()
+    mutate(a)
+    st = _call(lib, a)
+    assert st == expect, binding.paged_attn_last_error_message()
+    assert binding.paged_attn_last_error_message() != ""
+
+
+def test_group_times_query_len_over_64_is_unsupported(lib):
+    a = _good_args(T=6, Hq=32, Hkv=1)
+    a["k"] = torch.zeros(10, 16, 1, 128, dtype=torch.bfloat16)
+    a["v"] = torch.zeros(10, 16, 1, 128, dtype=torch.bfloat16)
+    a["qsl"] = torch.tensor([0, 2, 4, 6], dtype=torch.int32)
+    a["max_qlen"] = 3
+    assert _call(lib, a) == binding.PA_ERR_UNSUPPORTED
+
+
+def test_null_descriptor_pointer(lib):
+    a = _good_args()
+    descs = [binding.tensor_desc(a[n]) for n in ("q", "k", "v", "bt", "sl", "qsl", "out", "lse")]
+    refs = [ctypes.byref(d) for d in descs]
+    st = lib.paged_attn_decode(None, *refs[1:6], 1, 0.1, 1.0, 1.0, refs[6], refs[7], None)
+    assert st == binding.PA_ERR_INVALID_ARG
+
+
+def test_non_finite_scale_rejected(lib):
+    assert _call(lib, _good_args(), scale=float("nan")) == binding.PA_ERR_INVALID_ARG
+
+
+def test_valid_arguments_without_gpu_report_cuda_error(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(lib, _good_args()) == binding.PA_ERR_CUDA
+
+
+def test_plan_rejects_bad_shapes_without_device(lib):
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.paged_attn_plan(4, 8, 3, 128)
+    assert e.value.status == binding.PA_ERR_INVALID_ARG
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.paged_attn_plan(4, 8, 2, 80)
+    assert e.value.status == binding.PA_ERR_UNSUPPORTED
