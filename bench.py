@@ -190,7 +190,7 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     binding.load()
-    spec = wl.CONFIGS[args.config]
+    spec = _spec_for(args)
     base = wl.make_workload(spec, device=str(dev))
     step_bytes = base.kv_bytes()
     pools = max(1, math.ceil(2 * L2_BYTES / step_bytes))
@@ -216,6 +216,9 @@ def run_ours(args, world, rank, local):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for ev in starts + stops:      # torch only times events it has recorded once itself
+        ev.record(stream)
+    torch.cuda.synchronize()
     opts = [binding.make_options(split_start_event=starts[k], split_stop_event=stops[k]) for k in range(args.steps)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -282,14 +285,14 @@ def run_ours(args, world, rank, local):
     achieved = step_bytes / (split_mean * 1e-3) / 1e9
     plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                                    binding.kv_dtype_code(spec.kv_dtype), mq)
-    traffic = _traffic_from_profiles(args.config)
+    traffic = _traffic_from_profiles(spec.name)
     value = step_bytes * world / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
         "frac_of_hbm_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f8e4m3" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
-        "config": {"workload": args.config, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
+        "config": {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
                    "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_dtype": spec.kv_dtype,
                    "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
                    "l2": "no flush; each step reads >= 2x L2 of KV (pools rotated when one is smaller)",
@@ -304,12 +307,22 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
         "device_status": status,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not args.batch:
         gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def _spec_for(args):
+    import dataclasses
+
+    from paged_kv_decode_06_gb300 import workloads as wl
+    spec = wl.CONFIGS[args.config]
+    if args.batch:
+        spec = dataclasses.replace(spec, num_seqs=args.batch, name=f"{spec.name}_b{args.batch}")
+    return spec
 
 
 def _traffic_from_profiles(config):
@@ -337,6 +350,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="llama3_8b")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
