@@ -64,7 +64,7 @@ class ClockSampler:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -122,12 +122,13 @@ order = np.random.default_rng(123).permutation(spec.num_seqs)
 import torch
 budget = {budget_s}
 done_bytes = 0; t_used = 0.0; nseq = 0; ntok = 0
-for i in order:
+seq_iter = (int(i) for _ in range(1000) for i in order)
+for i in seq_iter:
     L = int(sl[i]); q = int(ql[i]); n = (L + 15) // 16
     sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
                          kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
                          k_scale=spec.k_scale, v_scale=spec.v_scale, fp8_source_scale=spec.fp8_source_scale,
-                         seed=int(i))
+                         seed=nseq)
     w = wl.make_workload(sub)
     t0 = time.perf_counter()
     oracle.run_workload(w)
@@ -144,8 +145,8 @@ print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": nto
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    sample = (f"float64 numpy oracle, {d['seqs']} whole sequences ({d['tokens']} cached tokens) of the "
-              f"{config} workload, {d['seconds']:.1f} s, single-threaded BLAS")
+    sample = (f"float64 numpy oracle, {d['seqs']} whole sequences ({d['tokens']} cached tokens) drawn from the "
+              f"{config} workload's length mix, {d['seconds']:.1f} s of oracle time, single-threaded BLAS")
     return d["gbs"], threads, sample
 
 
@@ -222,17 +223,22 @@ def run_ours(args, world, rank, local):
     opts = [binding.make_options(split_start_event=starts[k], split_stop_event=stops[k]) for k in range(args.steps)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # pass 1 (value): K whole steps back to back, bracketed by barrier + sync
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         t_begin.record(stream)
         for k in range(args.steps):
-            step(k, opts[k])
+            step(k)
         t_end.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+        if world > 1:
+            torch.distributed.barrier()
+        # pass 2 (roofline): the same K steps with events around each split launch
+        for k in range(args.steps):
+            step(k, opts[k])
+        torch.cuda.synchronize()
     ms = t_begin.elapsed_time(t_end) / args.steps
     split_ms = [starts[k].elapsed_time(stops[k]) for k in range(args.steps)]
     if world > 1:
@@ -347,8 +353,8 @@ def _traffic_from_profiles(config):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="llama3_8b")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -144,7 +144,7 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
   p.MT = (p.R_max + 15) / 16;
   p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
   const uint32_t bar_bytes = 8u * (2 * kMaxStages + 4);
-  const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (B + 1), 16));
+  const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));   // prefix, lengths, starts
   const int forced_hc = opts ? opts->heads_per_cta : 0;
   if (forced_hc < 0 || (forced_hc > 0 && Hkv % forced_hc != 0))
     return fail(PA_ERR_INVALID_ARG, "heads_per_cta %d must divide num_kv_heads %d", forced_hc, Hkv);
@@ -210,14 +210,18 @@ int check_tensor(const pa_tensor_t* t, const char* name, int ndim, bool allow_nu
   return PA_OK;
 }
 
-int encode_cache_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int D, int Hkv, int64_t NB) {
+// TMA map over a cache [NB, 16, Hkv, D] with dimensions ordered (d, slot, head,
+// page): one box is RB bytes of the row x 16 slots x HC heads, which lands in
+// shared memory head-major, 16 swizzled rows per head.
+int encode_cache_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int D, int Hkv, int HC, int64_t NB) {
   const int rowb = D * esz;
   const int rb = rowb >= 128 ? 128 : 64;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(kPageSize),
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(kPageSize), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(NB)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->stride[2]) * esz, static_cast<cuuint64_t>(t->stride[1]) * esz,
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->stride[1]) * esz, static_cast<cuuint64_t>(t->stride[2]) * esz,
                            static_cast<cuuint64_t>(t->stride[0]) * esz};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(rb / esz), 1u, static_cast<cuuint32_t>(kPageSize), 1u};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(rb / esz), static_cast<cuuint32_t>(kPageSize),
+                       static_cast<cuuint32_t>(HC), 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUresult r = g_encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                               t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -322,8 +326,8 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   }
 
   CUtensorMap tk, tv;
-  if ((st = encode_cache_map(&tk, kc, esz, static_cast<int>(D), static_cast<int>(Hkv), NB)) != PA_OK) return st;
-  if ((st = encode_cache_map(&tv, vc, esz, static_cast<int>(D), static_cast<int>(Hkv), NB)) != PA_OK) return st;
+  if ((st = encode_cache_map(&tk, kc, esz, static_cast<int>(D), static_cast<int>(Hkv), pl.HC, NB)) != PA_OK) return st;
+  if ((st = encode_cache_map(&tv, vc, esz, static_cast<int>(D), static_cast<int>(Hkv), pl.HC, NB)) != PA_OK) return st;
 
   const float kLog2e = 1.4426950408889634f;
   pa::SplitParams sp = {};
@@ -395,14 +399,21 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   cudaEvent_t ev0 = opts ? static_cast<cudaEvent_t>(opts->split_start_event) : nullptr;
   cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_stop_event) : nullptr;
   cudaError_t e;
+  // Both kernels use programmatic dependent launch: each waits for its
+  // predecessor in the stream before touching global memory, but its launch
+  // overlaps the predecessor's tail.
+  const bool pdl = !(opts && opts->disable_pdl);
   if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
-  e = (esz == 1) ? pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem), stream)
-                 : pa::launch_split_bf16(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem), stream);
+  e = (esz == 1) ? pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
+                                        pdl && !ev0, stream)
+                 : pa::launch_split_bf16(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads,
+                                         static_cast<int>(pl.smem), pdl && !ev0, stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stop)");
-  const bool pdl = !(opts && opts->disable_pdl) && !ev1;
-  const int merge_y = (pl.HC * pl.R_max + 7) / 8;
-  e = pa::launch_merge(static_cast<int>(D), mp, static_cast<int>(B) * pl.NC, merge_y, pdl, stream);
+  // Many pieces per unit on average (few long contexts over many CTAs): the
+  // wide merge reads a row's partials with a whole block.
+  const bool wide = pl.grid >= 4 * static_cast<int>(B) * pl.NC;
+  e = pa::launch_merge(static_cast<int>(D), mp, static_cast<int>(B) * pl.NC, pl.HC * pl.R_max, wide, pdl && !ev1, stream);
   if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   return PA_OK;
 }

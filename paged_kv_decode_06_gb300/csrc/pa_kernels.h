@@ -43,7 +43,7 @@ struct SplitParams {
   float* ws_o;              // [2 * grid][HC][R_max][D] unnormalised partial outputs
   uint32_t* err;            // device status word
   // shared-memory layout (bytes from the 1024-aligned base)
-  uint32_t off_prefix;
+  uint32_t off_prefix;      // int32 [B+1] page prefix, then [B] seq_lens, then [B+1] query starts
   uint32_t off_bar;
   uint32_t off_q;
   uint32_t q_slot_bytes;
@@ -72,10 +72,12 @@ struct MergeParams {
 // Launchers (one translation unit per cache dtype).  `pdl` requests
 // programmatic dependent launch for the merge kernel.
 cudaError_t launch_split_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
-                              int grid, int threads, int smem, cudaStream_t stream);
+                              int grid, int threads, int smem, bool pdl, cudaStream_t stream);
 cudaError_t launch_split_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
-                             int grid, int threads, int smem, cudaStream_t stream);
-cudaError_t launch_merge(int head_dim, const MergeParams& p, int grid_x, int grid_y, bool pdl,
+                             int grid, int threads, int smem, bool pdl, cudaStream_t stream);
+// wide: one 256-thread block per (unit, row), threads across partials (many
+// partials per unit); otherwise one warp per (unit, row), 8 rows per block.
+cudaError_t launch_merge(int head_dim, const MergeParams& p, int units, int rows, bool wide, bool pdl,
                          cudaStream_t stream);
 cudaError_t set_split_smem_limits_bf16(int smem);
 cudaError_t set_split_smem_limits_fp8(int smem);

@@ -16,10 +16,13 @@
 //
 // CTA layout: warp 0 is the producer, warps 1..HC*MT are consumers.
 //   * producer: for every page of its range, reads the block-table entry (32 at
-//     a time, one per lane) and issues TMA tile loads of that page's K and V rows
-//     for the HC heads into a ring of `nstage` shared-memory stages (128- or
-//     64-byte swizzled boxes of 16 rows); at the first page of a unit it also
-//     bulk-copies the unit's query rows into one of two query slots.
+//     a time, one per lane, the next 32 prefetched) and issues TMA tile loads of
+//     that page's K and V rows for the HC heads into a ring of `nstage`
+//     shared-memory stages: one box per tensor and 128-byte column block, box =
+//     (128 or 64 bytes of the row) x 16 slots x HC heads with the matching
+//     swizzle, so a page of all HC heads costs 2-4 TMA instructions; at the
+//     first page of a unit it also bulk-copies the unit's query rows into one of
+//     two query slots.
 //   * consumer (kv head hh of the chunk, 16-row tile w): query rows
 //     rho = 16w .. 16w+15 of that head, where rho = r*G + gg is query token r of
 //     the run and query head gg of the group.  Per page it computes
@@ -78,16 +81,13 @@ struct SeqInfo {
   int qn;   // query tokens (0 if the metadata is invalid)
 };
 
-__device__ __forceinline__ SeqInfo seq_info(const SplitParams& p, int i, bool report) {
+// Sequence metadata from the shared-memory copies made in the prologue.
+__device__ __forceinline__ SeqInfo seq_info(const SplitParams& p, const int32_t* s_len, const int32_t* s_qsl, int i,
+                                            bool report) {
   SeqInfo s;
-  s.L = p.seq_lens[i];
-  if (p.qsl != nullptr) {
-    s.t0 = p.qsl[i];
-    s.qn = p.qsl[i + 1] - s.t0;
-  } else {
-    s.t0 = i;
-    s.qn = 1;
-  }
+  s.L = s_len[i];
+  s.t0 = s_qsl[i];
+  s.qn = s_qsl[i + 1] - s.t0;
   if (s.qn < 1 || s.qn > p.max_qlen || s.t0 < 0 || s.t0 + s.qn > p.num_tokens) {
     if (report) atomicOr(p.err, kErrQueryLen);
     s.qn = 0;
@@ -105,16 +105,17 @@ struct Geo {
   static constexpr int NBOX = ROWB / RB;             // boxes per row
   static constexpr int CPB = RB / 16;                // 16-byte chunks per box row
   static constexpr int BOX_BYTES = 16 * RB;          // one 16-row box
-  static constexpr int HEAD_BYTES = NBOX * BOX_BYTES;
   static constexpr int KS = D / 16;                  // k-steps of Q K^T
   static constexpr int NT = D / 8;                   // n-tiles of P V
 };
 
-// Byte offset, inside one head's tiles, of 16-byte chunk `chunk` of row `row`.
+// Byte offset of 16-byte chunk `chunk` of row `row` of one head's tiles.  A
+// stage holds, per tensor, NBOX column blocks of HC heads x 16 rows; the column
+// blocks are `block_stride` = HC * BOX_BYTES apart, heads BOX_BYTES apart.
 template <int D, bool FP8>
-__device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
+__device__ __forceinline__ uint32_t tile_off(int row, int chunk, uint32_t block_stride) {
   using GG = Geo<D, FP8>;
-  return (chunk / GG::CPB) * GG::BOX_BYTES + swz<GG::RB>(row, chunk % GG::CPB);
+  return (chunk / GG::CPB) * block_stride + swz<GG::RB>(row, chunk % GG::CPB);
 }
 
 // Output feature index of element e (0/1) of accumulator tile J for lane tig.
@@ -140,20 +141,31 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
   int32_t* const s_pre = reinterpret_cast<int32_t*>(gbase + p.off_prefix);
+  int32_t* const s_len = s_pre + (p.num_seqs + 1);
+  int32_t* const s_qsl = s_len + p.num_seqs;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
   const int B = p.num_seqs;
+  if (tid == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  // Inputs may come from the previous kernel in the stream (programmatic
+  // dependent launch): nothing global is read before this point.
+  grid_dependency_wait();
 
-  // ---- prologue: pages per sequence, exclusive prefix in shared memory -----
+  // ---- prologue: metadata to shared memory, pages per sequence, prefix -----
   int carry = 0;
   for (int b0 = 0; b0 < B; b0 += blockDim.x) {
     const int i = b0 + tid;
     int v = 0;
     if (i < B) {
       const int L = p.seq_lens[i];
+      s_len[i] = L;
+      s_qsl[i] = p.qsl != nullptr ? p.qsl[i] : i;
       v = L > 0 ? (L + kPage - 1) / kPage : 0;
       if (v > p.max_blocks) {       // context longer than its block-table row: never read past the row
         atomicOr(p.err, kErrSeqLen);
@@ -184,7 +196,10 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     carry += s_total;
     __syncthreads();
   }
-  if (tid == 0) s_pre[B] = carry;
+  if (tid == 0) {
+    s_pre[B] = carry;
+    s_qsl[B] = p.qsl != nullptr ? p.qsl[B] : B;
+  }
 
   const uint32_t bar0 = base + p.off_bar;
   const int nstage = p.nstage;
@@ -231,14 +246,11 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 
   if (warp == 0) {
     // ============================ producer =================================
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
-    }
     Cursor cu = locate(s_pre, B, NC, start);
     int qseg = 0;
-    int bt_i = -1, bt_j0 = 0, bt_val = 0;
-    const int ntma = 2 * HC * GG::NBOX;
+    int bt_i = -1, bt_j0 = 0, bt_val = 0;   // block-table entries [bt_j0, bt_j0 + 32) of sequence bt_i
+    int nx_i = -1, nx_j0 = 0, nx_val = 0;   // the batch after it, loaded ahead of use
+    const uint32_t block_stride = static_cast<uint32_t>(HC * GG::BOX_BYTES);
     for (int64_t k = 0; k < count; ++k) {
       const int stage = static_cast<int>(k % nstage);
       if (k >= nstage) {
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             break;
           }
         }
-        const SeqInfo si = seq_info(p, cu.i, false);
+        const SeqInfo si = seq_info(p, s_len, s_qsl, cu.i, false);
         if (lane == 0) mbar_arrive_expect_tx(qfull_bar(qs), static_cast<uint32_t>(si.qn) * qrow_bytes);
         __syncwarp();
         const uint32_t qdst = base + p.off_q + static_cast<uint32_t>(qs) * p.q_slot_bytes;
@@ -267,26 +279,45 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         ++qseg;
       }
       if (cu.i != bt_i || cu.j < bt_j0 || cu.j >= bt_j0 + 32) {
+        if (cu.i == nx_i && cu.j == nx_j0) {
+          bt_val = nx_val;
+        } else {
+          const int jj = cu.j + lane;
+          bt_val = (jj < cu.n) ? p.block_tables[static_cast<int64_t>(cu.i) * p.bt_stride + jj] : 0;
+        }
         bt_i = cu.i;
         bt_j0 = cu.j;
-        const int jj = bt_j0 + lane;
-        bt_val = (jj < cu.n) ? p.block_tables[static_cast<int64_t>(cu.i) * p.bt_stride + jj] : 0;
+        // prefetch the batch the traversal reaches next
+        int ni = -1, nj = 0;
+        if (bt_j0 + 32 < cu.n) {
+          ni = cu.i;
+          nj = bt_j0 + 32;
+        } else if (cu.c + 1 < NC) {
+          ni = cu.i;
+        } else {
+          ni = cu.i + 1;
+          while (ni < B && pages_of(s_pre, ni) == 0) ++ni;
+          if (ni >= B) ni = -1;
+        }
+        nx_i = ni;
+        nx_j0 = nj;
+        if (ni >= 0) {
+          const int jj = nj + lane;
+          nx_val = (jj < pages_of(s_pre, ni)) ? p.block_tables[static_cast<int64_t>(ni) * p.bt_stride + jj] : 0;
+        }
       }
       const int phys = __shfl_sync(0xffffffffu, bt_val, cu.j - bt_j0);
       if ((phys < 0 || phys >= p.num_pages) && lane == 0) atomicOr(p.err, kErrPageRange);
       // An out-of-range page id reads as zeros (TMA fills outside the tensor).
       if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
       __syncwarp();
-      if (lane < ntma) {
-        const int tensor = lane / (HC * GG::NBOX);
-        const int rem = lane - tensor * (HC * GG::NBOX);
-        const int hh = rem / GG::NBOX;
-        const int bx = rem - hh * GG::NBOX;
+      if (lane < 2 * GG::NBOX) {
+        const int tensor = lane / GG::NBOX;
+        const int bx = lane - tensor * GG::NBOX;
         const uint32_t dst = base + p.off_stage + static_cast<uint32_t>(stage) * p.stage_bytes +
-                             static_cast<uint32_t>(tensor) * p.kv_bytes +
-                             static_cast<uint32_t>(hh * GG::HEAD_BYTES + bx * GG::BOX_BYTES);
-        tma_load_4d(dst, tensor ? &tmap_v : &tmap_k, bx * (GG::RB / GG::ESZ), cu.c * HC + hh, 0, phys,
-                    full_bar(stage));
+                             static_cast<uint32_t>(tensor) * p.kv_bytes + static_cast<uint32_t>(bx) * block_stride;
+        // box: RB bytes of the row x 16 slots x HC heads, starting at head c*HC of page phys
+        tma_load_4d(dst, tensor ? &tmap_v : &tmap_k, bx * (GG::RB / GG::ESZ), 0, cu.c * HC, phys, full_bar(stage));
       }
       advance(cu, s_pre, B, NC);
     }
@@ -304,6 +335,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   const int rr = lane & 7;          // ldmatrix row
   const int rho0 = 16 * w + gq;
   const int rho1 = rho0 + 8;
+  const uint32_t block_stride = static_cast<uint32_t>(HC * GG::BOX_BYTES);
 
   Cursor cu = locate(s_pre, B, NC, start);
   int qseg = 0;
@@ -328,7 +360,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     }
     if (k == 0 || cu.j == 0) {
       // ---- new segment: query rows into registers, state reset ----
-      si = seq_info(p, cu.i, lane == 0 && hh == 0 && w == 0);
+      si = seq_info(p, s_len, s_qsl, cu.i, lane == 0 && hh == 0 && w == 0);
       seg_k0 = k;
       seg_j0 = cu.j;
       const int qs = qseg & 1;
@@ -381,7 +413,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 
     if (active) {
       const uint32_t kb = base + p.off_stage + static_cast<uint32_t>(stage) * p.stage_bytes +
-                          static_cast<uint32_t>(hh * GG::HEAD_BYTES);
+                          static_cast<uint32_t>(hh * GG::BOX_BYTES);
       const uint32_t vb = kb + p.kv_bytes;
       // ---- S = Q K^T for the 16 tokens of this page ----
       float S[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -389,7 +421,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < GG::KS; ks += 2) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kb + tile_off<D, FP8>(rr + 8 * (mi & 1), ks + (mi >> 1)), r0, r1, r2, r3);
+          ldsm_x4(kb + tile_off<D, FP8>(rr + 8 * (mi & 1), ks + (mi >> 1), block_stride), r0, r1, r2, r3);
           mma_f16(S[0], Qf[ks], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
           mma_f16(S[1], Qf[ks], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
           mma_f16(S[0], Qf[ks + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < GG::KS; ++ks) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kb + tile_off<D, FP8>(rr + 8 * (mi >> 1), 2 * ks + (mi & 1)), r0, r1, r2, r3);
+          ldsm_x4(kb + tile_off<D, FP8>(rr + 8 * (mi >> 1), 2 * ks + (mi & 1), block_stride), r0, r1, r2, r3);
           mma_bf16(S[0], Qf[ks], r0, r1);
           mma_bf16(S[1], Qf[ks], r2, r3);
         }
@@ -478,7 +510,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 16; c += 2) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vb + tile_off<D, FP8>(rr + 8 * (mi & 1), c + (mi >> 1)), r0, r1, r2, r3);
+          ldsm_x4_t(vb + tile_off<D, FP8>(rr + 8 * (mi & 1), c + (mi >> 1), block_stride), r0, r1, r2, r3);
           const uint32_t u0 = prmt(r0, 0u, 0x3120u), u1 = prmt(r1, 0u, 0x3120u);
           const uint32_t u2 = prmt(r2, 0u, 0x3120u), u3 = prmt(r3, 0u, 0x3120u);
           mma_f16(O[2 * c], Pa, e4m3x2_to_f16x2(u0) & mb0, e4m3x2_to_f16x2(u1) & mb1);
@@ -490,7 +522,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 #pragma unroll
         for (int J = 0; J < GG::NT; J += 2) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vb + tile_off<D, FP8>(rr + 8 * (mi & 1), J + (mi >> 1)), r0, r1, r2, r3);
+          ldsm_x4_t(vb + tile_off<D, FP8>(rr + 8 * (mi & 1), J + (mi >> 1), block_stride), r0, r1, r2, r3);
           mma_bf16(O[J], Pa, r0 & mb0, r1 & mb1);
           mma_bf16(O[J + 1], Pa, r2 & mb0, r3 & mb1);
         }

@@ -4,15 +4,20 @@
 namespace pa {
 
 cudaError_t launch_split_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
-                             int grid, int threads, int smem, cudaStream_t stream) {
-  if (head_dim == 128) {
-    pa_split_kernel<128, true><<<grid, threads, smem, stream>>>(tk, tv, p);
-  } else if (head_dim == 64) {
-    pa_split_kernel<64, true><<<grid, threads, smem, stream>>>(tk, tv, p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+                              int grid, int threads, int smem, bool pdl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_kernel<128, true>, tk, tv, p);
+  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_split_kernel<64, true>, tk, tv, p);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t set_split_smem_limits_fp8(int smem) {
