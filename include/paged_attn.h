@@ -143,6 +143,31 @@ int paged_attn_decode_ex(const pa_tensor_t* q, const pa_tensor_t* k_cache, const
                          float k_scale, float v_scale, const pa_tensor_t* out, const pa_tensor_t* lse,
                          const pa_options_t* opts, pa_stream_t stream);
 
+/*
+ * paged_attn_decode_static_scratch - paged_attn_decode for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry point.
+ *
+ * Same operation, arguments, layouts and errors as paged_attn_decode, but the
+ * split scratch comes from a fixed 16 MiB (16777216-byte) array compiled into
+ * the library's device code, so the call never calls cudaMalloc/cudaFree or any
+ * other allocating routine.  It serves callers whose memory is owned by a pool
+ * or allocator they must not bypass, or that run where allocation is not
+ * allowed.  Every GPU on which the library's kernels are loaded holds that
+ * array until the process exits.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - A shape needing more scratch than 16 MiB (see paged_attn_workspace_size)
+ *     is rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *   - All calls share the one array and it keeps the last call's contents (no
+ *     part of it needs to start at zero); calls whose GPU work overlaps, e.g. on
+ *     two streams at once, race on it and must be serialised by the caller.
+ */
+int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_cache,
+                                     const pa_tensor_t* v_cache, const pa_tensor_t* block_tables,
+                                     const pa_tensor_t* seq_lens, const pa_tensor_t* query_start_loc,
+                                     int32_t max_query_len, float scale, float k_scale, float v_scale,
+                                     const pa_tensor_t* out, const pa_tensor_t* lse, pa_stream_t stream);
+
 /* Plan for a shape on the current device (kv_dtype: PA_BF16 or PA_FP8_E4M3).
  * opts may be NULL.  Reads device attributes only; enqueues nothing. */
 int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -55,6 +55,8 @@ _SIGNATURES = {
                                          ctypes.c_float, _P, _P, ctypes.c_void_p]),
     "paged_attn_decode_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                                             ctypes.c_float, _P, _P, ctypes.POINTER(PaOptions), ctypes.c_void_p]),
+    "paged_attn_decode_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float,
+                                                        ctypes.c_float, ctypes.c_float, _P, _P, ctypes.c_void_p]),
     "paged_attn_plan": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(PaOptions), ctypes.POINTER(PaPlan)]),
     "paged_attn_workspace_size": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
     "paged_attn_reserve": (ctypes.c_int, [ctypes.c_int32] * 6),
@@ -167,6 +169,28 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, query_start_l
         st = lib.paged_attn_decode_ex(*refs, int(max_query_len), float(scale), float(k_scale), float(v_scale),
                                       ctypes.byref(o_desc), ctypes.byref(l_desc), ctypes.byref(options),
                                       _stream_handle(stream))
+    _check(lib, st)
+    return out, lse
+
+
+def paged_attn_decode_static_scratch(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc=None,
+                                     max_query_len=1, scale=None, k_scale=1.0, v_scale=1.0, out=None, lse=None,
+                                     stream=None, want_lse=True):
+    """paged_attn_decode without any device allocation inside the library:
+    the split scratch is the library's fixed 16 MiB static device array.
+    Same arguments and results as ``paged_attn_decode``."""
+    lib = load()
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    args = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)]
+    o_desc, l_desc = tensor_desc(out), tensor_desc(lse)
+    st = lib.paged_attn_decode_static_scratch(*[ctypes.byref(a) for a in args], int(max_query_len), float(scale),
+                                              float(k_scale), float(v_scale), ctypes.byref(o_desc),
+                                              ctypes.byref(l_desc), _stream_handle(stream))
     _check(lib, st)
     return out, lse
 

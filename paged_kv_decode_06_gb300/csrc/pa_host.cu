@@ -420,6 +420,12 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
 
 }  // namespace
 
+namespace pa {
+// Lets other translation units of the library report a detailed message
+// through paged_attn_last_error_message().
+void set_last_error_message(const std::string& msg) { t_last_error = msg; }
+}  // namespace pa
+
 extern "C" {
 
 int paged_attn_decode_ex(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa_tensor_t* v_cache,
