@@ -80,7 +80,8 @@ typedef struct pa_options_t {
   int32_t num_ctas;            /* >0: launch this many split CTAs instead of one per SM */
   int32_t min_pages_per_cta;   /* >0: override the minimum pages of work per CTA (default 4) */
   int32_t heads_per_cta;       /* >0: KV heads per CTA (must divide Hkv); 0 = planner's choice */
-  int32_t disable_pdl;         /* !=0: launch the merge kernel without programmatic dependent launch */
+  int32_t disable_pdl;         /* !=0: launch both kernels without programmatic dependent launch */
+  int32_t page_pairing;        /* 0: planner's choice; 1: never; 2: always process two pages at once */
   void* workspace;             /* optional caller-owned device workspace ...                   */
   size_t workspace_bytes;      /* ... of this size (see paged_attn_workspace_size)            */
   void* split_start_event;     /* optional cudaEvent_t recorded just before the split kernel  */
@@ -98,6 +99,7 @@ typedef struct pa_plan_t {
   int32_t smem_bytes;        /* dynamic shared memory per CTA                           */
   int32_t min_pages_per_cta; /* work below which fewer CTAs are used                    */
   int32_t merge_rows;        /* rows per merge unit (heads_per_cta * G * max_query_len) */
+  int32_t page_pairing;      /* 1 if consumer warps take two pages of a sequence at once */
   int64_t workspace_bytes;   /* split workspace the call needs                          */
 } pa_plan_t;
 

@@ -29,6 +29,7 @@ class PaTensor(ctypes.Structure):
 class PaOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("min_pages_per_cta", ctypes.c_int32),
                 ("heads_per_cta", ctypes.c_int32), ("disable_pdl", ctypes.c_int32),
+                ("page_pairing", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p)]
 
@@ -37,6 +38,7 @@ class PaPlan(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("heads_per_cta", ctypes.c_int32), ("row_tiles", ctypes.c_int32),
                 ("num_stages", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("min_pages_per_cta", ctypes.c_int32), ("merge_rows", ctypes.c_int32),
+                ("page_pairing", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -130,12 +132,13 @@ def _stream_handle(stream) -> int:
 
 
 def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=False, workspace=None,
-                 workspace_bytes=0, split_start_event=None, split_stop_event=None) -> PaOptions:
+                 workspace_bytes=0, split_start_event=None, split_stop_event=None, page_pairing=0) -> PaOptions:
     o = PaOptions()
     o.num_ctas = num_ctas
     o.min_pages_per_cta = min_pages_per_cta
     o.heads_per_cta = heads_per_cta
     o.disable_pdl = int(bool(disable_pdl))
+    o.page_pairing = page_pairing
     o.workspace = workspace
     o.workspace_bytes = workspace_bytes
     o.split_start_event = int(split_start_event.cuda_event) if split_start_event is not None else None

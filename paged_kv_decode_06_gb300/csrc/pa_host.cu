@@ -109,7 +109,7 @@ int device_state(DeviceState** out, int* dev_out) {
 // ----------------------------------------------------------------- planning
 struct Plan {
   int B, Hq, Hkv, D, esz, max_qlen;
-  int G, R_max, MT, HC, NC, nstage, threads, grid, min_pages;
+  int G, R_max, MT, HC, NC, nstage, threads, grid, min_pages, pair;
   uint32_t stage_bytes, kv_bytes, q_slot_bytes;
   uint32_t off_stage, off_q, off_bar, off_prefix, smem;
   size_t ws_meta, ws_prefix, ws_ml, ws_o, ws_bytes;
@@ -177,6 +177,10 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
   if (!found) return fail(PA_ERR_UNSUPPORTED, "no launch configuration fits %d bytes of shared memory", smem_optin);
   p.NC = Hkv / p.HC;
   p.threads = 32 * (1 + p.HC * p.MT);
+  // Two pages per consumer step when the ring is deep enough that holding two
+  // stages still leaves most of it in flight.
+  const int pairing = opts ? opts->page_pairing : 0;
+  p.pair = pairing == 2 ? 1 : (pairing == 1 ? 0 : (p.nstage >= 5 ? 1 : 0));
   p.off_stage = 0;
   p.off_q = p.off_stage + p.nstage * p.stage_bytes;
   p.off_bar = p.off_q + 2 * p.q_slot_bytes;
@@ -357,6 +361,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   sp.R_max = pl.R_max;
   sp.nstage = pl.nstage;
   sp.min_pages = pl.min_pages;
+  sp.pair_pages = pl.pair;
   sp.scale_log2 = scale * (esz == 1 ? k_scale : 1.0f) * kLog2e;
   sp.v_scale = esz == 1 ? v_scale : 1.0f;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -467,6 +472,7 @@ int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   plan->smem_bytes = static_cast<int32_t>(pl.smem);
   plan->min_pages_per_cta = pl.min_pages;
   plan->merge_rows = pl.HC * pl.R_max;
+  plan->page_pairing = pl.pair;
   plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
   return PA_OK;
 }

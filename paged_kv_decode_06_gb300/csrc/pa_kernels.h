@@ -33,6 +33,7 @@ struct SplitParams {
   int32_t R_max;            // G * max_qlen rows per head
   int32_t nstage;
   int32_t min_pages;        // minimum pages of work per CTA
+  int32_t pair_pages;       // consumers take two pages of a segment at once
   // math
   float scale_log2;         // scale * k_scale * log2(e)
   float v_scale;            // applied to the output (1 for bf16 caches)

@@ -128,6 +128,246 @@ __device__ __forceinline__ int d_of(int J, int e, int tig) {
   }
 }
 
+// Per-warp online-softmax state for 16 query rows of one KV head.
+template <int D, bool FP8>
+struct ConsumerState {
+  using GG = Geo<D, FP8>;
+  float O[GG::NT][4];       // unnormalised output, mma C fragments
+  uint32_t Qf[GG::KS][4];   // query rows, mma A fragments
+  float m0, m1, l0, l1;     // running max (log2 units) and this lane's share of the sum, rows g and g+8
+
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int J = 0; J < GG::NT; ++J) O[J][0] = O[J][1] = O[J][2] = O[J][3] = 0.f;
+  }
+
+  // Query rows (bf16 in shared memory) into A fragments.  For fp8 caches the
+  // rows become f16 with the feature order of the fp8 K fragments: inside a
+  // k-step, k = 2*tig + {0,1} holds d = 16*ks + 4*tig + {0,1} and
+  // k = 2*tig + 8 + {0,1} holds d + 2.  Returns false if a value overflowed f16.
+  __device__ __forceinline__ bool load_query(const uint8_t* q0p, const uint8_t* q1p, bool ok0, bool ok1, int tig) {
+    bool fine = true;
+#pragma unroll
+    for (int ks = 0; ks < GG::KS; ++ks) {
+      if constexpr (FP8) {
+        const uint2 a = ok0 ? *reinterpret_cast<const uint2*>(q0p + (16 * ks + 4 * tig) * 2) : make_uint2(0u, 0u);
+        const uint2 b = ok1 ? *reinterpret_cast<const uint2*>(q1p + (16 * ks + 4 * tig) * 2) : make_uint2(0u, 0u);
+        Qf[ks][0] = pack_f16(bf16_lo(a.x), bf16_hi(a.x));
+        Qf[ks][1] = pack_f16(bf16_lo(b.x), bf16_hi(b.x));
+        Qf[ks][2] = pack_f16(bf16_lo(a.y), bf16_hi(a.y));
+        Qf[ks][3] = pack_f16(bf16_lo(b.y), bf16_hi(b.y));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t v = Qf[ks][e];
+          fine &= ((v & 0x7C00u) != 0x7C00u) && ((v & 0x7C000000u) != 0x7C000000u);
+        }
+      } else {
+        Qf[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0p + (16 * ks + 2 * tig) * 2) : 0u;
+        Qf[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1p + (16 * ks + 2 * tig) * 2) : 0u;
+        Qf[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0p + (16 * ks + 8 + 2 * tig) * 2) : 0u;
+        Qf[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1p + (16 * ks + 8 + 2 * tig) * 2) : 0u;
+      }
+    }
+    return fine;
+  }
+
+  // Two adjacent output features of row (half ? g+8 : g): values and the first
+  // feature index.  J is even; jj selects which pair.
+  __device__ __forceinline__ void pair_at(int J, int jj, int half, int tig, float& a, float& b, int& d) const {
+    if constexpr (FP8) {
+      // (even tile, odd tile) at element jj are adjacent features
+      a = O[J][2 * half + jj];
+      b = O[J + 1][2 * half + jj];
+      d = d_of<D, FP8>(J, jj, tig);
+    } else {
+      a = O[J + jj][2 * half];
+      b = O[J + jj][2 * half + 1];
+      d = d_of<D, FP8>(J + jj, 0, tig);
+    }
+  }
+};
+
+// P V for NP pages; MASK zeroes value rows at or past the sequence end.
+template <int D, bool FP8, int NP, bool MASK>
+__device__ __forceinline__ void pv_pages(ConsumerState<D, FP8>& cs, const uint32_t (&vb)[NP],
+                                         const uint32_t (&Pa)[NP][4], uint32_t block_stride,
+                                         const uint32_t (&mb0)[NP], const uint32_t (&mb1)[NP], int lane) {
+  const int mi = lane >> 3, rr = lane & 7;
+  if constexpr (FP8) {
+#pragma unroll
+    for (int c = 0; c < D / 16; c += 2) {
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vb[pg] + tile_off<D, FP8>(rr + 8 * (mi & 1), c + (mi >> 1), block_stride), r0, r1, r2, r3);
+        const uint32_t u0 = prmt(r0, 0u, 0x3120u), u1 = prmt(r1, 0u, 0x3120u);
+        const uint32_t u2 = prmt(r2, 0u, 0x3120u), u3 = prmt(r3, 0u, 0x3120u);
+        uint32_t b[8] = {e4m3x2_to_f16x2(u0), e4m3x2_to_f16x2(u1), e4m3x2_to_f16x2(u0 >> 16),
+                         e4m3x2_to_f16x2(u1 >> 16), e4m3x2_to_f16x2(u2), e4m3x2_to_f16x2(u3),
+                         e4m3x2_to_f16x2(u2 >> 16), e4m3x2_to_f16x2(u3 >> 16)};
+        if constexpr (MASK) {
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            b[e] &= mb0[pg];
+            b[e + 1] &= mb1[pg];
+          }
+        }
+        mma_f16(cs.O[2 * c], Pa[pg], b[0], b[1]);
+        mma_f16(cs.O[2 * c + 1], Pa[pg], b[2], b[3]);
+        mma_f16(cs.O[2 * c + 2], Pa[pg], b[4], b[5]);
+        mma_f16(cs.O[2 * c + 3], Pa[pg], b[6], b[7]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int J = 0; J < Geo<D, FP8>::NT; J += 2) {
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vb[pg] + tile_off<D, FP8>(rr + 8 * (mi & 1), J + (mi >> 1), block_stride), r0, r1, r2, r3);
+        if constexpr (MASK) {
+          r0 &= mb0[pg];
+          r1 &= mb1[pg];
+          r2 &= mb0[pg];
+          r3 &= mb1[pg];
+        }
+        mma_bf16(cs.O[J], Pa[pg], r0, r1);
+        mma_bf16(cs.O[J + 1], Pa[pg], r2, r3);
+      }
+    }
+  }
+}
+
+// One block of NP consecutive pages of a segment for one warp: S = Q K^T,
+// causal / tail mask by token index, online softmax (exp2 domain), O += P V.
+// hb[pg] is the shared-memory address of this warp's head in the page's stage;
+// V follows K at +kv_bytes.  tb = first token of the block; min_lim = L - qn.
+template <int D, bool FP8, int NP>
+__device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const uint32_t (&hb)[NP], uint32_t kv_bytes,
+                                              uint32_t block_stride, int tb, int L, int min_lim, int lim0, int lim1,
+                                              float scale_log2, int lane) {
+  using GG = Geo<D, FP8>;
+  const int tig = lane & 3, mi = lane >> 3, rr = lane & 7;
+  float S[2 * NP][4];
+#pragma unroll
+  for (int n = 0; n < 2 * NP; ++n) S[n][0] = S[n][1] = S[n][2] = S[n][3] = 0.f;
+  if constexpr (FP8) {
+#pragma unroll
+    for (int ks = 0; ks < GG::KS; ks += 2) {
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(hb[pg] + tile_off<D, FP8>(rr + 8 * (mi & 1), ks + (mi >> 1), block_stride), r0, r1, r2, r3);
+        mma_f16(S[2 * pg], cs.Qf[ks], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
+        mma_f16(S[2 * pg + 1], cs.Qf[ks], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+        mma_f16(S[2 * pg], cs.Qf[ks + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
+        mma_f16(S[2 * pg + 1], cs.Qf[ks + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < GG::KS; ++ks) {
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(hb[pg] + tile_off<D, FP8>(rr + 8 * (mi >> 1), 2 * ks + (mi & 1), block_stride), r0, r1, r2, r3);
+        mma_bf16(S[2 * pg], cs.Qf[ks], r0, r1);
+        mma_bf16(S[2 * pg + 1], cs.Qf[ks], r2, r3);
+      }
+    }
+  }
+  float x[2 * NP][4];
+#pragma unroll
+  for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[n][e] = S[n][e] * scale_log2;
+  if (tb + kPage * NP - 1 > min_lim) {
+#pragma unroll
+    for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = tb + 8 * n + 2 * tig + e;
+        if (tok > lim0) x[n][e] = -INFINITY;
+        if (tok > lim1) x[n][2 + e] = -INFINITY;
+      }
+  }
+  float mx0 = fmaxf(x[0][0], x[0][1]);
+  float mx1 = fmaxf(x[0][2], x[0][3]);
+#pragma unroll
+  for (int n = 1; n < 2 * NP; ++n) {
+    mx0 = fmaxf(mx0, fmaxf(x[n][0], x[n][1]));
+    mx1 = fmaxf(mx1, fmaxf(x[n][2], x[n][3]));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(cs.m0, mx0);
+  const float mn1 = fmaxf(cs.m1, mx1);
+  const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+  const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+  const float a0 = fast_exp2(cs.m0 - base0);
+  const float a1 = fast_exp2(cs.m1 - base1);
+  cs.m0 = mn0;
+  cs.m1 = mn1;
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int n = 0; n < 2 * NP; ++n) {
+    x[n][0] = fast_exp2(x[n][0] - base0);
+    x[n][1] = fast_exp2(x[n][1] - base0);
+    x[n][2] = fast_exp2(x[n][2] - base1);
+    x[n][3] = fast_exp2(x[n][3] - base1);
+    s0 += x[n][0] + x[n][1];
+    s1 += x[n][2] + x[n][3];
+  }
+  cs.l0 = cs.l0 * a0 + s0;
+  cs.l1 = cs.l1 * a1 + s1;
+  if (__any_sync(0xffffffffu, (a0 != 1.f) || (a1 != 1.f))) {
+#pragma unroll
+    for (int J = 0; J < GG::NT; ++J) {
+      cs.O[J][0] *= a0;
+      cs.O[J][1] *= a0;
+      cs.O[J][2] *= a1;
+      cs.O[J][3] *= a1;
+    }
+  }
+  uint32_t Pa[NP][4];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    if constexpr (FP8) {
+      Pa[pg][0] = pack_f16(x[2 * pg][0], x[2 * pg][1]);
+      Pa[pg][1] = pack_f16(x[2 * pg][2], x[2 * pg][3]);
+      Pa[pg][2] = pack_f16(x[2 * pg + 1][0], x[2 * pg + 1][1]);
+      Pa[pg][3] = pack_f16(x[2 * pg + 1][2], x[2 * pg + 1][3]);
+    } else {
+      Pa[pg][0] = pack_bf16(x[2 * pg][0], x[2 * pg][1]);
+      Pa[pg][1] = pack_bf16(x[2 * pg][2], x[2 * pg][3]);
+      Pa[pg][2] = pack_bf16(x[2 * pg + 1][0], x[2 * pg + 1][1]);
+      Pa[pg][3] = pack_bf16(x[2 * pg + 1][2], x[2 * pg + 1][3]);
+    }
+  }
+  uint32_t vb[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) vb[pg] = hb[pg] + kv_bytes;
+  // Value rows at or past the end of the sequence are zeroed so that stale
+  // (even non-finite) tail slots cannot leak through P == 0.
+  if (L - tb < kPage * NP) {
+    uint32_t mb0[NP], mb1[NP];
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const int vt = L - tb - kPage * pg;
+      mb0[pg] = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
+      mb1[pg] = (2 * tig + 8 < vt ? 0x0000ffffu : 0u) | (2 * tig + 9 < vt ? 0xffff0000u : 0u);
+    }
+    pv_pages<D, FP8, NP, true>(cs, vb, Pa, block_stride, mb0, mb1, lane);
+  } else {
+    const uint32_t none[NP] = {};
+    pv_pages<D, FP8, NP, false>(cs, vb, Pa, block_stride, none, none, lane);
+  }
+}
+
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -251,10 +491,11 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     int bt_i = -1, bt_j0 = 0, bt_val = 0;   // block-table entries [bt_j0, bt_j0 + 32) of sequence bt_i
     int nx_i = -1, nx_j0 = 0, nx_val = 0;   // the batch after it, loaded ahead of use
     const uint32_t block_stride = static_cast<uint32_t>(HC * GG::BOX_BYTES);
+    int stage = 0;
+    uint32_t round = 0;    // k / nstage
     for (int64_t k = 0; k < count; ++k) {
-      const int stage = static_cast<int>(k % nstage);
-      if (k >= nstage) {
-        if (!mbar_wait(empty_bar(stage), static_cast<uint32_t>((k / nstage) - 1) & 1u)) {
+      if (round > 0) {
+        if (!mbar_wait(empty_bar(stage), (round - 1) & 1u)) {
           if (lane == 0) atomicOr(p.err, kErrTimeout);
           break;
         }
@@ -320,6 +561,10 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         tma_load_4d(dst, tensor ? &tmap_v : &tmap_k, bx * (GG::RB / GG::ESZ), 0, cu.c * HC, phys, full_bar(stage));
       }
       advance(cu, s_pre, B, NC);
+      if (++stage == nstage) {
+        stage = 0;
+        ++round;
+      }
     }
     return;
   }
@@ -331,11 +576,10 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   const int w = cw - hh * p.MT;     // 16-row tile
   const int gq = lane >> 2;         // fragment row group
   const int tig = lane & 3;         // thread in group
-  const int mi = lane >> 3;         // ldmatrix matrix index
-  const int rr = lane & 7;          // ldmatrix row
   const int rho0 = 16 * w + gq;
   const int rho1 = rho0 + 8;
   const uint32_t block_stride = static_cast<uint32_t>(HC * GG::BOX_BYTES);
+  const uint32_t head_base = base + p.off_stage + static_cast<uint32_t>(hh * GG::BOX_BYTES);
 
   Cursor cu = locate(s_pre, B, NC, start);
   int qseg = 0;
@@ -344,17 +588,16 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   SeqInfo si = {0, 0, 0};
   bool active = false, ok0 = false, ok1 = false;
   int lim0 = 0, lim1 = 0;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float O[GG::NT][4];
-  uint32_t Qf[GG::KS][4];
+  ConsumerState<D, FP8> cs;
+  cs.reset();
 #pragma unroll
-  for (int J = 0; J < GG::NT; ++J) O[J][0] = O[J][1] = O[J][2] = O[J][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < GG::KS; ++ks) Qf[ks][0] = Qf[ks][1] = Qf[ks][2] = Qf[ks][3] = 0u;
+  for (int ks = 0; ks < GG::KS; ++ks) cs.Qf[ks][0] = cs.Qf[ks][1] = cs.Qf[ks][2] = cs.Qf[ks][3] = 0u;
 
-  for (int64_t k = 0; k < count; ++k) {
-    const int stage = static_cast<int>(k % nstage);
-    if (!mbar_wait(full_bar(stage), static_cast<uint32_t>(k / nstage) & 1u)) {
+  int stage = 0;
+  uint32_t round = 0;              // k / nstage for the page at `stage`
+  int64_t k = 0;
+  while (k < count) {
+    if (!mbar_wait(full_bar(stage), round & 1u)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
@@ -377,167 +620,53 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       const uint8_t* qslot = gbase + p.off_q + qs * p.q_slot_bytes;
       const uint8_t* q0p = qslot + static_cast<size_t>(((rho0 / G) * HC + hh) * G + rho0 % G) * (D * 2);
       const uint8_t* q1p = qslot + static_cast<size_t>(((rho1 / G) * HC + hh) * G + rho1 % G) * (D * 2);
-      bool f16_overflow = false;
-#pragma unroll
-      for (int ks = 0; ks < GG::KS; ++ks) {
-        if constexpr (FP8) {
-          // d-order inside a k-step matches the fp8 K fragments: k = 2*tig + {0,1}
-          // holds d = 16*ks + 4*tig + {0,1}; k = 2*tig + 8 + {0,1} holds d + 2.
-          uint2 a = ok0 ? *reinterpret_cast<const uint2*>(q0p + (16 * ks + 4 * tig) * 2) : make_uint2(0u, 0u);
-          uint2 b = ok1 ? *reinterpret_cast<const uint2*>(q1p + (16 * ks + 4 * tig) * 2) : make_uint2(0u, 0u);
-          Qf[ks][0] = pack_f16(bf16_lo(a.x), bf16_hi(a.x));
-          Qf[ks][1] = pack_f16(bf16_lo(b.x), bf16_hi(b.x));
-          Qf[ks][2] = pack_f16(bf16_lo(a.y), bf16_hi(a.y));
-          Qf[ks][3] = pack_f16(bf16_lo(b.y), bf16_hi(b.y));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t v = Qf[ks][e];
-            f16_overflow |= ((v & 0x7C00u) == 0x7C00u) || ((v & 0x7C000000u) == 0x7C000000u);
-          }
-        } else {
-          Qf[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0p + (16 * ks + 2 * tig) * 2) : 0u;
-          Qf[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1p + (16 * ks + 2 * tig) * 2) : 0u;
-          Qf[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0p + (16 * ks + 8 + 2 * tig) * 2) : 0u;
-          Qf[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1p + (16 * ks + 8 + 2 * tig) * 2) : 0u;
-        }
-      }
-      if (FP8 && f16_overflow) atomicOr(p.err, kErrF16Range);
+      if (!cs.load_query(q0p, q1p, ok0, ok1, tig)) atomicOr(p.err, kErrF16Range);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty_bar(qs));
       ++qseg;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
-#pragma unroll
-      for (int J = 0; J < GG::NT; ++J) O[J][0] = O[J][1] = O[J][2] = O[J][3] = 0.f;
+      cs.reset();
     }
-
+    // Two consecutive pages of the same segment are processed together when
+    // the ring is deep enough (32-token blocks: more independent MMA chains,
+    // one softmax reduction per 32 tokens).
+    int stage2 = stage + 1;
+    uint32_t round2 = round;
+    if (stage2 == nstage) {
+      stage2 = 0;
+      ++round2;
+    }
+    const bool pair = p.pair_pages && (k + 1 < count) && (cu.j + 1 < cu.n);
+    if (pair && !mbar_wait(full_bar(stage2), round2 & 1u)) {
+      if (lane == 0) atomicOr(p.err, kErrTimeout);
+      break;
+    }
+    const int tb = kPage * cu.j;
     if (active) {
-      const uint32_t kb = base + p.off_stage + static_cast<uint32_t>(stage) * p.stage_bytes +
-                          static_cast<uint32_t>(hh * GG::BOX_BYTES);
-      const uint32_t vb = kb + p.kv_bytes;
-      // ---- S = Q K^T for the 16 tokens of this page ----
-      float S[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if constexpr (FP8) {
-#pragma unroll
-        for (int ks = 0; ks < GG::KS; ks += 2) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(kb + tile_off<D, FP8>(rr + 8 * (mi & 1), ks + (mi >> 1), block_stride), r0, r1, r2, r3);
-          mma_f16(S[0], Qf[ks], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
-          mma_f16(S[1], Qf[ks], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
-          mma_f16(S[0], Qf[ks + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
-          mma_f16(S[1], Qf[ks + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
-        }
+      if (pair) {
+        const uint32_t hb[2] = {head_base + static_cast<uint32_t>(stage) * p.stage_bytes,
+                                head_base + static_cast<uint32_t>(stage2) * p.stage_bytes};
+        consume_pages<D, FP8, 2>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1,
+                                 p.scale_log2, lane);
       } else {
-#pragma unroll
-        for (int ks = 0; ks < GG::KS; ++ks) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(kb + tile_off<D, FP8>(rr + 8 * (mi >> 1), 2 * ks + (mi & 1), block_stride), r0, r1, r2, r3);
-          mma_bf16(S[0], Qf[ks], r0, r1);
-          mma_bf16(S[1], Qf[ks], r2, r3);
-        }
-      }
-      // ---- mask, online softmax (exp2 domain) ----
-      const int tb = kPage * cu.j;
-      float x[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[nt][e] = S[nt][e] * p.scale_log2;
-      if (tb + kPage - 1 > si.L - si.qn) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tok = tb + 8 * nt + 2 * tig + e;
-            if (tok > lim0) x[nt][e] = -INFINITY;
-            if (tok > lim1) x[nt][2 + e] = -INFINITY;
-          }
-      }
-      float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0);
-      const float mn1 = fmaxf(m1, mx1);
-      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float a0 = fast_exp2(m0 - base0);
-      const float a1 = fast_exp2(m1 - base1);
-      m0 = mn0;
-      m1 = mn1;
-      float pr[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        pr[nt][0] = fast_exp2(x[nt][0] - base0);
-        pr[nt][1] = fast_exp2(x[nt][1] - base0);
-        pr[nt][2] = fast_exp2(x[nt][2] - base1);
-        pr[nt][3] = fast_exp2(x[nt][3] - base1);
-      }
-      l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-      l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
-      if (__any_sync(0xffffffffu, (a0 != 1.f) || (a1 != 1.f))) {
-#pragma unroll
-        for (int J = 0; J < GG::NT; ++J) {
-          O[J][0] *= a0;
-          O[J][1] *= a0;
-          O[J][2] *= a1;
-          O[J][3] *= a1;
-        }
-      }
-      uint32_t Pa[4];
-      if constexpr (FP8) {
-        Pa[0] = pack_f16(pr[0][0], pr[0][1]);
-        Pa[1] = pack_f16(pr[0][2], pr[0][3]);
-        Pa[2] = pack_f16(pr[1][0], pr[1][1]);
-        Pa[3] = pack_f16(pr[1][2], pr[1][3]);
-      } else {
-        Pa[0] = pack_bf16(pr[0][0], pr[0][1]);
-        Pa[1] = pack_bf16(pr[0][2], pr[0][3]);
-        Pa[2] = pack_bf16(pr[1][0], pr[1][1]);
-        Pa[3] = pack_bf16(pr[1][2], pr[1][3]);
-      }
-      // ---- O += P V; value rows past the sequence end are zeroed so that
-      //      stale (even non-finite) tail slots cannot leak through P == 0 ----
-      const int vt = si.L - tb;
-      uint32_t mb0 = 0xffffffffu, mb1 = 0xffffffffu;
-      if (vt < kPage) {
-        mb0 = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
-        mb1 = (2 * tig + 8 < vt ? 0x0000ffffu : 0u) | (2 * tig + 9 < vt ? 0xffff0000u : 0u);
-      }
-      if constexpr (FP8) {
-#pragma unroll
-        for (int c = 0; c < D / 16; c += 2) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vb + tile_off<D, FP8>(rr + 8 * (mi & 1), c + (mi >> 1), block_stride), r0, r1, r2, r3);
-          const uint32_t u0 = prmt(r0, 0u, 0x3120u), u1 = prmt(r1, 0u, 0x3120u);
-          const uint32_t u2 = prmt(r2, 0u, 0x3120u), u3 = prmt(r3, 0u, 0x3120u);
-          mma_f16(O[2 * c], Pa, e4m3x2_to_f16x2(u0) & mb0, e4m3x2_to_f16x2(u1) & mb1);
-          mma_f16(O[2 * c + 1], Pa, e4m3x2_to_f16x2(u0 >> 16) & mb0, e4m3x2_to_f16x2(u1 >> 16) & mb1);
-          mma_f16(O[2 * c + 2], Pa, e4m3x2_to_f16x2(u2) & mb0, e4m3x2_to_f16x2(u3) & mb1);
-          mma_f16(O[2 * c + 3], Pa, e4m3x2_to_f16x2(u2 >> 16) & mb0, e4m3x2_to_f16x2(u3 >> 16) & mb1);
-        }
-      } else {
-#pragma unroll
-        for (int J = 0; J < GG::NT; J += 2) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vb + tile_off<D, FP8>(rr + 8 * (mi & 1), J + (mi >> 1), block_stride), r0, r1, r2, r3);
-          mma_bf16(O[J], Pa, r0 & mb0, r1 & mb1);
-          mma_bf16(O[J + 1], Pa, r2 & mb0, r3 & mb1);
-        }
+        const uint32_t hb[1] = {head_base + static_cast<uint32_t>(stage) * p.stage_bytes};
+        consume_pages<D, FP8, 1>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1,
+                                 p.scale_log2, lane);
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar(stage));
-
-    const bool seg_last = (k == count - 1) || (cu.j == cu.n - 1);
+    if (lane == 0) {
+      mbar_arrive(empty_bar(stage));
+      if (pair) mbar_arrive(empty_bar(stage2));
+    }
+    const int np = pair ? 2 : 1;
+    const int j_last = cu.j + np - 1;
+    const bool seg_last = (k + np == count) || (j_last == cu.n - 1);
     if (seg_last && active) {
-      float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+      const bool complete = (seg_j0 == 0) && (j_last == cu.n - 1);
+      float lt0 = cs.l0 + __shfl_xor_sync(0xffffffffu, cs.l0, 1);
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
-      float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+      float lt1 = cs.l1 + __shfl_xor_sync(0xffffffffu, cs.l1, 1);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-      const bool complete = (seg_j0 == 0) && (cu.j == cu.n - 1);
       if (complete) {
         const float inv0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
         const float inv1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
@@ -555,23 +684,15 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
           for (int J = 0; J < GG::NT; J += 2) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
-              if constexpr (FP8) {
-                // (even tile, odd tile) at element e are adjacent features
-                const int e = jj;
-                const float va = O[J][2 * half + e] * inv;
-                const float vb2 = O[J + 1][2 * half + e] * inv;
-                *reinterpret_cast<uint32_t*>(orow + d_of<D, FP8>(J, e, tig)) = pack_bf16(va, vb2);
-              } else {
-                const int Jt = J + jj;
-                const float va = O[Jt][2 * half] * inv;
-                const float vb2 = O[Jt][2 * half + 1] * inv;
-                *reinterpret_cast<uint32_t*>(orow + d_of<D, FP8>(Jt, 0, tig)) = pack_bf16(va, vb2);
-              }
+              float va, vb2;
+              int d;
+              cs.pair_at(J, jj, half, tig, va, vb2, d);
+              *reinterpret_cast<uint32_t*>(orow + d) = pack_bf16(va * inv, vb2 * inv);
             }
           }
           if (p.lse != nullptr && tig == 0) {
             const float lt = half ? lt1 : lt0;
-            const float mm = half ? m1 : m0;
+            const float mm = half ? cs.m1 : cs.m0;
             p.lse[static_cast<int64_t>(t) * p.lse_stride_t + static_cast<int64_t>(hq) * p.lse_stride_h] =
                 lt > 0.f ? (mm + fast_log2(lt)) * 0.69314718055994530942f : -INFINITY;
           }
@@ -589,22 +710,24 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
           for (int J = 0; J < GG::NT; J += 2) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
-              if constexpr (FP8) {
-                const int e = jj;
-                *reinterpret_cast<float2*>(orow + d_of<D, FP8>(J, e, tig)) =
-                    make_float2(O[J][2 * half + e], O[J + 1][2 * half + e]);
-              } else {
-                const int Jt = J + jj;
-                *reinterpret_cast<float2*>(orow + d_of<D, FP8>(Jt, 0, tig)) =
-                    make_float2(O[Jt][2 * half], O[Jt][2 * half + 1]);
-              }
+              float va, vb2;
+              int d;
+              cs.pair_at(J, jj, half, tig, va, vb2, d);
+              *reinterpret_cast<float2*>(orow + d) = make_float2(va, vb2);
             }
           }
-          if (tig == 0) p.ws_ml[rowbase + rho] = make_float2(half ? m1 : m0, half ? lt1 : lt0);
+          if (tig == 0) p.ws_ml[rowbase + rho] = make_float2(half ? cs.m1 : cs.m0, half ? lt1 : lt0);
         }
       }
     }
-    advance(cu, s_pre, B, NC);
+    for (int t = 0; t < np; ++t) {
+      advance(cu, s_pre, B, NC);
+      if (++stage == nstage) {
+        stage = 0;
+        ++round;
+      }
+    }
+    k += np;
   }
 }
 
