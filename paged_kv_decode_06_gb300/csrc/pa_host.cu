@@ -27,7 +27,7 @@ constexpr int kPageSize = 16;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSeqs = 8192;
 constexpr int kMaxConsumerWarps = 8;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 32;
 constexpr int kDefaultMinPages = 4;
 
 thread_local std::string t_last_error;
@@ -112,7 +112,7 @@ struct Plan {
   int G, R_max, MT, HC, NC, nstage, threads, grid, min_pages, pair;
   uint32_t stage_bytes, kv_bytes, q_slot_bytes;
   uint32_t off_stage, off_q, off_bar, off_prefix, smem;
-  size_t ws_meta, ws_prefix, ws_ml, ws_o, ws_bytes;
+  size_t ws_unit, ws_ml, ws_o, ws_bytes;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -148,9 +148,17 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
   const int forced_hc = opts ? opts->heads_per_cta : 0;
   if (forced_hc < 0 || (forced_hc > 0 && Hkv % forced_hc != 0))
     return fail(PA_ERR_INVALID_ARG, "heads_per_cta %d must divide num_kv_heads %d", forced_hc, Hkv);
+  // Ring depth wanted, in order of preference.  bf16 pages are light on math,
+  // so a deep ring (>= 5 stages, which lets consumers take page pairs) beats
+  // more heads per CTA; fp8 needs the most consumer warps per CTA (its e4m3
+  // conversions double the math per byte), so it takes the widest CTA with a
+  // 3-stage ring.
+  const int kWantBf16[3] = {5, 3, 2};
+  const int kWantFp8[3] = {3, 2, 2};
+  const int* want = p.esz == 1 ? kWantFp8 : kWantBf16;
   bool found = false;
-  for (int pass = 0; pass < 2 && !found; ++pass) {
-    const int want_stages = pass == 0 ? 3 : 2;
+  for (int pass = 0; pass < 3 && !found; ++pass) {
+    const int want_stages = want[pass];
     for (int hc = (forced_hc > 0 ? forced_hc : std::min(Hkv, kMaxConsumerWarps)); hc >= 1; --hc) {
       if (Hkv % hc != 0 || hc * p.MT > kMaxConsumerWarps) {
         if (forced_hc > 0) break;
@@ -188,9 +196,8 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
   p.smem = 1024 + p.off_prefix + prefix_bytes;
   p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
   const size_t rows = static_cast<size_t>(2) * p.grid * p.HC * p.R_max;
-  p.ws_meta = 0;
-  p.ws_prefix = 256;
-  p.ws_ml = align_up(p.ws_prefix + 4u * (B + 1), 256);
+  p.ws_unit = 0;
+  p.ws_ml = align_up(p.ws_unit + static_cast<size_t>(16) * B * p.NC, 256);
   p.ws_o = align_up(p.ws_ml + rows * 8, 256);
   p.ws_bytes = align_up(p.ws_o + rows * D * 4, 256);
   *pl = p;
@@ -365,8 +372,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   sp.scale_log2 = scale * (esz == 1 ? k_scale : 1.0f) * kLog2e;
   sp.v_scale = esz == 1 ? v_scale : 1.0f;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  sp.ws_meta = reinterpret_cast<int64_t*>(wsb + pl.ws_meta);
-  sp.ws_prefix = reinterpret_cast<int32_t*>(wsb + pl.ws_prefix);
+  sp.ws_unit = reinterpret_cast<int4*>(wsb + pl.ws_unit);
   sp.ws_ml = reinterpret_cast<float2*>(wsb + pl.ws_ml);
   sp.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
   sp.err = ds->status;
@@ -395,8 +401,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   mp.R_max = pl.R_max;
   mp.max_qlen = max_qlen;
   mp.v_scale = sp.v_scale;
-  mp.ws_meta = sp.ws_meta;
-  mp.ws_prefix = sp.ws_prefix;
+  mp.ws_unit = sp.ws_unit;
   mp.ws_ml = sp.ws_ml;
   mp.ws_o = sp.ws_o;
   mp.err = sp.err;
@@ -408,13 +413,16 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   // predecessor in the stream before touching global memory, but its launch
   // overlaps the predecessor's tail.
   const bool pdl = !(opts && opts->disable_pdl);
-  if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
+  // External records also become event nodes when the stream is being captured.
+  if (ev0 && (e = cudaEventRecordWithFlags(ev0, stream, cudaEventRecordExternal)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(start)");
   e = (esz == 1) ? pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
                                         pdl && !ev0, stream)
                  : pa::launch_split_bf16(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads,
                                          static_cast<int>(pl.smem), pdl && !ev0, stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
-  if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stop)");
+  if (ev1 && (e = cudaEventRecordWithFlags(ev1, stream, cudaEventRecordExternal)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(stop)");
   // Many pieces per unit on average (few long contexts over many CTAs): the
   // wide merge reads a row's partials with a whole block.
   const bool wide = pl.grid >= 4 * static_cast<int>(B) * pl.NC;

@@ -38,8 +38,7 @@ struct SplitParams {
   float scale_log2;         // scale * k_scale * log2(e)
   float v_scale;            // applied to the output (1 for bf16 caches)
   // workspace
-  int64_t* ws_meta;         // [0] = total pages X, [1] = CTAs used
-  int32_t* ws_prefix;       // [B+1] page prefix over sequences
+  int4* ws_unit;            // [B * NC] per unit: {first CTA, pieces | first-is-tail << 30, t0, qn}
   float2* ws_ml;            // [2 * grid][HC][R_max] (running max in log2 units, sum)
   float* ws_o;              // [2 * grid][HC][R_max][D] unnormalised partial outputs
   uint32_t* err;            // device status word
@@ -63,8 +62,7 @@ struct MergeParams {
   int32_t num_seqs, num_tokens;
   int32_t G, HC, NC, R_max, max_qlen;
   float v_scale;
-  const int64_t* ws_meta;
-  const int32_t* ws_prefix;
+  const int4* ws_unit;
   const float2* ws_ml;
   const float* ws_o;
   uint32_t* err;

@@ -2,20 +2,22 @@
 // Decode: Split Memory Work to Fill the Device": per-split log-sum-exp values
 // kept in fp32, merged afterwards).
 //
-// One warp per (unit, query row).  A unit (sequence i, head chunk c) whose page
-// range [a, b) lies inside one split CTA was finished by that CTA and is
-// skipped.  Otherwise the CTAs g_first..g_last that cut it each left, in slot
-// 2g (the CTA's first unit) or 2g+1 (its last unit), the unnormalised output
-// O_s, the running max m_s (log2 units) and the sum l_s.  With M = max_s m_s:
+// A unit (sequence i, head chunk c) whose page range lies inside one split CTA
+// was finished by that CTA and is skipped.  Otherwise the CTAs g_first..g_last
+// that cut it each left, in slot 2g (the CTA's first unit) or 2g+1 (its last
+// unit), the unnormalised output O_s, the running max m_s (log2 units) and the
+// sum l_s; the CTA holding the unit's first page also wrote the unit's
+// descriptor (g_first, piece count, query tokens).  With M = max_s m_s:
 //   out = v_scale * sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
 //   lse = ln 2 * (M + log2 sum_s 2^(m_s - M) l_s)
+// accumulated online (running max), so each partial is loaded once.
 #include "pa_device.cuh"
 #include "pa_kernels.h"
 
 namespace pa {
 
 constexpr int kMergeWarps = 8;
-constexpr int kWideThreads = 256;
+constexpr int kWideThreads = 1024;
 
 struct MergeRow {
   bool work;        // row exists and its unit was cut into >= 2 pieces
@@ -26,56 +28,50 @@ struct MergeRow {
   bool first_is_tail;
 };
 
-// Locates (unit u, row) and the CTAs whose ranges cut the unit.  Rows whose unit
-// was finished inside one CTA, or that do not exist for this sequence, report
-// work = false.  An empty context writes out = 0, lse = -inf here.
+// (unit u, row) -> output row and the pieces to merge, from the descriptor the
+// split kernel wrote for the unit (one metadata load).  Rows of a unit that was
+// finished inside one CTA, or that do not exist for the sequence, report
+// work = false.  An empty context (no page ever touched) writes out = 0 and
+// lse = -inf here.
 template <int D>
 __device__ __forceinline__ MergeRow merge_row(const MergeParams& p, int u, int row, int lane) {
   MergeRow m;
   m.work = false;
+  if (row >= p.HC * p.R_max) return m;
   const int i = u / p.NC;
   const int c = u - i * p.NC;
-  if (row >= p.HC * p.R_max) return m;
   m.hh = row / p.R_max;
   m.rho = row - m.hh * p.R_max;
-  int t0, qn;
-  if (p.qsl != nullptr) {
-    t0 = p.qsl[i];
-    qn = p.qsl[i + 1] - t0;
-  } else {
-    t0 = i;
-    qn = 1;
+  const int4 d = p.ws_unit[u];
+  const int L = p.seq_lens[i];
+  if (L <= 0) {
+    int t0 = i, qn = 1;
+    if (p.qsl != nullptr) {
+      t0 = p.qsl[i];
+      qn = p.qsl[i + 1] - t0;
+    }
+    if (qn < 1 || qn > p.max_qlen || t0 < 0 || t0 + qn > p.num_tokens || m.rho >= p.G * qn || lane < 0) return m;
+    uint16_t* orow = p.out + static_cast<int64_t>(t0 + m.rho / p.G) * p.out_stride_t +
+                     static_cast<int64_t>((c * p.HC + m.hh) * p.G + m.rho % p.G) * p.out_stride_h;
+    for (int dd = 2 * lane; dd < D; dd += 64) *reinterpret_cast<uint32_t*>(orow + dd) = 0u;
+    if (lane == 0) {
+      if (p.lse)
+        p.lse[static_cast<int64_t>(t0 + m.rho / p.G) * p.lse_stride_t +
+              static_cast<int64_t>((c * p.HC + m.hh) * p.G + m.rho % p.G) * p.lse_stride_h] = -INFINITY;
+      atomicOr(p.err, kErrSeqLen);
+    }
+    return m;
   }
-  if (qn < 1 || qn > p.max_qlen || t0 < 0 || t0 + qn > p.num_tokens) return m;   // reported by the split kernel
-  if (m.rho >= p.G * qn) return m;
+  m.gf = d.x;
+  m.nparts = d.y & 0x3fffffff;
+  m.first_is_tail = (d.y >> 30) & 1;
+  const int t0 = d.z, qn = d.w;
+  if (m.nparts <= 1 || m.rho >= p.G * qn) return m;
   const int t = t0 + m.rho / p.G;
   const int hq = (c * p.HC + m.hh) * p.G + m.rho % p.G;
   m.orow = p.out + static_cast<int64_t>(t) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h;
   m.lse_ptr = p.lse ? p.lse + static_cast<int64_t>(t) * p.lse_stride_t + static_cast<int64_t>(hq) * p.lse_stride_h
                     : nullptr;
-  const int pre_i = p.ws_prefix[i];
-  const int n = p.ws_prefix[i + 1] - pre_i;
-  if (n == 0) {
-    // empty context (invalid input): no split CTA touched this unit
-    if (lane >= 0) {
-      for (int d = 2 * lane; d < D; d += 64) *reinterpret_cast<uint32_t*>(m.orow + d) = 0u;
-      if (lane == 0) {
-        if (m.lse_ptr) *m.lse_ptr = -INFINITY;
-        atomicOr(p.err, kErrSeqLen);
-      }
-    }
-    return m;
-  }
-  const int64_t X = p.ws_meta[0];
-  const int64_t NG = p.ws_meta[1];
-  const int64_t a = static_cast<int64_t>(p.NC) * pre_i + static_cast<int64_t>(c) * n;
-  const int64_t b = a + n;
-  // largest g with floor(g*X/NG) <= x
-  m.gf = static_cast<int>(((a + 1) * NG - 1) / X);
-  const int gl = static_cast<int>((b * NG - 1) / X);
-  if (m.gf == gl) return m;
-  m.first_is_tail = (static_cast<int64_t>(m.gf) * X / NG) < a;   // the unit is CTA gf's last unit
-  m.nparts = gl - m.gf + 1;
   m.work = true;
   return m;
 }
@@ -85,17 +81,57 @@ __device__ __forceinline__ int64_t slot_row(const MergeParams& p, const MergeRow
   return (static_cast<int64_t>(2 * (m.gf + s) + which) * p.HC + m.hh) * p.R_max + m.rho;
 }
 
-__device__ __forceinline__ void write_merged(const MergeParams& p, const MergeRow& m, int dq, float4 acc, float lsum,
-                                             float M, bool write_lse) {
-  const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+// Online log-sum-exp accumulation of one partial (running max mx in log2 units).
+__device__ __forceinline__ void lse_acc(float& mx, float& l, float4& acc, float m_s, float l_s, const float4& o) {
+  if (m_s == -INFINITY) return;
+  const float nm = fmaxf(mx, m_s);
+  const float a = fast_exp2(mx - nm);     // 0 when mx = -inf
+  const float b = fast_exp2(m_s - nm);
+  acc.x = acc.x * a + o.x * b;
+  acc.y = acc.y * a + o.y * b;
+  acc.z = acc.z * a + o.z * b;
+  acc.w = acc.w * a + o.w * b;
+  l = l * a + l_s * b;
+  mx = nm;
+}
+
+// Partials s = first, first + stride, ... of row m: loads of four partials are
+// issued before any of them is combined.
+template <int D>
+__device__ __forceinline__ void gather_partials(const MergeParams& p, const MergeRow& m, int first, int stride, int dq,
+                                                float& mx, float& l, float4& acc) {
+  int s = first;
+  for (; s + 3 * stride < m.nparts; s += 4 * stride) {
+    float2 ml[4];
+    float4 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t sl = slot_row(p, m, s + u * stride);
+      ml[u] = p.ws_ml[sl];
+      o[u] = *reinterpret_cast<const float4*>(p.ws_o + sl * D + 4 * dq);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) lse_acc(mx, l, acc, ml[u].x, ml[u].y, o[u]);
+  }
+  for (; s < m.nparts; s += stride) {
+    const int64_t sl = slot_row(p, m, s);
+    const float2 ml = p.ws_ml[sl];
+    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + sl * D + 4 * dq);
+    lse_acc(mx, l, acc, ml.x, ml.y, o);
+  }
+}
+
+__device__ __forceinline__ void write_merged(const MergeParams& p, const MergeRow& m, int dq, float4 acc, float l,
+                                             float mx, bool write_lse) {
+  const float inv = l > 0.f ? p.v_scale / l : 0.f;
   uint2 pk;
   pk.x = pack_bf16(acc.x * inv, acc.y * inv);
   pk.y = pack_bf16(acc.z * inv, acc.w * inv);
   *reinterpret_cast<uint2*>(m.orow + 4 * dq) = pk;
-  if (write_lse && m.lse_ptr) *m.lse_ptr = lsum > 0.f ? (M + fast_log2(lsum)) * 0.69314718055994530942f : -INFINITY;
+  if (write_lse && m.lse_ptr) *m.lse_ptr = l > 0.f ? (mx + fast_log2(l)) * 0.69314718055994530942f : -INFINITY;
 }
 
-// One warp per (unit, row).
+// One warp per (unit, row): units cut into a few pieces.
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_kernel(const MergeParams p) {
   grid_dependency_wait();   // results of the split kernel (programmatic dependent launch)
@@ -104,102 +140,61 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_kernel(const MergeP
   const int lane = threadIdx.x & 31;
   const MergeRow m = merge_row<D>(p, blockIdx.x, blockIdx.y * kMergeWarps + warp, lane);
   if (!m.work) return;
-
-  float M = -INFINITY;
-  for (int s = lane; s < m.nparts; s += 32) M = fmaxf(M, p.ws_ml[slot_row(p, m, s)].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float Mb = (M == -INFINITY) ? 0.f : M;
-
   constexpr int LPD = D / 4;          // lanes per partial row (float4 each)
-  constexpr int PL = 32 / LPD;        // partials processed side by side
+  constexpr int PL = 32 / LPD;        // partials side by side
   const int dq = lane % LPD;
   const int pl = lane / LPD;
+  float mx = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-#pragma unroll 4
-  for (int s = pl; s < m.nparts; s += PL) {
-    const int64_t sl = slot_row(p, m, s);
-    const float2 ml = p.ws_ml[sl];
-    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + sl * D + 4 * dq);
-    const float wgt = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - Mb);
-    acc.x += wgt * o.x;
-    acc.y += wgt * o.y;
-    acc.z += wgt * o.z;
-    acc.w += wgt * o.w;
-    lsum += wgt * ml.y;
-  }
+  gather_partials<D>(p, m, pl, PL, dq, mx, l, acc);
 #pragma unroll
   for (int o = LPD; o < 32; o <<= 1) {
-    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
-    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
-    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
-    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float mo = __shfl_xor_sync(0xffffffffu, mx, o);
+    const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+    float4 ao;
+    ao.x = __shfl_xor_sync(0xffffffffu, acc.x, o);
+    ao.y = __shfl_xor_sync(0xffffffffu, acc.y, o);
+    ao.z = __shfl_xor_sync(0xffffffffu, acc.z, o);
+    ao.w = __shfl_xor_sync(0xffffffffu, acc.w, o);
+    lse_acc(mx, l, acc, mo, lo, ao);
   }
-  if (pl == 0) write_merged(p, m, dq, acc, lsum, M, lane == 0);
+  if (pl == 0) write_merged(p, m, dq, acc, l, mx, lane == 0);
 }
 
-// One 256-thread block per (unit, row): the partials of a unit cut into many
-// pieces (a long context spread over every SM) are read by all threads at once.
+// One 1024-thread block per (unit, row): units cut into many pieces (a long
+// context spread over every SM); each thread gathers a few partials in one
+// round of loads, then a tree in shared memory combines the groups.
 template <int D>
 __global__ void __launch_bounds__(kWideThreads) pa_merge_wide_kernel(const MergeParams p) {
   grid_dependency_wait();
   grid_launch_dependents();
   constexpr int LPD = D / 4;
   constexpr int PG = kWideThreads / LPD;
-  __shared__ float s_max[kWideThreads / 32];
   __shared__ float4 s_acc[PG][LPD];
-  __shared__ float s_l[PG];
+  __shared__ float2 s_ml[PG][LPD];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const MergeRow m = merge_row<D>(p, blockIdx.x, blockIdx.y, tid < 32 ? lane : -1);
   if (!m.work) return;
-
-  float M = -INFINITY;
-  for (int s = tid; s < m.nparts; s += kWideThreads) M = fmaxf(M, p.ws_ml[slot_row(p, m, s)].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_max[tid >> 5] = M;
-  __syncthreads();
-  M = s_max[0];
-#pragma unroll
-  for (int w = 1; w < kWideThreads / 32; ++w) M = fmaxf(M, s_max[w]);
-  const float Mb = (M == -INFINITY) ? 0.f : M;
-
   const int dq = tid % LPD;
   const int pg = tid / LPD;
+  float mx = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-#pragma unroll 4
-  for (int s = pg; s < m.nparts; s += PG) {
-    const int64_t sl = slot_row(p, m, s);
-    const float2 ml = p.ws_ml[sl];
-    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + sl * D + 4 * dq);
-    const float wgt = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - Mb);
-    acc.x += wgt * o.x;
-    acc.y += wgt * o.y;
-    acc.z += wgt * o.z;
-    acc.w += wgt * o.w;
-    lsum += wgt * ml.y;
-  }
+  gather_partials<D>(p, m, pg, PG, dq, mx, l, acc);
   s_acc[pg][dq] = acc;
-  if (dq == 0) s_l[pg] = lsum;
+  s_ml[pg][dq] = make_float2(mx, l);
   __syncthreads();
-  if (pg == 0) {
-    float4 t = s_acc[0][dq];
-    float l = s_l[0];
 #pragma unroll
-    for (int g = 1; g < PG; ++g) {
-      const float4 o = s_acc[g][dq];
-      t.x += o.x;
-      t.y += o.y;
-      t.z += o.z;
-      t.w += o.w;
-      l += s_l[g];
+  for (int half = PG / 2; half >= 1; half >>= 1) {
+    if (pg < half) {
+      const float2 ml = s_ml[pg + half][dq];
+      lse_acc(mx, l, acc, ml.x, ml.y, s_acc[pg + half][dq]);
+      s_acc[pg][dq] = acc;
+      s_ml[pg][dq] = make_float2(mx, l);
     }
-    write_merged(p, m, dq, t, l, M, dq == 0);
+    __syncthreads();
   }
+  if (pg == 0) write_merged(p, m, dq, acc, l, mx, dq == 0);
 }
 
 cudaError_t launch_merge(int head_dim, const MergeParams& p, int units, int rows, bool wide, bool pdl,

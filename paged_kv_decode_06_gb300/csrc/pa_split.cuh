@@ -465,13 +465,6 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   int64_t ng64 = (X + p.min_pages - 1) / p.min_pages;
   if (ng64 < 1) ng64 = 1;
   const int NG = static_cast<int>(ng64 < gridDim.x ? ng64 : gridDim.x);
-  if (blockIdx.x == 0) {
-    if (tid == 0) {
-      p.ws_meta[0] = X;
-      p.ws_meta[1] = NG;
-    }
-    for (int i = tid; i <= B; i += blockDim.x) p.ws_prefix[i] = s_pre[i];
-  }
   grid_launch_dependents();
 
   const int g = blockIdx.x;
@@ -610,6 +603,14 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg >> 1) & 1u)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
+      }
+      if (seg_j0 == 0 && cw == 0 && lane == 0) {
+        // This CTA holds the unit's first page: describe the unit for the merge.
+        const int64_t a = static_cast<int64_t>(NC) * s_pre[cu.i] + static_cast<int64_t>(cu.c) * cu.n;
+        const int last_cta = static_cast<int>(((a + cu.n) * NG - 1) / X);
+        const int pieces = last_cta - g + 1;
+        p.ws_unit[static_cast<int64_t>(cu.i) * NC + cu.c] =
+            make_int4(g, pieces | (k != 0 ? (1 << 30) : 0), si.t0, si.qn);
       }
       const int R = G * si.qn;
       active = 16 * w < R;
