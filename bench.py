@@ -37,6 +37,23 @@ def _dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's step time).  The
+    replicas exchange nothing else: the path itself has no collective."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(step_bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job KV throughput: every rank's step bytes over the slowest rank's step time."""
+    return step_bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -280,10 +297,7 @@ def run_ours(args, world, rank, local):
     d1.record(stream)
     torch.cuda.synchronize()
     direct_ms = d0.elapsed_time(d1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, device=dev)
 
     # end-to-end through the public API: pinned host inputs in, results out, every step
     h_q = [w.q.cpu().pin_memory() for w in works]
@@ -331,7 +345,7 @@ def run_ours(args, world, rank, local):
     plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                                    binding.kv_dtype_code(spec.kv_dtype), mq)
     traffic = _traffic_from_profiles(spec.name)
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    value = job_throughput_gbs(step_bytes, world, ms)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
