@@ -170,6 +170,32 @@ int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_
                                      int32_t max_query_len, float scale, float k_scale, float v_scale,
                                      const pa_tensor_t* out, const pa_tensor_t* lse, pa_stream_t stream);
 
+/*
+ * paged_attn_cache_write - write new tokens' K and V rows into the paged caches
+ * (ATOM model-operations guide, "KV cache operations": standard (bf16) and FP8
+ * KV cache write; token_layout/slots.py: slot_mapping, "which KV slot a token is
+ * written to").
+ *
+ *   key, value      bf16 [T, Hkv, D]; stride[2] == 1, other strides multiples of 8
+ *                   elements, data 16-byte aligned.
+ *   slot_mapping    int32 [T] contiguous.  Token t goes to page slot_mapping[t] / 16,
+ *                   slot slot_mapping[t] % 16; a negative entry (padding) writes
+ *                   nothing; an entry >= 16 * NB writes nothing and sets bit 0 of the
+ *                   device status word.  Two tokens with the same slot: which one
+ *                   lands is unspecified.
+ *   k_cache, v_cache bf16 or fp8e4m3 [NB, 16, Hkv, D], same rules as for
+ *                   paged_attn_decode.
+ *   k_scale, v_scale fp8 caches only: the stored code is e4m3fn(x / scale), IEEE fp32
+ *                   division, round to nearest even, finite magnitudes above 448 and
+ *                   infinities saturate to +-448.  bf16 caches store x unchanged.
+ *   stream          stream the work is enqueued on.
+ *
+ * Errors as for paged_attn_decode.  Asynchronous; allocates nothing.
+ */
+int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, const pa_tensor_t* slot_mapping,
+                           const pa_tensor_t* k_cache, const pa_tensor_t* v_cache, float k_scale, float v_scale,
+                           pa_stream_t stream);
+
 /* Plan for a shape on the current device (kv_dtype: PA_BF16 or PA_FP8_E4M3).
  * opts may be NULL.  Reads device attributes only; enqueues nothing. */
 int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -8,5 +8,7 @@ from .paged_attention import (PAGE_SIZE, attend, bf16_bits_to_float64, dequantiz
                               e4m3fn_to_float64, gather_sequence, paged_decode_attention,
                               run_workload)
 
-__all__ = ["PAGE_SIZE", "attend", "bf16_bits_to_float64", "dequantize", "e4m3fn_to_float64",
+from .cache_write import cache_write, e4m3fn_encode, quantize_rows
+
+__all__ = ["cache_write", "e4m3fn_encode", "quantize_rows", "PAGE_SIZE", "attend", "bf16_bits_to_float64", "dequantize", "e4m3fn_to_float64",
            "gather_sequence", "paged_decode_attention", "run_workload"]

@@ -59,6 +59,7 @@ _SIGNATURES = {
                                             ctypes.c_float, _P, _P, ctypes.POINTER(PaOptions), ctypes.c_void_p]),
     "paged_attn_decode_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float,
                                                         ctypes.c_float, ctypes.c_float, _P, _P, ctypes.c_void_p]),
+    "paged_attn_cache_write": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
     "paged_attn_plan": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(PaOptions), ctypes.POINTER(PaPlan)]),
     "paged_attn_workspace_size": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
     "paged_attn_reserve": (ctypes.c_int, [ctypes.c_int32] * 6),
@@ -196,6 +197,16 @@ def paged_attn_decode_static_scratch(q, k_cache, v_cache, block_tables, seq_lens
                                               ctypes.byref(l_desc), _stream_handle(stream))
     _check(lib, st)
     return out, lse
+
+
+def paged_attn_cache_write(key, value, slot_mapping, k_cache, v_cache, k_scale=1.0, v_scale=1.0, stream=None):
+    """Write new tokens' K/V rows into their page slots (see include/paged_attn.h).
+    key/value bf16 [T, Hkv, D]; slot_mapping int32 [T]; caches bf16 or uint8
+    (e4m3fn codes) [NB, 16, Hkv, D], updated in place."""
+    lib = load()
+    d = [tensor_desc(t) for t in (key, value, slot_mapping, k_cache, v_cache)]
+    _check(lib, lib.paged_attn_cache_write(*[ctypes.byref(x) for x in d], float(k_scale), float(v_scale),
+                                           _stream_handle(stream)))
 
 
 def paged_attn_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=PA_BF16, max_query_len=1,

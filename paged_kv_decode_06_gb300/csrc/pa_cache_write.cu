@@ -1,0 +1,80 @@
+// KV-cache write (ATOM model-operations guide, "KV cache operations": standard
+// and FP8 KV cache writes; token_layout/slots.py: slot_mapping): every new token
+// with slot s >= 0 stores its key and value rows of all KV heads at page s / 16,
+// slot s % 16 of the paged caches.  bf16 caches take the rows as they are; fp8
+// caches take e4m3fn codes of x / scale (IEEE fp32 division, round to nearest
+// even, saturating to +-448).
+//
+// One thread moves 8 consecutive features (16 bytes of bf16 input) of one
+// (token, head) row; the grid strides over all tokens x heads x 8-feature
+// chunks.  A token's rows of all heads are one contiguous run in the cache, so
+// the stores of a warp are contiguous.
+#include "pa_device.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWriteParams p) {
+  const int chunks_per_head = p.head_dim / 8;
+  const int64_t chunks_per_token = static_cast<int64_t>(p.num_kv_heads) * chunks_per_head;
+  const int64_t total = static_cast<int64_t>(p.num_tokens) * chunks_per_token;
+  const int64_t num_slots = static_cast<int64_t>(p.num_pages) * kPage;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = idx / chunks_per_token;
+    const int64_t rem = idx - t * chunks_per_token;
+    const int h = static_cast<int>(rem / chunks_per_head);
+    const int d0 = static_cast<int>(rem - static_cast<int64_t>(h) * chunks_per_head) * 8;
+    const int64_t slot = p.slot_mapping[t];
+    if (slot < 0) continue;                       // padding token
+    if (slot >= num_slots) {
+      if (d0 == 0 && h == 0) atomicOr(p.err, kErrPageRange);
+      continue;
+    }
+    const int64_t page = slot / kPage;
+    const int64_t off = slot - page * kPage;
+#pragma unroll
+    for (int tensor = 0; tensor < 2; ++tensor) {
+      const uint16_t* src = (tensor ? p.value : p.key) + t * (tensor ? p.v_stride_t : p.k_stride_t) +
+                            static_cast<int64_t>(h) * (tensor ? p.v_stride_h : p.k_stride_h) + d0;
+      const int64_t dst_elem = page * (tensor ? p.vc_stride_page : p.kc_stride_page) +
+                               off * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
+                               static_cast<int64_t>(h) * (tensor ? p.vc_stride_head : p.kc_stride_head) + d0;
+      const uint4 x = *reinterpret_cast<const uint4*>(src);
+      if constexpr (FP8) {
+        const float s = tensor ? p.v_scale : p.k_scale;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          q[e] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[e]), s), __fdiv_rn(bf16_hi(w[e]), s));
+        uint2 out;
+        out.x = q[0] | (q[1] << 16);
+        out.y = q[2] | (q[3] << 16);
+        uint8_t* dst = (tensor ? p.v_cache : p.k_cache) + dst_elem;
+        *reinterpret_cast<uint2*>(dst) = out;
+      } else {
+        uint8_t* dst = (tensor ? p.v_cache : p.k_cache) + dst_elem * 2;
+        *reinterpret_cast<uint4*>(dst) = x;
+      }
+    }
+  }
+}
+
+cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int grid, cudaStream_t stream) {
+  if (fp8) {
+    pa_cache_write_kernel<true><<<grid, 256, 0, stream>>>(p);
+  } else {
+    pa_cache_write_kernel<false><<<grid, 256, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

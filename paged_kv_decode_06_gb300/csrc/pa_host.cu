@@ -459,6 +459,81 @@ int paged_attn_decode(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa
                               k_scale, v_scale, out, lse, nullptr, stream);
 }
 
+int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, const pa_tensor_t* slot_mapping,
+                           const pa_tensor_t* k_cache, const pa_tensor_t* v_cache, float k_scale, float v_scale,
+                           pa_stream_t stream) {
+  t_last_error.clear();
+  int st;
+  if ((st = check_tensor(key, "key", 3, false)) || (st = check_tensor(value, "value", 3, false)) ||
+      (st = check_tensor(slot_mapping, "slot_mapping", 1, false)) || (st = check_tensor(k_cache, "k_cache", 4, false)) ||
+      (st = check_tensor(v_cache, "v_cache", 4, false)))
+    return st;
+  if (key->dtype != PA_BF16 || value->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "key and value must be bf16");
+  if (slot_mapping->dtype != PA_I32) return fail(PA_ERR_INVALID_ARG, "slot_mapping must be int32");
+  if (k_cache->dtype != PA_BF16 && k_cache->dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "k_cache must be bf16 or fp8 e4m3");
+  if (v_cache->dtype != k_cache->dtype) return fail(PA_ERR_INVALID_ARG, "v_cache dtype differs from k_cache");
+  const int64_t T = key->shape[0], Hkv = key->shape[1], D = key->shape[2];
+  for (int d = 0; d < 3; ++d)
+    if (value->shape[d] != key->shape[d]) return fail(PA_ERR_INVALID_ARG, "value shape differs from key");
+  if (slot_mapping->shape[0] != T) return fail(PA_ERR_INVALID_ARG, "slot_mapping needs one entry per token");
+  if (slot_mapping->stride[0] != 1) return fail(PA_ERR_INVALID_ARG, "slot_mapping must be contiguous");
+  if (k_cache->shape[1] != kPageSize) return fail(PA_ERR_UNSUPPORTED, "page size must be 16");
+  if (k_cache->shape[2] != Hkv || k_cache->shape[3] != D)
+    return fail(PA_ERR_INVALID_ARG, "cache [NB, 16, Hkv, D] does not match key [T, Hkv, D]");
+  for (int d = 0; d < 4; ++d)
+    if (v_cache->shape[d] != k_cache->shape[d]) return fail(PA_ERR_INVALID_ARG, "v_cache shape differs from k_cache");
+  if (D % 8 != 0 || D > 512) return fail(PA_ERR_UNSUPPORTED, "head_dim must be a multiple of 8 up to 512");
+  if (T > (int64_t(1) << 30) || Hkv > 4096 || k_cache->shape[0] > (int64_t(1) << 31) - 1)
+    return fail(PA_ERR_UNSUPPORTED, "tensor extents too large");
+  for (const pa_tensor_t* t : {key, value}) {
+    if (t->stride[2] != 1 || t->stride[1] % 8 != 0 || t->stride[0] % 8 != 0 || !aligned(t->data, 16))
+      return fail(PA_ERR_INVALID_ARG, "key/value rows must be contiguous and 16-byte aligned (strides multiple of 8)");
+  }
+  const int esz = k_cache->dtype == PA_FP8_E4M3 ? 1 : 2;
+  for (const pa_tensor_t* c : {k_cache, v_cache}) {
+    if (c->stride[3] != 1) return fail(PA_ERR_INVALID_ARG, "KV cache last dim must be contiguous");
+    for (int d = 0; d < 3; ++d)
+      if ((c->stride[d] * esz) % 16 != 0) return fail(PA_ERR_INVALID_ARG, "KV cache strides must be multiples of 16 bytes");
+    if (!aligned(c->data, 16)) return fail(PA_ERR_INVALID_ARG, "KV cache data must be 16-byte aligned");
+  }
+  if (esz == 1 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f))
+    return fail(PA_ERR_INVALID_ARG, "fp8 caches need finite, non-zero k_scale and v_scale");
+  if (T == 0) return PA_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  pa::CacheWriteParams p = {};
+  p.key = static_cast<const uint16_t*>(key->data);
+  p.value = static_cast<const uint16_t*>(value->data);
+  p.k_stride_t = key->stride[0];
+  p.k_stride_h = key->stride[1];
+  p.v_stride_t = value->stride[0];
+  p.v_stride_h = value->stride[1];
+  p.slot_mapping = static_cast<const int32_t*>(slot_mapping->data);
+  p.k_cache = static_cast<uint8_t*>(k_cache->data);
+  p.v_cache = static_cast<uint8_t*>(v_cache->data);
+  p.kc_stride_page = k_cache->stride[0];
+  p.kc_stride_slot = k_cache->stride[1];
+  p.kc_stride_head = k_cache->stride[2];
+  p.vc_stride_page = v_cache->stride[0];
+  p.vc_stride_slot = v_cache->stride[1];
+  p.vc_stride_head = v_cache->stride[2];
+  p.num_tokens = static_cast<int32_t>(T);
+  p.num_kv_heads = static_cast<int32_t>(Hkv);
+  p.head_dim = static_cast<int32_t>(D);
+  p.num_pages = static_cast<int32_t>(k_cache->shape[0]);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = ds->status;
+  const int64_t work = T * Hkv * (D / 8);
+  const int64_t blocks = (work + 255) / 256;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(blocks, int64_t(ds->num_sms) * 8)));
+  cudaError_t e = pa::launch_cache_write(esz == 1, p, grid, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cache write kernel launch");
+  return PA_OK;
+}
+
 int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype,
                     int32_t max_query_len, const pa_options_t* opts, pa_plan_t* plan) {
   t_last_error.clear();

@@ -68,6 +68,22 @@ struct MergeParams {
   uint32_t* err;
 };
 
+struct CacheWriteParams {
+  const uint16_t* key;      // bf16 [T, Hkv, D]
+  const uint16_t* value;
+  int64_t k_stride_t, k_stride_h, v_stride_t, v_stride_h;   // elements
+  const int32_t* slot_mapping;   // [T]
+  uint8_t* k_cache;         // [NB, 16, Hkv, D] bf16 or e4m3 bytes
+  uint8_t* v_cache;
+  int64_t kc_stride_page, kc_stride_slot, kc_stride_head;   // elements of the cache dtype
+  int64_t vc_stride_page, vc_stride_slot, vc_stride_head;
+  int32_t num_tokens, num_kv_heads, head_dim, num_pages;
+  float k_scale, v_scale;   // fp8 only: code = e4m3(x / scale)
+  uint32_t* err;
+};
+
+cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int grid, cudaStream_t stream);
+
 // Launchers (one translation unit per cache dtype).  `pdl` requests
 // programmatic dependent launch for the merge kernel.
 cudaError_t launch_split_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,

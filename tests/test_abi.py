@@ -127,3 +127,36 @@ def test_plan_rejects_bad_shapes_without_device(lib):
     with pytest.raises(binding.PagedAttnError) as e:
         binding.paged_attn_plan(4, 8, 2, 80)
     assert e.value.status == binding.PA_ERR_UNSUPPORTED
+
+
+def _cw_args(T=4, Hkv=2, D=64, NB=3, kv=torch.bfloat16):
+    return dict(key=torch.zeros(T, Hkv, D, dtype=torch.bfloat16), value=torch.zeros(T, Hkv, D, dtype=torch.bfloat16),
+                slots=torch.zeros(T, dtype=torch.int32), kc=torch.zeros(NB, 16, Hkv, D, dtype=kv),
+                vc=torch.zeros(NB, 16, Hkv, D, dtype=kv))
+
+
+def _cw_call(lib, a, ks=1.0, vs=1.0):
+    d = [binding.tensor_desc(a[n]) for n in ("key", "value", "slots", "kc", "vc")]
+    return lib.paged_attn_cache_write(*[ctypes.byref(x) for x in d], ks, vs, None)
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: a.update(key=a["key"].float()), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(slots=a["slots"].long()), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(slots=torch.zeros(3, dtype=torch.int32)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(kc=torch.zeros(3, 8, 2, 64, dtype=torch.bfloat16)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(kc=torch.zeros(3, 16, 4, 64, dtype=torch.bfloat16)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(vc=torch.zeros(3, 16, 2, 64, dtype=torch.uint8)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(key=torch.zeros(4, 2, 60, dtype=torch.bfloat16), value=torch.zeros(4, 2, 60, dtype=torch.bfloat16),
+                        kc=torch.zeros(3, 16, 2, 60, dtype=torch.bfloat16), vc=torch.zeros(3, 16, 2, 60, dtype=torch.bfloat16)),
+     binding.PA_ERR_UNSUPPORTED),
+])
+def test_cache_write_invalid_arguments(lib, mutate, expect):
+    a = _cw_args()
+    mutate(a)
+    assert _cw_call(lib, a) == expect, binding.paged_attn_last_error_message()
+
+
+def test_cache_write_fp8_needs_nonzero_scales(lib):
+    a = _cw_args(kv=torch.uint8)
+    assert _cw_call(lib, a, 0.0, 1.0) == binding.PA_ERR_INVALID_ARG
