@@ -378,6 +378,107 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def run_cache_write(args, world, rank, local):
+    """Throughput of paged_attn_cache_write: one step writes the K and V rows of
+    T new tokens (a prefill chunk of max_num_batched_tokens = 16384 tokens by
+    default) into randomly permuted page slots.  Bytes = rows read (bf16) +
+    rows written (cache dtype)."""
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_06_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    T, Hkv, D = args.tokens, 8, 128
+    fp8 = args.kv_dtype == "fp8"
+    esz = 1 if fp8 else 2
+    NB = (T + 15) // 16 + 64
+    g = torch.Generator(device=dev).manual_seed(77)
+    key = torch.randn(T, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+    val = torch.randn(T, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+    cdt = torch.uint8 if fp8 else torch.bfloat16
+    kc = torch.zeros(NB, 16, Hkv, D, dtype=cdt, device=dev)
+    vc = torch.zeros(NB, 16, Hkv, D, dtype=cdt, device=dev)
+    slots = torch.from_numpy(np.random.default_rng(5).permutation(NB * 16)[:T].astype(np.int32)).to(dev)
+    ks = vs = 0.05 if fp8 else 1.0
+    step_bytes = T * Hkv * D * 2 * (2 + esz)
+    # pools rotated so a step's bytes exceed 2x L2
+    pools = max(1, math.ceil(2 * L2_BYTES / step_bytes))
+    keys = [key] + [torch.randn_like(key, dtype=torch.float32).to(torch.bfloat16) for _ in range(pools - 1)]
+    vals = [val] + [torch.randn_like(val, dtype=torch.float32).to(torch.bfloat16) for _ in range(pools - 1)]
+    caches = [(kc, vc)] + [(torch.zeros_like(kc), torch.zeros_like(vc)) for _ in range(pools - 1)]
+    stream = torch.cuda.current_stream()
+
+    def step(k, stream_=None):
+        c = caches[k % pools]
+        binding.paged_attn_cache_write(keys[k % pools], vals[k % pools], slots, c[0], c[1], ks, vs, stream=stream_)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    gsteps = pools * max(1, 8 // pools)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for j in range(gsteps):
+            step(j, stream_=cap)
+    singles = []
+    for pidx in range(pools):
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gg, stream=cap):
+            step(pidx, stream_=cap)
+        singles.append(gg)
+    graph.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t0.record(stream)
+        k = 0
+        while k + gsteps <= args.steps:
+            graph.replay()
+            k += gsteps
+        while k < args.steps:
+            singles[k % pools].replay()
+            k += 1
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    # e2e: new rows copied in from pinned host memory each step
+    hk = key.cpu().pin_memory()
+    hv = val.cpu().pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(max(1, args.steps // 10)):
+        key.copy_(hk, non_blocking=True)
+        val.copy_(hv, non_blocking=True)
+        binding.paged_attn_cache_write(key, val, slots, kc, vc, ks, vs)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / max(1, args.steps // 10)
+    peak, peak_kind = _peaks()
+    value = step_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "paged KV cache write GB/s (rows read + written), 1 GPU", "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f8e4m3" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": f"cache_write_T{T}_{args.kv_dtype}", "tokens": T, "kv_heads": Hkv, "head_dim": D,
+                   "bytes_per_step": step_bytes, "pools_rotated": pools,
+                   "step_mode": "CUDA graph replay of paged_attn_cache_write"},
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": None, "kernel": "pa_cache_write_kernel", "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * key.numel() * 2, "d2h_bytes_per_step": 0},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def _spec_for(args):
     import dataclasses
 
@@ -416,12 +517,17 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode", choices=["decode", "cache_write"])
+    ap.add_argument("--tokens", type=int, default=16384, help="cache_write: tokens written per step")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     args = ap.parse_args()
     world, rank, local = _dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.op == "cache_write":
+        run_cache_write(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -185,9 +185,10 @@ int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_
  *                   lands is unspecified.
  *   k_cache, v_cache bf16 or fp8e4m3 [NB, 16, Hkv, D], same rules as for
  *                   paged_attn_decode.
- *   k_scale, v_scale fp8 caches only: the stored code is e4m3fn(x / scale), IEEE fp32
- *                   division, round to nearest even, finite magnitudes above 448 and
- *                   infinities saturate to +-448.  bf16 caches store x unchanged.
+ *   k_scale, v_scale fp8 caches only: the stored code is e4m3fn(x * r) with
+ *                   r = 1.0f / scale rounded once to fp32; round to nearest even,
+ *                   finite magnitudes above 448 and infinities saturate to +-448.
+ *                   bf16 caches store x unchanged.
  *   stream          stream the work is enqueued on.
  *
  * Errors as for paged_attn_decode.  Asynchronous; allocates nothing.

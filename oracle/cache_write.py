@@ -6,11 +6,14 @@ and FP8 KV cache write; model-operations guide, token_layout/slots.py:
 with slot s = slot_mapping[t] >= 0 stores its key and value rows of every KV
 head at physical page s // 16, slot s % 16 of the caches; tokens with a
 negative slot (padding) write nothing.  bf16 caches take the bf16 rows
-unchanged; fp8 caches take e4m3fn codes of ``float32(x) / float32(scale)``
-with one fp32 scale per tensor.
+unchanged; fp8 caches take e4m3fn codes of ``float32(x) * r`` with
+``r = float32(1) / float32(scale)`` (one fp32 scale per tensor, its reciprocal
+rounded once to fp32).
 
-Readings adopted where the pages are silent: the division is the IEEE float32
-one; the e4m3fn encoding rounds to nearest, ties to even, and saturates finite
+Readings adopted where the pages are silent: the scale is applied as one fp32
+multiplication by its fp32 reciprocal (it differs from an IEEE division only
+when x / scale falls within one fp32 ulp of an e4m3 rounding boundary); the
+e4m3fn encoding rounds to nearest, ties to even, and saturates finite
 magnitudes above 448 (and infinities) to +-448 (the "satfinite" convention);
 a slot at or past the end of the pool is an error and writes nothing.
 """
@@ -46,9 +49,10 @@ def e4m3fn_encode(x: np.ndarray) -> np.ndarray:
 
 
 def quantize_rows(bits: np.ndarray, scale: float) -> np.ndarray:
-    """bf16 rows -> e4m3fn codes of float32(x) / float32(scale)."""
+    """bf16 rows -> e4m3fn codes of float32(x) * (float32(1) / float32(scale))."""
     x32 = bf16_bits_to_float64(bits).astype(np.float32)
-    y32 = x32 / np.float32(scale)
+    r32 = np.float32(1.0) / np.float32(scale)
+    y32 = x32 * r32
     return e4m3fn_encode(y32.astype(np.float64))
 
 

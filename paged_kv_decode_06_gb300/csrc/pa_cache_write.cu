@@ -2,8 +2,8 @@
 // and FP8 KV cache writes; token_layout/slots.py: slot_mapping): every new token
 // with slot s >= 0 stores its key and value rows of all KV heads at page s / 16,
 // slot s % 16 of the paged caches.  bf16 caches take the rows as they are; fp8
-// caches take e4m3fn codes of x / scale (IEEE fp32 division, round to nearest
-// even, saturating to +-448).
+// caches take e4m3fn codes of x * (1 / scale) (the reciprocal rounded once to
+// fp32 on the host; round to nearest even, saturating to +-448).
 //
 // One thread moves 8 consecutive features (16 bytes of bf16 input) of one
 // (token, head) row; the grid strides over all tokens x heads x 8-feature
@@ -49,12 +49,12 @@ __global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWritePar
                                static_cast<int64_t>(h) * (tensor ? p.vc_stride_head : p.kc_stride_head) + d0;
       const uint4 x = *reinterpret_cast<const uint4*>(src);
       if constexpr (FP8) {
-        const float s = tensor ? p.v_scale : p.k_scale;
+        const float r = tensor ? p.v_rscale : p.k_rscale;
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t q[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          q[e] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[e]), s), __fdiv_rn(bf16_hi(w[e]), s));
+          q[e] = e4m3x2_from_f32(bf16_lo(w[e]) * r, bf16_hi(w[e]) * r);
         uint2 out;
         out.x = q[0] | (q[1] << 16);
         out.y = q[2] | (q[3] << 16);

@@ -523,8 +523,8 @@ int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, con
   p.num_kv_heads = static_cast<int32_t>(Hkv);
   p.head_dim = static_cast<int32_t>(D);
   p.num_pages = static_cast<int32_t>(k_cache->shape[0]);
-  p.k_scale = k_scale;
-  p.v_scale = v_scale;
+  p.k_rscale = 1.0f / k_scale;   // fp32 reciprocal, rounded once
+  p.v_rscale = 1.0f / v_scale;
   p.err = ds->status;
   const int64_t work = T * Hkv * (D / 8);
   const int64_t blocks = (work + 255) / 256;

@@ -78,7 +78,7 @@ struct CacheWriteParams {
   int64_t kc_stride_page, kc_stride_slot, kc_stride_head;   // elements of the cache dtype
   int64_t vc_stride_page, vc_stride_slot, vc_stride_head;
   int32_t num_tokens, num_kv_heads, head_dim, num_pages;
-  float k_scale, v_scale;   // fp8 only: code = e4m3(x / scale)
+  float k_rscale, v_rscale; // fp8 only: code = e4m3(x * rscale), rscale = fp32(1 / scale)
   uint32_t* err;
 };
 

@@ -40,10 +40,11 @@ def test_saturation_and_special_points(x, code):
     assert oracle.e4m3fn_encode(np.array([x]))[0] == code
 
 
-def test_quantize_divides_in_float32():
+def test_quantize_multiplies_by_the_fp32_reciprocal():
     bits = torch.tensor([0.3, -7.5, 15.0, 0.0123]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle.quantize_rows(bits, 0.05)
-    y = (torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float() / torch.tensor(0.05, dtype=torch.float32))
+    r = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(0.05, dtype=torch.float32)
+    y = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float() * r
     assert np.array_equal(got, y.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
     # 100 / 0.05 = 2000 is beyond the e4m3fn range: saturates (torch's cast would give NaN)
     big = torch.tensor([100.0, -100.0]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
@@ -71,8 +72,10 @@ def test_scatter_against_page_offset_arithmetic(kv_dtype):
         if kv_dtype == "bf16":
             flat_k[slots[t]], flat_v[slots[t]] = kb[t], vb[t]
         else:
-            kq = (torch.from_numpy(kb[t].view(np.int16)).view(torch.bfloat16).float() / torch.tensor(0.05)).to(torch.float8_e4m3fn)
-            vq = (torch.from_numpy(vb[t].view(np.int16)).view(torch.bfloat16).float() / torch.tensor(0.07)).to(torch.float8_e4m3fn)
+            rk = torch.tensor(1.0) / torch.tensor(0.05)
+            rv = torch.tensor(1.0) / torch.tensor(0.07)
+            kq = (torch.from_numpy(kb[t].view(np.int16)).view(torch.bfloat16).float() * rk).to(torch.float8_e4m3fn)
+            vq = (torch.from_numpy(vb[t].view(np.int16)).view(torch.bfloat16).float() * rv).to(torch.float8_e4m3fn)
             flat_k[slots[t]], flat_v[slots[t]] = kq.view(torch.uint8).numpy(), vq.view(torch.uint8).numpy()
     assert np.array_equal(k2, flat_k.reshape(kc.shape)) and np.array_equal(v2, flat_v.reshape(vc.shape))
 
@@ -97,7 +100,7 @@ _real_cw = _il.import_module("oracle.cache_write")   # the module (the package r
 _CW_MUTANTS = {
     "ties_away_from_zero": ("(d_lo == d_hi) & (lo % 2 == 0)", "(d_lo == d_hi) & False"),
     "no_saturation": ("np.minimum(a, _VALUES[-1])", "np.minimum(a, _VALUES[-2])"),
-    "multiply_by_scale": ("y32 = x32 / np.float32(scale)", "y32 = x32 * np.float32(scale)"),
+    "multiply_by_scale": ("y32 = x32 * r32", "y32 = x32 * np.float32(scale)"),
     "slot_offset_swapped": ("page, off = int(s) // PAGE_SIZE, int(s) % PAGE_SIZE",
                             "off, page = int(s) // PAGE_SIZE, int(s) % PAGE_SIZE"),
     "sign_dropped": ("code = np.where(np.signbit(x), code | 0x80, code)", "code = np.where(np.signbit(x), code, code)"),
@@ -119,7 +122,7 @@ def test_cache_write_pins_catch_mutant(name):
     pins.oracle = _types.SimpleNamespace(e4m3fn_encode=mod.e4m3fn_encode, quantize_rows=mod.quantize_rows,
                                          cache_write=mod.cache_write)
     calls = [(pins.test_encoder_matches_torch_inside_the_finite_range, ()), (pins.test_every_grid_value_and_midpoint, ()),
-             (pins.test_quantize_divides_in_float32, ()), (pins.test_out_of_range_slots_write_nothing, ())]
+             (pins.test_quantize_multiplies_by_the_fp32_reciprocal, ()), (pins.test_out_of_range_slots_write_nothing, ())]
     calls += [(pins.test_saturation_and_special_points, args) for args in
               [(448.0, 0x7E), (1e30, 0x7E), (-500.0, 0xFE), (-0.0, 0x80)]]
     calls += [(pins.test_scatter_against_page_offset_arithmetic, (k,)) for k in ("bf16", "fp8")]
