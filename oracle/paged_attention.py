@@ -24,7 +24,11 @@ notes):
 * fp8 is OCP e4m3fn; a cached value is ``code * k_scale`` (K) or
   ``code * v_scale`` (V) with one fp32 scale per tensor; bf16 caches carry no
   scale;
-* ``lse`` is the natural-log log-sum-exp of the scaled logits.
+* ``lse`` is the natural-log log-sum-exp of the scaled logits;
+* sliding window W (``sliding_window`` > 0; the pages' models with
+  ``sliding_window != -1``): query row r sees keys ``p_r - W < j <= p_r``;
+* attention sinks (per query head logit ``sink[hq]``, as in GPT-OSS): the sink
+  joins the softmax normaliser with a zero value row, and ``lse`` includes it.
 
 Every function works in float64 on values decoded bit-exactly from the bf16
 and e4m3 encodings.
@@ -89,18 +93,27 @@ def gather_sequence(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int
 
 
 def attend(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float,
-           key_limits: np.ndarray):
-    """Softmax attention of each query row over keys ``0 .. key_limits[r]``.
+           key_limits: np.ndarray, window: int = 0, sinks=None):
+    """Softmax attention of each query row over keys ``0 .. key_limits[r]``
+    (and, with window W > 0, only keys ``> key_limits[r] - W``).
 
-    q_rows [R, D], keys/values [L, D] float64.  Returns (out [R, D], lse [R]):
-    lse = m + ln sum_j exp(s_j - m) with m = max_j s_j, and
-    out = sum_j exp(s_j - lse) V_j, where s_j = scale * <q, k_j>.
+    q_rows [R, D], keys/values [L, D] float64; sinks: optional per-row logit
+    (float64 [R]) with a zero value row.  Returns (out [R, D], lse [R]):
+    lse = m + ln sum_j exp(s_j - m) with m = max_j s_j over the allowed keys and
+    the sink, and out = sum_j exp(s_j - lse) V_j, where s_j = scale * <q, k_j>.
     """
     R = q_rows.shape[0]
     L = keys.shape[0]
     s = scale * (q_rows @ keys.T)                       # [R, L]
-    allowed = np.arange(L)[None, :] <= np.asarray(key_limits)[:, None]
+    j = np.arange(L)[None, :]
+    lim = np.asarray(key_limits)[:, None]
+    allowed = j <= lim
+    if window > 0:
+        allowed &= j > lim - window
     s = np.where(allowed, s, -np.inf)
+    if sinks is not None:
+        s = np.concatenate([s, np.asarray(sinks, dtype=np.float64)[:, None]], axis=1)
+        values = np.concatenate([values, np.zeros((1, values.shape[1]))], axis=0)
     m = s.max(axis=1, keepdims=True)
     lse = m[:, 0] + np.log(np.exp(s - m).sum(axis=1))
     w = np.exp(s - lse[:, None])                        # 0 where not allowed
@@ -113,7 +126,7 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
                            block_tables: np.ndarray, seq_lens: np.ndarray,
                            query_start_loc, scale: float, k_scale: float = 1.0,
                            v_scale: float = 1.0, kv_dtype: str = "bf16",
-                           seqs=None):
+                           seqs=None, sliding_window: int = 0, sinks=None):
     """Decode attention for a batch.
 
     q_bits      uint16 bf16 patterns [T, Hq, D]
@@ -122,6 +135,8 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
     query_start_loc int [B+1] or None (one query token per sequence)
     seqs        optional iterable of sequence indices to evaluate (others are
                 left as NaN), for sampled checks of large batches.
+    sliding_window  W > 0: each query sees only its last W positions (0 = off)
+    sinks       optional float [Hq] per-query-head sink logits (taken as fp32)
 
     Returns (out float64 [T, Hq, D], lse float64 [T, Hq]).
     """
@@ -149,17 +164,20 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
             V = dequantize(gather_sequence(v_cache, block_tables[i], L, hk), kv_dtype, v_scale)
             heads = np.arange(hk * G, (hk + 1) * G)
             qr = bf16_bits_to_float64(q_bits[t0:t1][:, heads, :])      # [qn, G, D]
-            o, l = attend(qr.reshape(qn * G, D), K, V, sc, np.repeat(limits, G))
+            sk = None
+            if sinks is not None:
+                sk = np.tile(np.asarray(sinks, dtype=np.float32).astype(np.float64)[heads], qn)
+            o, l = attend(qr.reshape(qn * G, D), K, V, sc, np.repeat(limits, G), sliding_window, sk)
             out[t0:t1, hk * G:(hk + 1) * G, :] = o.reshape(qn, G, D)
             lse[t0:t1, hk * G:(hk + 1) * G] = l.reshape(qn, G)
     return out, lse
 
 
-def run_workload(w, seqs=None):
+def run_workload(w, seqs=None, sliding_window=0, sinks=None):
     """Oracle outputs for a ``paged_kv_decode_06_gb300.workloads.Workload``."""
     from paged_kv_decode_06_gb300.workloads import host_arrays
     q_bits, k, v = host_arrays(w)
     s = w.spec
     return paged_decode_attention(q_bits, k, v, w.block_tables, w.seq_lens,
                                   w.query_start_loc, s.scale, s.k_scale, s.v_scale,
-                                  s.kv_dtype, seqs=seqs)
+                                  s.kv_dtype, seqs=seqs, sliding_window=sliding_window, sinks=sinks)

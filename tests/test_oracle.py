@@ -70,7 +70,7 @@ def test_fp8_scale_is_fp32_rounded():
 
 # ---------------------------------------------------------- brute force
 
-def _torch_reference(w):
+def _torch_reference(w, window=0):
     """Attention recomputed from scratch with torch: pages reshaped into a
     contiguous cache (a different indexing route from the oracle's per-token
     gather), K/V heads repeated per group, and the library's float64
@@ -99,7 +99,10 @@ def _torch_reference(w):
         t0, t1 = int(qsl[i]), int(qsl[i + 1])
         Q = q[t0:t1].permute(1, 0, 2)                              # [Hq, qn, D]
         qn = t1 - t0
-        mask = torch.arange(L)[None, :] <= (L - qn + torch.arange(qn))[:, None]
+        lim = (L - qn + torch.arange(qn))[:, None]
+        mask = torch.arange(L)[None, :] <= lim
+        if window > 0:
+            mask &= torch.arange(L)[None, :] > lim - window
         o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale)
         out[t0:t1] = o.permute(1, 0, 2)
         logits = scale * (Q @ K.transpose(1, 2))
@@ -344,3 +347,50 @@ def test_entries_past_the_last_page_and_tail_slots_are_never_read():
     bt2[bt2 < 0] = 10 ** 6           # out of range: would fail if read
     out2, lse2 = _call(w, k=k2, v=v2, bt=bt2)
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+# ---------------------------------------------- sliding window and attention sinks
+
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 40])
+@pytest.mark.parametrize("qlens", [(1,), (2, 3, 4)])
+def test_sliding_window_matches_sdpa_with_window_mask(window, qlens):
+    spec = wl.custom_spec(num_q_heads=8, num_kv_heads=2, head_dim=64, seq_lens=(4, 16, 17, 50, 97),
+                          query_len_choices=qlens, seed=31)
+    w = wl.make_workload(spec)
+    out, lse = oracle.run_workload(w, sliding_window=window)
+    ref_out, ref_lse = _torch_reference(w, window=window)
+    assert np.abs(out - ref_out).max() < 1e-12
+    assert np.abs(lse - ref_lse).max() < 1e-12
+
+
+def test_window_of_one_returns_own_value_and_wide_window_changes_nothing():
+    w = _small(seq_lens=(3, 18, 40), G=2, Hkv=2, D=32)
+    q, k, v = wl.host_arrays(w)
+    s = w.spec
+    o1, l1 = oracle.paged_decode_attention(q, k, v, w.block_tables, w.seq_lens, None, s.scale, sliding_window=1)
+    G = s.group_size
+    for i, L in enumerate(w.seq_lens):
+        page, slot = w.block_tables[i, (L - 1) // 16], (L - 1) % 16
+        for hq in range(s.num_q_heads):
+            vrow = oracle.bf16_bits_to_float64(v[page, slot, hq // G])
+            krow = oracle.bf16_bits_to_float64(k[page, slot, hq // G])
+            assert np.array_equal(o1[i, hq], vrow)
+            assert abs(l1[i, hq] - float(np.float32(s.scale)) * float(oracle.bf16_bits_to_float64(q[i, hq]) @ krow)) < 1e-12
+    o_full, l_full = _call(w)
+    o_w, l_w = oracle.paged_decode_attention(q, k, v, w.block_tables, w.seq_lens, None, s.scale, sliding_window=40)
+    assert np.array_equal(o_full, o_w) and np.array_equal(l_full, l_w)
+
+
+def test_sink_closed_form_against_the_sinkless_result():
+    """A sink logit s with a zero value row: out_s = out * Z / (Z + e^s) and
+    lse_s = ln(Z + e^s), with Z = e^lse of the sinkless attention."""
+    w = _small(qlens=(1, 2), seq_lens=(5, 30, 47), G=4, Hkv=2, D=32, seed=8)
+    q, k, v = wl.host_arrays(w)
+    s = w.spec
+    sinks = np.array([-3.0, 0.0, 0.5, 2.0, 7.25, -1.5, 0.1, 3.0], dtype=np.float32)
+    o, l = _call(w)
+    os_, ls_ = oracle.paged_decode_attention(q, k, v, w.block_tables, w.seq_lens, w.query_start_loc, s.scale,
+                                             sinks=sinks)
+    sk = sinks.astype(np.float64)[None, :]
+    assert np.abs(ls_ - np.logaddexp(l, sk)).max() < 1e-12
+    assert np.abs(os_ - o / (1.0 + np.exp(sk - l))[:, :, None]).max() < 1e-12

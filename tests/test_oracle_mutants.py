@@ -30,6 +30,10 @@ MUTANTS = {
     "weights_unnormalised": ("w = np.exp(s - lse[:, None])", "w = np.exp(s - m)"),
     "values_are_keys": ("out = w @ values", "out = w @ keys"),
     "bf16_shift": ("<< np.uint32(16)", "<< np.uint32(15)"),
+    "window_off_by_one": ("allowed &= j > lim - window", "allowed &= j >= lim - window"),
+    "window_from_sequence_start": ("allowed &= j > lim - window", "allowed &= j < window"),
+    "sink_value_row_nonzero": ("np.zeros((1, values.shape[1]))", "np.ones((1, values.shape[1]))"),
+    "sink_scaled": ("np.asarray(sinks, dtype=np.float64)[:, None]", "scale * np.asarray(sinks, dtype=np.float64)[:, None]"),
 }
 
 
@@ -62,6 +66,10 @@ def _pin_calls(pins):
     yield pins.test_gqa_mapping_consecutive_heads_share_kv_head, ()
     yield pins.test_mtp_row_equals_prefix_attention, ()
     yield pins.test_fp8_scale_folding_and_linearity, ()
+    for win in (1, 5, 17):
+        yield pins.test_sliding_window_matches_sdpa_with_window_mask, (win, (2, 3, 4))
+    yield pins.test_window_of_one_returns_own_value_and_wide_window_changes_nothing, ()
+    yield pins.test_sink_closed_form_against_the_sinkless_result, ()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
