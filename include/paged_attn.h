@@ -82,6 +82,12 @@ typedef struct pa_options_t {
   int32_t heads_per_cta;       /* >0: KV heads per CTA (must divide Hkv); 0 = planner's choice */
   int32_t disable_pdl;         /* !=0: launch both kernels without programmatic dependent launch */
   int32_t page_pairing;        /* 0: planner's choice; 1: never; 2: always process two pages at once */
+  int32_t sliding_window;      /* W > 0: query at position p sees only keys p-W < j <= p (the pages'
+                                  sliding_window; <= 0 = off); pages wholly before the window are
+                                  never read */
+  const void* sinks;           /* optional device pointer to float[Hq]: per-query-head attention sink
+                                  logits (GPT-OSS style): each joins its row's softmax normaliser with
+                                  a zero value row and is included in lse; NULL = none */
   void* workspace;             /* optional caller-owned device workspace ...                   */
   size_t workspace_bytes;      /* ... of this size (see paged_attn_workspace_size)            */
   void* split_start_event;     /* optional cudaEvent_t recorded just before the split kernel  */

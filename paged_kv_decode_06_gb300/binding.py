@@ -29,7 +29,8 @@ class PaTensor(ctypes.Structure):
 class PaOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("min_pages_per_cta", ctypes.c_int32),
                 ("heads_per_cta", ctypes.c_int32), ("disable_pdl", ctypes.c_int32),
-                ("page_pairing", ctypes.c_int32),
+                ("page_pairing", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
+                ("sinks", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p)]
 
@@ -133,13 +134,23 @@ def _stream_handle(stream) -> int:
 
 
 def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=False, workspace=None,
-                 workspace_bytes=0, split_start_event=None, split_stop_event=None, page_pairing=0) -> PaOptions:
+                 workspace_bytes=0, split_start_event=None, split_stop_event=None, page_pairing=0,
+                 sliding_window=0, sinks=None) -> PaOptions:
+    """Options for paged_attn_decode_ex.  sinks: CUDA float32 tensor [Hq] (kept
+    alive by the caller) or None."""
     o = PaOptions()
     o.num_ctas = num_ctas
     o.min_pages_per_cta = min_pages_per_cta
     o.heads_per_cta = heads_per_cta
     o.disable_pdl = int(bool(disable_pdl))
     o.page_pairing = page_pairing
+    o.sliding_window = sliding_window
+    if sinks is not None:
+        if sinks.dtype != torch.float32 or not sinks.is_contiguous():
+            raise TypeError("sinks must be a contiguous float32 tensor")
+        o.sinks = sinks.data_ptr()
+    else:
+        o.sinks = None
     o.workspace = workspace
     o.workspace_bytes = workspace_bytes
     o.split_start_event = int(split_start_event.cuda_event) if split_start_event is not None else None

@@ -298,6 +298,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   }
   if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return fail(PA_ERR_INVALID_ARG, "scale, k_scale and v_scale must be finite");
+  if (opts && opts->sinks && !aligned(opts->sinks, 4)) return fail(PA_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
   if ((st = check_shape_args(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq),
                              static_cast<int>(Hkv), static_cast<int>(D), kc->dtype, max_qlen)) != PA_OK)
     return st;
@@ -369,6 +370,8 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   sp.nstage = pl.nstage;
   sp.min_pages = pl.min_pages;
   sp.pair_pages = pl.pair;
+  sp.window = (opts && opts->sliding_window > 0) ? opts->sliding_window : 0;
+  sp.sinks = opts ? static_cast<const float*>(opts->sinks) : nullptr;
   sp.scale_log2 = scale * (esz == 1 ? k_scale : 1.0f) * kLog2e;
   sp.v_scale = esz == 1 ? v_scale : 1.0f;
   uint8_t* wsb = static_cast<uint8_t*>(ws);

@@ -34,6 +34,8 @@ struct SplitParams {
   int32_t nstage;
   int32_t min_pages;        // minimum pages of work per CTA
   int32_t pair_pages;       // consumers take two pages of a segment at once
+  int32_t window;           // sliding window (keys p-W < j <= p), 0 = off
+  const float* sinks;       // [Hq] sink logits or nullptr
   // math
   float scale_log2;         // scale * k_scale * log2(e)
   float v_scale;            // applied to the output (1 for bf16 caches)

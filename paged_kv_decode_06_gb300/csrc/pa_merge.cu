@@ -23,7 +23,7 @@ struct MergeRow {
   bool work;        // row exists and its unit was cut into >= 2 pieces
   uint16_t* orow;
   float* lse_ptr;
-  int hh, rho;
+  int hh, rho, hq;
   int gf, nparts;
   bool first_is_tail;
 };
@@ -69,6 +69,7 @@ __device__ __forceinline__ MergeRow merge_row(const MergeParams& p, int u, int r
   if (m.nparts <= 1 || m.rho >= p.G * qn) return m;
   const int t = t0 + m.rho / p.G;
   const int hq = (c * p.HC + m.hh) * p.G + m.rho % p.G;
+  m.hq = hq;
   m.orow = p.out + static_cast<int64_t>(t) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h;
   m.lse_ptr = p.lse ? p.lse + static_cast<int64_t>(t) * p.lse_stride_t + static_cast<int64_t>(hq) * p.lse_stride_h
                     : nullptr;

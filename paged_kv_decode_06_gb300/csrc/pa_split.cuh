@@ -32,6 +32,8 @@
 // All waits are bounded (they report a timeout in the status word and stop).
 #pragma once
 
+#include <climits>
+
 #include "pa_device.cuh"
 #include "pa_kernels.h"
 
@@ -79,11 +81,21 @@ struct SeqInfo {
   int L;    // cached tokens (including the query tokens)
   int t0;   // first query token
   int qn;   // query tokens (0 if the metadata is invalid)
+  int js;   // first page any query row can see (sliding window), else 0
 };
+
+// First page a sequence's query rows can see: with a sliding window of W keys
+// the earliest visible key is L - qn - W + 1 (query row 0); pages before it are
+// never fetched.
+__device__ __forceinline__ int first_visible_page(int L, int qn, int window) {
+  if (window <= 0 || qn < 1) return 0;
+  const int first_key = L - qn - window + 1;
+  return first_key > 0 ? first_key / kPage : 0;
+}
 
 // Sequence metadata from the shared-memory copies made in the prologue.
 __device__ __forceinline__ SeqInfo seq_info(const SplitParams& p, const int32_t* s_len, const int32_t* s_qsl, int i,
-                                            bool report) {
+                                            bool report, int window) {
   SeqInfo s;
   s.L = s_len[i];
   s.t0 = s_qsl[i];
@@ -94,6 +106,7 @@ __device__ __forceinline__ SeqInfo seq_info(const SplitParams& p, const int32_t*
   } else if (s.qn > s.L && report) {
     atomicOr(p.err, kErrSeqLen);
   }
+  s.js = first_visible_page(s.L, s.qn, window);
   return s;
 }
 
@@ -247,7 +260,7 @@ __device__ __forceinline__ void pv_pages(ConsumerState<D, FP8>& cs, const uint32
 template <int D, bool FP8, int NP>
 __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const uint32_t (&hb)[NP], uint32_t kv_bytes,
                                               uint32_t block_stride, int tb, int L, int min_lim, int lim0, int lim1,
-                                              float scale_log2, int lane) {
+                                              int window, float scale_log2, int lane) {
   using GG = Geo<D, FP8>;
   const int tig = lane & 3, mi = lane >> 3, rr = lane & 7;
   float S[2 * NP][4];
@@ -283,14 +296,18 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
   for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) x[n][e] = S[n][e] * scale_log2;
-  if (tb + kPage * NP - 1 > min_lim) {
+  // keys allowed for a row: lim - W < token <= lim (causal run end; sliding
+  // window start when W > 0, whose largest start is L - W for the last row)
+  if (tb + kPage * NP - 1 > min_lim || (window > 0 && tb < L - window)) {
+    const int lo0 = window > 0 ? lim0 - window + 1 : INT_MIN;
+    const int lo1 = window > 0 ? lim1 - window + 1 : INT_MIN;
 #pragma unroll
     for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int tok = tb + 8 * n + 2 * tig + e;
-        if (tok > lim0) x[n][e] = -INFINITY;
-        if (tok > lim1) x[n][2 + e] = -INFINITY;
+        if (tok > lim0 || tok < lo0) x[n][e] = -INFINITY;
+        if (tok > lim1 || tok < lo1) x[n][2 + e] = -INFINITY;
       }
   }
   float mx0 = fmaxf(x[0][0], x[0][1]);
@@ -368,11 +385,14 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
   }
 }
 
-template <int D, bool FP8>
+// WINDOW: the sliding-window variant (a separate instantiation, so the
+// windowless kernels carry none of its code).
+template <int D, bool FP8, bool WINDOW>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const SplitParams p) {
   using GG = Geo<D, FP8>;
+  const int window = WINDOW ? p.window : 0;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_scan[kSplitMaxThreads / 32 + 1];
   __shared__ int s_total;
@@ -411,6 +431,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         atomicOr(p.err, kErrSeqLen);
         v = p.max_blocks;
       }
+      const int qn = p.qsl != nullptr ? p.qsl[i + 1] - p.qsl[i] : 1;
+      v -= min(v, first_visible_page(L, qn, window));   // pages before the sliding window are skipped
     }
     int x = v;
 #pragma unroll
@@ -501,7 +523,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             break;
           }
         }
-        const SeqInfo si = seq_info(p, s_len, s_qsl, cu.i, false);
+        const SeqInfo si = seq_info(p, s_len, s_qsl, cu.i, false, window);
         if (lane == 0) mbar_arrive_expect_tx(qfull_bar(qs), static_cast<uint32_t>(si.qn) * qrow_bytes);
         __syncwarp();
         const uint32_t qdst = base + p.off_q + static_cast<uint32_t>(qs) * p.q_slot_bytes;
@@ -517,7 +539,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
           bt_val = nx_val;
         } else {
           const int jj = cu.j + lane;
-          bt_val = (jj < cu.n) ? p.block_tables[static_cast<int64_t>(cu.i) * p.bt_stride + jj] : 0;
+          const int js = first_visible_page(s_len[cu.i], s_qsl[cu.i + 1] - s_qsl[cu.i], window);
+          bt_val = (jj < cu.n) ? p.block_tables[static_cast<int64_t>(cu.i) * p.bt_stride + js + jj] : 0;
         }
         bt_i = cu.i;
         bt_j0 = cu.j;
@@ -537,7 +560,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         nx_j0 = nj;
         if (ni >= 0) {
           const int jj = nj + lane;
-          nx_val = (jj < pages_of(s_pre, ni)) ? p.block_tables[static_cast<int64_t>(ni) * p.bt_stride + jj] : 0;
+          const int js = first_visible_page(s_len[ni], s_qsl[ni + 1] - s_qsl[ni], window);
+          nx_val = (jj < pages_of(s_pre, ni)) ? p.block_tables[static_cast<int64_t>(ni) * p.bt_stride + js + jj] : 0;
         }
       }
       const int phys = __shfl_sync(0xffffffffu, bt_val, cu.j - bt_j0);
@@ -596,7 +620,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     }
     if (k == 0 || cu.j == 0) {
       // ---- new segment: query rows into registers, state reset ----
-      si = seq_info(p, s_len, s_qsl, cu.i, lane == 0 && hh == 0 && w == 0);
+      si = seq_info(p, s_len, s_qsl, cu.i, lane == 0 && hh == 0 && w == 0, window);
       seg_k0 = k;
       seg_j0 = cu.j;
       const int qs = qseg & 1;
@@ -626,6 +650,20 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       if (lane == 0) mbar_arrive(qempty_bar(qs));
       ++qseg;
       cs.reset();
+      if (p.sinks != nullptr && seg_j0 == 0) {
+        // The sink is a virtual first key with logit sinks[hq] and a zero value
+        // row: the piece holding the unit's first page starts from it, so every
+        // row counts it exactly once (the merge needs no special case).
+        const int hq_base = (cu.c * HC + hh) * G;
+        if (ok0) {
+          cs.m0 = p.sinks[hq_base + rho0 % G] * 1.4426950408889634f;
+          cs.l0 = tig == 0 ? 1.f : 0.f;
+        }
+        if (ok1) {
+          cs.m1 = p.sinks[hq_base + rho1 % G] * 1.4426950408889634f;
+          cs.l1 = tig == 0 ? 1.f : 0.f;
+        }
+      }
     }
     // Two consecutive pages of the same segment are processed together when
     // the ring is deep enough (32-token blocks: more independent MMA chains,
@@ -641,16 +679,16 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
-    const int tb = kPage * cu.j;
+    const int tb = kPage * (si.js + cu.j);
     if (active) {
       if (pair) {
         const uint32_t hb[2] = {head_base + static_cast<uint32_t>(stage) * p.stage_bytes,
                                 head_base + static_cast<uint32_t>(stage2) * p.stage_bytes};
-        consume_pages<D, FP8, 2>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1,
+        consume_pages<D, FP8, 2>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1, window,
                                  p.scale_log2, lane);
       } else {
         const uint32_t hb[1] = {head_base + static_cast<uint32_t>(stage) * p.stage_bytes};
-        consume_pages<D, FP8, 1>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1,
+        consume_pages<D, FP8, 1>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1, window,
                                  p.scale_log2, lane);
       }
     }
@@ -669,9 +707,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       float lt1 = cs.l1 + __shfl_xor_sync(0xffffffffu, cs.l1, 1);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
       if (complete) {
+        const int hq_base = (cu.c * HC + hh) * G;
         const float inv0 = lt0 > 0.f ? p.v_scale / lt0 : 0.f;
         const float inv1 = lt1 > 0.f ? p.v_scale / lt1 : 0.f;
-        const int hq_base = (cu.c * HC + hh) * G;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const bool ok = half ? ok1 : ok0;

@@ -15,15 +15,26 @@ cudaError_t launch_split_bf16(int head_dim, const CUtensorMap& tk, const CUtenso
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_split_kernel<128, false>, tk, tv, p);
-  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_split_kernel<64, false>, tk, tv, p);
+  const bool win = p.window > 0;
+  if (head_dim == 128)
+    return win ? cudaLaunchKernelEx(&cfg, pa_split_kernel<128, false, true>, tk, tv, p)
+               : cudaLaunchKernelEx(&cfg, pa_split_kernel<128, false, false>, tk, tv, p);
+  if (head_dim == 64)
+    return win ? cudaLaunchKernelEx(&cfg, pa_split_kernel<64, false, true>, tk, tv, p)
+               : cudaLaunchKernelEx(&cfg, pa_split_kernel<64, false, false>, tk, tv, p);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t set_split_smem_limits_bf16(int smem) {
-  cudaError_t e = cudaFuncSetAttribute(pa_split_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pa_split_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const void* fns[4] = {reinterpret_cast<const void*>(pa_split_kernel<128, false, false>),
+                        reinterpret_cast<const void*>(pa_split_kernel<128, false, true>),
+                        reinterpret_cast<const void*>(pa_split_kernel<64, false, false>),
+                        reinterpret_cast<const void*>(pa_split_kernel<64, false, true>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace pa

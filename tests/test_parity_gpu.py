@@ -211,3 +211,52 @@ def test_full_size_configs_sampled(name):
     seqs = _sample_seqs(w, 6, seed=wl.CONFIG_ORDER.index(name))
     _, _, eo, el = check(w, seqs=seqs)
     print(f"{name}: sampled seqs {seqs}: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
+
+
+# ------------------------------------------------ sliding window and attention sinks
+
+def _check_opts(w, window=0, sinks=None, options_kw=None, ref=None):
+    kw = dict(options_kw or {})
+    sk_t = None
+    if sinks is not None:
+        sk_t = torch.from_numpy(np.asarray(sinks, dtype=np.float32)).cuda()
+    opts = binding.make_options(sliding_window=window, sinks=sk_t, **kw)
+    if ref is None:
+        ref = oracle.run_workload(w, sliding_window=window, sinks=sinks)
+    return check(w, options=opts, ref=ref)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 100, 1000])
+def test_sliding_window(kv, window):
+    w = wl.make_workload(_spec(kv=kv, G=4, Hkv=2, qlens=(1, 2, 4), seq_lens=(3, 16, 17, 64, 250, 700), seed=window),
+                         device="cuda")
+    ref = oracle.run_workload(w, sliding_window=window)
+    _check_opts(w, window=window, ref=ref)
+    _check_opts(w, window=window, ref=ref, options_kw=dict(num_ctas=7, min_pages_per_cta=1))
+
+
+def test_pages_before_the_window_are_never_read():
+    w = wl.make_workload(_spec(G=4, Hkv=2, seq_lens=(300, 520, 77), seed=9), device="cuda")
+    window = 40
+    ref = oracle.run_workload(w, sliding_window=window)
+    bt = w.block_tables.copy()
+    for i, L in enumerate(w.seq_lens):
+        first_page = max(0, int(L) - 1 - window + 1) // 16
+        bt[i, :first_page] = w.num_pages + 1000          # out of range: reported if ever read
+    w.block_tables = bt
+    _check_opts(w, window=window, ref=ref)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("window", [0, 33])
+@pytest.mark.parametrize("num_ctas", [0, 3, 64])
+def test_attention_sinks(kv, window, num_ctas):
+    w = wl.make_workload(_spec(kv=kv, G=8, Hkv=2, qlens=(1, 3), seq_lens=(1, 20, 200, 900), seed=num_ctas + 2),
+                         device="cuda")
+    rng = np.random.default_rng(num_ctas)
+    sinks = rng.normal(0, 2, size=16).astype(np.float32)
+    sinks[3] = 30.0                                   # a sink that dominates its rows
+    ref = oracle.run_workload(w, sliding_window=window, sinks=sinks)
+    kw = dict(num_ctas=num_ctas, min_pages_per_cta=1) if num_ctas else None
+    _check_opts(w, window=window, sinks=sinks, options_kw=kw, ref=ref)
