@@ -211,7 +211,17 @@ def run_ours(args, world, rank, local):
     spec = _spec_for(args)
     base = wl.make_workload(spec, device=str(dev))
     step_bytes = base.kv_bytes()
-    pools = max(1, math.ceil(2 * L2_BYTES / step_bytes))
+    sinks_t = None
+    if args.window > 0:
+        # algorithmic bytes with a sliding window: the union of the query rows'
+        # windows, min(L, W + q - 1) keys per sequence
+        eb = 1 if spec.kv_dtype == "fp8" else 2
+        seen = np.minimum(base.seq_lens.astype(np.int64), args.window + base.query_lens.astype(np.int64) - 1)
+        step_bytes = int(seen.sum()) * spec.num_kv_heads * spec.head_dim * 2 * eb
+    if args.sinks:
+        sinks_t = torch.randn(spec.num_q_heads, generator=torch.Generator().manual_seed(3)).to(dev)
+    win_opts = binding.make_options(sliding_window=args.window, sinks=sinks_t) if (args.window > 0 or args.sinks) else None
+    pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
     works = [base] + [wl.make_workload(spec, device=str(dev), seed=spec.seed + 100 * k) for k in range(1, pools)]
     # every pool shares the metadata of the first (same lengths, same page ids)
     bt = torch.from_numpy(base.block_tables).to(dev)
@@ -224,6 +234,8 @@ def run_ours(args, world, rank, local):
 
     def step(k, opts=None, stream_=None):
         w = works[k % pools]
+        if opts is None:
+            opts = win_opts
         binding.paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
                                   spec.v_scale, out=out, lse=lse, options=opts, stream=stream_)
 
@@ -263,7 +275,8 @@ def run_ours(args, world, rank, local):
     ev_b = torch.cuda.Event(enable_timing=True)
     ev_a.record(stream); ev_b.record(stream)     # torch times only events it has recorded once itself
     torch.cuda.synchronize()
-    ev_opts = binding.make_options(split_start_event=ev_a, split_stop_event=ev_b)
+    ev_opts = binding.make_options(split_start_event=ev_a, split_stop_event=ev_b, sliding_window=args.window,
+                                   sinks=sinks_t)
     rgraphs = [capture(pidx, 1, opts=ev_opts) for pidx in range(pools)]
     run_steps(max(args.warmup, gstep))
     torch.cuda.synchronize()
@@ -316,7 +329,7 @@ def run_ours(args, world, rank, local):
         if qsl is not None:
             qsl.copy_(h_qsl, non_blocking=True)
         binding.paged_attn_decode(d_q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
-                                  spec.v_scale, out=out, lse=lse)
+                                  spec.v_scale, out=out, lse=lse, options=win_opts)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -354,6 +367,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
                    "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_dtype": spec.kv_dtype,
                    "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
+                   "sliding_window": args.window, "sinks": bool(args.sinks),
                    "l2": "no flush; each step reads >= 2x L2 of KV (pools rotated when one is smaller)",
                    "step_mode": "CUDA graph replay; a step = one paged_attn_decode call (split + merge)",
                    "plan": plan},
@@ -518,6 +532,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="decode", choices=["decode", "cache_write"])
+    ap.add_argument("--window", type=int, default=0, help="decode: sliding window of W keys (0 = off)")
+    ap.add_argument("--sinks", action="store_true", help="decode: per-query-head attention sinks")
     ap.add_argument("--tokens", type=int, default=16384, help="cache_write: tokens written per step")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
