@@ -220,7 +220,8 @@ def run_ours(args, world, rank, local):
         step_bytes = int(seen.sum()) * spec.num_kv_heads * spec.head_dim * 2 * eb
     if args.sinks:
         sinks_t = torch.randn(spec.num_q_heads, generator=torch.Generator().manual_seed(3)).to(dev)
-    win_opts = binding.make_options(sliding_window=args.window, sinks=sinks_t) if (args.window > 0 or args.sinks) else None
+    win_opts = (binding.make_options(sliding_window=args.window, sinks=sinks_t, use_tcgen05=args.tc)
+                if (args.window > 0 or args.sinks or args.tc) else None)
     pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
     works = [base] + [wl.make_workload(spec, device=str(dev), seed=spec.seed + 100 * k) for k in range(1, pools)]
     # every pool shares the metadata of the first (same lengths, same page ids)
@@ -276,7 +277,7 @@ def run_ours(args, world, rank, local):
     ev_a.record(stream); ev_b.record(stream)     # torch times only events it has recorded once itself
     torch.cuda.synchronize()
     ev_opts = binding.make_options(split_start_event=ev_a, split_stop_event=ev_b, sliding_window=args.window,
-                                   sinks=sinks_t)
+                                   sinks=sinks_t, use_tcgen05=args.tc)
     rgraphs = [capture(pidx, 1, opts=ev_opts) for pidx in range(pools)]
     run_steps(max(args.warmup, gstep))
     torch.cuda.synchronize()
@@ -356,8 +357,10 @@ def run_ours(args, world, rank, local):
     split_mean = statistics.mean(split_ms)
     achieved = step_bytes / (split_mean * 1e-3) / 1e9
     plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
-                                   binding.kv_dtype_code(spec.kv_dtype), mq)
-    traffic = _traffic_from_profiles(spec.name)
+                                   binding.kv_dtype_code(spec.kv_dtype), mq,
+                                   options=binding.make_options(use_tcgen05=args.tc))
+    kernel = "pa_split_tc_kernel" if plan["variant"] == 1 else "pa_split_kernel"
+    traffic = _traffic_from_profiles(spec.name, kernel)
     value = job_throughput_gbs(step_bytes, world, ms)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -367,12 +370,12 @@ def run_ours(args, world, rank, local):
         "config": {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
                    "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_dtype": spec.kv_dtype,
                    "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
-                   "sliding_window": args.window, "sinks": bool(args.sinks),
+                   "sliding_window": args.window, "sinks": bool(args.sinks), "use_tcgen05": args.tc,
                    "l2": "no flush; each step reads >= 2x L2 of KV (pools rotated when one is smaller)",
                    "step_mode": "CUDA graph replay; a step = one paged_attn_decode call (split + merge)",
                    "plan": plan},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": "pa_split_kernel",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
                      "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
                      "per_launch_bytes": step_bytes},
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -503,21 +506,27 @@ def _spec_for(args):
     return spec
 
 
-def _traffic_from_profiles(config):
+def kernel_source_sha256(kernel):
+    """Hash of the sources a split kernel is compiled from (stamps ncu figures)."""
+    import hashlib
+    names = ["pa_split.cuh", "pa_device.cuh"] + (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else [])
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic_from_profiles(config, kernel):
     """DRAM bytes per launch of the split kernel from the committed ncu summary,
     when it was taken on the current kernel source (else None)."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    h = hashlib.sha256()
-    for name in ("pa_split.cuh", "pa_device.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
     entry = d.get(config)
-    if not entry or entry.get("kernel_source_sha256") != h.hexdigest():
+    if not entry or entry.get("kernel") != kernel or entry.get("kernel_source_sha256") != kernel_source_sha256(kernel):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -534,6 +543,8 @@ def main():
     ap.add_argument("--op", default="decode", choices=["decode", "cache_write"])
     ap.add_argument("--window", type=int, default=0, help="decode: sliding window of W keys (0 = off)")
     ap.add_argument("--sinks", action="store_true", help="decode: per-query-head attention sinks")
+    ap.add_argument("--tc", type=int, default=0, choices=[0, 1, 2],
+                    help="decode split kernel: 0 planner's choice, 1 mma.sync, 2 tcgen05 (bf16)")
     ap.add_argument("--tokens", type=int, default=16384, help="cache_write: tokens written per step")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -92,6 +92,9 @@ typedef struct pa_options_t {
   size_t workspace_bytes;      /* ... of this size (see paged_attn_workspace_size)            */
   void* split_start_event;     /* optional cudaEvent_t recorded just before the split kernel  */
   void* split_stop_event;      /* optional cudaEvent_t recorded just after the split kernel   */
+  int32_t use_tcgen05;         /* split kernel: 0 = planner's choice (the tensor-memory kernel when
+                                  G * max_query_len > 64, else the mma.sync kernel); 1 = never
+                                  (PA_ERR_UNSUPPORTED above 64 rows); 2 = always (bf16 caches only) */
 } pa_options_t;
 
 /* Launch plan the library picks for a problem shape (for tests, tuning and
@@ -99,14 +102,16 @@ typedef struct pa_options_t {
 typedef struct pa_plan_t {
   int32_t num_ctas;          /* split-kernel grid size                                  */
   int32_t heads_per_cta;     /* KV heads a CTA processes per page (HC)                  */
-  int32_t row_tiles;         /* 16-row MMA tiles per KV head (ceil(G*max_query_len/16)) */
+  int32_t row_tiles;         /* 16-row tiles per KV head (ceil(G*max_query_len/16); 8 for tcgen05) */
   int32_t num_stages;        /* depth of the shared-memory page ring                    */
-  int32_t threads_per_cta;   /* 32 * (1 producer warp + heads_per_cta * row_tiles)      */
+  int32_t threads_per_cta;   /* 32 * (1 producer + heads_per_cta * row_tiles); tcgen05: 384 */
   int32_t smem_bytes;        /* dynamic shared memory per CTA                           */
   int32_t min_pages_per_cta; /* work below which fewer CTAs are used                    */
   int32_t merge_rows;        /* rows per merge unit (heads_per_cta * G * max_query_len) */
   int32_t page_pairing;      /* 1 if consumer warps take two pages of a sequence at once */
   int64_t workspace_bytes;   /* split workspace the call needs                          */
+  int32_t variant;           /* 0: mma.sync warps; 1: tcgen05 / tensor-memory kernel    */
+  int32_t block_pages;       /* pages a consumer step takes (1, 2 paired, 4 tcgen05)    */
 } pa_plan_t;
 
 /*
@@ -123,7 +128,9 @@ typedef struct pa_plan_t {
  *   query_start_loc int32 [B+1] contiguous cumulative query-token offsets (ragged MTP
  *                   runs), or data == NULL: one query token per sequence (T == B).
  *   max_query_len   host-known upper bound of q_i (1 when query_start_loc is NULL);
- *                   chooses the tile without a device read.  G * max_query_len <= 64.
+ *                   chooses the tile without a device read.  G * max_query_len <= 128
+ *                   for bf16 caches (above 64 rows the tcgen05 / tensor-memory kernel
+ *                   runs), <= 64 for fp8 caches.
  *   scale           softmax scale applied to <q, k> (e.g. 1/sqrt(D)).
  *   k_scale, v_scale per-tensor dequantisation scales of fp8 caches (ignored for bf16).
  *   out             bf16 [T, Hq, D], stride[2] == 1; written.

@@ -32,7 +32,8 @@ class PaOptions(ctypes.Structure):
                 ("page_pairing", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
                 ("sinks", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p)]
+                ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p),
+                ("use_tcgen05", ctypes.c_int32)]
 
 
 class PaPlan(ctypes.Structure):
@@ -40,7 +41,8 @@ class PaPlan(ctypes.Structure):
                 ("num_stages", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("min_pages_per_cta", ctypes.c_int32), ("merge_rows", ctypes.c_int32),
                 ("page_pairing", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("variant", ctypes.c_int32),
+                ("block_pages", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -135,9 +137,10 @@ def _stream_handle(stream) -> int:
 
 def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=False, workspace=None,
                  workspace_bytes=0, split_start_event=None, split_stop_event=None, page_pairing=0,
-                 sliding_window=0, sinks=None) -> PaOptions:
+                 sliding_window=0, sinks=None, use_tcgen05=0) -> PaOptions:
     """Options for paged_attn_decode_ex.  sinks: CUDA float32 tensor [Hq] (kept
-    alive by the caller) or None."""
+    alive by the caller) or None.  use_tcgen05: 0 planner's choice, 1 never,
+    2 always (bf16 caches)."""
     o = PaOptions()
     o.num_ctas = num_ctas
     o.min_pages_per_cta = min_pages_per_cta
@@ -145,6 +148,7 @@ def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=F
     o.disable_pdl = int(bool(disable_pdl))
     o.page_pairing = page_pairing
     o.sliding_window = sliding_window
+    o.use_tcgen05 = use_tcgen05
     if sinks is not None:
         if sinks.dtype != torch.float32 or not sinks.is_contiguous():
             raise TypeError("sinks must be a contiguous float32 tensor")

@@ -29,6 +29,10 @@ constexpr int kMaxSeqs = 8192;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxStages = 32;
 constexpr int kDefaultMinPages = 4;
+constexpr int kMaxRowsMma = 64;      // query rows per KV head of the mma.sync kernel
+constexpr int kMaxRowsTc = 128;      // ... and of the tensor-memory kernel (bf16 caches)
+constexpr int kTcBlockPages = 4;
+constexpr int kTcThreads = 384;
 
 thread_local std::string t_last_error;
 
@@ -87,6 +91,8 @@ int device_state(DeviceState** out, int* dev_out) {
       return cuda_fail(e, "cudaFuncSetAttribute(split bf16)");
     if ((e = pa::set_split_smem_limits_fp8(s.smem_optin)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(split fp8)");
+    if ((e = pa::set_split_smem_limits_tc(s.smem_optin)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(split tcgen05)");
     void* ptr = nullptr;
     if ((e = cudaGetSymbolAddress(&ptr, g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
@@ -110,8 +116,10 @@ int device_state(DeviceState** out, int* dev_out) {
 struct Plan {
   int B, Hq, Hkv, D, esz, max_qlen;
   int G, R_max, MT, HC, NC, nstage, threads, grid, min_pages, pair;
+  bool tc;            // tensor-memory (tcgen05) kernel
+  int block_pages;    // tc: pages per ring stage
   uint32_t stage_bytes, kv_bytes, q_slot_bytes;
-  uint32_t off_stage, off_q, off_bar, off_prefix, smem;
+  uint32_t off_stage, off_q, off_bar, off_prefix, off_xchg, smem;
   size_t ws_unit, ws_ml, ws_o, ws_bytes;
 };
 
@@ -126,23 +134,28 @@ int check_shape_args(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen) 
     return fail(PA_ERR_INVALID_ARG, "kv dtype %d is neither PA_BF16 nor PA_FP8_E4M3", kv_dtype);
   if (max_qlen < 1) return fail(PA_ERR_INVALID_ARG, "max_query_len %d < 1", max_qlen);
   const int G = Hq / Hkv;
-  if (static_cast<int64_t>(G) * max_qlen > 64)
-    return fail(PA_ERR_UNSUPPORTED, "group size %d x max_query_len %d exceeds 64 query rows per KV head", G,
-                max_qlen);
+  const int64_t rows = static_cast<int64_t>(G) * max_qlen;
+  const int limit = kv_dtype == PA_BF16 ? kMaxRowsTc : kMaxRowsMma;
+  if (rows > limit)
+    return fail(PA_ERR_UNSUPPORTED, "group size %d x max_query_len %d exceeds %d query rows per KV head (%s cache)", G,
+                max_qlen, limit, kv_dtype == PA_BF16 ? "bf16" : "fp8");
   return PA_OK;
 }
 
-int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const pa_options_t* opts, int num_sms,
-              int smem_optin, Plan* pl) {
-  int st = check_shape_args(B, Hq, Hkv, D, kv_dtype, max_qlen);
-  if (st != PA_OK) return st;
-  Plan p = {};
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.max_qlen = max_qlen;
-  p.esz = (kv_dtype == PA_FP8_E4M3) ? 1 : 2;
-  p.G = Hq / Hkv;
-  p.R_max = p.G * max_qlen;
-  p.MT = (p.R_max + 15) / 16;
-  p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
+// Kernel-choice options that the host can check before touching the device.
+int check_variant_option(const pa_options_t* opts, int kv_dtype, int64_t rows) {
+  const int use_tc = opts ? opts->use_tcgen05 : 0;
+  if (use_tc < 0 || use_tc > 2) return fail(PA_ERR_INVALID_ARG, "use_tcgen05 %d not in {0, 1, 2}", use_tc);
+  if (use_tc == 2 && kv_dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs a bf16 cache");
+  if (rows > kMaxRowsMma && use_tc == 1)
+    return fail(PA_ERR_UNSUPPORTED, "%lld query rows per KV head need the tcgen05 kernel", (long long)rows);
+  if (opts && opts->heads_per_cta > 1 && (use_tc == 2 || rows > kMaxRowsMma))
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel takes one KV head per CTA");
+  return PA_OK;
+}
+
+// mma.sync kernel: heads per CTA, ring depth and shared-memory layout.
+int plan_mma(Plan& p, int B, int Hkv, int D, int max_qlen, const pa_options_t* opts, int smem_optin) {
   const uint32_t bar_bytes = 8u * (2 * kMaxStages + 4);
   const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));   // prefix, lengths, starts
   const int forced_hc = opts ? opts->heads_per_cta : 0;
@@ -194,7 +207,53 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
   p.off_bar = p.off_q + 2 * p.q_slot_bytes;
   p.off_prefix = p.off_bar + bar_bytes;
   p.smem = 1024 + p.off_prefix + prefix_bytes;
+  return PA_OK;
+}
+
+int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const pa_options_t* opts, int num_sms,
+              int smem_optin, Plan* pl) {
+  int st = check_shape_args(B, Hq, Hkv, D, kv_dtype, max_qlen);
+  if (st != PA_OK) return st;
+  Plan p = {};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.max_qlen = max_qlen;
+  p.esz = (kv_dtype == PA_FP8_E4M3) ? 1 : 2;
+  p.G = Hq / Hkv;
+  p.R_max = p.G * max_qlen;
+  p.MT = (p.R_max + 15) / 16;
+  p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
   p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
+  if ((st = check_variant_option(opts, kv_dtype, p.R_max)) != PA_OK) return st;
+  p.tc = (opts && opts->use_tcgen05 == 2) || p.R_max > kMaxRowsMma;
+  if (p.tc) {
+    // One KV head per CTA; shared memory: ring stages of kTcBlockPages pages
+    // (K and V), barriers, exchange buffers, sequence metadata (Q is in TMEM).
+    p.HC = 1;
+    p.NC = Hkv;
+    p.MT = 8;
+    p.threads = kTcThreads;
+    p.pair = 0;
+    p.block_pages = kTcBlockPages;
+    p.kv_bytes = static_cast<uint32_t>(kPageSize * D * 2);
+    p.stage_bytes = static_cast<uint32_t>(2 * p.block_pages) * p.kv_bytes;
+    p.q_slot_bytes = 0;
+    const uint32_t tc_bar_bytes = static_cast<uint32_t>(align_up(8u * (2 * kMaxStages + 24), 1024));
+    const uint32_t tc_xchg_bytes = 4096;   // softmax warps' partial maxima and sums
+    const uint32_t tc_prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));
+    const int64_t room = smem_optin - (1024 + static_cast<int64_t>(tc_bar_bytes) + tc_xchg_bytes + tc_prefix_bytes);
+    p.nstage = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / p.stage_bytes)) : 0;
+    if (p.nstage < 2)
+      return fail(PA_ERR_UNSUPPORTED, "no tcgen05 launch configuration fits %d bytes of shared memory", smem_optin);
+    p.off_stage = 0;
+    p.off_q = p.nstage * p.stage_bytes;
+    p.off_bar = p.off_q;
+    p.off_xchg = p.off_bar + tc_bar_bytes;
+    p.off_prefix = p.off_xchg + tc_xchg_bytes;
+    p.smem = 1024 + p.off_prefix + tc_prefix_bytes;
+  }
+  if (!p.tc) {
+    const int st2 = plan_mma(p, B, Hkv, D, max_qlen, opts, smem_optin);
+    if (st2 != PA_OK) return st2;
+  }
   const size_t rows = static_cast<size_t>(2) * p.grid * p.HC * p.R_max;
   p.ws_unit = 0;
   p.ws_ml = align_up(p.ws_unit + static_cast<size_t>(16) * B * p.NC, 256);
@@ -302,6 +361,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   if ((st = check_shape_args(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq),
                              static_cast<int>(Hkv), static_cast<int>(D), kc->dtype, max_qlen)) != PA_OK)
     return st;
+  if ((st = check_variant_option(opts, kc->dtype, (Hq / Hkv) * static_cast<int64_t>(max_qlen))) != PA_OK) return st;
 
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
@@ -386,6 +446,8 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   sp.off_stage = pl.off_stage;
   sp.stage_bytes = pl.stage_bytes;
   sp.kv_bytes = pl.kv_bytes;
+  sp.block_pages = pl.block_pages;
+  sp.off_xchg = pl.off_xchg;
 
   pa::MergeParams mp = {};
   mp.out = sp.out;
@@ -416,15 +478,26 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   // predecessor in the stream before touching global memory, but its launch
   // overlaps the predecessor's tail.
   const bool pdl = !(opts && opts->disable_pdl);
-  // External records also become event nodes when the stream is being captured.
-  if (ev0 && (e = cudaEventRecordWithFlags(ev0, stream, cudaEventRecordExternal)) != cudaSuccess)
+  // Under stream capture the records become external event nodes (so a replay
+  // records them); outside capture they are ordinary records.
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (ev0 || ev1) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
+  if (ev0 && (e = cudaEventRecordWithFlags(ev0, stream, rec_flags)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(start)");
-  e = (esz == 1) ? pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
-                                        pdl && !ev0, stream)
-                 : pa::launch_split_bf16(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads,
-                                         static_cast<int>(pl.smem), pdl && !ev0, stream);
+  if (pl.tc)
+    e = pa::launch_split_tc(static_cast<int>(D), tk, tv, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
+  else if (esz == 1)
+    e = pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
+                             pdl && !ev0, stream);
+  else
+    e = pa::launch_split_bf16(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
+                              pdl && !ev0, stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
-  if (ev1 && (e = cudaEventRecordWithFlags(ev1, stream, cudaEventRecordExternal)) != cudaSuccess)
+  if (ev1 && (e = cudaEventRecordWithFlags(ev1, stream, rec_flags)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(stop)");
   // Many pieces per unit on average (few long contexts over many CTAs): the
   // wide merge reads a row's partials with a whole block.
@@ -543,6 +616,9 @@ int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   if (plan == nullptr) return fail(PA_ERR_INVALID_ARG, "plan pointer is NULL");
   int st = check_shape_args(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len);
   if (st != PA_OK) return st;
+  if ((st = check_variant_option(opts, kv_dtype, (num_q_heads / num_kv_heads) * static_cast<int64_t>(max_query_len))) !=
+      PA_OK)
+    return st;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
@@ -560,6 +636,8 @@ int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   plan->merge_rows = pl.HC * pl.R_max;
   plan->page_pairing = pl.pair;
   plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
+  plan->variant = pl.tc ? 1 : 0;
+  plan->block_pages = pl.tc ? pl.block_pages : (pl.pair ? 2 : 1);
   return PA_OK;
 }
 

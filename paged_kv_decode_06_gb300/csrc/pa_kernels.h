@@ -52,6 +52,8 @@ struct SplitParams {
   uint32_t off_stage;
   uint32_t stage_bytes;     // K tiles + V tiles of one page
   uint32_t kv_bytes;        // K (or V) tiles of one page: HC * 16 * D * elem
+  int32_t block_pages;      // tensor-memory variant: pages per ring stage (block)
+  uint32_t off_xchg;        // tensor-memory variant: softmax warps' exchange buffers (4 KB)
 };
 
 struct MergeParams {
@@ -96,6 +98,11 @@ cudaError_t launch_split_fp8(int head_dim, const CUtensorMap& tk, const CUtensor
 // partials per unit); otherwise one warp per (unit, row), 8 rows per block.
 cudaError_t launch_merge(int head_dim, const MergeParams& p, int units, int rows, bool wide, bool pdl,
                          cudaStream_t stream);
+// Tensor-memory (tcgen05) variant for up to 128 query rows per KV head (bf16
+// caches, one KV head per CTA, 192 threads).
+cudaError_t launch_split_tc(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                            int grid, int smem, bool pdl, cudaStream_t stream);
+cudaError_t set_split_smem_limits_tc(int smem);
 cudaError_t set_split_smem_limits_bf16(int smem);
 cudaError_t set_split_smem_limits_fp8(int smem);
 

@@ -141,6 +141,105 @@ __device__ __forceinline__ int d_of(int J, int e, int tig) {
   }
 }
 
+// Prologue shared by the split kernels (all threads of the CTA call it):
+// sequence lengths and query starts copied to shared memory, pages of work per
+// sequence (pages before a sliding window excluded) and their exclusive prefix.
+__device__ __forceinline__ void page_prefix(const SplitParams& p, int window, int32_t* s_pre, int32_t* s_len,
+                                            int32_t* s_qsl, int* s_scan, int* s_total) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int B = p.num_seqs;
+  int carry = 0;
+  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+    const int i = b0 + tid;
+    int v = 0;
+    if (i < B) {
+      const int L = p.seq_lens[i];
+      s_len[i] = L;
+      s_qsl[i] = p.qsl != nullptr ? p.qsl[i] : i;
+      v = L > 0 ? (L + kPage - 1) / kPage : 0;
+      if (v > p.max_blocks) {       // context longer than its block-table row: never read past the row
+        atomicOr(p.err, kErrSeqLen);
+        v = p.max_blocks;
+      }
+      const int qn = p.qsl != nullptr ? p.qsl[i + 1] - p.qsl[i] : 1;
+      v -= min(v, first_visible_page(L, qn, window));   // pages before the sliding window are skipped
+    }
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_scan[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const int wv = lane < nwarps ? s_scan[lane] : 0;
+      int xs = wv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, xs, o);
+        if (lane >= o) xs += y;
+      }
+      if (lane < nwarps) s_scan[lane] = xs - wv;
+      if (lane == 31) *s_total = xs;
+    }
+    __syncthreads();
+    if (i < B) s_pre[i] = carry + s_scan[warp] + x - v;
+    carry += *s_total;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    s_pre[B] = carry;
+    s_qsl[B] = p.qsl != nullptr ? p.qsl[B] : B;
+  }
+}
+
+// Block-table entries for the producer warp: 32 at a time (one per lane),
+// the batch the traversal reaches next loaded ahead of use.  All lanes call
+// lookup() with the same cursor; it returns the physical page of cu.
+struct BlockTableCache {
+  int bt_i = -1, bt_j0 = 0, bt_val = 0;   // entries [bt_j0, bt_j0 + 32) of sequence bt_i
+  int nx_i = -1, nx_j0 = 0, nx_val = 0;   // the batch after it
+
+  __device__ __forceinline__ int lookup(const SplitParams& p, const Cursor& cu, const int32_t* s_pre,
+                                        const int32_t* s_len, const int32_t* s_qsl, int B, int NC, int window,
+                                        int lane) {
+    if (cu.i != bt_i || cu.j < bt_j0 || cu.j >= bt_j0 + 32) {
+      if (cu.i == nx_i && cu.j == nx_j0) {
+        bt_val = nx_val;
+      } else {
+        const int jj = cu.j + lane;
+        const int js = first_visible_page(s_len[cu.i], s_qsl[cu.i + 1] - s_qsl[cu.i], window);
+        bt_val = (jj < cu.n) ? p.block_tables[static_cast<int64_t>(cu.i) * p.bt_stride + js + jj] : 0;
+      }
+      bt_i = cu.i;
+      bt_j0 = cu.j;
+      int ni = -1, nj = 0;
+      if (bt_j0 + 32 < cu.n) {
+        ni = cu.i;
+        nj = bt_j0 + 32;
+      } else if (cu.c + 1 < NC) {
+        ni = cu.i;
+      } else {
+        ni = cu.i + 1;
+        while (ni < B && pages_of(s_pre, ni) == 0) ++ni;
+        if (ni >= B) ni = -1;
+      }
+      nx_i = ni;
+      nx_j0 = nj;
+      if (ni >= 0) {
+        const int jj = nj + lane;
+        const int js = first_visible_page(s_len[ni], s_qsl[ni + 1] - s_qsl[ni], window);
+        nx_val = (jj < pages_of(s_pre, ni)) ? p.block_tables[static_cast<int64_t>(ni) * p.bt_stride + js + jj] : 0;
+      }
+    }
+    return __shfl_sync(0xffffffffu, bt_val, cu.j - bt_j0);
+  }
+};
+
 // Per-warp online-softmax state for 16 query rows of one KV head.
 template <int D, bool FP8>
 struct ConsumerState {
@@ -407,7 +506,6 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int nwarps = blockDim.x >> 5;
   const int B = p.num_seqs;
   if (tid == 0) {
     prefetch_tensormap(&tmap_k);
@@ -418,50 +516,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   grid_dependency_wait();
 
   // ---- prologue: metadata to shared memory, pages per sequence, prefix -----
-  int carry = 0;
-  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
-    const int i = b0 + tid;
-    int v = 0;
-    if (i < B) {
-      const int L = p.seq_lens[i];
-      s_len[i] = L;
-      s_qsl[i] = p.qsl != nullptr ? p.qsl[i] : i;
-      v = L > 0 ? (L + kPage - 1) / kPage : 0;
-      if (v > p.max_blocks) {       // context longer than its block-table row: never read past the row
-        atomicOr(p.err, kErrSeqLen);
-        v = p.max_blocks;
-      }
-      const int qn = p.qsl != nullptr ? p.qsl[i + 1] - p.qsl[i] : 1;
-      v -= min(v, first_visible_page(L, qn, window));   // pages before the sliding window are skipped
-    }
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_scan[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      const int wv = lane < nwarps ? s_scan[lane] : 0;
-      int xs = wv;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, xs, o);
-        if (lane >= o) xs += y;
-      }
-      if (lane < nwarps) s_scan[lane] = xs - wv;
-      if (lane == 31) s_total = xs;
-    }
-    __syncthreads();
-    if (i < B) s_pre[i] = carry + s_scan[warp] + x - v;
-    carry += s_total;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    s_pre[B] = carry;
-    s_qsl[B] = p.qsl != nullptr ? p.qsl[B] : B;
-  }
+  page_prefix(p, window, s_pre, s_len, s_qsl, s_scan, &s_total);
 
   const uint32_t bar0 = base + p.off_bar;
   const int nstage = p.nstage;
@@ -503,8 +558,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     // ============================ producer =================================
     Cursor cu = locate(s_pre, B, NC, start);
     int qseg = 0;
-    int bt_i = -1, bt_j0 = 0, bt_val = 0;   // block-table entries [bt_j0, bt_j0 + 32) of sequence bt_i
-    int nx_i = -1, nx_j0 = 0, nx_val = 0;   // the batch after it, loaded ahead of use
+    BlockTableCache btc;
     const uint32_t block_stride = static_cast<uint32_t>(HC * GG::BOX_BYTES);
     int stage = 0;
     uint32_t round = 0;    // k / nstage
@@ -534,37 +588,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         }
         ++qseg;
       }
-      if (cu.i != bt_i || cu.j < bt_j0 || cu.j >= bt_j0 + 32) {
-        if (cu.i == nx_i && cu.j == nx_j0) {
-          bt_val = nx_val;
-        } else {
-          const int jj = cu.j + lane;
-          const int js = first_visible_page(s_len[cu.i], s_qsl[cu.i + 1] - s_qsl[cu.i], window);
-          bt_val = (jj < cu.n) ? p.block_tables[static_cast<int64_t>(cu.i) * p.bt_stride + js + jj] : 0;
-        }
-        bt_i = cu.i;
-        bt_j0 = cu.j;
-        // prefetch the batch the traversal reaches next
-        int ni = -1, nj = 0;
-        if (bt_j0 + 32 < cu.n) {
-          ni = cu.i;
-          nj = bt_j0 + 32;
-        } else if (cu.c + 1 < NC) {
-          ni = cu.i;
-        } else {
-          ni = cu.i + 1;
-          while (ni < B && pages_of(s_pre, ni) == 0) ++ni;
-          if (ni >= B) ni = -1;
-        }
-        nx_i = ni;
-        nx_j0 = nj;
-        if (ni >= 0) {
-          const int jj = nj + lane;
-          const int js = first_visible_page(s_len[ni], s_qsl[ni + 1] - s_qsl[ni], window);
-          nx_val = (jj < pages_of(s_pre, ni)) ? p.block_tables[static_cast<int64_t>(ni) * p.bt_stride + js + jj] : 0;
-        }
-      }
-      const int phys = __shfl_sync(0xffffffffu, bt_val, cu.j - bt_j0);
+      const int phys = btc.lookup(p, cu, s_pre, s_len, s_qsl, B, NC, window, lane);
       if ((phys < 0 || phys >= p.num_pages) && lane == 0) atomicOr(p.err, kErrPageRange);
       // An out-of-range page id reads as zeros (TMA fills outside the tensor).
       if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);

@@ -1,0 +1,662 @@
+// Split-KV paged decode on the 5th-generation tensor cores (tcgen05 + TMEM),
+// for long verification runs: up to 128 query rows per KV head (G query heads
+// x up to 128/G tokens of a ragged MTP run), bf16 caches.
+//
+// Work decomposition, workspace and merge are those of the mma.sync split
+// kernel with one KV head per CTA: units (sequence, KV head) laid end to end
+// in (sequence, head, page) order, each CTA a contiguous page range, cut units
+// leaving fp32 partials for the same merge kernel.  What changes is the math:
+// with 65-128 rows per KV head, Q K^T and P V are dense 128 x 16n and
+// 128 x D products, which the tensor cores run from shared memory into tensor
+// memory while the CUDA cores do only the softmax.
+//
+// A block is up to block_pages (4) pages of one segment (a segment is the
+// part of one unit inside this CTA's range); the shared-memory ring holds one
+// block per stage: [K d0..63 | K d64..127 | V d0..63 | V d64..127], each
+// part block_pages x 16 rows x 128 bytes, 128-byte swizzled as TMA writes it.
+//
+// Roles (256 threads):
+//   warps 0-2 producers: block-table lookups and TMA loads of each page's K
+//             and V rows into the block's stage, page pg of a block by warp
+//             pg % 3 (a warp's TMA issue is serial, about 90 ns per 2 KB box,
+//             so one warp alone could not keep HBM busy with one-head boxes);
+//   warp 3    MMA issuer (one lane) and owner of the TMEM allocation:
+//               S[b%2]  = Q[s%2] K_b^T     (TS-MMA, Q read from TMEM, N = 16 * pages)
+//               O      += (P_hi + P_lo)[b%2] V_b   (TS-MMA, P read from TMEM, N = D)
+//             with S of block b+1 issued before P V of block b, so the tensor
+//             core and the softmax overlap;
+//   warps 4-11 softmax, two per TMEM lane quarter: thread = query row = TMEM
+//             lane, each of a row's two threads taking two pages of a block
+//             and half of O's columns.  Per block: load S, mask (causal run,
+//             context tail, sliding window), exchange the partial row max, update the
+//             running max, rescale O in TMEM only when the max grew by more
+//             than 2^8 (lazy rescale), write P to TMEM as two bf16 terms
+//             P_hi = bf16(P), P_lo = bf16(P - P_hi), so P V carries P to about
+//             16 bits instead of bf16's 8 (a row dominated by one or two keys
+//             would otherwise lose up to 2^-9 |v| to P's rounding); at a segment's
+//             end normalise O and write out / lse or the partials.  They also
+//             store each segment's Q rows into one of two TMEM slots.
+// TMEM columns: O [0,128) S0 [128,192) S1 [192,256) P_hi0 [256,288)
+//               P_hi1 [288,320) P_lo0 [320,352) P_lo1 [352,384) Q0 [384,448)
+//               Q1 [448,512) (bf16 pairs: 8 columns per 16 keys or features).
+// Shared memory holds only the ring (6 stages of 4 pages at D = 128) and
+// metadata: Q lives in TMEM, as the A operand of a TS-MMA.
+// Every wait is bounded (kErrTimeout); the CTA drains its MMAs before it frees
+// tensor memory.
+#pragma once
+
+#include "pa_split.cuh"
+
+namespace pa {
+
+constexpr int kTcProducers = 3;
+constexpr int kTcMmaWarp = 3;
+constexpr int kTcSoftmaxWarp0 = 4;   // warps 4..11; a multiple of 4, so warp % 4 is the TMEM lane quarter
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcThreads = 32 * (kTcSoftmaxWarp0 + kTcSoftmaxWarps);
+constexpr int kTcMaxBlockPages = 4;
+constexpr uint32_t kTcCols = 512;
+constexpr uint32_t kTmemO = 0;     // fp32 O, D columns
+constexpr uint32_t kTmemS = 128;   // + 64 * (block % 2): fp32 S, 16 columns per page
+constexpr uint32_t kTmemP = 256;   // + 32 * (block % 2): bf16 P rounded to nearest, 8 columns per page
+constexpr uint32_t kTmemPlo = 320; // + 32 * (block % 2): bf16 of the rounding residue
+constexpr uint32_t kTmemQ = 384;   // + 64 * (segment % 2): bf16 Q, D / 2 columns
+constexpr uint32_t kTcBox = 2048;  // one page of one 64-column half: 16 rows x 128 bytes
+constexpr uint32_t kTcHalf = kTcMaxBlockPages * kTcBox;   // one 64-column half of a stage's K or V
+
+// One block of the traversal.
+struct TcBlock {
+  int i, c;        // sequence, KV head
+  int j0;          // first page (index among the sequence's visible pages)
+  int n;           // visible pages of the sequence
+  int np;          // pages in the block
+  int64_t k0;      // position of the first page in the CTA's range
+  bool first;      // first block of a segment
+  bool last;       // last block of a segment
+};
+
+// Walks a CTA's page range block by block.  Producer, MMA issuer and softmax
+// warps each run one and see the same sequence of blocks.
+struct BlockWalker {
+  Cursor cu;
+  int64_t k, count;
+  int npb;
+
+  __device__ __forceinline__ BlockWalker(const int32_t* pre, int B, int NC, int64_t start, int64_t cnt, int block_pages)
+      : cu(locate(pre, B, NC, start)), k(0), count(cnt), npb(block_pages) {}
+
+  __device__ __forceinline__ bool more() const { return k < count; }
+
+  __device__ __forceinline__ TcBlock next(const int32_t* pre, int B, int NC) {
+    TcBlock t;
+    t.i = cu.i;
+    t.c = cu.c;
+    t.j0 = cu.j;
+    t.n = cu.n;
+    t.k0 = k;
+    t.first = (k == 0) || (cu.j == 0);
+    int np = min(npb, cu.n - cu.j);
+    if (count - k < np) np = static_cast<int>(count - k);
+    t.np = np;
+    t.last = (cu.j + np == cu.n) || (k + np == count);
+    for (int q = 0; q < np; ++q) advance(cu, pre, B, NC);
+    k += np;
+    return t;
+  }
+};
+
+// Warp-uniform bounded wait: true only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+template <int D>
+struct TcGeo {
+  static constexpr int NH = D / 64;                    // 64-column halves
+  static constexpr int KSTEPS = D / 16;
+};
+
+// Shared-memory descriptors.  A descriptor's address field is the byte
+// address >> 4, so a descriptor for base + off is the base descriptor + off/16
+// (no carry: shared addresses are below 2^18).  The kernel builds one base
+// descriptor per operand and block and adds compile-time offsets, which keeps
+// the MMA issue loop free of per-instruction descriptor arithmetic.
+//   K  (K-major, 16 * np rows): k-step s at (s / 4) * kTcHalf + (s % 4) * 32
+//   V  (MN-major, d contiguous): page pg at pg * kTcBox; 8-row groups 1 KB
+//      apart (SBO), the two 64-column halves kTcHalf apart (LBO)
+__device__ __forceinline__ constexpr uint32_t k_step(int s) { return ((s >> 2) * kTcHalf + (s & 3) * 32u) >> 4; }
+
+template <int D, bool WINDOW>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    pa_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                       const SplitParams p) {
+  using TG = TcGeo<D>;
+  const int window = WINDOW ? p.window : 0;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_scan[kTcThreads / 32 + 1];
+  __shared__ int s_total;
+  __shared__ uint32_t s_tmem;
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  int32_t* const s_pre = reinterpret_cast<int32_t*>(gbase + p.off_prefix);
+  int32_t* const s_len = s_pre + (p.num_seqs + 1);
+  int32_t* const s_qsl = s_len + p.num_seqs;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int B = p.num_seqs;
+  if (tid == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  grid_dependency_wait();
+  page_prefix(p, window, s_pre, s_len, s_qsl, s_scan, &s_total);
+
+  const uint32_t bar0 = base + p.off_bar;
+  const int nstage = p.nstage;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (nstage + s); };
+  const uint32_t xb = bar0 + 8u * (2 * nstage);
+  auto sfull_bar = [&](int x) { return xb + 8u * x; };
+  auto sfree_bar = [&](int x) { return xb + 8u * (2 + x); };
+  auto pfull_bar = [&](int x) { return xb + 8u * (4 + x); };
+  auto odone_bar = [&](int x) { return xb + 8u * (6 + x); };
+  auto qfull_bar = [&](int x) { return xb + 8u * (8 + x); };
+  auto ofree_bar = [&](int x) { return xb + 8u * (10 + x); };
+  const uint32_t drain_bar = xb + 8u * 12;
+  auto xmax_bar = [&](int x) { return xb + 8u * (13 + x); };
+  auto xsum_bar = [&](int x) { return xb + 8u * (15 + x); };
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(full_bar(s), kTcProducers);   // each producer warp arrives once per block
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(sfull_bar(x), 1);
+      mbar_init(sfree_bar(x), kTcSoftmaxWarps);
+      mbar_init(pfull_bar(x), kTcSoftmaxWarps);
+      mbar_init(odone_bar(x), 1);
+      mbar_init(qfull_bar(x), kTcSoftmaxWarps);
+      if (x == 0) mbar_init(ofree_bar(x), kTcSoftmaxWarps);   // O is single: one barrier
+      mbar_init(xmax_bar(x), kTcSoftmaxWarps);
+      mbar_init(xsum_bar(x), kTcSoftmaxWarps);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int NC = p.NC;   // == Hkv (one KV head per unit)
+  const int64_t X = static_cast<int64_t>(NC) * s_pre[B];
+  int64_t ng64 = (X + p.min_pages - 1) / p.min_pages;
+  if (ng64 < 1) ng64 = 1;
+  const int NG = static_cast<int>(ng64 < gridDim.x ? ng64 : gridDim.x);
+  grid_launch_dependents();
+
+  const int g = blockIdx.x;
+  if (g >= NG || X == 0) return;
+  const int64_t start = static_cast<int64_t>(g) * X / NG;
+  const int64_t end = static_cast<int64_t>(g + 1) * X / NG;
+  const int64_t count = end - start;
+  if (count <= 0) return;
+
+  if (warp == kTcMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTcCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = warp_uniform(s_tmem);
+
+  const int G = p.G;
+  constexpr uint32_t half_stride = kTcHalf;
+  const uint32_t stage0 = base + p.off_stage;
+
+  if (warp < kTcProducers) {
+    // ============================ producers ================================
+    BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
+    BlockTableCache btc;
+    int stage = 0;
+    uint32_t round = 0;
+    while (wk.more()) {
+      const TcBlock t = wk.next(s_pre, B, NC);
+      if (round > 0 && !warp_wait(empty_bar(stage), (round - 1) & 1u)) {
+        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        break;
+      }
+      // The block's 2 * NH boxes per page are dealt round-robin over the three
+      // producer warps, one box per lane (box x = 3 * lane + warp), so each
+      // warp issues its share with one TMA instruction; each warp announces
+      // its bytes with its own arrival, before its copies.
+      constexpr int BPP = 2 * TG::NH;                // boxes per page: K and V, each NH halves
+      const int nbox = t.np * BPP;
+      const int mine = nbox > warp ? (nbox - warp + kTcProducers - 1) / kTcProducers : 0;
+      if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(mine) * kTcBox);
+      __syncwarp();
+      int phys[kTcMaxBlockPages];
+#pragma unroll
+      for (int pg = 0; pg < kTcMaxBlockPages; ++pg) {
+        phys[pg] = 0;
+        if (pg < t.np) {
+          Cursor pc;
+          pc.i = t.i;
+          pc.c = t.c;
+          pc.j = t.j0 + pg;
+          pc.n = t.n;
+          phys[pg] = btc.lookup(p, pc, s_pre, s_len, s_qsl, B, NC, window, lane);
+          if ((phys[pg] < 0 || phys[pg] >= p.num_pages) && lane == 0 && warp == 0) atomicOr(p.err, kErrPageRange);
+        }
+      }
+      const int x = kTcProducers * lane + warp;
+      if (x < nbox) {
+        const int pg = x / BPP;
+        const int kind = x - pg * BPP;
+        const int tensor = kind / TG::NH;
+        const int h = kind - tensor * TG::NH;
+        int ph = phys[0];
+#pragma unroll
+        for (int q = 1; q < kTcMaxBlockPages; ++q) ph = pg == q ? phys[q] : ph;
+        const uint32_t sb = stage0 + static_cast<uint32_t>(stage) * p.stage_bytes;
+        const uint32_t dst = sb + static_cast<uint32_t>(tensor * TG::NH + h) * half_stride + static_cast<uint32_t>(pg) * kTcBox;
+        // An out-of-range page id reads as zeros (TMA fills outside the tensor).
+        tma_load_4d(dst, tensor ? &tmap_v : &tmap_k, h * 64, 0, t.c, ph, full_bar(stage));
+      }
+      if (++stage == nstage) {
+        stage = 0;
+        ++round;
+      }
+    }
+  } else if (warp == kTcMmaWarp) {
+    // ============================ MMA issuer ===============================
+    const uint32_t idesc_s_base = umma_idesc_bf16(128, 16, false) & ~(0x3Fu << 17);
+    const uint32_t idesc_o = umma_idesc_bf16(128, D, true);
+    BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
+    int stage = 0;
+    uint32_t round = 0;
+    int b = 0, seg = -1;
+    // the previous block, whose P V is issued after this block's Q K^T
+    int pv_stage = 0, pv_np = 0, pv_seg = 0, pv_vt = 16;
+    bool pv_valid = false, pv_first = false;
+    bool ok = true;
+    auto issue_pv = [&](int bb) -> bool {
+      if (!warp_wait(pfull_bar(bb & 1), static_cast<uint32_t>(bb >> 1) & 1u)) return false;
+      // O is overwritten by a segment's first P V: the previous segment's
+      // epilogue must have read it.
+      if (pv_first && pv_seg >= 1 && !warp_wait(ofree_bar(0), static_cast<uint32_t>(pv_seg - 1) & 1u)) return false;
+      const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(pv_stage) * p.stage_bytes);
+      if (pv_vt < kPage) {
+        // Rows past the context in the unit's last page: zero them so that
+        // whatever the pool holds there cannot reach O through 0 * NaN.
+        uint8_t* const vg = gbase + (sb - base) + TG::NH * half_stride + (pv_np - 1) * kTcBox;
+        const int nbytes = (kPage - pv_vt) * 128;
+        for (int h = 0; h < TG::NH; ++h)
+          for (int o = lane * 16; o < nbytes; o += 32 * 16)
+            *reinterpret_cast<uint4*>(vg + h * half_stride + pv_vt * 128 + o) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      const uint64_t vd0 = umma_sdesc_sw128(sb + TG::NH * half_stride, half_stride, 1024u);
+      const uint32_t tO = tbase + kTmemO;
+      const uint32_t tP = warp_uniform(tbase + kTmemP + 32u * static_cast<uint32_t>(bb & 1));
+      const uint32_t tPlo = tP + (kTmemPlo - kTmemP);
+      if (lane == 0) {
+#pragma unroll
+        for (int pg = 0; pg < kTcMaxBlockPages; ++pg) {
+          if (pg < pv_np) {
+            const uint64_t vd = vd0 + static_cast<uint64_t>((pg * kTcBox) >> 4);
+            umma_ts(tO, tP + 8u * pg, vd, idesc_o, !(pv_first && pg == 0));
+            umma_ts(tO, tPlo + 8u * pg, vd, idesc_o, true);
+          }
+        }
+        umma_commit(odone_bar(bb & 1));
+        umma_commit(empty_bar(pv_stage));
+      }
+      __syncwarp();
+      return true;
+    };
+    while (wk.more()) {
+      const TcBlock t = wk.next(s_pre, B, NC);
+      if (t.first) ++seg;
+      if (!warp_wait(full_bar(stage), round & 1u) ||
+          (b >= 2 && !warp_wait(sfree_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u)) ||
+          (t.first && !warp_wait(qfull_bar(seg & 1), static_cast<uint32_t>(seg >> 1) & 1u))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const uint32_t tQ = warp_uniform(tbase + kTmemQ + 64u * static_cast<uint32_t>(seg & 1));
+        const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(stage) * p.stage_bytes);
+        const uint64_t kd = umma_sdesc_sw128(sb, 16u, 1024u);
+        const uint32_t idesc_s = warp_uniform(idesc_s_base | (static_cast<uint32_t>(2 * t.np) << 17));   // N = 16 * np
+        const uint32_t tS = warp_uniform(tbase + kTmemS + 64u * static_cast<uint32_t>(b & 1));
+        if (lane == 0) {
+#pragma unroll
+          for (int s = 0; s < TG::KSTEPS; ++s) umma_ts(tS, tQ + 8u * s, kd + k_step(s), idesc_s, s > 0);
+          umma_commit(sfull_bar(b & 1));
+        }
+      }
+      __syncwarp();
+      if (pv_valid && !issue_pv(b - 1)) {
+        ok = false;
+        break;
+      }
+      pv_valid = true;
+      pv_stage = stage;
+      pv_np = t.np;
+      pv_seg = seg;
+      pv_first = t.first;
+      pv_vt = kPage;
+      if (t.j0 + t.np == t.n) {
+        const SeqInfo si = seq_info(p, s_len, s_qsl, t.i, false, window);
+        pv_vt = si.L - kPage * (si.js + t.n - 1);
+      }
+      ++b;
+      if (++stage == nstage) {
+        stage = 0;
+        ++round;
+      }
+    }
+    if (ok && pv_valid && !issue_pv(b - 1)) ok = false;
+    if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
+    // Every MMA this CTA issued must be complete before tensor memory is freed.
+    if (lane == 0) umma_commit(drain_bar);
+    __syncwarp();
+    if (!warp_wait(drain_bar, 0u) && lane == 0) atomicOr(p.err, kErrTimeout);
+  } else {
+    // ============================ softmax ==================================
+    // Two warps per TMEM lane quarter: warp sw = warp - 4 owns rows
+    // 32 * (sw % 4) .. +31 and half hf = sw / 4 of every block (pages 2hf and
+    // 2hf+1) and of O's columns.  The two warps of a row exchange their partial
+    // row max every block, and their partial sums at a segment's end, through
+    // shared memory and a bounded mbarrier round.
+    const int sw = warp - kTcSoftmaxWarp0;
+    const int q4 = warp & 3;               // TMEM lane quarter this warp may access (== sw % 4)
+    const int hf = sw >> 2;
+    const int rho = 32 * q4 + lane;        // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+    float* const xmax = reinterpret_cast<float*>(gbase + p.off_xchg);   // [block % 2][half][128] partial max
+    float* const xsum = xmax + 512;                                     // [segment % 2][half][128] partial sum
+    constexpr int HD = D / 2;              // O columns per half
+    BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
+    int b = 0, seg = -1;
+    SeqInfo si = {0, 0, 0, 0};
+    bool row_ok = false;
+    int lim = 0, seg_j0 = 0;
+    int64_t seg_k0 = 0;
+    float m = -INFINITY, l = 0.f;          // running max (log2 units, shared by both halves), this half's sum
+    bool ok = true;
+
+    // This thread's half of row rho of the segment starting at block t, into
+    // TMEM Q slot `slot` (rows past G * qn are zero); q_full counts the 8 warps.
+    auto stage_q = [&](const TcBlock& t, int slot) {
+      const SeqInfo s2 = seq_info(p, s_len, s_qsl, t.i, false, window);
+      const bool have = rho < G * s2.qn;
+      const uint4* src = nullptr;
+      if (have)
+        src = reinterpret_cast<const uint4*>(p.q + static_cast<int64_t>(s2.t0 + rho / G) * p.q_stride_t +
+                                             static_cast<int64_t>(t.c * G + rho % G) * D);
+      const uint32_t tq = tbase + lane_off + kTmemQ + 64u * static_cast<uint32_t>(slot) + (D / 4) * hf;
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) {      // 16 columns (32 features) at a time
+        uint32_t w[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = have ? src[(D / 16) * hf + 4 * k + u] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * u] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
+        }
+        tmem_st16(tq + 16u * k, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qfull_bar(slot));
+    };
+
+    while (wk.more()) {
+      const TcBlock t = wk.next(s_pre, B, NC);
+      if (t.first) {
+        ++seg;
+        if (seg == 0) stage_q(t, 0);
+        si = seq_info(p, s_len, s_qsl, t.i, rho == 0 && hf == 0, window);
+        row_ok = rho < G * si.qn;
+        lim = si.L - si.qn + (row_ok ? rho / G : 0);
+        seg_j0 = t.j0;
+        seg_k0 = t.k0;
+        m = -INFINITY;
+        l = 0.f;
+        if (seg_j0 == 0 && rho == 0 && hf == 0) {
+          // This CTA holds the unit's first page: describe the unit for the merge.
+          const int64_t a = static_cast<int64_t>(NC) * s_pre[t.i] + static_cast<int64_t>(t.c) * t.n;
+          const int last_cta = static_cast<int>(((a + t.n) * NG - 1) / X);
+          const int pieces = last_cta - g + 1;
+          p.ws_unit[static_cast<int64_t>(t.i) * NC + t.c] =
+              make_int4(g, pieces | (t.k0 != 0 ? (1 << 30) : 0), si.t0, si.qn);
+        }
+        if (p.sinks != nullptr && seg_j0 == 0 && row_ok) {
+          // The sink is a virtual first key (logit sinks[hq], zero value row),
+          // counted once (in half 0's sum) by the piece holding the unit's first page.
+          m = p.sinks[t.c * G + rho % G] * 1.4426950408889634f;
+          l = hf == 0 ? 1.f : 0.f;
+        }
+      }
+      // ---- this half's S row of the block ----------------------------------
+      if (!warp_wait(sfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[2][16];
+      {
+        const uint32_t tS = tbase + lane_off + kTmemS + 64u * static_cast<uint32_t>(b & 1) + 32u * hf;
+        uint32_t r[2][16];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (2 * hf + k < t.np) tmem_ld16(tS + 16u * k, r[k]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) sv[k][e] = __uint_as_float(r[k][e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree_bar(b & 1));
+      // ---- mask, block max ---------------------------------------------------
+      // An interior block (all four pages present, every token visible to
+      // every row of the run, no window edge inside) needs no per-element
+      // mask: its max is taken over the raw scores and the scale is folded
+      // into the exponent's FFMA.  Rows past G * qn hold zero queries there
+      // and produce values nobody reads.
+      const int tb = kPage * (si.js + t.j0);
+      const float c = p.scale_log2;
+      bool interior = t.np == kTcMaxBlockPages && c > 0.f && tb + kTcMaxBlockPages * kPage <= si.L - si.qn + 1;
+      if (WINDOW && window > 0) interior = interior && tb > si.L - 1 - window;
+      float mp;
+      if (interior) {
+        float mx[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(sv[0][e], sv[1][e]);
+#pragma unroll
+        for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
+        mp = mx[0] * c;
+      } else {
+        mp = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int pg = 2 * hf + k;
+            const int tok = tb + 16 * pg + e;
+            bool vis = row_ok && pg < t.np && tok <= lim;
+            if (WINDOW && window > 0) vis = vis && tok > lim - window;
+            const float x = vis ? sv[k][e] * c : -INFINITY;
+            sv[k][e] = x;
+            mp = fmaxf(mp, x);
+          }
+      }
+      // partner's half of the row max
+      xmax[(b & 1) * 256 + hf * 128 + rho] = mp;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xmax_bar(b & 1));
+      if (!warp_wait(xmax_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      const float mb = fmaxf(mp, xmax[(b & 1) * 256 + (hf ^ 1) * 128 + rho]);
+      const float m_new = fmaxf(m, mb);
+      const bool grow = m_new > m + 8.f;   // also true when m = -inf and m_new is finite
+      if (t.first) {
+        if (grow) {
+          l *= fast_exp2(m - m_new);       // sink only: O has no history in this segment
+          m = m_new;
+        }
+      } else if (__any_sync(0xffffffffu, grow)) {
+        // O must hold P V of the previous block before it is rescaled.
+        if (!warp_wait(odone_bar((b - 1) & 1), static_cast<uint32_t>((b - 1) >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = grow ? fast_exp2(m - m_new) : 1.f;
+        const uint32_t tO = tbase + lane_off + kTmemO + HD * hf;
+#pragma unroll
+        for (int ch = 0; ch < HD / 16; ++ch) {
+          uint32_t r[16];
+          tmem_ld16(tO + 16u * ch, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st16(tO + 16u * ch, r);
+        }
+        tmem_wait_st();
+        if (grow) {
+          l *= alpha;
+          m = m_new;
+        }
+      }
+      // ---- P (bf16 hi + lo) into TMEM ------------------------------------------
+      // P[b%2] was last read by the P V of block b-2.
+      if (b >= 2 && !warp_wait(odone_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        // exp2 of -inf is +0, so masked scores need no select once the
+        // subtracted max is finite (it is -inf only while no key was visible).
+        const float mneg = m == -INFINITY ? 0.f : -m;
+        const float mult = interior ? c : 1.f;   // masked scores are already scaled
+        const uint32_t tP = tbase + lane_off + kTmemP + 32u * static_cast<uint32_t>(b & 1) + 16u * hf;
+        const uint32_t tPlo = tP + (kTmemPlo - kTmemP);
+        float lsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (2 * hf + k < t.np) {
+            uint32_t w[8], wl[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float a0 = fast_exp2(fmaf(sv[k][2 * e], mult, mneg));
+              const float a1 = fast_exp2(fmaf(sv[k][2 * e + 1], mult, mneg));
+              w[e] = pack_bf16(a0, a1);
+              wl[e] = pack_bf16(a0 - bf16_lo(w[e]), a1 - bf16_hi(w[e]));   // exact residues, rounded once
+              lsum += a0 + a1;
+            }
+            tmem_st8(tP + 8u * k, w);
+            tmem_st8(tPlo + 8u * k, wl);
+          }
+        }
+        l += lsum;
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull_bar(b & 1));
+
+      if (t.last) {
+        // The next segment's Q goes into the other slot now, so its S can be
+        // computed while this segment's output is written.
+        if (wk.more()) {
+          BlockWalker peek = wk;
+          const TcBlock nt = peek.next(s_pre, B, NC);
+          stage_q(nt, (seg + 1) & 1);
+        }
+        // the row's total sum
+        xsum[(seg & 1) * 256 + hf * 128 + rho] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xsum_bar(seg & 1));
+        if (!warp_wait(xsum_bar(seg & 1), static_cast<uint32_t>(seg >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        const float lt = l + xsum[(seg & 1) * 256 + (hf ^ 1) * 128 + rho];
+        if (!warp_wait(odone_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool complete = (seg_j0 == 0) && (t.j0 + t.np == t.n);
+        const uint32_t tO = tbase + lane_off + kTmemO + HD * hf;
+        const int tok = si.t0 + rho / G;
+        const int hq = t.c * G + rho % G;
+        const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
+        uint16_t* orow =
+            p.out + static_cast<int64_t>(tok) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h + HD * hf;
+        const int which = (seg_k0 == 0) ? 0 : 1;
+        const int64_t prow = static_cast<int64_t>(2 * g + which) * p.R_max + rho;
+        float* wrow = p.ws_o + prow * D + HD * hf;
+#pragma unroll
+        for (int ch = 0; ch < HD / 16; ++ch) {
+          uint32_t r[16];
+          tmem_ld16(tO + 16u * ch, r);
+          tmem_wait_ld();
+          if (row_ok) {
+            if (complete) {
+#pragma unroll
+              for (int e = 0; e < 16; e += 4) {
+                uint2 v;
+                v.x = pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
+                v.y = pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+                *reinterpret_cast<uint2*>(orow + 16 * ch + e) = v;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4*>(wrow + 16 * ch + e) =
+                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                __uint_as_float(r[e + 3]));
+            }
+          }
+        }
+        if (row_ok && hf == 0) {
+          if (complete) {
+            if (p.lse != nullptr)
+              p.lse[static_cast<int64_t>(tok) * p.lse_stride_t + static_cast<int64_t>(hq) * p.lse_stride_h] =
+                  lt > 0.f ? (m + fast_log2(lt)) * 0.69314718055994530942f : -INFINITY;
+          } else {
+            p.ws_ml[prow] = make_float2(m, lt);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ofree_bar(0));
+      }
+      ++b;
+    }
+    if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kTcMmaWarp) tmem_dealloc(tbase, kTcCols);
+}
+
+}  // namespace pa

@@ -64,9 +64,9 @@ class WorkloadSpec:
         return 1.0 / math.sqrt(self.head_dim)
 
 
-# The five decode regimes: a tiny parity case, a Llama-3-8B-shaped batch, a
-# single long-context user, an fp8-KV batch at batch 256 and an MTP
-# verification batch with ragged query runs.
+# The decode regimes: a tiny parity case, a Llama-3-8B-shaped batch, a single
+# long-context user, an fp8-KV batch at batch 256, an MTP verification batch
+# with ragged query runs, and a longer verification batch.
 CONFIGS = {
     "tiny": WorkloadSpec(
         name="tiny", num_seqs=4, num_q_heads=8, num_kv_heads=2, head_dim=128,
@@ -86,9 +86,16 @@ CONFIGS = {
         name="mtp", num_seqs=32, num_q_heads=64, num_kv_heads=8, head_dim=128,
         kv_dtype="bf16", seq_len_kind="uniform", seq_len_args=(1024, 16384),
         query_len_choices=(2, 3, 4), seed=1004),
+    # Longer speculative verification: runs of 1 + up to 7 draft tokens over a
+    # 16-query-head group (Llama-3-405B-shaped heads, 128 over 8), so a KV
+    # head serves up to 128 query rows, a dense tile for the tensor cores.
+    "verify8": WorkloadSpec(
+        name="verify8", num_seqs=32, num_q_heads=128, num_kv_heads=8, head_dim=128,
+        kv_dtype="bf16", seq_len_kind="uniform", seq_len_args=(1024, 16384),
+        query_len_choices=(2, 3, 4, 5, 6, 7, 8), seed=1005),
 }
 
-CONFIG_ORDER = ["tiny", "llama3_8b", "batch1_32k", "fp8", "mtp"]
+CONFIG_ORDER = ["tiny", "llama3_8b", "batch1_32k", "fp8", "mtp", "verify8"]
 
 
 @dataclasses.dataclass

@@ -93,13 +93,48 @@ def test_invalid_arguments_rejected_on_host(lib, mutate, expect):
     assert binding.paged_attn_last_error_message() != ""
 
 
-def test_group_times_query_len_over_64_is_unsupported(lib):
-    a = _good_args(T=6, Hq=32, Hkv=1)
-    a["k"] = torch.zeros(10, 16, 1, 128, dtype=torch.bfloat16)
-    a["v"] = torch.zeros(10, 16, 1, 128, dtype=torch.bfloat16)
-    a["qsl"] = torch.tensor([0, 2, 4, 6], dtype=torch.int32)
-    a["max_qlen"] = 3
-    assert _call(lib, a) == binding.PA_ERR_UNSUPPORTED
+def _rows_args(max_qlen, kv):
+    """G = 32 query heads on one KV head; three sequences of max_qlen tokens."""
+    a = _good_args(T=3 * max_qlen, Hq=32, Hkv=1)
+    a["k"] = torch.zeros(10, 16, 1, 128, dtype=kv)
+    a["v"] = torch.zeros(10, 16, 1, 128, dtype=kv)
+    a["qsl"] = torch.arange(0, 3 * max_qlen + 1, max_qlen, dtype=torch.int32)
+    a["max_qlen"] = max_qlen
+    return a
+
+
+def test_more_than_128_rows_per_kv_head_is_unsupported(lib):
+    assert _call(lib, _rows_args(5, torch.bfloat16)) == binding.PA_ERR_UNSUPPORTED   # 160 rows
+    assert "128" in binding.paged_attn_last_error_message()
+
+
+def test_fp8_cache_over_64_rows_is_unsupported(lib):
+    assert _call(lib, _rows_args(3, torch.float8_e4m3fn)) == binding.PA_ERR_UNSUPPORTED   # 96 rows
+    assert "64" in binding.paged_attn_last_error_message()
+
+
+def test_bf16_cache_up_to_128_rows_passes_host_validation(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # 96 and 128 rows pass every host check; without a GPU the call then fails
+    # at device set-up.
+    for ql in (3, 4):
+        assert _call(lib, _rows_args(ql, torch.bfloat16)) == binding.PA_ERR_CUDA
+
+
+def _plan_status(lib, use_tcgen05, kv=binding.PA_BF16, Hq=8, max_qlen=1, heads_per_cta=0):
+    opts = binding.make_options(use_tcgen05=use_tcgen05, heads_per_cta=heads_per_cta)
+    plan = binding.PaPlan()
+    return lib.paged_attn_plan(4, Hq, 1, 128, kv, max_qlen, ctypes.byref(opts), ctypes.byref(plan))
+
+
+def test_tcgen05_switch_checked_on_the_host(lib):
+    for bad in (-1, 3):
+        assert _plan_status(lib, bad) == binding.PA_ERR_INVALID_ARG
+    # forced on for an fp8 cache, forced off above 64 rows, more than one head per CTA
+    assert _plan_status(lib, 2, kv=binding.PA_FP8_E4M3) == binding.PA_ERR_UNSUPPORTED
+    assert _plan_status(lib, 1, Hq=32, max_qlen=3) == binding.PA_ERR_UNSUPPORTED
+    assert _plan_status(lib, 0, Hq=32, max_qlen=3, heads_per_cta=2) == binding.PA_ERR_UNSUPPORTED
 
 
 def test_null_descriptor_pointer(lib):

@@ -260,3 +260,32 @@ def test_attention_sinks(kv, window, num_ctas):
     ref = oracle.run_workload(w, sliding_window=window, sinks=sinks)
     kw = dict(num_ctas=num_ctas, min_pages_per_cta=1) if num_ctas else None
     _check_opts(w, window=window, sinks=sinks, options_kw=kw, ref=ref)
+
+
+def test_split_timing_events_direct_and_captured():
+    """split_start_event / split_stop_event bracket the split kernel both in a
+    direct call and inside a captured graph (where they become event nodes)."""
+    w = wl.make_workload(_spec(seq_lens=(300, 900, 40), G=4, Hkv=2), device="cuda")
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(); b.record()                      # torch times only events it has recorded once
+    torch.cuda.synchronize()
+    opts = binding.make_options(split_start_event=a, split_stop_event=b)
+    out, lse = binding.decode_workload(w, options=opts)
+    b.synchronize()
+    assert a.elapsed_time(b) > 0.0
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    s = w.spec
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        binding.paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, None, 1, s.scale, out=out2, lse=lse2,
+                                  options=opts, stream=cap)
+    g.replay()
+    b.synchronize()
+    assert a.elapsed_time(b) > 0.0
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
