@@ -10,6 +10,15 @@ unchanged; fp8 caches take e4m3fn codes of ``float32(x) * r`` with
 ``r = float32(1) / float32(scale)`` (one fp32 scale per tensor, its reciprocal
 rounded once to fp32).
 
+Per-token quantisation (the pages' ``reshape_and_cache_with_pertoken_quant``,
+FP8 KV cache write of MHA layers): every written (token, KV head) row gets its
+own scale.  Readings adopted: the row's scale is ``float32(amax) / 448`` with
+``amax = max_d |x_d|`` (448 = the largest finite e4m3fn magnitude), one IEEE
+fp32 division; the codes are ``e4m3fn(float32(x) * r)`` with
+``r = float32(448) / float32(amax)`` (one fp32 division, so the largest element
+lands on +-448 up to one rounding); an all-zero row stores scale 0 and zero
+codes.  Scales are stored ``[num_pages, num_kv_heads, 16]`` float32.
+
 Readings adopted where the pages are silent: the scale is applied as one fp32
 multiplication by its fp32 reciprocal (it differs from an IEEE division only
 when x / scale falls within one fp32 ulp of an e4m3 rounding boundary); the
@@ -77,3 +86,41 @@ def cache_write(key_bits, value_bits, slot_mapping, k_cache, v_cache, k_scale=1.
             k_out[page, off] = quantize_rows(key_bits[t], k_scale)
             v_out[page, off] = quantize_rows(value_bits[t], v_scale)
     return k_out, v_out
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_rows_per_token(bits: np.ndarray):
+    """bf16 rows [..., D] -> (e4m3fn codes [..., D], float32 scales [...]).
+
+    amax = max_d |x_d|; scale = float32(amax) / float32(448);
+    codes = e4m3fn(float32(x) * (float32(448) / float32(amax))), or zeros with
+    scale 0 when amax == 0."""
+    x32 = bf16_bits_to_float64(bits).astype(np.float32)
+    amax = np.abs(x32).max(axis=-1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        r = np.where(amax > 0, np.float32(E4M3_MAX) / np.where(amax > 0, amax, np.float32(1)), np.float32(0))
+    y32 = (x32 * r.astype(np.float32)[..., None]).astype(np.float32)
+    return e4m3fn_encode(y32.astype(np.float64)), scale
+
+
+def cache_write_per_token(key_bits, value_bits, slot_mapping, k_cache, v_cache, k_scales, v_scales):
+    """Per-token fp8 write: new (k_cache, v_cache, k_scales, v_scales).
+
+    key_bits/value_bits uint16 bf16 [T, Hkv, D]; caches uint8 [NB, 16, Hkv, D];
+    scales float32 [NB, Hkv, 16].  Slots as in ``cache_write``."""
+    k_out, v_out = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    ks_out = np.array(k_scales, dtype=np.float32, copy=True)
+    vs_out = np.array(v_scales, dtype=np.float32, copy=True)
+    NB = k_out.shape[0]
+    for t, s in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if not 0 <= s < NB * PAGE_SIZE:        # padding or past the pool
+            continue
+        page, off = divmod(int(s), PAGE_SIZE)
+        kc, ksc = quantize_rows_per_token(key_bits[t])          # [Hkv, D], [Hkv]
+        vc, vsc = quantize_rows_per_token(value_bits[t])
+        k_out[page, off], v_out[page, off] = kc, vc
+        ks_out[page, :, off], vs_out[page, :, off] = ksc, vsc
+    return k_out, v_out, ks_out, vs_out

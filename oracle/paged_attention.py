@@ -24,6 +24,11 @@ notes):
 * fp8 is OCP e4m3fn; a cached value is ``code * k_scale`` (K) or
   ``code * v_scale`` (V) with one fp32 scale per tensor; bf16 caches carry no
   scale;
+* per-token fp8 scales (the pages' ``reshape_and_cache_with_pertoken_quant``
+  write): one fp32 scale per cached (token slot, KV head) row, stored
+  ``[num_pages, num_kv_heads, 16]``; the row's value is
+  ``code * tensor_scale * token_scale`` (the per-tensor scale still multiplies;
+  callers of a purely per-token cache pass 1.0);
 * ``lse`` is the natural-log log-sum-exp of the scaled logits;
 * sliding window W (``sliding_window`` > 0; the pages' models with
   ``sliding_window != -1``): query row r sees keys ``p_r - W < j <= p_r``;
@@ -70,15 +75,29 @@ def e4m3fn_to_float64(codes: np.ndarray) -> np.ndarray:
     return out.astype(np.float64)
 
 
-def dequantize(raw: np.ndarray, kv_dtype: str, tensor_scale: float) -> np.ndarray:
+def dequantize(raw: np.ndarray, kv_dtype: str, tensor_scale: float, token_scales=None) -> np.ndarray:
     """Cached element -> float64.  bf16: the value itself.  fp8: code value
     times the tensor's scale, the scale taken as the fp32 number the kernel
-    receives."""
+    receives, and times the row's own fp32 scale when ``token_scales`` (one
+    per row of ``raw``) is given."""
     if kv_dtype == "bf16":
         return bf16_bits_to_float64(raw)
     if kv_dtype == "fp8":
-        return e4m3fn_to_float64(raw) * np.float64(np.float32(tensor_scale))
+        v = e4m3fn_to_float64(raw) * np.float64(np.float32(tensor_scale))
+        if token_scales is not None:
+            v = v * np.asarray(token_scales, dtype=np.float32).astype(np.float64)[:, None]
+        return v
     raise ValueError(kv_dtype)
+
+
+def gather_token_scales(scales: np.ndarray, block_table_row: np.ndarray, seq_len: int,
+                        kv_head: int) -> np.ndarray:
+    """Per-token scales ``[num_pages, num_kv_heads, 16]`` of one KV head for
+    logical tokens 0..seq_len-1 (token j: page ``block_table_row[j // 16]``,
+    slot ``j % 16``)."""
+    tok = np.arange(seq_len)
+    pages = np.asarray(block_table_row)[tok // PAGE_SIZE].astype(np.int64)
+    return np.asarray(scales)[pages, kv_head, tok % PAGE_SIZE]
 
 
 def gather_sequence(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int,
@@ -126,7 +145,8 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
                            block_tables: np.ndarray, seq_lens: np.ndarray,
                            query_start_loc, scale: float, k_scale: float = 1.0,
                            v_scale: float = 1.0, kv_dtype: str = "bf16",
-                           seqs=None, sliding_window: int = 0, sinks=None):
+                           seqs=None, sliding_window: int = 0, sinks=None,
+                           k_token_scales=None, v_token_scales=None):
     """Decode attention for a batch.
 
     q_bits      uint16 bf16 patterns [T, Hq, D]
@@ -137,6 +157,8 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
                 left as NaN), for sampled checks of large batches.
     sliding_window  W > 0: each query sees only its last W positions (0 = off)
     sinks       optional float [Hq] per-query-head sink logits (taken as fp32)
+    k_token_scales, v_token_scales  optional float32 [NB, Hkv, 16] per-token
+                scales of fp8 caches (both or neither)
 
     Returns (out float64 [T, Hq, D], lse float64 [T, Hq]).
     """
@@ -160,8 +182,12 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
         assert 1 <= qn <= L
         limits = L - qn + np.arange(qn)          # last key index each query token sees
         for hk in range(Hkv):
-            K = dequantize(gather_sequence(k_cache, block_tables[i], L, hk), kv_dtype, k_scale)
-            V = dequantize(gather_sequence(v_cache, block_tables[i], L, hk), kv_dtype, v_scale)
+            ks = vs = None
+            if k_token_scales is not None:
+                ks = gather_token_scales(k_token_scales, block_tables[i], L, hk)
+                vs = gather_token_scales(v_token_scales, block_tables[i], L, hk)
+            K = dequantize(gather_sequence(k_cache, block_tables[i], L, hk), kv_dtype, k_scale, ks)
+            V = dequantize(gather_sequence(v_cache, block_tables[i], L, hk), kv_dtype, v_scale, vs)
             heads = np.arange(hk * G, (hk + 1) * G)
             qr = bf16_bits_to_float64(q_bits[t0:t1][:, heads, :])      # [qn, G, D]
             sk = None
@@ -175,9 +201,11 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
 
 def run_workload(w, seqs=None, sliding_window=0, sinks=None):
     """Oracle outputs for a ``paged_kv_decode_06_gb300.workloads.Workload``."""
-    from paged_kv_decode_06_gb300.workloads import host_arrays
+    from paged_kv_decode_06_gb300.workloads import host_arrays, host_token_scales
     q_bits, k, v = host_arrays(w)
     s = w.spec
+    ks, vs = host_token_scales(w)
     return paged_decode_attention(q_bits, k, v, w.block_tables, w.seq_lens,
                                   w.query_start_loc, s.scale, s.k_scale, s.v_scale,
-                                  s.kv_dtype, seqs=seqs, sliding_window=sliding_window, sinks=sinks)
+                                  s.kv_dtype, seqs=seqs, sliding_window=sliding_window, sinks=sinks,
+                                  k_token_scales=ks, v_token_scales=vs)

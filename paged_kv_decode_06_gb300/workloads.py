@@ -16,6 +16,10 @@ operations"; configuration guide, ``kv_cache_block_size``):
                    query tokens (their K/V are already in the cache)
 * ``query_start_loc`` int32 ``[B+1]`` cumulative query-token offsets, or
                    ``None`` when every sequence has exactly one query token.
+* ``k_token_scales``, ``v_token_scales`` (per-token fp8 workloads only) fp32
+                   ``[NB, Hkv, 16]``: one positive scale per cached row, drawn
+                   log-uniformly; the codes of such a cache are drawn from
+                   N(0,1) / fp8_source_scale clamped to the e4m3 range.
 
 Every page of the pool is filled with random data (never NaN), including the
 tail slots of a sequence's last page and the pages no sequence uses.
@@ -50,6 +54,7 @@ class WorkloadSpec:
     v_scale: float = 1.0
     fp8_source_scale: float = 1.0      # fp8 codes = e4m3(N(0,1) / fp8_source_scale)
     seed: int = 0
+    token_scale_range: Optional[tuple] = None   # fp8: per-token scales ~ log-U[lo, hi] (None = per-tensor only)
 
     @property
     def group_size(self) -> int:
@@ -86,6 +91,13 @@ CONFIGS = {
         name="mtp", num_seqs=32, num_q_heads=64, num_kv_heads=8, head_dim=128,
         kv_dtype="bf16", seq_len_kind="uniform", seq_len_args=(1024, 16384),
         query_len_choices=(2, 3, 4), seed=1004),
+    # fp8 cache quantised per token (one scale per cached row and KV head),
+    # the batch-256 shape of the per-tensor fp8 workload: codes spread over
+    # the e4m3 range, row scales log-uniform around 1/128.
+    "fp8_pertoken": WorkloadSpec(
+        name="fp8_pertoken", num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        kv_dtype="fp8", seq_len_kind="loguniform", seq_len_args=(128, 8192),
+        fp8_source_scale=1.0 / 128, token_scale_range=(0.5 / 128, 2.0 / 128), seed=1006),
     # Longer speculative verification: runs of 1 + up to 7 draft tokens over a
     # 16-query-head group (Llama-3-405B-shaped heads, 128 over 8), so a KV
     # head serves up to 128 query rows, a dense tile for the tensor cores.
@@ -95,7 +107,7 @@ CONFIGS = {
         query_len_choices=(2, 3, 4, 5, 6, 7, 8), seed=1005),
 }
 
-CONFIG_ORDER = ["tiny", "llama3_8b", "batch1_32k", "fp8", "mtp", "verify8"]
+CONFIG_ORDER = ["tiny", "llama3_8b", "batch1_32k", "fp8", "mtp", "verify8", "fp8_pertoken"]
 
 
 @dataclasses.dataclass
@@ -109,6 +121,8 @@ class Workload:
     q: torch.Tensor                 # bf16 [T, Hq, D]
     k_cache: torch.Tensor           # bf16 or uint8 (e4m3 codes) [NB, 16, Hkv, D]
     v_cache: torch.Tensor
+    k_token_scales: Optional[torch.Tensor] = None   # fp32 [NB, Hkv, 16] (per-token fp8 only)
+    v_token_scales: Optional[torch.Tensor] = None
 
     @property
     def num_tokens(self) -> int:
@@ -177,7 +191,7 @@ def _fill_normal(t: torch.Tensor, gen: torch.Generator, divisor: float, fp8: boo
         if divisor != 1.0:
             x = x / divisor
         if fp8:
-            flat[s:e] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+            flat[s:e] = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
         else:
             flat[s:e] = x.to(torch.bfloat16)
 
@@ -202,15 +216,21 @@ def make_workload(spec: WorkloadSpec, device: str = "cpu", seed: Optional[int] =
     div = spec.fp8_source_scale if fp8 else 1.0
     _fill_normal(k_cache, gen, div, fp8)
     _fill_normal(v_cache, gen, div, fp8)
+    ks = vs = None
+    if fp8 and spec.token_scale_range is not None:
+        lo, hi = (math.log(x) for x in spec.token_scale_range)
+        shape = (pool, spec.num_kv_heads, PAGE_SIZE)
+        ks = torch.exp(torch.rand(shape, generator=gen, device=device) * (hi - lo) + lo)
+        vs = torch.exp(torch.rand(shape, generator=gen, device=device) * (hi - lo) + lo)
     return Workload(spec=spec, seq_lens=seq_lens, query_lens=query_lens,
                     query_start_loc=qsl, block_tables=block_tables, num_pages=pool,
-                    q=q, k_cache=k_cache, v_cache=v_cache)
+                    q=q, k_cache=k_cache, v_cache=v_cache, k_token_scales=ks, v_token_scales=vs)
 
 
 def custom_spec(name="custom", num_seqs=None, num_q_heads=4, num_kv_heads=2, head_dim=64,
                 kv_dtype="bf16", seq_lens=(5, 16, 33), query_len_choices=(1,),
                 pool_pages=None, k_scale=1.0, v_scale=1.0, fp8_source_scale=1.0,
-                seed=7) -> WorkloadSpec:
+                seed=7, token_scale_range=None) -> WorkloadSpec:
     """A small spec with explicit sequence lengths (for edge cases)."""
     return WorkloadSpec(name=name, num_seqs=len(seq_lens) if num_seqs is None else num_seqs,
                         num_q_heads=num_q_heads,
@@ -218,7 +238,7 @@ def custom_spec(name="custom", num_seqs=None, num_q_heads=4, num_kv_heads=2, hea
                         seq_len_kind="fixed", seq_len_args=tuple(seq_lens),
                         query_len_choices=tuple(query_len_choices), pool_pages=pool_pages,
                         k_scale=k_scale, v_scale=v_scale, fp8_source_scale=fp8_source_scale,
-                        seed=seed)
+                        seed=seed, token_scale_range=token_scale_range)
 
 
 def host_arrays(w: Workload):
@@ -232,3 +252,11 @@ def host_arrays(w: Workload):
         k = w.k_cache.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
         v = w.v_cache.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     return q_bits, k, v
+
+
+def host_token_scales(w: Workload):
+    """Host float32 copies of the per-token scales, or (None, None)."""
+    if w.k_token_scales is None:
+        return None, None
+    return (w.k_token_scales.detach().cpu().contiguous().numpy(),
+            w.v_token_scales.detach().cpu().contiguous().numpy())

@@ -87,6 +87,89 @@ def test_out_of_range_slots_write_nothing():
     assert k2[0, 5].tolist() == [[0x3F80] * 4] and int(k2.sum()) == 4 * 0x3F80
 
 
+# ------------------------------------------------- per-token quantisation
+
+def _bf16_bits(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_per_token_quantize_matches_torch_ops():
+    rng = np.random.default_rng(8)
+    x = rng.normal(size=(50, 4, 64)) * np.exp(rng.uniform(-8, 8, size=(50, 4, 1)))
+    bits = _bf16_bits(x)
+    codes, scales = oracle.quantize_rows_per_token(bits)
+    xt = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float()
+    amax = xt.abs().amax(dim=-1)
+    ref_scale = amax / 448.0
+    r = torch.tensor(448.0) / amax
+    ref_codes = (xt * r[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(scales, ref_scale.numpy())
+    assert np.array_equal(codes, ref_codes)
+
+
+def test_per_token_row_max_lands_on_the_top_code():
+    bits = _bf16_bits([[0.25, -3.0, 1.5, 2.0], [1.0, 7.0, -7.0, 0.0]])
+    codes, scales = oracle.quantize_rows_per_token(bits)
+    assert codes[0, 1] == 0xFE and set(codes[1, 1:3].tolist()) == {0x7E, 0xFE}
+    assert scales[0] == np.float32(3.0) / np.float32(448.0)
+    deq = oracle.e4m3fn_to_float64(codes) * scales[:, None].astype(np.float64)
+    assert abs(deq[0, 1] + 3.0) <= 3.0 * 2.0 ** -23 and abs(deq[1, 1] - 7.0) <= 7.0 * 2.0 ** -23
+
+
+def test_per_token_zero_row_and_power_of_two_rows():
+    zero = np.zeros((1, 8), dtype=np.uint16)
+    codes, scales = oracle.quantize_rows_per_token(zero)
+    assert scales[0] == 0.0 and not codes.any()
+    rng = np.random.default_rng(9)
+    x = rng.normal(size=(1, 32)).astype(np.float32)
+    c1, s1 = oracle.quantize_rows_per_token(_bf16_bits(x))
+    c2, s2 = oracle.quantize_rows_per_token(_bf16_bits(x * 2.0 ** 20))      # exact in bf16
+    assert np.array_equal(c1, c2) and s2[0] == s1[0] * np.float32(2.0 ** 20)
+
+
+def test_per_token_round_trip_error_bound():
+    # e4m3fn keeps 3 mantissa bits: |deq - x| <= 2^-4 |x| on the normal range,
+    # and <= 2^-10 * scale on the subnormal one (plus fp32 rounding of r)
+    rng = np.random.default_rng(10)
+    x = rng.normal(size=(200, 128)) * np.exp(rng.uniform(-5, 5, size=(200, 1)))
+    bits = _bf16_bits(x)
+    xv = oracle.bf16_bits_to_float64(bits)
+    codes, scales = oracle.quantize_rows_per_token(bits)
+    deq = oracle.e4m3fn_to_float64(codes) * scales[:, None].astype(np.float64)
+    bound = np.maximum(2.0 ** -4 * np.abs(xv), 2.0 ** -10 * scales[:, None]) * (1 + 2.0 ** -20) + 1e-30
+    assert (np.abs(deq - xv) <= bound).all()
+
+
+def test_per_token_scatter_against_page_offset_arithmetic():
+    rng = np.random.default_rng(12)
+    T, Hkv, D, NB = 29, 3, 16, 7
+    kb = _bf16_bits(rng.normal(size=(T, Hkv, D)))
+    vb = _bf16_bits(rng.normal(size=(T, Hkv, D)) * 5)
+    slots = rng.permutation(NB * 16)[:T].astype(np.int32)
+    slots[[2, 9]] = -1
+    slots[5] = NB * 16 + 3                                       # past the pool: skipped
+    kc = rng.integers(0, 256, size=(NB, 16, Hkv, D)).astype(np.uint8)
+    vc = rng.integers(0, 256, size=(NB, 16, Hkv, D)).astype(np.uint8)
+    ks = rng.uniform(size=(NB, Hkv, 16)).astype(np.float32)
+    vs = rng.uniform(size=(NB, Hkv, 16)).astype(np.float32)
+    k2, v2, ks2, vs2 = oracle.cache_write_per_token(kb, vb, slots, kc, vc, ks, vs)
+    fk, fv = kc.reshape(NB * 16, Hkv, D).copy(), vc.reshape(NB * 16, Hkv, D).copy()
+    fks, fvs = ks.transpose(0, 2, 1).reshape(NB * 16, Hkv).copy(), vs.transpose(0, 2, 1).reshape(NB * 16, Hkv).copy()
+    for t in range(T):
+        if not 0 <= slots[t] < NB * 16:
+            continue
+        for h in range(Hkv):
+            xk = torch.from_numpy(kb[t, h].view(np.int16)).view(torch.bfloat16).float()
+            xv = torch.from_numpy(vb[t, h].view(np.int16)).view(torch.bfloat16).float()
+            for x, fc, fs in ((xk, fk, fks), (xv, fv, fvs)):
+                amax = x.abs().max()
+                fc[slots[t], h] = (x * (torch.tensor(448.0) / amax)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                fs[slots[t], h] = (amax / 448.0).item()
+    assert np.array_equal(k2, fk.reshape(kc.shape)) and np.array_equal(v2, fv.reshape(vc.shape))
+    assert np.array_equal(ks2, fks.reshape(NB, 16, Hkv).transpose(0, 2, 1))
+    assert np.array_equal(vs2, fvs.reshape(NB, 16, Hkv).transpose(0, 2, 1))
+
+
 # ------------------------------------------------- planted mistakes are caught
 import importlib.util as _ilu
 import inspect as _inspect
@@ -105,6 +188,14 @@ _CW_MUTANTS = {
                             "off, page = int(s) // PAGE_SIZE, int(s) % PAGE_SIZE"),
     "sign_dropped": ("code = np.where(np.signbit(x), code | 0x80, code)", "code = np.where(np.signbit(x), code, code)"),
     "padding_written": ("if s < 0 or s >= NB * PAGE_SIZE:", "if s >= NB * PAGE_SIZE:"),
+    "pt_padding_written": ("if not 0 <= s < NB * PAGE_SIZE:", "if not s < NB * PAGE_SIZE:"),
+    "pt_slot_offset_swapped": ("page, off = divmod(int(s), PAGE_SIZE)", "off, page = divmod(int(s), PAGE_SIZE)"),
+    "pt_signed_max": ("amax = np.abs(x32).max(axis=-1)", "amax = x32.max(axis=-1)"),
+    "pt_scale_inverted": ("scale = (amax / np.float32(E4M3_MAX))", "scale = (np.float32(E4M3_MAX) / amax)"),
+    "pt_scale_slot_head_swapped": ("ks_out[page, :, off], vs_out[page, :, off] = ksc, vsc",
+                                   "ks_out[page, off % ks_out.shape[1], :ksc.shape[0]], vs_out[page, off % vs_out.shape[1], :vsc.shape[0]] = ksc, vsc"),
+    "pt_reciprocal_of_scale": ("np.float32(E4M3_MAX) / np.where(amax > 0, amax, np.float32(1))",
+                               "np.float32(1) / (np.where(amax > 0, amax, np.float32(1)) / np.float32(E4M3_MAX))"),
 }
 
 
@@ -120,12 +211,18 @@ def test_cache_write_pins_catch_mutant(name):
     pins = _ilu.module_from_spec(spec)
     spec.loader.exec_module(pins)
     pins.oracle = _types.SimpleNamespace(e4m3fn_encode=mod.e4m3fn_encode, quantize_rows=mod.quantize_rows,
-                                         cache_write=mod.cache_write)
+                                         cache_write=mod.cache_write, quantize_rows_per_token=mod.quantize_rows_per_token,
+                                         cache_write_per_token=mod.cache_write_per_token,
+                                         e4m3fn_to_float64=oracle.e4m3fn_to_float64,
+                                         bf16_bits_to_float64=oracle.bf16_bits_to_float64)
     calls = [(pins.test_encoder_matches_torch_inside_the_finite_range, ()), (pins.test_every_grid_value_and_midpoint, ()),
              (pins.test_quantize_multiplies_by_the_fp32_reciprocal, ()), (pins.test_out_of_range_slots_write_nothing, ())]
     calls += [(pins.test_saturation_and_special_points, args) for args in
               [(448.0, 0x7E), (1e30, 0x7E), (-500.0, 0xFE), (-0.0, 0x80)]]
     calls += [(pins.test_scatter_against_page_offset_arithmetic, (k,)) for k in ("bf16", "fp8")]
+    calls += [(pins.test_per_token_quantize_matches_torch_ops, ()), (pins.test_per_token_row_max_lands_on_the_top_code, ()),
+              (pins.test_per_token_zero_row_and_power_of_two_rows, ()), (pins.test_per_token_round_trip_error_bound, ()),
+              (pins.test_per_token_scatter_against_page_offset_arithmetic, ())]
     caught = 0
     for fn, args in calls:
         try:

@@ -24,8 +24,8 @@ MUTANTS = {
     "e4m3_subnormal": ("* np.ldexp(1.0, -6)", "* np.ldexp(1.0, -7)"),
     "e4m3_mantissa": ("(1.0 + m / 8.0)", "(1.0 + m / 16.0)"),
     "e4m3_sign": ("np.where(s == 1, -1.0, 1.0)", "np.where(s == 1, 1.0, 1.0)"),
-    "fp8_scale_dropped": ("return e4m3fn_to_float64(raw) * np.float64(np.float32(tensor_scale))",
-                          "return e4m3fn_to_float64(raw)"),
+    "fp8_scale_dropped": ("v = e4m3fn_to_float64(raw) * np.float64(np.float32(tensor_scale))",
+                          "v = e4m3fn_to_float64(raw)"),
     "lse_max_dropped": ("lse = m[:, 0] + np.log", "lse = np.log"),
     "weights_unnormalised": ("w = np.exp(s - lse[:, None])", "w = np.exp(s - m)"),
     "values_are_keys": ("out = w @ values", "out = w @ keys"),
@@ -34,6 +34,11 @@ MUTANTS = {
     "window_from_sequence_start": ("allowed &= j > lim - window", "allowed &= j < window"),
     "sink_value_row_nonzero": ("np.zeros((1, values.shape[1]))", "np.ones((1, values.shape[1]))"),
     "sink_scaled": ("np.asarray(sinks, dtype=np.float64)[:, None]", "scale * np.asarray(sinks, dtype=np.float64)[:, None]"),
+    "token_scale_dropped": ("v = v * np.asarray(token_scales", "v = v + 0 * np.asarray(token_scales"),
+    "token_scale_slot_reversed": ("[pages, kv_head, tok % PAGE_SIZE]", "[pages, kv_head, PAGE_SIZE - 1 - tok % PAGE_SIZE]"),
+    "token_scale_head_ignored": ("[pages, kv_head, tok % PAGE_SIZE]", "[pages, 0, tok % PAGE_SIZE]"),
+    "token_scale_page_shifted": ("[tok // PAGE_SIZE]", "[(tok + 1) // PAGE_SIZE]"),
+    "value_scales_for_keys": ("ks = gather_token_scales(k_token_scales", "ks = gather_token_scales(v_token_scales"),
 }
 
 
@@ -45,8 +50,8 @@ def _mutant_module(name, old, new):
     return mod
 
 
-def _pins_module():
-    spec = importlib.util.spec_from_file_location("_pins_for_mutants", os.path.join(HERE, "test_oracle.py"))
+def _pins_module(name="test_oracle.py"):
+    spec = importlib.util.spec_from_file_location("_pins_for_mutants_" + name[:-3], os.path.join(HERE, name))
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     return mod
@@ -72,16 +77,26 @@ def _pin_calls(pins):
     yield pins.test_sink_closed_form_against_the_sinkless_result, ()
 
 
+def _pertoken_pin_calls(pt):
+    for ql in ((1,), (2, 3, 4)):
+        yield pt.test_per_token_oracle_matches_sdpa, (ql, (0.5, 3.0))
+    yield pt.test_equal_token_scales_reduce_to_the_per_tensor_scale, ()
+    yield pt.test_one_value_scale_doubled_adds_its_weighted_row, ()
+    yield pt.test_per_token_page_permutation_invariance_bit_exact, ()
+    yield pt.test_key_scale_is_indexed_by_head_then_slot, ()
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_mutant(name):
     old, new = MUTANTS[name]
     mutant = _mutant_module(name, old, new)
     pins = _pins_module()
-    pins.oracle = types.SimpleNamespace(**{k: getattr(mutant, k) for k in (
+    pt = _pins_module("test_oracle_pertoken.py")
+    pins.oracle = pt.oracle = types.SimpleNamespace(**{k: getattr(mutant, k) for k in (
         "PAGE_SIZE", "attend", "bf16_bits_to_float64", "dequantize", "e4m3fn_to_float64",
-        "gather_sequence", "paged_decode_attention", "run_workload")})
+        "gather_sequence", "gather_token_scales", "paged_decode_attention", "run_workload")})
     caught = []
-    for fn, args in _pin_calls(pins):
+    for fn, args in list(_pin_calls(pins)) + list(_pertoken_pin_calls(pt)):
         try:
             fn(*args)
         except (AssertionError, ValueError, IndexError, FloatingPointError):
@@ -91,5 +106,6 @@ def test_pins_catch_mutant(name):
 
 def test_unmutated_oracle_passes_the_same_calls():
     pins = _pins_module()
-    for fn, args in _pin_calls(pins):
+    pt = _pins_module("test_oracle_pertoken.py")
+    for fn, args in list(_pin_calls(pins)) + list(_pertoken_pin_calls(pt)):
         fn(*args)
