@@ -145,7 +145,7 @@ for i in seq_iter:
     sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
                          kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
                          k_scale=spec.k_scale, v_scale=spec.v_scale, fp8_source_scale=spec.fp8_source_scale,
-                         seed=nseq)
+                         seed=nseq, token_scale_range=spec.token_scale_range)
     w = wl.make_workload(sub)
     t0 = time.perf_counter()
     oracle.run_workload(w)
@@ -182,7 +182,8 @@ def run_reference(args, world, rank):
     spec = wl.CONFIGS[args.config]
     sl, *_ = wl.draw_metadata(spec, np.random.default_rng(spec.seed))
     eb = 1 if spec.kv_dtype == "fp8" else 2
-    step_bytes = int(sl.astype(np.int64).sum()) * spec.num_kv_heads * spec.head_dim * 2 * eb
+    per_row = spec.head_dim * eb + (4 if spec.token_scale_range is not None else 0)
+    step_bytes = int(sl.astype(np.int64).sum()) * spec.num_kv_heads * 2 * per_row
     v = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
@@ -220,10 +221,16 @@ def run_ours(args, world, rank, local):
         step_bytes = int(seen.sum()) * spec.num_kv_heads * spec.head_dim * 2 * eb
     if args.sinks:
         sinks_t = torch.randn(spec.num_q_heads, generator=torch.Generator().manual_seed(3)).to(dev)
-    win_opts = (binding.make_options(sliding_window=args.window, sinks=sinks_t, use_tcgen05=args.tc)
-                if (args.window > 0 or args.sinks or args.tc) else None)
     pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
     works = [base] + [wl.make_workload(spec, device=str(dev), seed=spec.seed + 100 * k) for k in range(1, pools)]
+
+    def pool_options(w, **extra):
+        # per-token fp8 scales belong to each pool's cache
+        if args.window > 0 or args.sinks or args.tc or w.k_token_scales is not None or extra:
+            return binding.make_options(sliding_window=args.window, sinks=sinks_t, use_tcgen05=args.tc,
+                                        k_token_scales=w.k_token_scales, v_token_scales=w.v_token_scales, **extra)
+        return None
+    pool_opts = [pool_options(w) for w in works]
     # every pool shares the metadata of the first (same lengths, same page ids)
     bt = torch.from_numpy(base.block_tables).to(dev)
     sl = torch.from_numpy(base.seq_lens).to(dev)
@@ -236,7 +243,7 @@ def run_ours(args, world, rank, local):
     def step(k, opts=None, stream_=None):
         w = works[k % pools]
         if opts is None:
-            opts = win_opts
+            opts = pool_opts[k % pools]
         binding.paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
                                   spec.v_scale, out=out, lse=lse, options=opts, stream=stream_)
 
@@ -276,9 +283,8 @@ def run_ours(args, world, rank, local):
     ev_b = torch.cuda.Event(enable_timing=True)
     ev_a.record(stream); ev_b.record(stream)     # torch times only events it has recorded once itself
     torch.cuda.synchronize()
-    ev_opts = binding.make_options(split_start_event=ev_a, split_stop_event=ev_b, sliding_window=args.window,
-                                   sinks=sinks_t, use_tcgen05=args.tc)
-    rgraphs = [capture(pidx, 1, opts=ev_opts) for pidx in range(pools)]
+    ev_opts = [pool_options(w, split_start_event=ev_a, split_stop_event=ev_b) for w in works]
+    rgraphs = [capture(pidx, 1, opts=ev_opts[pidx]) for pidx in range(pools)]
     run_steps(max(args.warmup, gstep))
     torch.cuda.synchronize()
 
@@ -330,7 +336,7 @@ def run_ours(args, world, rank, local):
         if qsl is not None:
             qsl.copy_(h_qsl, non_blocking=True)
         binding.paged_attn_decode(d_q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
-                                  spec.v_scale, out=out, lse=lse, options=win_opts)
+                                  spec.v_scale, out=out, lse=lse, options=pool_opts[k % pools])
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -420,17 +426,26 @@ def run_cache_write(args, world, rank, local):
     vc = torch.zeros(NB, 16, Hkv, D, dtype=cdt, device=dev)
     slots = torch.from_numpy(np.random.default_rng(5).permutation(NB * 16)[:T].astype(np.int32)).to(dev)
     ks = vs = 0.05 if fp8 else 1.0
-    step_bytes = T * Hkv * D * 2 * (2 + esz)
+    per_token = bool(args.per_token)
+    if per_token and not fp8:
+        raise SystemExit("--per-token needs --kv-dtype fp8")
+    step_bytes = T * Hkv * D * 2 * (2 + esz) + (T * Hkv * 2 * 4 if per_token else 0)   # + the row scales
     # pools rotated so a step's bytes exceed 2x L2
     pools = max(1, math.ceil(2 * L2_BYTES / step_bytes))
     keys = [key] + [torch.randn_like(key, dtype=torch.float32).to(torch.bfloat16) for _ in range(pools - 1)]
     vals = [val] + [torch.randn_like(val, dtype=torch.float32).to(torch.bfloat16) for _ in range(pools - 1)]
     caches = [(kc, vc)] + [(torch.zeros_like(kc), torch.zeros_like(vc)) for _ in range(pools - 1)]
+    scales = [(torch.zeros(NB, Hkv, 16, device=dev), torch.zeros(NB, Hkv, 16, device=dev)) for _ in range(pools)]
     stream = torch.cuda.current_stream()
 
+    def write(key_, val_, c, sc, stream_=None):
+        if per_token:
+            binding.paged_attn_cache_write_per_token(key_, val_, slots, c[0], c[1], sc[0], sc[1], stream=stream_)
+        else:
+            binding.paged_attn_cache_write(key_, val_, slots, c[0], c[1], ks, vs, stream=stream_)
+
     def step(k, stream_=None):
-        c = caches[k % pools]
-        binding.paged_attn_cache_write(keys[k % pools], vals[k % pools], slots, c[0], c[1], ks, vs, stream=stream_)
+        write(keys[k % pools], vals[k % pools], caches[k % pools], scales[k % pools], stream_)
 
     for k in range(args.warmup):
         step(k)
@@ -473,7 +488,7 @@ def run_cache_write(args, world, rank, local):
     for _ in range(max(1, args.steps // 10)):
         key.copy_(hk, non_blocking=True)
         val.copy_(hv, non_blocking=True)
-        binding.paged_attn_cache_write(key, val, slots, kc, vc, ks, vs)
+        write(key, val, (kc, vc), scales[0])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / max(1, args.steps // 10)
@@ -484,11 +499,13 @@ def run_cache_write(args, world, rank, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f8e4m3" if fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": f"cache_write_T{T}_{args.kv_dtype}", "tokens": T, "kv_heads": Hkv, "head_dim": D,
+        "config": {"workload": f"cache_write_T{T}_{args.kv_dtype}" + ("_per_token" if per_token else ""),
+                   "tokens": T, "kv_heads": Hkv, "head_dim": D,
                    "bytes_per_step": step_bytes, "pools_rotated": pools,
                    "step_mode": "CUDA graph replay of paged_attn_cache_write"},
         "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
-                     "traffic": None, "kernel": "pa_cache_write_kernel", "peak_source": f"{peak_kind} hbm_gbs"},
+                     "traffic": None, "kernel": "pa_cache_write_tok_kernel" if per_token else "pa_cache_write_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * key.numel() * 2, "d2h_bytes_per_step": 0},
         "gpu_launches": args.steps, "clocks": clk.summary(),
@@ -547,6 +564,7 @@ def main():
                     help="decode split kernel: 0 planner's choice, 1 mma.sync, 2 tcgen05 (bf16)")
     ap.add_argument("--tokens", type=int, default=16384, help="cache_write: tokens written per step")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
+    ap.add_argument("--per-token", action="store_true", help="cache_write: fp8 with one scale per row")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     args = ap.parse_args()

@@ -95,6 +95,16 @@ typedef struct pa_options_t {
   int32_t use_tcgen05;         /* split kernel: 0 = planner's choice (the tensor-memory kernel when
                                   G * max_query_len > 64, else the mma.sync kernel); 1 = never
                                   (PA_ERR_UNSUPPORTED above 64 rows); 2 = always (bf16 caches only) */
+  const struct pa_tensor_t* k_token_scales;  /* optional per-token scales of an fp8 cache (the pages'
+                                  reshape_and_cache_with_pertoken_quant layout: one fp32 scale per
+                                  cached row): f32 [NB, Hkv, 16], entry [page][head][slot];
+                                  stride[2] == 1, stride[1] == 16, stride[0] % 4 == 0, data 16-byte
+                                  aligned.  A cached K element's value is then
+                                  code * k_scale * k_token_scales[page][head][slot] (pass k_scale =
+                                  1 for a purely per-token cache).  NULL (or data NULL) = none.
+                                  Requires v_token_scales too and an fp8 cache; entries of slots
+                                  past a sequence's end may hold anything, even non-finite values */
+  const struct pa_tensor_t* v_token_scales;  /* the same for V (value = code * v_scale * scale) */
 } pa_options_t;
 
 /* Launch plan the library picks for a problem shape (for tests, tuning and
@@ -209,6 +219,32 @@ int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_
 int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, const pa_tensor_t* slot_mapping,
                            const pa_tensor_t* k_cache, const pa_tensor_t* v_cache, float k_scale, float v_scale,
                            pa_stream_t stream);
+
+/*
+ * paged_attn_cache_write_per_token - the fp8 KV-cache write with one scale per
+ * written row (ATOM model-operations guide, "KV cache operations": FP8 KV cache
+ * write, aiter.reshape_and_cache_with_pertoken_quant; the attention-dispatch
+ * note that per-token quantised layers carry more than one descale per tensor).
+ *
+ *   key, value, slot_mapping  as for paged_attn_cache_write.
+ *   k_cache, v_cache          fp8e4m3 [NB, 16, Hkv, D] (bf16 caches are rejected).
+ *   k_token_scales, v_token_scales  f32 [NB, Hkv, 16], any non-negative strides,
+ *                   4-byte aligned: entry [page][head][slot] receives the row's scale.
+ *   For every written (token, head) row x (bf16, D values): amax = max_d |x_d|;
+ *   scale = amax / 448 and r = 448 / amax (IEEE fp32 divisions); code_d =
+ *   e4m3fn(x_d * r), round to nearest even, saturating to +-448; an all-zero row
+ *   stores scale 0 and zero codes.  Rows must be finite with amax either 0 or at
+ *   least 448 / FLT_MAX (else r overflows and the codes are undefined).
+ *   paged_attn_decode_ex reads such a cache with pa_options_t.k_token_scales /
+ *   v_token_scales and k_scale = v_scale = 1.
+ *
+ * Errors, padding slots and out-of-range slots as for paged_attn_cache_write.
+ * Asynchronous; allocates nothing.
+ */
+int paged_attn_cache_write_per_token(const pa_tensor_t* key, const pa_tensor_t* value,
+                                     const pa_tensor_t* slot_mapping, const pa_tensor_t* k_cache,
+                                     const pa_tensor_t* v_cache, const pa_tensor_t* k_token_scales,
+                                     const pa_tensor_t* v_token_scales, pa_stream_t stream);
 
 /* Plan for a shape on the current device (kv_dtype: PA_BF16 or PA_FP8_E4M3).
  * opts may be NULL.  Reads device attributes only; enqueues nothing. */

@@ -33,7 +33,8 @@ class PaOptions(ctypes.Structure):
                 ("sinks", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p),
-                ("use_tcgen05", ctypes.c_int32)]
+                ("use_tcgen05", ctypes.c_int32),
+                ("k_token_scales", ctypes.POINTER(PaTensor)), ("v_token_scales", ctypes.POINTER(PaTensor))]
 
 
 class PaPlan(ctypes.Structure):
@@ -63,6 +64,7 @@ _SIGNATURES = {
     "paged_attn_decode_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float,
                                                         ctypes.c_float, ctypes.c_float, _P, _P, ctypes.c_void_p]),
     "paged_attn_cache_write": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
+    "paged_attn_cache_write_per_token": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_void_p]),
     "paged_attn_plan": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(PaOptions), ctypes.POINTER(PaPlan)]),
     "paged_attn_workspace_size": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
     "paged_attn_reserve": (ctypes.c_int, [ctypes.c_int32] * 6),
@@ -137,10 +139,12 @@ def _stream_handle(stream) -> int:
 
 def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=False, workspace=None,
                  workspace_bytes=0, split_start_event=None, split_stop_event=None, page_pairing=0,
-                 sliding_window=0, sinks=None, use_tcgen05=0) -> PaOptions:
+                 sliding_window=0, sinks=None, use_tcgen05=0, k_token_scales=None,
+                 v_token_scales=None) -> PaOptions:
     """Options for paged_attn_decode_ex.  sinks: CUDA float32 tensor [Hq] (kept
     alive by the caller) or None.  use_tcgen05: 0 planner's choice, 1 never,
-    2 always (bf16 caches)."""
+    2 always (bf16 caches).  k_token_scales / v_token_scales: CUDA float32
+    [NB, Hkv, 16] per-token scales of an fp8 cache (kept alive by the caller)."""
     o = PaOptions()
     o.num_ctas = num_ctas
     o.min_pages_per_cta = min_pages_per_cta
@@ -159,6 +163,11 @@ def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=F
     o.workspace_bytes = workspace_bytes
     o.split_start_event = int(split_start_event.cuda_event) if split_start_event is not None else None
     o.split_stop_event = int(split_stop_event.cuda_event) if split_stop_event is not None else None
+    if k_token_scales is not None or v_token_scales is not None:
+        # the descriptors live as long as the options object
+        o._tok_descs = (tensor_desc(k_token_scales), tensor_desc(v_token_scales))
+        o.k_token_scales = ctypes.pointer(o._tok_descs[0])
+        o.v_token_scales = ctypes.pointer(o._tok_descs[1])
     return o
 
 
@@ -224,6 +233,17 @@ def paged_attn_cache_write(key, value, slot_mapping, k_cache, v_cache, k_scale=1
                                            _stream_handle(stream)))
 
 
+def paged_attn_cache_write_per_token(key, value, slot_mapping, k_cache, v_cache, k_token_scales, v_token_scales,
+                                     stream=None):
+    """Per-token fp8 cache write (see include/paged_attn.h): codes of each
+    (token, head) row quantised with its own scale amax / 448, written into
+    the uint8 caches [NB, 16, Hkv, D]; the scales go to the float32 tensors
+    [NB, Hkv, 16].  All updated in place."""
+    lib = load()
+    d = [tensor_desc(t) for t in (key, value, slot_mapping, k_cache, v_cache, k_token_scales, v_token_scales)]
+    _check(lib, lib.paged_attn_cache_write_per_token(*[ctypes.byref(x) for x in d], _stream_handle(stream)))
+
+
 def paged_attn_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=PA_BF16, max_query_len=1,
                     options=None) -> dict:
     lib = load()
@@ -283,6 +303,13 @@ def decode_workload(w, out=None, lse=None, stream=None, options=None, want_lse=T
     sl = torch.from_numpy(w.seq_lens).to(dev)
     qsl = torch.from_numpy(w.query_start_loc).to(dev) if w.query_start_loc is not None else None
     s = w.spec
+    if w.k_token_scales is not None:
+        if options is None:
+            options = make_options()
+        if not options.k_token_scales:
+            options._tok_descs = (tensor_desc(w.k_token_scales), tensor_desc(w.v_token_scales))
+            options.k_token_scales = ctypes.pointer(options._tok_descs[0])
+            options.v_token_scales = ctypes.pointer(options._tok_descs[1])
     return paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, s.max_query_len if qsl is not None else 1,
                              s.scale, s.k_scale, s.v_scale, out=out, lse=lse, stream=stream, options=options,
                              want_lse=want_lse)

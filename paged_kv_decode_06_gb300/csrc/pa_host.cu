@@ -91,6 +91,8 @@ int device_state(DeviceState** out, int* dev_out) {
       return cuda_fail(e, "cudaFuncSetAttribute(split bf16)");
     if ((e = pa::set_split_smem_limits_fp8(s.smem_optin)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(split fp8)");
+    if ((e = pa::set_split_smem_limits_fp8_tok(s.smem_optin)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(split fp8, per-token scales)");
     if ((e = pa::set_split_smem_limits_tc(s.smem_optin)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(split tcgen05)");
     void* ptr = nullptr;
@@ -117,6 +119,8 @@ struct Plan {
   int B, Hq, Hkv, D, esz, max_qlen;
   int G, R_max, MT, HC, NC, nstage, threads, grid, min_pages, pair;
   bool tc;            // tensor-memory (tcgen05) kernel
+  bool tok;           // per-token fp8 scales staged behind each page's K and V tiles
+  uint32_t tok_bytes; // tok: one tensor's scales of one page (HC * 16 * 4)
   int block_pages;    // tc: pages per ring stage
   uint32_t stage_bytes, kv_bytes, q_slot_bytes;
   uint32_t off_stage, off_q, off_bar, off_prefix, off_xchg, smem;
@@ -154,6 +158,11 @@ int check_variant_option(const pa_options_t* opts, int kv_dtype, int64_t rows) {
   return PA_OK;
 }
 
+bool has_token_scales(const pa_options_t* opts) {
+  return opts && ((opts->k_token_scales && opts->k_token_scales->data) ||
+                  (opts->v_token_scales && opts->v_token_scales->data));
+}
+
 // mma.sync kernel: heads per CTA, ring depth and shared-memory layout.
 int plan_mma(Plan& p, int B, int Hkv, int D, int max_qlen, const pa_options_t* opts, int smem_optin) {
   const uint32_t bar_bytes = 8u * (2 * kMaxStages + 4);
@@ -178,13 +187,16 @@ int plan_mma(Plan& p, int B, int Hkv, int D, int max_qlen, const pa_options_t* o
         continue;
       }
       const uint32_t kv = static_cast<uint32_t>(hc) * kPageSize * D * p.esz;
-      const uint32_t stage = 2 * kv;
+      // per-token scales ride behind K and V; stages stay 1024-byte aligned (swizzle span)
+      const uint32_t stage =
+          2 * kv + (p.tok ? static_cast<uint32_t>(align_up(2u * hc * kPageSize * 4u, 1024)) : 0u);
       const uint32_t qslot = static_cast<uint32_t>(align_up(static_cast<size_t>(max_qlen) * hc * p.G * D * 2, 128));
       const int64_t fixed = 1024 + 2 * qslot + bar_bytes + prefix_bytes;
       const int64_t room = smem_optin - fixed;
       const int nst = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / stage)) : 0;
       if (nst >= want_stages) {
         p.HC = hc;
+        p.tok_bytes = p.tok ? static_cast<uint32_t>(hc) * kPageSize * 4u : 0u;
         p.kv_bytes = kv;
         p.stage_bytes = stage;
         p.q_slot_bytes = qslot;
@@ -224,6 +236,8 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
   p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
   if ((st = check_variant_option(opts, kv_dtype, p.R_max)) != PA_OK) return st;
   p.tc = (opts && opts->use_tcgen05 == 2) || p.R_max > kMaxRowsMma;
+  p.tok = has_token_scales(opts);
+  if (p.tok && kv_dtype != PA_FP8_E4M3) return fail(PA_ERR_INVALID_ARG, "per-token scales need an fp8 cache");
   if (p.tc) {
     // One KV head per CTA; shared memory: ring stages of kTcBlockPages pages
     // (K and V), barriers, exchange buffers, sequence metadata (Q is in TMEM).
@@ -358,6 +372,27 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return fail(PA_ERR_INVALID_ARG, "scale, k_scale and v_scale must be finite");
   if (opts && opts->sinks && !aligned(opts->sinks, 4)) return fail(PA_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
+  const bool tok = has_token_scales(opts);
+  if (tok) {
+    if (kc->dtype != PA_FP8_E4M3) return fail(PA_ERR_INVALID_ARG, "per-token scales need an fp8 cache");
+    const pa_tensor_t* ts[2] = {opts->k_token_scales, opts->v_token_scales};
+    const char* nm[2] = {"k_token_scales", "v_token_scales"};
+    for (int x = 0; x < 2; ++x) {
+      if (ts[x] == nullptr || ts[x]->data == nullptr)
+        return fail(PA_ERR_INVALID_ARG, "k_token_scales and v_token_scales must be given together");
+      if ((st = check_tensor(ts[x], nm[x], 3, false)) != PA_OK) return st;
+      if (ts[x]->dtype != PA_F32) return fail(PA_ERR_INVALID_ARG, "%s must be float32", nm[x]);
+      if (ts[x]->shape[0] != NB || ts[x]->shape[1] != Hkv || ts[x]->shape[2] != kPageSize)
+        return fail(PA_ERR_INVALID_ARG, "%s must have shape [NB, Hkv, 16] = [%lld, %lld, 16]", nm[x], (long long)NB,
+                    (long long)Hkv);
+      if (ts[x]->stride[2] != 1 || ts[x]->stride[1] != kPageSize || ts[x]->stride[0] % 4 != 0 ||
+          !aligned(ts[x]->data, 16))
+        return fail(PA_ERR_INVALID_ARG, "%s: each page's [Hkv, 16] block must be contiguous and 16-byte aligned",
+                    nm[x]);
+    }
+    if (ts[0]->stride[0] != ts[1]->stride[0])
+      return fail(PA_ERR_INVALID_ARG, "k_token_scales and v_token_scales need the same page stride");
+  }
   if ((st = check_shape_args(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq),
                              static_cast<int>(Hkv), static_cast<int>(D), kc->dtype, max_qlen)) != PA_OK)
     return st;
@@ -448,6 +483,12 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   sp.kv_bytes = pl.kv_bytes;
   sp.block_pages = pl.block_pages;
   sp.off_xchg = pl.off_xchg;
+  if (pl.tok) {
+    sp.k_tok = static_cast<const float*>(opts->k_token_scales->data);
+    sp.v_tok = static_cast<const float*>(opts->v_token_scales->data);
+    sp.tok_stride_page = opts->k_token_scales->stride[0];
+    sp.tok_bytes = pl.tok_bytes;
+  }
 
   pa::MergeParams mp = {};
   mp.out = sp.out;
@@ -490,6 +531,9 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
     return cuda_fail(e, "cudaEventRecord(start)");
   if (pl.tc)
     e = pa::launch_split_tc(static_cast<int>(D), tk, tv, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
+  else if (pl.tok)
+    e = pa::launch_split_fp8_tok(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
+                                 pdl && !ev0, stream);
   else if (esz == 1)
     e = pa::launch_split_fp8(static_cast<int>(D), tk, tv, sp, pl.grid, pl.threads, static_cast<int>(pl.smem),
                              pdl && !ev0, stream);
@@ -535,9 +579,9 @@ int paged_attn_decode(const pa_tensor_t* q, const pa_tensor_t* k_cache, const pa
                               k_scale, v_scale, out, lse, nullptr, stream);
 }
 
-int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, const pa_tensor_t* slot_mapping,
-                           const pa_tensor_t* k_cache, const pa_tensor_t* v_cache, float k_scale, float v_scale,
-                           pa_stream_t stream) {
+static int cache_write_impl(const pa_tensor_t* key, const pa_tensor_t* value, const pa_tensor_t* slot_mapping,
+                            const pa_tensor_t* k_cache, const pa_tensor_t* v_cache, float k_scale, float v_scale,
+                            const pa_tensor_t* kts, const pa_tensor_t* vts, pa_stream_t stream) {
   t_last_error.clear();
   int st;
   if ((st = check_tensor(key, "key", 3, false)) || (st = check_tensor(value, "value", 3, false)) ||
@@ -573,8 +617,21 @@ int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, con
       if ((c->stride[d] * esz) % 16 != 0) return fail(PA_ERR_INVALID_ARG, "KV cache strides must be multiples of 16 bytes");
     if (!aligned(c->data, 16)) return fail(PA_ERR_INVALID_ARG, "KV cache data must be 16-byte aligned");
   }
-  if (esz == 1 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f))
+  const bool tok = kts != nullptr;
+  if (tok) {
+    if (esz != 1) return fail(PA_ERR_INVALID_ARG, "per-token quantisation needs fp8 caches");
+    const pa_tensor_t* ts[2] = {kts, vts};
+    const char* nm[2] = {"k_token_scales", "v_token_scales"};
+    for (int x = 0; x < 2; ++x) {
+      if ((st = check_tensor(ts[x], nm[x], 3, false)) != PA_OK) return st;
+      if (ts[x]->dtype != PA_F32) return fail(PA_ERR_INVALID_ARG, "%s must be float32", nm[x]);
+      if (ts[x]->shape[0] != k_cache->shape[0] || ts[x]->shape[1] != Hkv || ts[x]->shape[2] != kPageSize)
+        return fail(PA_ERR_INVALID_ARG, "%s must have shape [NB, Hkv, 16]", nm[x]);
+      if (!aligned(ts[x]->data, 4)) return fail(PA_ERR_INVALID_ARG, "%s must be 4-byte aligned", nm[x]);
+    }
+  } else if (esz == 1 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f)) {
     return fail(PA_ERR_INVALID_ARG, "fp8 caches need finite, non-zero k_scale and v_scale");
+  }
   if (T == 0) return PA_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
@@ -599,8 +656,18 @@ int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, con
   p.num_kv_heads = static_cast<int32_t>(Hkv);
   p.head_dim = static_cast<int32_t>(D);
   p.num_pages = static_cast<int32_t>(k_cache->shape[0]);
-  p.k_rscale = 1.0f / k_scale;   // fp32 reciprocal, rounded once
-  p.v_rscale = 1.0f / v_scale;
+  p.k_rscale = tok ? 0.f : 1.0f / k_scale;   // fp32 reciprocal, rounded once
+  p.v_rscale = tok ? 0.f : 1.0f / v_scale;
+  if (tok) {
+    p.k_tok = static_cast<float*>(kts->data);
+    p.v_tok = static_cast<float*>(vts->data);
+    p.ks_stride_page = kts->stride[0];
+    p.ks_stride_head = kts->stride[1];
+    p.ks_stride_slot = kts->stride[2];
+    p.vs_stride_page = vts->stride[0];
+    p.vs_stride_head = vts->stride[1];
+    p.vs_stride_slot = vts->stride[2];
+  }
   p.err = ds->status;
   const int64_t work = T * Hkv * (D / 8);
   const int64_t blocks = (work + 255) / 256;
@@ -608,6 +675,24 @@ int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, con
   cudaError_t e = pa::launch_cache_write(esz == 1, p, grid, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cache write kernel launch");
   return PA_OK;
+}
+
+int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, const pa_tensor_t* slot_mapping,
+                           const pa_tensor_t* k_cache, const pa_tensor_t* v_cache, float k_scale, float v_scale,
+                           pa_stream_t stream) {
+  return cache_write_impl(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale, nullptr, nullptr, stream);
+}
+
+int paged_attn_cache_write_per_token(const pa_tensor_t* key, const pa_tensor_t* value,
+                                     const pa_tensor_t* slot_mapping, const pa_tensor_t* k_cache,
+                                     const pa_tensor_t* v_cache, const pa_tensor_t* k_token_scales,
+                                     const pa_tensor_t* v_token_scales, pa_stream_t stream) {
+  if (k_token_scales == nullptr || v_token_scales == nullptr) {
+    t_last_error.clear();
+    return fail(PA_ERR_INVALID_ARG, "k_token_scales and v_token_scales descriptors are required");
+  }
+  return cache_write_impl(key, value, slot_mapping, k_cache, v_cache, 1.f, 1.f, k_token_scales, v_token_scales,
+                          stream);
 }
 
 int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype,

@@ -54,6 +54,12 @@ struct SplitParams {
   uint32_t kv_bytes;        // K (or V) tiles of one page: HC * 16 * D * elem
   int32_t block_pages;      // tensor-memory variant: pages per ring stage (block)
   uint32_t off_xchg;        // tensor-memory variant: softmax warps' exchange buffers (4 KB)
+  // per-token fp8 scales (token-scale variant of the split kernel): f32 [NB, Hkv, 16],
+  // staged per page behind the K and V tiles: [HC][16] K scales, then [HC][16] V scales
+  const float* k_tok;
+  const float* v_tok;
+  int64_t tok_stride_page;  // floats between pages of the scale tensors
+  uint32_t tok_bytes;       // HC * 16 * 4: one tensor's scales of one page
 };
 
 struct MergeParams {
@@ -84,6 +90,12 @@ struct CacheWriteParams {
   int32_t num_tokens, num_kv_heads, head_dim, num_pages;
   float k_rscale, v_rscale; // fp8 only: code = e4m3(x * rscale), rscale = fp32(1 / scale)
   uint32_t* err;
+  // per-token quantisation (fp8 only): row scale = amax / 448 stored at
+  // [page, head, slot] of f32 [NB, Hkv, 16] tensors; nullptr = per-tensor scales
+  float* k_tok;
+  float* v_tok;
+  int64_t ks_stride_page, ks_stride_head, ks_stride_slot;   // floats
+  int64_t vs_stride_page, vs_stride_head, vs_stride_slot;
 };
 
 cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int grid, cudaStream_t stream);
@@ -94,6 +106,10 @@ cudaError_t launch_split_bf16(int head_dim, const CUtensorMap& tk, const CUtenso
                               int grid, int threads, int smem, bool pdl, cudaStream_t stream);
 cudaError_t launch_split_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                              int grid, int threads, int smem, bool pdl, cudaStream_t stream);
+// fp8 caches with per-token scales (p.k_tok / p.v_tok set).
+cudaError_t launch_split_fp8_tok(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                                 int grid, int threads, int smem, bool pdl, cudaStream_t stream);
+cudaError_t set_split_smem_limits_fp8_tok(int smem);
 // wide: one 256-thread block per (unit, row), threads across partials (many
 // partials per unit); otherwise one warp per (unit, row), 8 rows per block.
 cudaError_t launch_merge(int head_dim, const MergeParams& p, int units, int rows, bool wide, bool pdl,

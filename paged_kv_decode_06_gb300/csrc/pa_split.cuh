@@ -356,10 +356,13 @@ __device__ __forceinline__ void pv_pages(ConsumerState<D, FP8>& cs, const uint32
 // causal / tail mask by token index, online softmax (exp2 domain), O += P V.
 // hb[pg] is the shared-memory address of this warp's head in the page's stage;
 // V follows K at +kv_bytes.  tb = first token of the block; min_lim = L - qn.
-template <int D, bool FP8, int NP>
+// TOKS: per-token scales; ts[pg] is the shared-memory address of this warp's
+// head's 16 K scales in page pg's stage, its 16 V scales tok_bytes further.
+template <int D, bool FP8, int NP, bool TOKS = false>
 __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const uint32_t (&hb)[NP], uint32_t kv_bytes,
                                               uint32_t block_stride, int tb, int L, int min_lim, int lim0, int lim1,
-                                              int window, float scale_log2, int lane) {
+                                              int window, float scale_log2, int lane, const uint32_t (&ts)[NP],
+                                              uint32_t tok_bytes) {
   using GG = Geo<D, FP8>;
   const int tig = lane & 3, mi = lane >> 3, rr = lane & 7;
   float S[2 * NP][4];
@@ -391,10 +394,26 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
     }
   }
   float x[2 * NP][4];
+  if constexpr (TOKS) {
+    // key token 8n + 2*tig + e of the block: the logit takes that key's scale
 #pragma unroll
-  for (int n = 0; n < 2 * NP; ++n)
+    for (int pg = 0; pg < NP; ++pg) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[n][e] = S[n][e] * scale_log2;
+      for (int h8 = 0; h8 < 2; ++h8) {
+        const float2 ks = lds_f2(ts[pg] + 32u * h8 + 8u * tig);
+        const float c0 = scale_log2 * ks.x, c1 = scale_log2 * ks.y;
+        x[2 * pg + h8][0] = S[2 * pg + h8][0] * c0;
+        x[2 * pg + h8][1] = S[2 * pg + h8][1] * c1;
+        x[2 * pg + h8][2] = S[2 * pg + h8][2] * c0;
+        x[2 * pg + h8][3] = S[2 * pg + h8][3] * c1;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] = S[n][e] * scale_log2;
+  }
   // keys allowed for a row: lim - W < token <= lim (causal run end; sliding
   // window start when W > 0, whose largest start is L - W for the last row)
   if (tb + kPage * NP - 1 > min_lim || (window > 0 && tb < L - window)) {
@@ -449,6 +468,30 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
       cs.O[J][3] *= a1;
     }
   }
+  if constexpr (TOKS) {
+    // P V with per-token value scales: each weight takes its value row's scale
+    // (the sum l above keeps the unscaled weights).  Slots past the sequence
+    // end take 0, so a non-finite scale there cannot reach O.
+    const bool tail = L - tb < kPage * NP;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const int vt = L - tb - kPage * pg;   // value rows of this page inside the sequence
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8) {
+        const float2 vs = lds_f2(ts[pg] + tok_bytes + 32u * h8 + 8u * tig);
+        const int t0 = 8 * h8 + 2 * tig;
+        float c0 = vs.x, c1 = vs.y;
+        if (tail) {
+          c0 = t0 < vt ? c0 : 0.f;
+          c1 = t0 + 1 < vt ? c1 : 0.f;
+        }
+        x[2 * pg + h8][0] *= c0;
+        x[2 * pg + h8][1] *= c1;
+        x[2 * pg + h8][2] *= c0;
+        x[2 * pg + h8][3] *= c1;
+      }
+    }
+  }
   uint32_t Pa[NP][4];
 #pragma unroll
   for (int pg = 0; pg < NP; ++pg) {
@@ -485,8 +528,9 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
 }
 
 // WINDOW: the sliding-window variant (a separate instantiation, so the
-// windowless kernels carry none of its code).
-template <int D, bool FP8, bool WINDOW>
+// windowless kernels carry none of its code).  TOKS: fp8 caches with per-token
+// scales, staged by the producer behind each page's K and V tiles.
+template <int D, bool FP8, bool WINDOW, bool TOKS = false>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const SplitParams p) {
@@ -589,10 +633,25 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         ++qseg;
       }
       const int phys = btc.lookup(p, cu, s_pre, s_len, s_qsl, B, NC, window, lane);
-      if ((phys < 0 || phys >= p.num_pages) && lane == 0) atomicOr(p.err, kErrPageRange);
+      const bool bad_page = phys < 0 || phys >= p.num_pages;
+      if (bad_page && lane == 0) atomicOr(p.err, kErrPageRange);
       // An out-of-range page id reads as zeros (TMA fills outside the tensor).
-      if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
-      __syncwarp();
+      if constexpr (TOKS) {
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * p.kv_bytes + 2 * p.tok_bytes);
+        __syncwarp();
+        if (lane >= 30) {
+          // the page's [HC][16] K (lane 30) or V (lane 31) scales; an
+          // out-of-range page id reads page 0's (its rows are undefined anyway)
+          const float* src = (lane == 30 ? p.k_tok : p.v_tok) +
+                             static_cast<int64_t>(bad_page ? 0 : phys) * p.tok_stride_page + cu.c * HC * kPage;
+          const uint32_t dst = base + p.off_stage + static_cast<uint32_t>(stage) * p.stage_bytes + 2 * p.kv_bytes +
+                               static_cast<uint32_t>(lane - 30) * p.tok_bytes;
+          bulk_load(dst, src, p.tok_bytes, full_bar(stage));
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), p.stage_bytes);
+        __syncwarp();
+      }
       if (lane < 2 * GG::NBOX) {
         const int tensor = lane / GG::NBOX;
         const int bx = lane - tensor * GG::NBOX;
@@ -621,6 +680,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   const int rho1 = rho0 + 8;
   const uint32_t block_stride = static_cast<uint32_t>(HC * GG::BOX_BYTES);
   const uint32_t head_base = base + p.off_stage + static_cast<uint32_t>(hh * GG::BOX_BYTES);
+  // per-token scales of this warp's head in stage 0 (TOKS only)
+  const uint32_t tok_base = base + p.off_stage + 2 * p.kv_bytes + static_cast<uint32_t>(hh * kPage * 4);
 
   Cursor cu = locate(s_pre, B, NC, start);
   int qseg = 0;
@@ -708,12 +769,15 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       if (pair) {
         const uint32_t hb[2] = {head_base + static_cast<uint32_t>(stage) * p.stage_bytes,
                                 head_base + static_cast<uint32_t>(stage2) * p.stage_bytes};
-        consume_pages<D, FP8, 2>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1, window,
-                                 p.scale_log2, lane);
+        const uint32_t ts[2] = {tok_base + static_cast<uint32_t>(stage) * p.stage_bytes,
+                                tok_base + static_cast<uint32_t>(stage2) * p.stage_bytes};
+        consume_pages<D, FP8, 2, TOKS>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1, window,
+                                       p.scale_log2, lane, ts, p.tok_bytes);
       } else {
         const uint32_t hb[1] = {head_base + static_cast<uint32_t>(stage) * p.stage_bytes};
-        consume_pages<D, FP8, 1>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1, window,
-                                 p.scale_log2, lane);
+        const uint32_t ts[1] = {tok_base + static_cast<uint32_t>(stage) * p.stage_bytes};
+        consume_pages<D, FP8, 1, TOKS>(cs, hb, p.kv_bytes, block_stride, tb, si.L, si.L - si.qn, lim0, lim1, window,
+                                       p.scale_log2, lane, ts, p.tok_bytes);
       }
     }
     __syncwarp();

@@ -93,11 +93,12 @@ CONFIGS = {
         query_len_choices=(2, 3, 4), seed=1004),
     # fp8 cache quantised per token (one scale per cached row and KV head),
     # the batch-256 shape of the per-tensor fp8 workload: codes spread over
-    # the e4m3 range, row scales log-uniform around 1/128.
+    # the e4m3 range, row scales log-uniform in [1/512, 1/128] (dequantised
+    # values N(0,1) times 1/4 to 1).
     "fp8_pertoken": WorkloadSpec(
         name="fp8_pertoken", num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
         kv_dtype="fp8", seq_len_kind="loguniform", seq_len_args=(128, 8192),
-        fp8_source_scale=1.0 / 128, token_scale_range=(0.5 / 128, 2.0 / 128), seed=1006),
+        fp8_source_scale=1.0 / 128, token_scale_range=(0.25 / 128, 1.0 / 128), seed=1006),
     # Longer speculative verification: runs of 1 + up to 7 draft tokens over a
     # 16-query-head group (Llama-3-405B-shaped heads, 128 over 8), so a KV
     # head serves up to 128 query rows, a dense tile for the tensor cores.
@@ -134,9 +135,11 @@ class Workload:
 
     def kv_bytes(self) -> int:
         """Algorithmic KV bytes of one step: every cached token's K and V row
-        of every KV head, read once."""
+        of every KV head, read once (with per-token scales, also the two fp32
+        scales of each row)."""
         s = self.spec
-        return int(self.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2 * self.kv_elem_bytes
+        per_row = s.head_dim * self.kv_elem_bytes + (4 if self.k_token_scales is not None else 0)
+        return int(self.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * 2 * per_row
 
 
 def draw_metadata(spec: WorkloadSpec, rng: np.random.Generator):

@@ -195,3 +195,59 @@ def test_cache_write_invalid_arguments(lib, mutate, expect):
 def test_cache_write_fp8_needs_nonzero_scales(lib):
     a = _cw_args(kv=torch.uint8)
     assert _cw_call(lib, a, 0.0, 1.0) == binding.PA_ERR_INVALID_ARG
+
+
+# ------------------------------------------------ per-token fp8 scales (host checks)
+
+def _tok_call(lib, a, ks, vs):
+    opts = binding.make_options(k_token_scales=ks, v_token_scales=vs)
+    descs = [binding.tensor_desc(a[n]) for n in ("q", "k", "v", "bt", "sl", "qsl", "out", "lse")]
+    refs = [ctypes.byref(d) for d in descs]
+    return lib.paged_attn_decode_ex(*refs[:6], a["max_qlen"], 0.1, 1.0, 1.0, refs[6], refs[7], ctypes.byref(opts),
+                                    None)
+
+
+def _fp8_args():
+    return _good_args(kv=torch.uint8)
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a, s: a.update(k=torch.zeros(10, 16, 2, 128, dtype=torch.bfloat16),
+                           v=torch.zeros(10, 16, 2, 128, dtype=torch.bfloat16)), binding.PA_ERR_INVALID_ARG),  # bf16 cache
+    (lambda a, s: s.update(ks=s["ks"].double()), binding.PA_ERR_INVALID_ARG),
+    (lambda a, s: s.update(vs=torch.zeros(10, 2, 8)), binding.PA_ERR_INVALID_ARG),                   # shape
+    (lambda a, s: s.update(ks=torch.zeros(9, 2, 16)), binding.PA_ERR_INVALID_ARG),                   # pages
+    (lambda a, s: s.update(ks=torch.zeros(10, 16, 2).transpose(1, 2)), binding.PA_ERR_INVALID_ARG),  # layout
+    (lambda a, s: s.update(vs=None), binding.PA_ERR_INVALID_ARG),                                    # only one
+    (lambda a, s: s.update(ks=torch.zeros(10, 2, 17)[:, :, :16], vs=torch.zeros(10, 2, 17)[:, :, :16]),
+     binding.PA_ERR_INVALID_ARG),                                                                    # head stride 17
+])
+def test_token_scale_arguments_rejected_on_host(lib, mutate, expect):
+    a = _fp8_args()
+    s = dict(ks=torch.zeros(10, 2, 16), vs=torch.zeros(10, 2, 16))
+    mutate(a, s)
+    assert _tok_call(lib, a, s["ks"], s["vs"]) == expect, binding.paged_attn_last_error_message()
+    assert binding.paged_attn_last_error_message() != ""
+
+
+def test_token_scales_pass_host_validation(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _tok_call(lib, _fp8_args(), torch.zeros(10, 2, 16), torch.zeros(10, 2, 16)) == binding.PA_ERR_CUDA
+
+
+def _cwt_call(lib, a, ks, vs):
+    d = [binding.tensor_desc(t) for t in (a["key"], a["value"], a["slots"], a["kc"], a["vc"], ks, vs)]
+    return lib.paged_attn_cache_write_per_token(*[ctypes.byref(x) for x in d], None)
+
+
+def test_per_token_cache_write_arguments(lib):
+    a = _cw_args(kv=torch.uint8)
+    ok = torch.zeros(3, 2, 16)
+    assert _cwt_call(lib, _cw_args(), ok, ok) == binding.PA_ERR_INVALID_ARG          # bf16 cache
+    assert _cwt_call(lib, a, torch.zeros(3, 2, 8), ok) == binding.PA_ERR_INVALID_ARG  # scale shape
+    assert _cwt_call(lib, a, ok, ok.double()) == binding.PA_ERR_INVALID_ARG          # scale dtype
+    d = [binding.tensor_desc(t) for t in (a["key"], a["value"], a["slots"], a["kc"], a["vc"], ok)]
+    assert lib.paged_attn_cache_write_per_token(*[ctypes.byref(x) for x in d], None, None) == binding.PA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert _cwt_call(lib, a, ok, ok) == binding.PA_ERR_CUDA
