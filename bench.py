@@ -121,50 +121,86 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
-def cpu_oracle_sample(config: str, budget_s: float = 15.0, threads: int = 1):
-    """Time the float64 oracle on a bounded sample of the workload (whole
-    sequences, added until ~budget_s of CPU work) in a child process with
-    single-threaded BLAS.  Returns (GB/s of KV processed, cores, sample text)."""
+def cpu_oracle_sample(config: str, budget_s: float = 15.0, threads: int = 1, impl: str = "c"):
+    """Time a float64 oracle on a bounded sample of the workload (whole
+    sequences, added until ~budget_s of oracle time) in a child process.
+    impl "c": the plain-C oracle with ``threads`` OpenMP threads (0 = all host
+    cores); impl "numpy": the NumPy oracle, single-threaded BLAS.  Returns
+    (GB/s of KV processed, threads used, sample text)."""
     code = f"""
 import json, os, sys, time
 sys.path.insert(0, {ROOT!r})
 import numpy as np
 import oracle
+from oracle import c_oracle
 from paged_kv_decode_06_gb300 import workloads as wl
 spec = wl.CONFIGS[{config!r}]
 rng = np.random.default_rng(spec.seed)
 sl, ql, qsl, bt, pool = wl.draw_metadata(spec, rng)
 order = np.random.default_rng(123).permutation(spec.num_seqs)
-# a private pool holding only the sampled sequences' pages (same shapes and values' distribution)
-import torch
+impl, threads = {impl!r}, {threads}
+used = c_oracle.max_threads() if (impl == "c" and threads <= 0) else (threads if impl == "c" else 1)
 budget = {budget_s}
 done_bytes = 0; t_used = 0.0; nseq = 0; ntok = 0
 seq_iter = (int(i) for _ in range(1000) for i in order)
 for i in seq_iter:
     L = int(sl[i]); q = int(ql[i]); n = (L + 15) // 16
+    # a private pool holding only this sequence's pages (same shapes and value distribution)
     sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
                          kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
                          k_scale=spec.k_scale, v_scale=spec.v_scale, fp8_source_scale=spec.fp8_source_scale,
                          seed=nseq, token_scale_range=spec.token_scale_range)
     w = wl.make_workload(sub)
     t0 = time.perf_counter()
-    oracle.run_workload(w)
+    if impl == "c":
+        c_oracle.run_workload(w, threads=used)
+    else:
+        oracle.run_workload(w)
     t_used += time.perf_counter() - t0
     done_bytes += w.kv_bytes(); nseq += 1; ntok += L
     if t_used >= budget:
         break
-print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": ntok, "seconds": t_used}}))
+print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": ntok, "seconds": t_used, "threads": used}}))
 """
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = str(threads)
+        env.pop(k, None)
+    if impl == "numpy":
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k] = "1"
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    sample = (f"float64 numpy oracle, {d['seqs']} whole sequences ({d['tokens']} cached tokens) drawn from the "
-              f"{config} workload's length mix, {d['seconds']:.1f} s of oracle time, single-threaded BLAS")
-    return d["gbs"], threads, sample
+    what = (f"plain-C float64 oracle, {d['threads']} OpenMP thread(s)" if impl == "c"
+            else "float64 NumPy oracle, single-threaded BLAS")
+    sample = (f"{what}, {d['seqs']} whole sequences ({d['tokens']} cached tokens) drawn from the {config} "
+              f"workload's length mix, {d['seconds']:.1f} s of oracle time")
+    return d["gbs"], d["threads"], sample
+
+
+def cpu_baseline(config: str, budget_s: float):
+    """The ``cpu_baseline`` object: the C oracle on all host cores (value), on
+    one core, and the NumPy oracle on one core, each on its own bounded sample."""
+    gbs, cores, sample = cpu_oracle_sample(config, budget_s=0.4 * budget_s, threads=0, impl="c")
+    g1, _, s1 = cpu_oracle_sample(config, budget_s=0.3 * budget_s, threads=1, impl="c")
+    gn, _, sn = cpu_oracle_sample(config, budget_s=0.3 * budget_s, threads=1, impl="numpy")
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "host_cores": os.cpu_count(), "host_cpu": _cpu_model(),
+            "single_core": {"value": g1, "unit": "GB/s", "cores": 1, "sample": s1},
+            "numpy_single_core": {"value": gn, "unit": "GB/s", "cores": 1, "sample": sn}}
+
+
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def run_reference(args, world, rank):
@@ -172,10 +208,11 @@ def run_reference(args, world, rank):
         return
     vals = []
     sample = ""
+    cores = 1
     for _ in range(max(1, args.warmup)):
-        cpu_oracle_sample(args.config, budget_s=2.0)
+        cpu_oracle_sample(args.config, budget_s=1.0, threads=0, impl="c")
     for _ in range(args.steps):
-        gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.ref_budget)
+        gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.ref_budget, threads=0, impl="c")
         vals.append(gbs)
     from paged_kv_decode_06_gb300 import workloads as wl
     import numpy as np
@@ -190,7 +227,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_bytes / (v * 1e9) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.config, "kv_bytes_per_step": step_bytes},
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -394,8 +431,7 @@ def run_ours(args, world, rank, local):
         "device_status": status,
     }
     if not args.no_cpu_baseline and not args.batch:
-        gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
