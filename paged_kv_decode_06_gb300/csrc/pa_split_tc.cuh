@@ -15,16 +15,18 @@
 // block per stage: [K d0..63 | K d64..127 | V d0..63 | V d64..127], each
 // part block_pages x 16 rows x 128 bytes, 128-byte swizzled as TMA writes it.
 //
-// Roles (256 threads):
-//   warps 0-2 producers: block-table lookups and TMA loads of each page's K
-//             and V rows into the block's stage, page pg of a block by warp
-//             pg % 3 (a warp's TMA issue is serial, about 90 ns per 2 KB box,
-//             so one warp alone could not keep HBM busy with one-head boxes);
-//   warp 3    MMA issuer (one lane) and owner of the TMEM allocation:
+// Roles (384 threads):
+//   warps 0-1 producers: block-table lookups and TMA loads of each page's K
+//             and V rows into the block's stage, the block's 2 KB boxes dealt
+//             one per lane over both warps (a warp's TMA issue is serial, about
+//             90 ns per 2 KB box, so one warp alone could not keep HBM busy);
+//   warp 3    Q K^T issuer (one lane) and owner of the TMEM allocation:
 //               S[b%2]  = Q[s%2] K_b^T     (TS-MMA, Q read from TMEM, N = 16 * pages)
+//   warp 2    P V issuer (one lane):
 //               O      += (P_hi + P_lo)[b%2] V_b   (TS-MMA, P read from TMEM, N = D)
-//             with S of block b+1 issued before P V of block b, so the tensor
-//             core and the softmax overlap;
+//             Two issuers, because one lane issues a tcgen05.mma every ~60
+//             cycles at best and a single issuer interleaving both streams
+//             (S of block b+1 between P V of blocks b-1 and b) set the pace;
 //   warps 4-11 softmax, two per TMEM lane quarter: thread = query row = TMEM
 //             lane, each of a row's two threads taking two pages of a block
 //             and half of O's columns.  Per block: load S, mask (causal run,
@@ -49,7 +51,8 @@
 
 namespace pa {
 
-constexpr int kTcProducers = 3;
+constexpr int kTcProducers = 2;
+constexpr int kTcPvWarp = 2;
 constexpr int kTcMmaWarp = 3;
 constexpr int kTcSoftmaxWarp0 = 4;   // warps 4..11; a multiple of 4, so warp % 4 is the TMEM lane quarter
 constexpr int kTcSoftmaxWarps = 8;
@@ -167,8 +170,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto qfull_bar = [&](int x) { return xb + 8u * (8 + x); };
   auto ofree_bar = [&](int x) { return xb + 8u * (10 + x); };
   const uint32_t drain_bar = xb + 8u * 12;
-  auto xmax_bar = [&](int x) { return xb + 8u * (13 + x); };
-  auto xsum_bar = [&](int x) { return xb + 8u * (15 + x); };
+  // partial-max / partial-sum exchange: one barrier per TMEM lane quarter and
+  // parity, shared only by that quarter's two softmax warps
+  auto xmax_bar = [&](int q, int x) { return xb + 8u * (18 + 2 * q + x); };
+  auto xsum_bar = [&](int q, int x) { return xb + 8u * (26 + 2 * q + x); };
+  const uint32_t drain2_bar = xb + 8u * 17;
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
       mbar_init(full_bar(s), kTcProducers);   // each producer warp arrives once per block
@@ -181,10 +187,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(odone_bar(x), 1);
       mbar_init(qfull_bar(x), kTcSoftmaxWarps);
       if (x == 0) mbar_init(ofree_bar(x), kTcSoftmaxWarps);   // O is single: one barrier
-      mbar_init(xmax_bar(x), kTcSoftmaxWarps);
-      mbar_init(xsum_bar(x), kTcSoftmaxWarps);
+      for (int q = 0; q < 4; ++q) {
+        mbar_init(xmax_bar(q, x), kTcSoftmaxWarps / 4);
+        mbar_init(xsum_bar(q, x), kTcSoftmaxWarps / 4);
+      }
     }
     mbar_init(drain_bar, 1);
+    mbar_init(drain2_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -268,54 +277,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == kTcMmaWarp) {
-    // ============================ MMA issuer ===============================
+    // ============================ Q K^T issuer =============================
     const uint32_t idesc_s_base = umma_idesc_bf16(128, 16, false) & ~(0x3Fu << 17);
-    const uint32_t idesc_o = umma_idesc_bf16(128, D, true);
     BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
     int stage = 0;
     uint32_t round = 0;
     int b = 0, seg = -1;
-    // the previous block, whose P V is issued after this block's Q K^T
-    int pv_stage = 0, pv_np = 0, pv_seg = 0, pv_vt = 16;
-    bool pv_valid = false, pv_first = false;
     bool ok = true;
-    auto issue_pv = [&](int bb) -> bool {
-      if (!warp_wait(pfull_bar(bb & 1), static_cast<uint32_t>(bb >> 1) & 1u)) return false;
-      // O is overwritten by a segment's first P V: the previous segment's
-      // epilogue must have read it.
-      if (pv_first && pv_seg >= 1 && !warp_wait(ofree_bar(0), static_cast<uint32_t>(pv_seg - 1) & 1u)) return false;
-      const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(pv_stage) * p.stage_bytes);
-      if (pv_vt < kPage) {
-        // Rows past the context in the unit's last page: zero them so that
-        // whatever the pool holds there cannot reach O through 0 * NaN.
-        uint8_t* const vg = gbase + (sb - base) + TG::NH * half_stride + (pv_np - 1) * kTcBox;
-        const int nbytes = (kPage - pv_vt) * 128;
-        for (int h = 0; h < TG::NH; ++h)
-          for (int o = lane * 16; o < nbytes; o += 32 * 16)
-            *reinterpret_cast<uint4*>(vg + h * half_stride + pv_vt * 128 + o) = make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      tc_fence_after();
-      const uint64_t vd0 = umma_sdesc_sw128(sb + TG::NH * half_stride, half_stride, 1024u);
-      const uint32_t tO = tbase + kTmemO;
-      const uint32_t tP = warp_uniform(tbase + kTmemP + 32u * static_cast<uint32_t>(bb & 1));
-      const uint32_t tPlo = tP + (kTmemPlo - kTmemP);
-      if (lane == 0) {
-#pragma unroll
-        for (int pg = 0; pg < kTcMaxBlockPages; ++pg) {
-          if (pg < pv_np) {
-            const uint64_t vd = vd0 + static_cast<uint64_t>((pg * kTcBox) >> 4);
-            umma_ts(tO, tP + 8u * pg, vd, idesc_o, !(pv_first && pg == 0));
-            umma_ts(tO, tPlo + 8u * pg, vd, idesc_o, true);
-          }
-        }
-        umma_commit(odone_bar(bb & 1));
-        umma_commit(empty_bar(pv_stage));
-      }
-      __syncwarp();
-      return true;
-    };
     while (wk.more()) {
       const TcBlock t = wk.next(s_pre, B, NC);
       if (t.first) ++seg;
@@ -326,45 +294,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      {
-        const uint32_t tQ = warp_uniform(tbase + kTmemQ + 64u * static_cast<uint32_t>(seg & 1));
-        const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(stage) * p.stage_bytes);
-        const uint64_t kd = umma_sdesc_sw128(sb, 16u, 1024u);
-        const uint32_t idesc_s = warp_uniform(idesc_s_base | (static_cast<uint32_t>(2 * t.np) << 17));   // N = 16 * np
-        const uint32_t tS = warp_uniform(tbase + kTmemS + 64u * static_cast<uint32_t>(b & 1));
-        if (lane == 0) {
+      const uint32_t tQ = warp_uniform(tbase + kTmemQ + 64u * static_cast<uint32_t>(seg & 1));
+      const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(stage) * p.stage_bytes);
+      const uint64_t kd = umma_sdesc_sw128(sb, 16u, 1024u);
+      const uint32_t idesc_s = warp_uniform(idesc_s_base | (static_cast<uint32_t>(2 * t.np) << 17));   // N = 16 * np
+      const uint32_t tS = warp_uniform(tbase + kTmemS + 64u * static_cast<uint32_t>(b & 1));
+      if (lane == 0) {
 #pragma unroll
-          for (int s = 0; s < TG::KSTEPS; ++s) umma_ts(tS, tQ + 8u * s, kd + k_step(s), idesc_s, s > 0);
-          umma_commit(sfull_bar(b & 1));
-        }
+        for (int s = 0; s < TG::KSTEPS; ++s) umma_ts(tS, tQ + 8u * s, kd + k_step(s), idesc_s, s > 0);
+        umma_commit(sfull_bar(b & 1));
       }
       __syncwarp();
-      if (pv_valid && !issue_pv(b - 1)) {
-        ok = false;
-        break;
-      }
-      pv_valid = true;
-      pv_stage = stage;
-      pv_np = t.np;
-      pv_seg = seg;
-      pv_first = t.first;
-      pv_vt = kPage;
-      if (t.j0 + t.np == t.n) {
-        const SeqInfo si = seq_info(p, s_len, s_qsl, t.i, false, window);
-        pv_vt = si.L - kPage * (si.js + t.n - 1);
-      }
       ++b;
       if (++stage == nstage) {
         stage = 0;
         ++round;
       }
     }
-    if (ok && pv_valid && !issue_pv(b - 1)) ok = false;
     if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
-    // Every MMA this CTA issued must be complete before tensor memory is freed.
+    // Every MMA this warp issued must be complete before tensor memory is freed.
     if (lane == 0) umma_commit(drain_bar);
     __syncwarp();
     if (!warp_wait(drain_bar, 0u) && lane == 0) atomicOr(p.err, kErrTimeout);
+  } else if (warp == kTcPvWarp) {
+    // ============================ P V issuer ===============================
+    // Runs beside the Q K^T issuer, so the two MMA streams do not wait on
+    // each other's barriers; the ordering they need comes through the
+    // softmax: P V of block b waits for P(b), which the softmax writes only
+    // after it has read S(b).
+    const uint32_t idesc_o = umma_idesc_bf16(128, D, true);
+    BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
+    int stage = 0;
+    uint32_t round = 0;
+    int b = 0, seg = -1;
+    bool ok = true;
+    while (wk.more()) {
+      const TcBlock t = wk.next(s_pre, B, NC);
+      if (t.first) ++seg;
+      // full(stage) has completed before P(b) exists; waiting on it here makes
+      // the stage's TMA data visible to this warp directly.
+      if (!warp_wait(pfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u) ||
+          !warp_wait(full_bar(stage), round & 1u) ||
+          // O is overwritten by a segment's first P V: the previous segment's
+          // epilogue must have read it.
+          (t.first && seg >= 1 && !warp_wait(ofree_bar(0), static_cast<uint32_t>(seg - 1) & 1u))) {
+        ok = false;
+        break;
+      }
+      int vt = kPage;
+      if (t.j0 + t.np == t.n) {
+        const SeqInfo si = seq_info(p, s_len, s_qsl, t.i, false, window);
+        vt = si.L - kPage * (si.js + t.n - 1);
+      }
+      const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(stage) * p.stage_bytes);
+      if (vt < kPage) {
+        // Rows past the context in the unit's last page: zero them so that
+        // whatever the pool holds there cannot reach O through 0 * NaN.
+        uint8_t* const vg = gbase + (sb - base) + TG::NH * half_stride + (t.np - 1) * kTcBox;
+        const int nbytes = (kPage - vt) * 128;
+        for (int h = 0; h < TG::NH; ++h)
+          for (int o = lane * 16; o < nbytes; o += 32 * 16)
+            *reinterpret_cast<uint4*>(vg + h * half_stride + vt * 128 + o) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      const uint64_t vd0 = umma_sdesc_sw128(sb + TG::NH * half_stride, half_stride, 1024u);
+      const uint32_t tO = tbase + kTmemO;
+      const uint32_t tP = warp_uniform(tbase + kTmemP + 32u * static_cast<uint32_t>(b & 1));
+      const uint32_t tPlo = tP + (kTmemPlo - kTmemP);
+      if (lane == 0) {
+#pragma unroll
+        for (int pg = 0; pg < kTcMaxBlockPages; ++pg) {
+          if (pg < t.np) {
+            const uint64_t vd = vd0 + static_cast<uint64_t>((pg * kTcBox) >> 4);
+            umma_ts(tO, tP + 8u * pg, vd, idesc_o, !(t.first && pg == 0));
+            umma_ts(tO, tPlo + 8u * pg, vd, idesc_o, true);
+          }
+        }
+        umma_commit(odone_bar(b & 1));
+        umma_commit(empty_bar(stage));
+      }
+      __syncwarp();
+      ++b;
+      if (++stage == nstage) {
+        stage = 0;
+        ++round;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
+    if (lane == 0) umma_commit(drain2_bar);
+    __syncwarp();
+    if (!warp_wait(drain2_bar, 0u) && lane == 0) atomicOr(p.err, kErrTimeout);
   } else {
     // ============================ softmax ==================================
     // Two warps per TMEM lane quarter: warp sw = warp - 4 owns rows
@@ -505,8 +526,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // partner's half of the row max
       xmax[(b & 1) * 256 + hf * 128 + rho] = mp;
       __syncwarp();
-      if (lane == 0) mbar_arrive(xmax_bar(b & 1));
-      if (!warp_wait(xmax_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
+      if (lane == 0) mbar_arrive(xmax_bar(q4, b & 1));
+      if (!warp_wait(xmax_bar(q4, b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
         ok = false;
         break;
       }
@@ -591,8 +612,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the row's total sum
         xsum[(seg & 1) * 256 + hf * 128 + rho] = l;
         __syncwarp();
-        if (lane == 0) mbar_arrive(xsum_bar(seg & 1));
-        if (!warp_wait(xsum_bar(seg & 1), static_cast<uint32_t>(seg >> 1) & 1u)) {
+        if (lane == 0) mbar_arrive(xsum_bar(q4, seg & 1));
+        if (!warp_wait(xsum_bar(q4, seg & 1), static_cast<uint32_t>(seg >> 1) & 1u)) {
           ok = false;
           break;
         }
