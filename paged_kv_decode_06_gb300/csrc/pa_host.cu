@@ -506,6 +506,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   mp.NC = pl.NC;
   mp.R_max = pl.R_max;
   mp.max_qlen = max_qlen;
+  mp.split_grid = pl.grid;
   mp.v_scale = sp.v_scale;
   mp.ws_unit = sp.ws_unit;
   mp.ws_ml = sp.ws_ml;

@@ -71,6 +71,7 @@ struct MergeParams {
   const int32_t* qsl;
   int32_t num_seqs, num_tokens;
   int32_t G, HC, NC, R_max, max_qlen;
+  int32_t split_grid;       // CTAs the split kernel was launched with
   float v_scale;
   const int4* ws_unit;
   const float2* ws_ml;

@@ -175,13 +175,39 @@ __global__ void __launch_bounds__(kWideThreads) pa_merge_wide_kernel(const Merge
   __shared__ float2 s_ml[PG][LPD];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const MergeRow m = merge_row<D>(p, blockIdx.x, blockIdx.y, tid < 32 ? lane : -1);
-  if (!m.work) return;
   const int dq = tid % LPD;
   const int pg = tid / LPD;
+  // A single unit (one sequence and head chunk over the whole grid, the
+  // batch-1 case) starts at CTA 0's first page, so its piece s is CTA s's
+  // slot 2s: those loads go out before the unit's descriptor returns (slots
+  // past the piece count hold stale values and are dropped below).
+  constexpr int kSpec = 256 / PG;   // up to 256 split CTAs
+  const bool spec = gridDim.x == 1 && p.split_grid <= kSpec * PG;
+  float2 sml[kSpec];
+  float4 so[kSpec];
+  if (spec) {
+    const int hh = blockIdx.y / p.R_max, rho = blockIdx.y - hh * p.R_max;
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) {
+      const int sp = pg + u * PG;
+      if (sp < p.split_grid && blockIdx.y < p.HC * p.R_max) {
+        const int64_t sl = (static_cast<int64_t>(2 * sp) * p.HC + hh) * p.R_max + rho;
+        sml[u] = p.ws_ml[sl];
+        so[u] = *reinterpret_cast<const float4*>(p.ws_o + sl * D + 4 * dq);
+      }
+    }
+  }
+  const MergeRow m = merge_row<D>(p, blockIdx.x, blockIdx.y, tid < 32 ? lane : -1);
+  if (!m.work) return;
   float mx = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  gather_partials<D>(p, m, pg, PG, dq, mx, l, acc);
+  if (spec && m.gf == 0 && !m.first_is_tail) {
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u)
+      if (pg + u * PG < m.nparts) lse_acc(mx, l, acc, sml[u].x, sml[u].y, so[u]);
+  } else {
+    gather_partials<D>(p, m, pg, PG, dq, mx, l, acc);
+  }
   s_acc[pg][dq] = acc;
   s_ml[pg][dq] = make_float2(mx, l);
   __syncthreads();

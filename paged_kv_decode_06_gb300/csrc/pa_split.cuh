@@ -557,11 +557,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   }
   // Inputs may come from the previous kernel in the stream (programmatic
   // dependent launch): nothing global is read before this point.
-  grid_dependency_wait();
-
-  // ---- prologue: metadata to shared memory, pages per sequence, prefix -----
-  page_prefix(p, window, s_pre, s_len, s_qsl, s_scan, &s_total);
-
+  // The pipeline barriers live in shared memory only, so they are set up
+  // while the previous kernel may still be running.
   const uint32_t bar0 = base + p.off_bar;
   const int nstage = p.nstage;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -580,7 +577,12 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     }
     fence_mbar_init();
   }
-  __syncthreads();
+
+  grid_dependency_wait();
+
+  // ---- prologue: metadata to shared memory, pages per sequence, prefix -----
+  page_prefix(p, window, s_pre, s_len, s_qsl, s_scan, &s_total);
+  __syncthreads();   // the prefix totals and the mbarrier initialisation above
 
   const int64_t X = static_cast<int64_t>(p.NC) * s_pre[B];
   int64_t ng64 = (X + p.min_pages - 1) / p.min_pages;
