@@ -27,20 +27,23 @@
 //             Two issuers, because one lane issues a tcgen05.mma every ~60
 //             cycles at best and a single issuer interleaving both streams
 //             (S of block b+1 between P V of blocks b-1 and b) set the pace;
-//   warps 4-11 softmax, two per TMEM lane quarter: thread = query row = TMEM
-//             lane, each of a row's two threads taking two pages of a block
-//             and half of O's columns.  Per block: load S, mask (causal run,
-//             context tail, sliding window), exchange the partial row max, update the
-//             running max, rescale O in TMEM only when the max grew by more
-//             than 2^8 (lazy rescale), write P to TMEM as two bf16 terms
-//             P_hi = bf16(P), P_lo = bf16(P - P_hi), so P V carries P to about
-//             16 bits instead of bf16's 8 (a row dominated by one or two keys
-//             would otherwise lose up to 2^-9 |v| to P's rounding); at a segment's
-//             end normalise O and write out / lse or the partials.  They also
-//             store each segment's Q rows into one of two TMEM slots.
-// TMEM columns: O [0,128) S0 [128,192) S1 [192,256) P_hi0 [256,288)
-//               P_hi1 [288,320) P_lo0 [320,352) P_lo1 [352,384) Q0 [384,448)
-//               Q1 [448,512) (bf16 pairs: 8 columns per 16 keys or features).
+//   warps 4-11 softmax, two groups of four: group g takes the blocks b with
+//             b % 2 == g, so two blocks' softmax work overlaps; in a group,
+//             thread = query row = TMEM lane and owns all of a block's keys,
+//             with the group's own running max, sum and O accumulator.  Per
+//             block: load S, mask (causal run, context tail, sliding window),
+//             update the running max, rescale O in TMEM only when the max grew
+//             by more than 2^8 (lazy rescale), write P over the block's S as two
+//             bf16 terms P_hi = bf16(P), P_lo = bf16(P - P_hi), so P V carries P
+//             to about 16 bits instead of bf16's 8 (a row dominated by one or two
+//             keys would otherwise lose up to 2^-9 |v| to P's rounding).  At a
+//             segment's end the two threads of a row exchange (max, sum), each
+//             combines half of the two O accumulators and writes out / lse or the
+//             partials.  They also store each segment's Q rows into one of two
+//             TMEM slots.
+// TMEM columns: O_0 [0,128) O_1 [128,256) S/P of group 0 [256,320) and of
+//               group 1 [320,384) (S fp32, 16 columns per page; P_hi at +8 per
+//               page, P_lo at +32 + 8 per page) Q0 [384,448) Q1 [448,512).
 // Shared memory holds only the ring (6 stages of 4 pages at D = 128) and
 // metadata: Q lives in TMEM, as the A operand of a TS-MMA.
 // Every wait is bounded (kErrTimeout); the CTA drains its MMAs before it frees
@@ -59,10 +62,10 @@ constexpr int kTcSoftmaxWarps = 8;
 constexpr int kTcThreads = 32 * (kTcSoftmaxWarp0 + kTcSoftmaxWarps);
 constexpr int kTcMaxBlockPages = 4;
 constexpr uint32_t kTcCols = 512;
-constexpr uint32_t kTmemO = 0;     // fp32 O, D columns
-constexpr uint32_t kTmemS = 128;   // + 64 * (block % 2): fp32 S, 16 columns per page
-constexpr uint32_t kTmemP = 256;   // + 32 * (block % 2): bf16 P rounded to nearest, 8 columns per page
-constexpr uint32_t kTmemPlo = 320; // + 32 * (block % 2): bf16 of the rounding residue
+constexpr uint32_t kTmemO = 0;     // + 128 * group: fp32 O of softmax group g, D columns
+constexpr uint32_t kTmemSP = 256;  // + 64 * group: fp32 S of the group's block, 16 columns per page;
+constexpr uint32_t kTmemPhi = 0;   //   P overwrites it: bf16 P at + 8 * page,
+constexpr uint32_t kTmemPlo = 32;  //   bf16 rounding residue at + 32 + 8 * page
 constexpr uint32_t kTmemQ = 384;   // + 64 * (segment % 2): bf16 Q, D / 2 columns
 constexpr uint32_t kTcBox = 2048;  // one page of one 64-column half: 16 rows x 128 bytes
 constexpr uint32_t kTcHalf = kTcMaxBlockPages * kTcBox;   // one 64-column half of a stage's K or V
@@ -163,17 +166,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (nstage + s); };
   const uint32_t xb = bar0 + 8u * (2 * nstage);
-  auto sfull_bar = [&](int x) { return xb + 8u * x; };
-  auto sfree_bar = [&](int x) { return xb + 8u * (2 + x); };
-  auto pfull_bar = [&](int x) { return xb + 8u * (4 + x); };
-  auto odone_bar = [&](int x) { return xb + 8u * (6 + x); };
+  // per softmax group g (blocks b with b % 2 == g): S ready, P ready, P V done
+  auto sfull_bar = [&](int g) { return xb + 8u * g; };
+  auto pfull_bar = [&](int g) { return xb + 8u * (4 + g); };
+  auto odone_bar = [&](int g) { return xb + 8u * (6 + g); };
   auto qfull_bar = [&](int x) { return xb + 8u * (8 + x); };
-  auto ofree_bar = [&](int x) { return xb + 8u * (10 + x); };
+  const uint32_t ofree_bar = xb + 8u * 10;   // both O accumulators read by a segment's epilogue
   const uint32_t drain_bar = xb + 8u * 12;
-  // partial-max / partial-sum exchange: one barrier per TMEM lane quarter and
-  // parity, shared only by that quarter's two softmax warps
-  auto xmax_bar = [&](int q, int x) { return xb + 8u * (18 + 2 * q + x); };
-  auto xsum_bar = [&](int q, int x) { return xb + 8u * (26 + 2 * q + x); };
+  // a segment's (max, sum) exchange between the two groups' warps of one
+  // TMEM lane quarter
+  auto xstat_bar = [&](int q) { return xb + 8u * (18 + q); };
   const uint32_t drain2_bar = xb + 8u * 17;
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
@@ -182,16 +184,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(sfull_bar(x), 1);
-      mbar_init(sfree_bar(x), kTcSoftmaxWarps);
-      mbar_init(pfull_bar(x), kTcSoftmaxWarps);
+      mbar_init(pfull_bar(x), kTcSoftmaxWarps / 2);
       mbar_init(odone_bar(x), 1);
       mbar_init(qfull_bar(x), kTcSoftmaxWarps);
-      if (x == 0) mbar_init(ofree_bar(x), kTcSoftmaxWarps);   // O is single: one barrier
-      for (int q = 0; q < 4; ++q) {
-        mbar_init(xmax_bar(q, x), kTcSoftmaxWarps / 4);
-        mbar_init(xsum_bar(q, x), kTcSoftmaxWarps / 4);
-      }
     }
+    mbar_init(ofree_bar, kTcSoftmaxWarps);
+    for (int q = 0; q < 4; ++q) mbar_init(xstat_bar(q), 2);
     mbar_init(drain_bar, 1);
     mbar_init(drain2_bar, 1);
     fence_mbar_init();
@@ -287,8 +285,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     while (wk.more()) {
       const TcBlock t = wk.next(s_pre, B, NC);
       if (t.first) ++seg;
+      // S(b) goes where P(b-2), the same group's previous block, was: its P V
+      // must be done (the group read S(b-2) before it wrote P(b-2)).
       if (!warp_wait(full_bar(stage), round & 1u) ||
-          (b >= 2 && !warp_wait(sfree_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u)) ||
+          (b >= 2 && !warp_wait(odone_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u)) ||
           (t.first && !warp_wait(qfull_bar(seg & 1), static_cast<uint32_t>(seg >> 1) & 1u))) {
         ok = false;
         break;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t sb = warp_uniform(stage0 + static_cast<uint32_t>(stage) * p.stage_bytes);
       const uint64_t kd = umma_sdesc_sw128(sb, 16u, 1024u);
       const uint32_t idesc_s = warp_uniform(idesc_s_base | (static_cast<uint32_t>(2 * t.np) << 17));   // N = 16 * np
-      const uint32_t tS = warp_uniform(tbase + kTmemS + 64u * static_cast<uint32_t>(b & 1));
+      const uint32_t tS = warp_uniform(tbase + kTmemSP + 64u * static_cast<uint32_t>(b & 1));
       if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < TG::KSTEPS; ++s) umma_ts(tS, tQ + 8u * s, kd + k_step(s), idesc_s, s > 0);
@@ -326,18 +326,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
     int stage = 0;
     uint32_t round = 0;
-    int b = 0, seg = -1;
+    int b = 0, seg = -1, b0 = 0;
     bool ok = true;
     while (wk.more()) {
       const TcBlock t = wk.next(s_pre, B, NC);
-      if (t.first) ++seg;
+      if (t.first) {
+        ++seg;
+        b0 = b;
+      }
+      // a group's first block of the segment overwrites its O
+      const bool ofirst = b - b0 < 2;
       // full(stage) has completed before P(b) exists; waiting on it here makes
       // the stage's TMA data visible to this warp directly.
       if (!warp_wait(pfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u) ||
           !warp_wait(full_bar(stage), round & 1u) ||
-          // O is overwritten by a segment's first P V: the previous segment's
-          // epilogue must have read it.
-          (t.first && seg >= 1 && !warp_wait(ofree_bar(0), static_cast<uint32_t>(seg - 1) & 1u))) {
+          // the previous segment's epilogue must have read both O accumulators
+          (ofirst && seg >= 1 && !warp_wait(ofree_bar, static_cast<uint32_t>(seg - 1) & 1u))) {
         ok = false;
         break;
       }
@@ -360,15 +364,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_after();
       const uint64_t vd0 = umma_sdesc_sw128(sb + TG::NH * half_stride, half_stride, 1024u);
-      const uint32_t tO = tbase + kTmemO;
-      const uint32_t tP = warp_uniform(tbase + kTmemP + 32u * static_cast<uint32_t>(b & 1));
-      const uint32_t tPlo = tP + (kTmemPlo - kTmemP);
+      const uint32_t tO = warp_uniform(tbase + kTmemO + 128u * static_cast<uint32_t>(b & 1));
+      const uint32_t tP = warp_uniform(tbase + kTmemSP + 64u * static_cast<uint32_t>(b & 1) + kTmemPhi);
+      const uint32_t tPlo = tP + (kTmemPlo - kTmemPhi);
       if (lane == 0) {
 #pragma unroll
         for (int pg = 0; pg < kTcMaxBlockPages; ++pg) {
           if (pg < t.np) {
             const uint64_t vd = vd0 + static_cast<uint64_t>((pg * kTcBox) >> 4);
-            umma_ts(tO, tP + 8u * pg, vd, idesc_o, !(t.first && pg == 0));
+            umma_ts(tO, tP + 8u * pg, vd, idesc_o, !(ofirst && pg == 0));
             umma_ts(tO, tPlo + 8u * pg, vd, idesc_o, true);
           }
         }
@@ -388,30 +392,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!warp_wait(drain2_bar, 0u) && lane == 0) atomicOr(p.err, kErrTimeout);
   } else {
     // ============================ softmax ==================================
-    // Two warps per TMEM lane quarter: warp sw = warp - 4 owns rows
-    // 32 * (sw % 4) .. +31 and half hf = sw / 4 of every block (pages 2hf and
-    // 2hf+1) and of O's columns.  The two warps of a row exchange their partial
-    // row max every block, and their partial sums at a segment's end, through
-    // shared memory and a bounded mbarrier round.
-    const int sw = warp - kTcSoftmaxWarp0;
-    const int q4 = warp & 3;               // TMEM lane quarter this warp may access (== sw % 4)
-    const int hf = sw >> 2;
+    // Two groups of four warps; group gi = (warp - 4) / 4 takes the blocks b
+    // with b % 2 == gi, so two blocks' softmax work overlaps.  Warp q4 = warp % 4
+    // of a group owns rows 32 * q4 .. +31 (thread = query row = TMEM lane) and
+    // all of a block's keys, with its own running max and sum and its own O
+    // accumulator in tensor memory.  At a segment's end the two threads of a
+    // row exchange (max, sum) through shared memory and a bounded mbarrier
+    // round and each combines half of O's columns.
+    const int gi = (warp - kTcSoftmaxWarp0) >> 2;
+    const int q4 = warp & 3;               // TMEM lane quarter this warp may access
     const int rho = 32 * q4 + lane;        // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    float* const xmax = reinterpret_cast<float*>(gbase + p.off_xchg);   // [block % 2][half][128] partial max
-    float* const xsum = xmax + 512;                                     // [segment % 2][half][128] partial sum
-    constexpr int HD = D / 2;              // O columns per half
+    float2* const xstat = reinterpret_cast<float2*>(gbase + p.off_xchg);   // [segment % 2][group][128] (max, sum)
+    constexpr int HD = D / 2;              // O columns each group's thread writes out
+    constexpr int NP4 = kTcMaxBlockPages;
     BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
-    int b = 0, seg = -1;
+    int b = 0, seg = -1, b0 = 0;
     SeqInfo si = {0, 0, 0, 0};
     bool row_ok = false;
     int lim = 0, seg_j0 = 0;
     int64_t seg_k0 = 0;
-    float m = -INFINITY, l = 0.f;          // running max (log2 units, shared by both halves), this half's sum
+    float m = -INFINITY, l = 0.f;          // this group's running max (log2 units) and sum of the row
     bool ok = true;
 
-    // This thread's half of row rho of the segment starting at block t, into
-    // TMEM Q slot `slot` (rows past G * qn are zero); q_full counts the 8 warps.
+    // This thread's half (by group) of row rho of the segment starting at
+    // block t, into TMEM Q slot `slot` (rows past G * qn are zero); q_full
+    // counts the 8 warps.
     auto stage_q = [&](const TcBlock& t, int slot) {
       const SeqInfo s2 = seq_info(p, s_len, s_qsl, t.i, false, window);
       const bool have = rho < G * s2.qn;
@@ -419,13 +425,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (have)
         src = reinterpret_cast<const uint4*>(p.q + static_cast<int64_t>(s2.t0 + rho / G) * p.q_stride_t +
                                              static_cast<int64_t>(t.c * G + rho % G) * D);
-      const uint32_t tq = tbase + lane_off + kTmemQ + 64u * static_cast<uint32_t>(slot) + (D / 4) * hf;
+      const uint32_t tq = tbase + lane_off + kTmemQ + 64u * static_cast<uint32_t>(slot) + (D / 4) * gi;
 #pragma unroll
       for (int k = 0; k < D / 64; ++k) {      // 16 columns (32 features) at a time
         uint32_t w[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 v = have ? src[(D / 16) * hf + 4 * k + u] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 v = have ? src[(D / 16) * gi + 4 * k + u] : make_uint4(0u, 0u, 0u, 0u);
           w[4 * u] = v.x;
           w[4 * u + 1] = v.y;
           w[4 * u + 2] = v.z;
@@ -443,15 +449,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TcBlock t = wk.next(s_pre, B, NC);
       if (t.first) {
         ++seg;
+        b0 = b;
         if (seg == 0) stage_q(t, 0);
-        si = seq_info(p, s_len, s_qsl, t.i, rho == 0 && hf == 0, window);
+        si = seq_info(p, s_len, s_qsl, t.i, rho == 0 && gi == 0, window);
         row_ok = rho < G * si.qn;
         lim = si.L - si.qn + (row_ok ? rho / G : 0);
         seg_j0 = t.j0;
         seg_k0 = t.k0;
         m = -INFINITY;
         l = 0.f;
-        if (seg_j0 == 0 && rho == 0 && hf == 0) {
+        if (seg_j0 == 0 && rho == 0 && gi == 0) {
           // This CTA holds the unit's first page: describe the unit for the merge.
           const int64_t a = static_cast<int64_t>(NC) * s_pre[t.i] + static_cast<int64_t>(t.c) * t.n;
           const int last_cta = static_cast<int>(((a + t.n) * NG - 1) / X);
@@ -459,128 +466,119 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.ws_unit[static_cast<int64_t>(t.i) * NC + t.c] =
               make_int4(g, pieces | (t.k0 != 0 ? (1 << 30) : 0), si.t0, si.qn);
         }
-        if (p.sinks != nullptr && seg_j0 == 0 && row_ok) {
+        if (p.sinks != nullptr && seg_j0 == 0 && row_ok && gi == (b & 1)) {
           // The sink is a virtual first key (logit sinks[hq], zero value row),
-          // counted once (in half 0's sum) by the piece holding the unit's first page.
+          // counted once, by the group taking the segment's first block in the
+          // piece holding the unit's first page.
           m = p.sinks[t.c * G + rho % G] * 1.4426950408889634f;
-          l = hf == 0 ? 1.f : 0.f;
+          l = 1.f;
         }
       }
-      // ---- this half's S row of the block ----------------------------------
-      if (!warp_wait(sfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[2][16];
-      {
-        const uint32_t tS = tbase + lane_off + kTmemS + 64u * static_cast<uint32_t>(b & 1) + 32u * hf;
-        uint32_t r[2][16];
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          if (2 * hf + k < t.np) tmem_ld16(tS + 16u * k, r[k]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) sv[k][e] = __uint_as_float(r[k][e]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sfree_bar(b & 1));
-      // ---- mask, block max ---------------------------------------------------
-      // An interior block (all four pages present, every token visible to
-      // every row of the run, no window edge inside) needs no per-element
-      // mask: its max is taken over the raw scores and the scale is folded
-      // into the exponent's FFMA.  Rows past G * qn hold zero queries there
-      // and produce values nobody reads.
-      const int tb = kPage * (si.js + t.j0);
-      const float c = p.scale_log2;
-      bool interior = t.np == kTcMaxBlockPages && c > 0.f && tb + kTcMaxBlockPages * kPage <= si.L - si.qn + 1;
-      if (WINDOW && window > 0) interior = interior && tb > si.L - 1 - window;
-      float mp;
-      if (interior) {
-        float mx[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(sv[0][e], sv[1][e]);
-#pragma unroll
-        for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-          for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
-        mp = mx[0] * c;
-      } else {
-        mp = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int pg = 2 * hf + k;
-            const int tok = tb + 16 * pg + e;
-            bool vis = row_ok && pg < t.np && tok <= lim;
-            if (WINDOW && window > 0) vis = vis && tok > lim - window;
-            const float x = vis ? sv[k][e] * c : -INFINITY;
-            sv[k][e] = x;
-            mp = fmaxf(mp, x);
-          }
-      }
-      // partner's half of the row max
-      xmax[(b & 1) * 256 + hf * 128 + rho] = mp;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xmax_bar(q4, b & 1));
-      if (!warp_wait(xmax_bar(q4, b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      const float mb = fmaxf(mp, xmax[(b & 1) * 256 + (hf ^ 1) * 128 + rho]);
-      const float m_new = fmaxf(m, mb);
-      const bool grow = m_new > m + 8.f;   // also true when m = -inf and m_new is finite
-      if (t.first) {
-        if (grow) {
-          l *= fast_exp2(m - m_new);       // sink only: O has no history in this segment
-          m = m_new;
-        }
-      } else if (__any_sync(0xffffffffu, grow)) {
-        // O must hold P V of the previous block before it is rescaled.
-        if (!warp_wait(odone_bar((b - 1) & 1), static_cast<uint32_t>((b - 1) >> 1) & 1u)) {
+      if ((b & 1) == gi) {
+        // ---- the block's S row ----------------------------------------------
+        if (!warp_wait(sfull_bar(gi), static_cast<uint32_t>(b >> 1) & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float alpha = grow ? fast_exp2(m - m_new) : 1.f;
-        const uint32_t tO = tbase + lane_off + kTmemO + HD * hf;
+        const uint32_t tSP = tbase + lane_off + kTmemSP + 64u * static_cast<uint32_t>(gi);
+        float sv[NP4][16];
+        {
+          // every page's columns are read; pages past the block's end hold
+          // stale scores that the mask below discards
+          uint32_t r[NP4][16];
 #pragma unroll
-        for (int ch = 0; ch < HD / 16; ++ch) {
-          uint32_t r[16];
-          tmem_ld16(tO + 16u * ch, r);
+          for (int k = 0; k < NP4; ++k) tmem_ld16(tSP + 16u * k, r[k]);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tmem_st16(tO + 16u * ch, r);
-        }
-        tmem_wait_st();
-        if (grow) {
-          l *= alpha;
-          m = m_new;
-        }
-      }
-      // ---- P (bf16 hi + lo) into TMEM ------------------------------------------
-      // P[b%2] was last read by the P V of block b-2.
-      if (b >= 2 && !warp_wait(odone_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      {
-        // exp2 of -inf is +0, so masked scores need no select once the
-        // subtracted max is finite (it is -inf only while no key was visible).
-        const float mneg = m == -INFINITY ? 0.f : -m;
-        const float mult = interior ? c : 1.f;   // masked scores are already scaled
-        const uint32_t tP = tbase + lane_off + kTmemP + 32u * static_cast<uint32_t>(b & 1) + 16u * hf;
-        const uint32_t tPlo = tP + (kTmemPlo - kTmemP);
-        float lsum = 0.f;
+          for (int k = 0; k < NP4; ++k)
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (2 * hf + k < t.np) {
+            for (int e = 0; e < 16; ++e) sv[k][e] = __uint_as_float(r[k][e]);
+        }
+        // ---- mask, block max -------------------------------------------------
+        // An interior block (all pages present, every token visible to every
+        // row of the run, no window edge inside) needs no per-element mask:
+        // its max is taken over the raw scores and the scale is folded into
+        // the exponent's FFMA.  Rows past G * qn hold zero queries there and
+        // produce values nobody reads.
+        const int tb = kPage * (si.js + t.j0);
+        const float c = p.scale_log2;
+        bool interior = t.np == NP4 && c > 0.f && tb + NP4 * kPage <= si.L - si.qn + 1;
+        if (WINDOW && window > 0) interior = interior && tb > si.L - 1 - window;
+        float mb;
+        if (interior) {
+          float mx[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            mx[e] = sv[0][e];
+#pragma unroll
+            for (int k = 1; k < NP4; ++k) mx[e] = fmaxf(mx[e], sv[k][e]);
+          }
+#pragma unroll
+          for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+            for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
+          mb = mx[0] * c;
+        } else {
+          mb = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < NP4; ++k)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int tok = tb + 16 * k + e;
+              bool vis = row_ok && k < t.np && tok <= lim;
+              if (WINDOW && window > 0) vis = vis && tok > lim - window;
+              const float x = vis ? sv[k][e] * c : -INFINITY;
+              sv[k][e] = x;
+              mb = fmaxf(mb, x);
+            }
+        }
+        const float m_new = fmaxf(m, mb);
+        const bool grow = m_new > m + 8.f;   // also true when m = -inf and m_new is finite
+        if (b - b0 < 2) {
+          // the group's first block of the segment: O has no history yet
+          if (grow) {
+            l *= fast_exp2(m - m_new);       // only a sink carries weight here
+            m = m_new;
+          }
+        } else if (__any_sync(0xffffffffu, grow)) {
+          // O must hold P V of the group's previous block before it is rescaled.
+          if (!warp_wait(odone_bar(gi), static_cast<uint32_t>((b >> 1) - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = grow ? fast_exp2(m - m_new) : 1.f;
+          const uint32_t tO = tbase + lane_off + kTmemO + 128u * static_cast<uint32_t>(gi);
+#pragma unroll
+          for (int ch = 0; ch < D / 16; ++ch) {
+            uint32_t r[16];
+            tmem_ld16(tO + 16u * ch, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st16(tO + 16u * ch, r);
+          }
+          tmem_wait_st();
+          if (grow) {
+            l *= alpha;
+            m = m_new;
+          }
+        }
+        // ---- P (bf16 hi + lo) over the block's S ------------------------------
+        // This thread has read its whole S row above; P V of the group's
+        // previous block read P from these columns before Q K^T of this block
+        // was issued into them.
+        {
+          // exp2 of -inf is +0, so masked scores need no select once the
+          // subtracted max is finite (it is -inf only while no key was visible).
+          const float mneg = m == -INFINITY ? 0.f : -m;
+          const float mult = interior ? c : 1.f;   // masked scores are already scaled
+          const uint32_t tP = tSP + kTmemPhi;
+          const uint32_t tPlo = tSP + kTmemPlo;
+          float lsum = 0.f;
+#pragma unroll
+          for (int k = 0; k < NP4; ++k) {
             uint32_t w[8], wl[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -593,13 +591,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tmem_st8(tP + 8u * k, w);
             tmem_st8(tPlo + 8u * k, wl);
           }
+          l += lsum;
+          tmem_wait_st();
         }
-        l += lsum;
-        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull_bar(gi));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pfull_bar(b & 1));
 
       if (t.last) {
         // The next segment's Q goes into the other slot now, so its S can be
@@ -609,65 +607,88 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const TcBlock nt = peek.next(s_pre, B, NC);
           stage_q(nt, (seg + 1) & 1);
         }
-        // the row's total sum
-        xsum[(seg & 1) * 256 + hf * 128 + rho] = l;
+        // the other group's (max, sum) of the row
+        xstat[(seg & 1) * 256 + gi * 128 + rho] = make_float2(m, l);
         __syncwarp();
-        if (lane == 0) mbar_arrive(xsum_bar(q4, seg & 1));
-        if (!warp_wait(xsum_bar(q4, seg & 1), static_cast<uint32_t>(seg >> 1) & 1u)) {
+        if (lane == 0) mbar_arrive(xstat_bar(q4));
+        if (!warp_wait(xstat_bar(q4), static_cast<uint32_t>(seg) & 1u)) {
           ok = false;
           break;
         }
-        const float lt = l + xsum[(seg & 1) * 256 + (hf ^ 1) * 128 + rho];
-        if (!warp_wait(odone_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u)) {
+        const float2 other = xstat[(seg & 1) * 256 + (gi ^ 1) * 128 + rho];
+        // group 0's and group 1's statistics
+        const float m0 = gi == 0 ? m : other.x, l0 = gi == 0 ? l : other.y;
+        const float m1 = gi == 0 ? other.x : m, l1 = gi == 0 ? other.y : l;
+        const float mt = fmaxf(m0, m1);
+        const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mt);
+        const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mt);
+        const float lt = l0 * a0 + l1 * a1;
+        // Each group's last block of the segment: b and b - 1 (this block is
+        // the segment's last); a group with no block in it has no O to read.
+        const int bl0 = (b & 1) == 0 ? b : b - 1;
+        const int bl1 = (b & 1) == 1 ? b : b - 1;
+        const bool has0 = bl0 >= b0, has1 = bl1 >= b0;
+        if ((has0 && !warp_wait(odone_bar(0), static_cast<uint32_t>(bl0 >> 1) & 1u)) ||
+            (has1 && !warp_wait(odone_bar(1), static_cast<uint32_t>(bl1 >> 1) & 1u))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const bool complete = (seg_j0 == 0) && (t.j0 + t.np == t.n);
-        const uint32_t tO = tbase + lane_off + kTmemO + HD * hf;
+        const uint32_t tO0 = tbase + lane_off + kTmemO + HD * gi;   // this thread's half of the columns
+        const uint32_t tO1 = tO0 + 128u;
         const int tok = si.t0 + rho / G;
         const int hq = t.c * G + rho % G;
         const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
         uint16_t* orow =
-            p.out + static_cast<int64_t>(tok) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h + HD * hf;
+            p.out + static_cast<int64_t>(tok) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h + HD * gi;
         const int which = (seg_k0 == 0) ? 0 : 1;
         const int64_t prow = static_cast<int64_t>(2 * g + which) * p.R_max + rho;
-        float* wrow = p.ws_o + prow * D + HD * hf;
+        float* wrow = p.ws_o + prow * D + HD * gi;
 #pragma unroll
         for (int ch = 0; ch < HD / 16; ++ch) {
-          uint32_t r[16];
-          tmem_ld16(tO + 16u * ch, r);
-          tmem_wait_ld();
+          float o[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = 0.f;
+#pragma unroll
+          for (int gg = 0; gg < 2; ++gg) {
+            if (gg == 0 ? has0 : has1) {
+              uint32_t r[16];
+              tmem_ld16((gg == 0 ? tO0 : tO1) + 16u * ch, r);
+              tmem_wait_ld();
+              const float a = gg == 0 ? a0 : a1;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] = fmaf(__uint_as_float(r[e]), a, o[e]);
+            }
+          }
           if (row_ok) {
             if (complete) {
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
                 uint2 v;
-                v.x = pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
-                v.y = pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+                v.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
+                v.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
                 *reinterpret_cast<uint2*>(orow + 16 * ch + e) = v;
               }
             } else {
 #pragma unroll
               for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4*>(wrow + 16 * ch + e) =
-                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                                __uint_as_float(r[e + 3]));
+                *reinterpret_cast<float4*>(wrow + 16 * ch + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
             }
           }
         }
-        if (row_ok && hf == 0) {
+        if (row_ok && gi == 0) {
           if (complete) {
             if (p.lse != nullptr)
               p.lse[static_cast<int64_t>(tok) * p.lse_stride_t + static_cast<int64_t>(hq) * p.lse_stride_h] =
-                  lt > 0.f ? (m + fast_log2(lt)) * 0.69314718055994530942f : -INFINITY;
+                  lt > 0.f ? (mt + fast_log2(lt)) * 0.69314718055994530942f : -INFINITY;
           } else {
-            p.ws_ml[prow] = make_float2(m, lt);
+            p.ws_ml[prow] = make_float2(mt, lt);
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(ofree_bar(0));
+        if (lane == 0) mbar_arrive(ofree_bar);
       }
       ++b;
     }
