@@ -263,3 +263,134 @@ def host_token_scales(w: Workload):
         return None, None
     return (w.k_token_scales.detach().cpu().contiguous().numpy(),
             w.v_token_scales.detach().cpu().contiguous().numpy())
+
+
+# ---------------------------------------------------------------------------
+# Multi-head latent attention (MLA) decode inputs.
+#
+# Layout (ATOM model-operations guide, "Multi-head latent attention": the
+# ``MLAModules`` fields and the decode flow, where the absorbed query and one
+# concatenated latent row per token meet in the decode kernel):
+#
+# * ``q``         bf16 ``[T, Hq, kv_lora_rank + rope]``: per query head the
+#                 absorbed no-position part followed by the rotary part
+# * ``kv_cache``  bf16 or fp8-e4m3 codes ``[NB, 16, kv_lora_rank + rope]``:
+#                 per token the compressed latent followed by the rotary key
+# * ``block_tables``, ``seq_lens``, ``query_start_loc`` as above.
+#
+# Dimensions are DeepSeek-V3's public ones (kv_lora_rank 512, rope 64, 128
+# heads of qk_nope 128 + rope 64): the softmax scale is 1/sqrt(128 + 64).
+
+@dataclasses.dataclass
+class MlaSpec:
+    """Shape and distribution of one synthetic MLA decode batch."""
+
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    kv_dtype: str                      # "bf16" or "fp8"
+    seq_len_kind: str
+    seq_len_args: tuple
+    query_len_choices: tuple = (1,)
+    pool_pages: Optional[int] = None
+    kv_lora_rank: int = 512
+    rope_dim: int = 64
+    qk_nope_head_dim: int = 128
+    kv_scale: float = 1.0
+    fp8_source_scale: float = 1.0
+    seed: int = 0
+
+    @property
+    def head_dim(self) -> int:
+        """Width of a cached row and of a query row."""
+        return self.kv_lora_rank + self.rope_dim
+
+    @property
+    def max_query_len(self) -> int:
+        return max(self.query_len_choices)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.qk_nope_head_dim + self.rope_dim)
+
+
+# DeepSeek-V3-shaped MLA decode on one GPU of an 8-way tensor-parallel group
+# (128 heads / 8 = 16 per GPU): a bf16 single-token batch, and an fp8 batch
+# verifying query runs of four tokens (the MTP verification shape).
+MLA_CONFIGS = {
+    "mla_tiny": MlaSpec(
+        name="mla_tiny", num_seqs=4, num_q_heads=16, kv_dtype="bf16", seq_len_kind="fixed",
+        seq_len_args=(1, 17, 64, 200), pool_pages=64, seed=1007),
+    "mla_tp8": MlaSpec(
+        name="mla_tp8", num_seqs=64, num_q_heads=16, kv_dtype="bf16", seq_len_kind="uniform",
+        seq_len_args=(512, 4096), seed=1008),
+    "mla_mtp_fp8": MlaSpec(
+        name="mla_mtp_fp8", num_seqs=32, num_q_heads=16, kv_dtype="fp8", seq_len_kind="uniform",
+        seq_len_args=(1024, 16384), query_len_choices=(4,), kv_scale=0.05, fp8_source_scale=0.05, seed=1009),
+}
+
+
+@dataclasses.dataclass
+class MlaWorkload:
+    spec: MlaSpec
+    seq_lens: np.ndarray
+    query_lens: np.ndarray
+    query_start_loc: Optional[np.ndarray]
+    block_tables: np.ndarray
+    num_pages: int
+    q: torch.Tensor                 # bf16 [T, Hq, Dqk]
+    kv_cache: torch.Tensor          # bf16 or uint8 (e4m3 codes) [NB, 16, Dqk]
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_lens.sum())
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.spec.kv_dtype == "fp8" else 2
+
+    def kv_bytes(self) -> int:
+        """Algorithmic cache bytes of one step: every cached token's latent row
+        (latent and rotary parts) read once; the value is part of that row."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.spec.head_dim * self.kv_elem_bytes
+
+
+def make_mla_workload(spec: MlaSpec, device: str = "cpu", seed: Optional[int] = None) -> MlaWorkload:
+    """One seeded MLA batch: metadata from numpy's PCG64, tensor contents from
+    torch's generator on ``device`` (q and cache rows N(0,1); fp8 codes
+    e4m3(N(0,1) / fp8_source_scale))."""
+    seed = spec.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    seq_lens, query_lens, qsl, block_tables, pool = draw_metadata(spec, rng)
+    T = int(query_lens.sum())
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    fp8 = spec.kv_dtype == "fp8"
+    q = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=device)
+    _fill_normal(q, gen, 1.0, False)
+    cache = torch.empty((pool, PAGE_SIZE, spec.head_dim), dtype=torch.uint8 if fp8 else torch.bfloat16,
+                        device=device)
+    _fill_normal(cache, gen, spec.fp8_source_scale if fp8 else 1.0, fp8)
+    return MlaWorkload(spec=spec, seq_lens=seq_lens, query_lens=query_lens, query_start_loc=qsl,
+                       block_tables=block_tables, num_pages=pool, q=q, kv_cache=cache)
+
+
+def custom_mla_spec(name="custom_mla", num_q_heads=16, kv_dtype="bf16", seq_lens=(5, 16, 33),
+                    query_len_choices=(1,), pool_pages=None, kv_scale=1.0, fp8_source_scale=1.0, seed=11,
+                    kv_lora_rank=512, rope_dim=64) -> MlaSpec:
+    """A small MLA spec with explicit sequence lengths (for edge cases)."""
+    return MlaSpec(name=name, num_seqs=len(seq_lens), num_q_heads=num_q_heads, kv_dtype=kv_dtype,
+                   seq_len_kind="fixed", seq_len_args=tuple(seq_lens), query_len_choices=tuple(query_len_choices),
+                   pool_pages=pool_pages, kv_lora_rank=kv_lora_rank, rope_dim=rope_dim, kv_scale=kv_scale,
+                   fp8_source_scale=fp8_source_scale, seed=seed)
+
+
+def host_mla_arrays(w: MlaWorkload):
+    """Host copies for the CPU side: q as uint16 bf16 patterns, the cache as
+    uint16 patterns (bf16) or uint8 codes (fp8)."""
+    q_bits = w.q.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    if w.spec.kv_dtype == "fp8":
+        c = w.kv_cache.detach().cpu().contiguous().numpy()
+    else:
+        c = w.kv_cache.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return q_bits, c

@@ -61,3 +61,27 @@ def test_fp8_codes_are_finite_and_spread():
 def test_kv_bytes_counts_every_cached_token_once():
     w = wl.make_workload(wl.CONFIGS["tiny"])
     assert w.kv_bytes() == 282 * 2 * 128 * 2 * 2
+
+
+@pytest.mark.parametrize("name", sorted(wl.MLA_CONFIGS))
+def test_mla_metadata_and_shapes(name):
+    spec = wl.MLA_CONFIGS[name]
+    sl, ql, qsl, bt, pool = wl.draw_metadata(spec, np.random.default_rng(spec.seed))
+    n = (sl + 15) // 16
+    used = np.concatenate([bt[i, :n[i]] for i in range(spec.num_seqs)])
+    assert len(np.unique(used)) == len(used) and used.max() < pool
+    assert (sl >= ql).all() and (ql <= spec.max_query_len).all()
+    assert spec.head_dim == spec.kv_lora_rank + spec.rope_dim == 576
+    assert abs(spec.scale - 192 ** -0.5) < 1e-15
+
+
+def test_mla_workload_is_reproducible_and_laid_out():
+    spec = wl.MLA_CONFIGS["mla_tiny"]
+    a, b = wl.make_mla_workload(spec), wl.make_mla_workload(spec)
+    assert torch.equal(a.q, b.q) and torch.equal(a.kv_cache, b.kv_cache)
+    assert a.q.shape == (4, 16, 576) and a.kv_cache.shape == (64, 16, 576)
+    assert a.kv_bytes() == int(a.seq_lens.sum()) * 576 * 2
+    f = wl.make_mla_workload(wl.custom_mla_spec(kv_dtype="fp8", kv_scale=0.05, fp8_source_scale=0.05))
+    assert f.kv_cache.dtype == torch.uint8 and f.kv_bytes() == int(f.seq_lens.sum()) * 576
+    codes = f.kv_cache.flatten()
+    assert not ((codes & 0x7F) == 0x7F).any()          # no NaN codes
