@@ -134,7 +134,8 @@ import numpy as np
 import oracle
 from oracle import c_oracle
 from paged_kv_decode_06_gb300 import workloads as wl
-spec = wl.CONFIGS[{config!r}]
+mla = {config!r} in wl.MLA_CONFIGS
+spec = wl.MLA_CONFIGS[{config!r}] if mla else wl.CONFIGS[{config!r}]
 rng = np.random.default_rng(spec.seed)
 sl, ql, qsl, bt, pool = wl.draw_metadata(spec, rng)
 order = np.random.default_rng(123).permutation(spec.num_seqs)
@@ -145,6 +146,18 @@ done_bytes = 0; t_used = 0.0; nseq = 0; ntok = 0
 seq_iter = (int(i) for _ in range(1000) for i in order)
 for i in seq_iter:
     L = int(sl[i]); q = int(ql[i]); n = (L + 15) // 16
+    if mla:
+        sub = wl.custom_mla_spec(num_q_heads=spec.num_q_heads, kv_dtype=spec.kv_dtype, seq_lens=(L,),
+                                 query_len_choices=(q,), pool_pages=n, kv_scale=spec.kv_scale,
+                                 fp8_source_scale=spec.fp8_source_scale, seed=nseq)
+        w = wl.make_mla_workload(sub)
+        t0 = time.perf_counter()
+        oracle.run_mla_workload(w)
+        t_used += time.perf_counter() - t0
+        done_bytes += w.kv_bytes(); nseq += 1; ntok += L
+        if t_used >= budget:
+            break
+        continue
     # a private pool holding only this sequence's pages (same shapes and value distribution)
     sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
                          kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
@@ -165,14 +178,16 @@ print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": nto
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env.pop(k, None)
-    if impl == "numpy":
+    if impl == "numpy" or config.startswith("mla"):
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             env[k] = "1"
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    what = (f"plain-C float64 oracle, {d['threads']} OpenMP thread(s)" if impl == "c"
+    if config.startswith("mla"):
+        d["threads"] = 1
+    what = (f"plain-C float64 oracle, {d['threads']} OpenMP thread(s)" if impl == "c" and not config.startswith("mla")
             else "float64 NumPy oracle, single-threaded BLAS")
     sample = (f"{what}, {d['seqs']} whole sequences ({d['tokens']} cached tokens) drawn from the {config} "
               f"workload's length mix, {d['seconds']:.1f} s of oracle time")
@@ -181,7 +196,12 @@ print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": nto
 
 def cpu_baseline(config: str, budget_s: float):
     """The ``cpu_baseline`` object: the C oracle on all host cores (value), on
-    one core, and the NumPy oracle on one core, each on its own bounded sample."""
+    one core, and the NumPy oracle on one core, each on its own bounded sample
+    (MLA workloads: the NumPy MLA oracle on one core)."""
+    if config.startswith("mla"):
+        g, cores, sample = cpu_oracle_sample(config, budget_s=budget_s, threads=1, impl="numpy")
+        return {"value": g, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                "host_cores": os.cpu_count(), "host_cpu": _cpu_model()}
     gbs, cores, sample = cpu_oracle_sample(config, budget_s=0.4 * budget_s, threads=0, impl="c")
     g1, _, s1 = cpu_oracle_sample(config, budget_s=0.3 * budget_s, threads=1, impl="c")
     gn, _, sn = cpu_oracle_sample(config, budget_s=0.3 * budget_s, threads=1, impl="numpy")
@@ -216,11 +236,15 @@ def run_reference(args, world, rank):
         vals.append(gbs)
     from paged_kv_decode_06_gb300 import workloads as wl
     import numpy as np
-    spec = wl.CONFIGS[args.config]
+    mla = args.config in wl.MLA_CONFIGS
+    spec = wl.MLA_CONFIGS[args.config] if mla else wl.CONFIGS[args.config]
     sl, *_ = wl.draw_metadata(spec, np.random.default_rng(spec.seed))
     eb = 1 if spec.kv_dtype == "fp8" else 2
-    per_row = spec.head_dim * eb + (4 if spec.token_scale_range is not None else 0)
-    step_bytes = int(sl.astype(np.int64).sum()) * spec.num_kv_heads * 2 * per_row
+    if mla:
+        step_bytes = int(sl.astype(np.int64).sum()) * spec.head_dim * eb
+    else:
+        per_row = spec.head_dim * eb + (4 if spec.token_scale_range is not None else 0)
+        step_bytes = int(sl.astype(np.int64).sum()) * spec.num_kv_heads * 2 * per_row
     v = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
@@ -259,7 +283,9 @@ def run_ours(args, world, rank, local):
     if args.sinks:
         sinks_t = torch.randn(spec.num_q_heads, generator=torch.Generator().manual_seed(3)).to(dev)
     pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
-    works = [base] + [wl.make_workload(spec, device=str(dev), seed=spec.seed + 100 * k) for k in range(1, pools)]
+    # every pool shares the first one's metadata (lengths, page ids); only the contents differ
+    works = [base] + [wl.make_workload(spec, device=str(dev), content_seed=spec.seed + 100 * k)
+                      for k in range(1, pools)]
 
     def pool_options(w, **extra):
         # per-token fp8 scales belong to each pool's cache
@@ -437,6 +463,184 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def run_mla(args, world, rank, local):
+    """MLA decode (paged_attn_mla_decode): the same measurement as run_ours,
+    on a latent cache [NB, 16, 576] (every cached row read once per step)."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_06_gb300 import binding
+    from paged_kv_decode_06_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    binding.load()
+    spec = wl.MLA_CONFIGS[args.config]
+    if args.batch:
+        spec = dataclasses.replace(spec, num_seqs=args.batch, name=f"{spec.name}_b{args.batch}")
+    base = wl.make_mla_workload(spec, device=str(dev))
+    step_bytes = base.kv_bytes()
+    pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
+    # every pool shares the first one's metadata (lengths, page ids); only the contents differ
+    works = [base] + [wl.make_mla_workload(spec, device=str(dev), content_seed=spec.seed + 100 * k)
+                      for k in range(1, pools)]
+    bt = torch.from_numpy(base.block_tables).to(dev)
+    sl = torch.from_numpy(base.seq_lens).to(dev)
+    qsl = torch.from_numpy(base.query_start_loc).to(dev) if base.query_start_loc is not None else None
+    mq = spec.max_query_len if qsl is not None else 1
+    T = base.q.shape[0]
+    out = torch.empty((T, spec.num_q_heads, spec.kv_lora_rank), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, spec.num_q_heads), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(k, opts=None, stream_=None, q=None):
+        w = works[k % pools]
+        binding.paged_attn_mla_decode(w.q if q is None else q, w.kv_cache, bt, sl, qsl, mq, spec.scale, spec.kv_scale,
+                                      out=out, lse=lse, options=opts, stream=stream_)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    cap = torch.cuda.Stream()
+    gstep = pools * max(1, 8 // pools)
+
+    def capture(first, n, opts=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for j in range(n):
+                step(first + j, opts=opts, stream_=cap)
+        return g
+
+    big = capture(0, gstep)
+    singles = [capture(pidx, 1) for pidx in range(pools)]
+
+    def run_steps(count):
+        k = 0
+        while k + gstep <= count:
+            big.replay()
+            k += gstep
+        while k < count:
+            singles[k % pools].replay()
+            k += 1
+    ev_a = torch.cuda.Event(enable_timing=True)
+    ev_b = torch.cuda.Event(enable_timing=True)
+    ev_a.record(stream); ev_b.record(stream)
+    torch.cuda.synchronize()
+    ev_opt = binding.make_options(split_start_event=ev_a, split_stop_event=ev_b)
+    rgraphs = [capture(pidx, 1, opts=ev_opt) for pidx in range(pools)]
+    run_steps(max(args.warmup, gstep))
+    torch.cuda.synchronize()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t_begin.record(stream)
+        run_steps(args.steps)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        split_ms = []
+        for k in range(args.steps):
+            rgraphs[k % pools].replay()
+            ev_b.synchronize()
+            split_ms.append(ev_a.elapsed_time(ev_b))
+    ms = t_begin.elapsed_time(t_end) / args.steps
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    direct_ms = d0.elapsed_time(d1) / args.steps
+    ms = max_over_ranks(ms, world, device=dev)
+    # end to end through the public API: pinned host inputs in, results out, every step
+    h_q = [w.q.cpu().pin_memory() for w in works]
+    h_bt = torch.from_numpy(base.block_tables).pin_memory()
+    h_sl = torch.from_numpy(base.seq_lens).pin_memory()
+    h_qsl = torch.from_numpy(base.query_start_loc).pin_memory() if qsl is not None else None
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q = torch.empty_like(base.q)
+
+    def e2e_step(k):
+        d_q.copy_(h_q[k % pools], non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        sl.copy_(h_sl, non_blocking=True)
+        if qsl is not None:
+            qsl.copy_(h_qsl, non_blocking=True)
+        step(k, q=d_q)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for k in range(args.warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = d_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4 + (h_qsl.numel() * 4 if h_qsl is not None else 0)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    status = binding.paged_attn_device_status(clear=True)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    split_mean = statistics.mean(split_ms)
+    achieved = step_bytes / (split_mean * 1e-3) / 1e9
+    plan = binding.paged_attn_mla_plan(spec.num_seqs, spec.num_q_heads, binding.kv_dtype_code(spec.kv_dtype), mq)
+    kernel = "pa_mla_kernel"
+    value = job_throughput_gbs(step_bytes, world, ms)
+    # tensor work per step: 2 * rows * (576 + 512) flops per cached token of each row's sequence
+    rows_tokens = int((base.seq_lens.astype(np.int64) * base.query_lens.astype(np.int64)).sum()) * spec.num_q_heads
+    flops = 2 * rows_tokens * (spec.head_dim + spec.kv_lora_rank)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
+        "frac_of_hbm_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f8e4m3" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
+        "config": {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
+                   "kv_lora_rank": spec.kv_lora_rank, "rope_dim": spec.rope_dim, "kv_dtype": spec.kv_dtype,
+                   "max_query_len": spec.max_query_len, "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
+                   "flops_per_step": flops,
+                   "l2": "no flush; each step reads >= 2x L2 of latent cache (pools rotated when one is smaller)",
+                   "step_mode": "CUDA graph replay; a step = one paged_attn_mla_decode call (split + merge)",
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _traffic_from_profiles(spec.name, kernel), "kernel": kernel,
+                     "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
+                     "per_launch_bytes": step_bytes, "tensor_tflops": flops / (split_mean * 1e-3) / 1e12},
+        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "direct_call": {"value": step_bytes * world / (direct_ms * 1e-3) / 1e9, "unit": "GB/s",
+                        "ms_per_step": direct_ms,
+                        "note": "paged_attn_mla_decode called from Python each step (no CUDA graph)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and not args.batch:
+        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_cache_write(args, world, rank, local):
     """Throughput of paged_attn_cache_write: one step writes the K and V rows of
     T new tokens (a prefill chunk of max_num_batched_tokens = 16384 tokens by
@@ -562,7 +766,8 @@ def _spec_for(args):
 def kernel_source_sha256(kernel):
     """Hash of the sources a split kernel is compiled from (stamps ncu figures)."""
     import hashlib
-    names = ["pa_split.cuh", "pa_device.cuh"] + (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else [])
+    names = ["pa_split.cuh", "pa_device.cuh"] + (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else []) + \
+        (["pa_mla.cu"] if kernel == "pa_mla_kernel" else [])
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:
@@ -609,6 +814,8 @@ def main():
         run_reference(args, world, rank)
     elif args.op == "cache_write":
         run_cache_write(args, world, rank, local)
+    elif args.config.startswith("mla"):
+        run_mla(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

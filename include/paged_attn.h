@@ -246,6 +246,70 @@ int paged_attn_cache_write_per_token(const pa_tensor_t* key, const pa_tensor_t* 
                                      const pa_tensor_t* v_cache, const pa_tensor_t* k_token_scales,
                                      const pa_tensor_t* v_token_scales, pa_stream_t stream);
 
+/*
+ * paged_attn_mla_decode - multi-head latent attention (MLA) decode over a paged
+ * latent cache (ATOM model-operations guide, "Multi-head latent attention
+ * (attention_mla.py)": MLAModules kv_lora_rank / qk_rope_head_dim, decode flow
+ * step 2, mla_decode_fwd after fused_qk_rope_concat_and_cache_mla; high-
+ * interactivity blog, "Attention Decode" (MLA split count, fp32 per-split
+ * log-sum-exp) and "Multi-Token Prediction" (query length four)).
+ *
+ * Each cached token is one row C_j = [c_kv (kv_lora_rank) | k_pe (rope)] shared by
+ * every query head; the query arrives absorbed (q_nope times the K up-projection,
+ * then q_pe), as wide as a cached row.  For query token t of sequence i (query row r
+ * of its run, position p = L_i - q_i + r) and head h:
+ *
+ *     s_j          = scale * <q[t, h, :], C_j>                     j = 0 .. p
+ *     out[t, h, :] = sum_j softmax_j(s) * C_j[0 : kv_lora_rank]    (latent space)
+ *     lse[t, h]    = ln sum_j exp(s_j)
+ *
+ * with C_j found at page block_tables[i][j / 16], slot j % 16.  An fp8 cache holds
+ * e4m3fn codes; an element's value is code * kv_scale in the logit and in the output.
+ *
+ *   q               bf16 [T, Hq, 576] (kv_lora_rank 512 + rope 64); stride[2] == 1,
+ *                   stride[1] == 576, stride[0] * 2 % 16 == 0, data 16-byte aligned.
+ *   kv_cache        bf16 or fp8e4m3 [NB, 16, 576]; stride[2] == 1, other strides times
+ *                   the element size multiples of 16 bytes, data 16-byte aligned.
+ *   block_tables, seq_lens, query_start_loc, max_query_len   as for paged_attn_decode;
+ *                   the query heads of one sequence form Hq * max_query_len rows per
+ *                   latent row, processed in chunks of at most 32 rows (max_query_len
+ *                   <= 32).
+ *   scale           softmax scale (e.g. 1/sqrt(qk_nope_head_dim + qk_rope_head_dim)).
+ *   kv_scale        fp8 caches: dequantisation scale (ignored for bf16).
+ *   out             bf16 [T, Hq, 512]; stride[2] == 1, other strides multiples of 4.
+ *   lse             f32 [T, Hq] or data == NULL.
+ *   opts            (the _ex form) num_ctas, min_pages_per_cta, disable_pdl,
+ *                   workspace / workspace_bytes and the split events apply; the
+ *                   grouped-query options (heads_per_cta, sliding_window, sinks,
+ *                   use_tcgen05 = 2, token scales) are rejected with PA_ERR_UNSUPPORTED.
+ *
+ * Errors, device status bits, workspace and graph-capture rules as for
+ * paged_attn_decode (paged_attn_mla_workspace_size gives the workspace a shape needs).
+ */
+int paged_attn_mla_decode(const pa_tensor_t* q, const pa_tensor_t* kv_cache, const pa_tensor_t* block_tables,
+                          const pa_tensor_t* seq_lens, const pa_tensor_t* query_start_loc,
+                          int32_t max_query_len, float scale, float kv_scale, const pa_tensor_t* out,
+                          const pa_tensor_t* lse, pa_stream_t stream);
+
+int paged_attn_mla_decode_ex(const pa_tensor_t* q, const pa_tensor_t* kv_cache,
+                             const pa_tensor_t* block_tables, const pa_tensor_t* seq_lens,
+                             const pa_tensor_t* query_start_loc, int32_t max_query_len, float scale,
+                             float kv_scale, const pa_tensor_t* out, const pa_tensor_t* lse,
+                             const pa_options_t* opts, pa_stream_t stream);
+
+/* Launch plan of paged_attn_mla_decode for a shape (kv_dtype: PA_BF16 or PA_FP8_E4M3);
+ * opts may be NULL.  heads_per_cta reports the query heads of one chunk, row_tiles the
+ * 16-row tiles of a chunk, num_ctas the split CTAs (each runs threads_per_cta threads in
+ * one or two independent teams).  Reads device attributes only. */
+int paged_attn_mla_plan(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype, int32_t max_query_len,
+                        const pa_options_t* opts, pa_plan_t* plan);
+
+/* Bytes of split workspace an MLA call with this shape needs; paged_attn_mla_reserve grows
+ * the library-owned workspace to fit it (call before capturing a CUDA graph). */
+int paged_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype,
+                                  int32_t max_query_len, size_t* bytes);
+int paged_attn_mla_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype, int32_t max_query_len);
+
 /* Plan for a shape on the current device (kv_dtype: PA_BF16 or PA_FP8_E4M3).
  * opts may be NULL.  Reads device attributes only; enqueues nothing. */
 int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

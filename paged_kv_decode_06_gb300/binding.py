@@ -65,6 +65,13 @@ _SIGNATURES = {
                                                         ctypes.c_float, ctypes.c_float, _P, _P, ctypes.c_void_p]),
     "paged_attn_cache_write": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
     "paged_attn_cache_write_per_token": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_void_p]),
+    "paged_attn_mla_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, ctypes.c_float, _P,
+                                             _P, ctypes.c_void_p]),
+    "paged_attn_mla_decode_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                                _P, _P, ctypes.POINTER(PaOptions), ctypes.c_void_p]),
+    "paged_attn_mla_plan": (ctypes.c_int, [ctypes.c_int32] * 4 + [ctypes.POINTER(PaOptions), ctypes.POINTER(PaPlan)]),
+    "paged_attn_mla_workspace_size": (ctypes.c_int, [ctypes.c_int32] * 4 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "paged_attn_mla_reserve": (ctypes.c_int, [ctypes.c_int32] * 4),
     "paged_attn_plan": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(PaOptions), ctypes.POINTER(PaPlan)]),
     "paged_attn_workspace_size": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
     "paged_attn_reserve": (ctypes.c_int, [ctypes.c_int32] * 6),
@@ -313,3 +320,64 @@ def decode_workload(w, out=None, lse=None, stream=None, options=None, want_lse=T
     return paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, s.max_query_len if qsl is not None else 1,
                              s.scale, s.k_scale, s.v_scale, out=out, lse=lse, stream=stream, options=options,
                              want_lse=want_lse)
+
+
+def paged_attn_mla_decode(q, kv_cache, block_tables, seq_lens, query_start_loc=None, max_query_len=1, scale=None,
+                          kv_scale=1.0, out=None, lse=None, stream=None, options=None, want_lse=True):
+    """MLA decode over a paged latent cache (see include/paged_attn.h).
+
+    q bf16 [T, Hq, 576]; kv_cache bf16 or uint8 (e4m3fn codes) [NB, 16, 576];
+    block_tables int32 [B, max_blocks]; seq_lens int32 [B]; query_start_loc
+    int32 [B+1] or None.  Returns (out bf16 [T, Hq, 512], lse f32 [T, Hq] or
+    None)."""
+    lib = load()
+    if scale is None:
+        scale = 192 ** -0.5
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    args = [tensor_desc(t) for t in (q, kv_cache, block_tables, seq_lens, query_start_loc)]
+    o_desc, l_desc = tensor_desc(out), tensor_desc(lse)
+    refs = [ctypes.byref(a) for a in args]
+    if options is None:
+        st = lib.paged_attn_mla_decode(*refs, int(max_query_len), float(scale), float(kv_scale), ctypes.byref(o_desc),
+                                       ctypes.byref(l_desc), _stream_handle(stream))
+    else:
+        st = lib.paged_attn_mla_decode_ex(*refs, int(max_query_len), float(scale), float(kv_scale),
+                                          ctypes.byref(o_desc), ctypes.byref(l_desc), ctypes.byref(options),
+                                          _stream_handle(stream))
+    _check(lib, st)
+    return out, lse
+
+
+def paged_attn_mla_plan(num_seqs, num_q_heads, kv_dtype=PA_BF16, max_query_len=1, options=None) -> dict:
+    lib = load()
+    plan = PaPlan()
+    _check(lib, lib.paged_attn_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len,
+                                        ctypes.byref(options) if options is not None else None, ctypes.byref(plan)))
+    return plan.as_dict()
+
+
+def paged_attn_mla_workspace_size(num_seqs, num_q_heads, kv_dtype=PA_BF16, max_query_len=1) -> int:
+    lib = load()
+    n = ctypes.c_size_t(0)
+    _check(lib, lib.paged_attn_mla_workspace_size(num_seqs, num_q_heads, kv_dtype, max_query_len, ctypes.byref(n)))
+    return int(n.value)
+
+
+def paged_attn_mla_reserve(num_seqs, num_q_heads, kv_dtype=PA_BF16, max_query_len=1):
+    lib = load()
+    _check(lib, lib.paged_attn_mla_reserve(num_seqs, num_q_heads, kv_dtype, max_query_len))
+
+
+def mla_decode_workload(w, out=None, lse=None, stream=None, options=None, want_lse=True):
+    """Run the MLA kernel on a ``workloads.MlaWorkload`` whose tensors live on
+    the GPU (metadata is copied to the device here)."""
+    dev = w.q.device
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    qsl = torch.from_numpy(w.query_start_loc).to(dev) if w.query_start_loc is not None else None
+    s = w.spec
+    return paged_attn_mla_decode(w.q, w.kv_cache, bt, sl, qsl, s.max_query_len if qsl is not None else 1, s.scale,
+                                 s.kv_scale, out=out, lse=lse, stream=stream, options=options, want_lse=want_lse)

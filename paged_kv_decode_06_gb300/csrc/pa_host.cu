@@ -95,6 +95,8 @@ int device_state(DeviceState** out, int* dev_out) {
       return cuda_fail(e, "cudaFuncSetAttribute(split fp8, per-token scales)");
     if ((e = pa::set_split_smem_limits_tc(s.smem_optin)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(split tcgen05)");
+    if ((e = pa::set_mla_smem_limits(s.smem_optin)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(MLA)");
     void* ptr = nullptr;
     if ((e = cudaGetSymbolAddress(&ptr, g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
@@ -552,6 +554,285 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   return PA_OK;
 }
 
+// ------------------------------------------------------------------- MLA
+// Latent rows of 512 (c_kv) + 64 (k_pe) features; the value is the latent part.
+constexpr int kMlaDqk = 576;
+constexpr int kMlaDv = 512;
+constexpr int kMlaMaxRows = 32;   // query rows of one head chunk (2 tiles of 16)
+
+struct MlaPlan {
+  int B, Hq, max_qlen, esz;
+  int Gc, NC, R_max, RT, nteam, threads, grid, min_pages, nstage;
+  uint32_t stage_bytes, q_slot_bytes, off_stage, off_q, off_xchg, off_bar, team_bytes, off_prefix, smem;
+  size_t ws_unit, ws_ml, ws_o, ws_bytes;
+};
+
+int check_mla_options(const pa_options_t* opts) {
+  if (opts == nullptr) return PA_OK;
+  if (opts->use_tcgen05 < 0 || opts->use_tcgen05 > 2)
+    return fail(PA_ERR_INVALID_ARG, "use_tcgen05 %d not in {0, 1, 2}", opts->use_tcgen05);
+  if (opts->page_pairing < 0 || opts->page_pairing > 2)
+    return fail(PA_ERR_INVALID_ARG, "page_pairing %d not in {0, 1, 2}", opts->page_pairing);
+  if (opts->heads_per_cta != 0 || opts->sliding_window > 0 || opts->sinks != nullptr || opts->use_tcgen05 == 2 ||
+      opts->page_pairing == 2 || has_token_scales(opts))
+    return fail(PA_ERR_UNSUPPORTED, "MLA decode takes none of heads_per_cta, sliding_window, sinks, use_tcgen05 = 2, "
+                "page_pairing = 2, token scales");
+  return PA_OK;
+}
+
+// Shape checks that need no device.
+int check_mla_shape(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t* opts) {
+  if (B < 1 || B > kMaxSeqs) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d outside [1, %d]", B, kMaxSeqs);
+  if (Hq < 1) return fail(PA_ERR_INVALID_ARG, "num_q_heads %d < 1", Hq);
+  if (kv_dtype != PA_BF16 && kv_dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "kv dtype %d is neither PA_BF16 nor PA_FP8_E4M3", kv_dtype);
+  if (max_qlen < 1) return fail(PA_ERR_INVALID_ARG, "max_query_len %d < 1", max_qlen);
+  if (max_qlen > kMlaMaxRows)
+    return fail(PA_ERR_UNSUPPORTED, "max_query_len %d > %d for MLA decode", max_qlen, kMlaMaxRows);
+  return check_mla_options(opts);
+}
+
+int make_mla_plan(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t* opts, int num_sms, int smem_optin,
+                  MlaPlan* out) {
+  const int st = check_mla_shape(B, Hq, kv_dtype, max_qlen, opts);
+  if (st != PA_OK) return st;
+  MlaPlan p = {};
+  p.B = B; p.Hq = Hq; p.max_qlen = max_qlen;
+  p.esz = kv_dtype == PA_FP8_E4M3 ? 1 : 2;
+  // heads per chunk: the largest divisor of Hq whose rows fit two 16-row tiles
+  p.Gc = 1;
+  for (int d = 1; d <= Hq; ++d)
+    if (Hq % d == 0 && d * max_qlen <= kMlaMaxRows) p.Gc = d;
+  p.NC = Hq / p.Gc;
+  p.R_max = p.Gc * max_qlen;
+  p.RT = (p.R_max + 15) / 16;
+  p.nteam = pa::mla_teams(p.RT);
+  p.threads = pa::mla_threads(p.RT);
+  p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
+  p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
+  p.stage_bytes = static_cast<uint32_t>(kPageSize * kMlaDqk * p.esz);
+  p.q_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(max_qlen) * p.Gc * kMlaDqk * 2, 1024));
+  const uint32_t xchg = 8192u * static_cast<uint32_t>(p.RT);
+  const uint32_t bars = static_cast<uint32_t>(align_up(8u * (2 * kMaxStages + 4 + 2 * p.RT), 128));
+  const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));
+  const int64_t room = (static_cast<int64_t>(smem_optin) - 1024 - prefix_bytes) / p.nteam / 1024 * 1024;
+  const int64_t fixed = 2 * static_cast<int64_t>(p.q_slot_bytes) + xchg + bars;
+  p.nstage = room > fixed ? static_cast<int>(std::min<int64_t>(kMaxStages, (room - fixed) / p.stage_bytes)) : 0;
+  if (p.nstage < 2) return fail(PA_ERR_UNSUPPORTED, "no MLA launch configuration fits %d bytes of shared memory", smem_optin);
+  p.off_stage = 0;
+  p.off_q = p.off_stage + p.nstage * p.stage_bytes;
+  p.off_xchg = p.off_q + 2 * p.q_slot_bytes;
+  p.off_bar = p.off_xchg + xchg;
+  p.team_bytes = static_cast<uint32_t>(align_up(p.off_bar + bars, 1024));
+  p.off_prefix = p.team_bytes * static_cast<uint32_t>(p.nteam);
+  p.smem = 1024 + p.off_prefix + prefix_bytes;
+  const size_t rows = static_cast<size_t>(2) * p.grid * p.nteam * p.R_max;
+  p.ws_unit = 0;
+  p.ws_ml = align_up(p.ws_unit + static_cast<size_t>(16) * B * p.NC, 256);
+  p.ws_o = align_up(p.ws_ml + rows * 8, 256);
+  p.ws_bytes = align_up(p.ws_o + rows * kMlaDv * 4, 256);
+  *out = p;
+  return PA_OK;
+}
+
+// TMA map over a latent cache [NB, 16, 576] with dimensions (feature within a
+// 64-feature block, slot, block, page): one box = a whole page, landing as 9
+// column blocks of 16 swizzled rows.
+int encode_mla_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int64_t NB) {
+  cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(kPageSize), static_cast<cuuint64_t>(kMlaDqk / 64),
+                        static_cast<cuuint64_t>(NB)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->stride[1]) * esz, static_cast<cuuint64_t>(64 * esz),
+                           static_cast<cuuint64_t>(t->stride[0]) * esz};
+  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(kPageSize), static_cast<cuuint32_t>(kMlaDqk / 64), 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = g_encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                              t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              esz == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for the latent cache", r);
+  return PA_OK;
+}
+
+int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* bt, const pa_tensor_t* sl,
+                    const pa_tensor_t* qsl, int32_t max_qlen, float scale, float kv_scale, const pa_tensor_t* out,
+                    const pa_tensor_t* lse, const pa_options_t* opts, cudaStream_t stream) {
+  int st;
+  if ((st = check_tensor(q, "q", 3, false)) || (st = check_tensor(kc, "kv_cache", 3, false)) ||
+      (st = check_tensor(bt, "block_tables", 2, false)) || (st = check_tensor(sl, "seq_lens", 1, false)) ||
+      (st = check_tensor(qsl, "query_start_loc", 1, true)) || (st = check_tensor(out, "out", 3, false)) ||
+      (st = check_tensor(lse, "lse", 2, true)))
+    return st;
+  if (q->dtype != PA_BF16 || out->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "q and out must be bf16");
+  if (kc->dtype != PA_BF16 && kc->dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "kv_cache must be bf16 or fp8 e4m3");
+  if (bt->dtype != PA_I32 || sl->dtype != PA_I32) return fail(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32");
+  if (qsl->data && qsl->dtype != PA_I32) return fail(PA_ERR_INVALID_ARG, "query_start_loc must be int32");
+  if (lse->data && lse->dtype != PA_F32) return fail(PA_ERR_INVALID_ARG, "lse must be float32");
+  const int64_t T = q->shape[0], Hq = q->shape[1], Dqk = q->shape[2];
+  const int64_t NB = kc->shape[0], P = kc->shape[1];
+  const int64_t B = bt->shape[0], MB = bt->shape[1];
+  if (P != kPageSize) return fail(PA_ERR_UNSUPPORTED, "page size %lld, only 16 is supported", (long long)P);
+  if (Dqk != kMlaDqk || kc->shape[2] != kMlaDqk)
+    return fail(PA_ERR_UNSUPPORTED, "MLA rows of %lld (q) and %lld (cache) features; only 512 + 64 = 576 is supported",
+                (long long)Dqk, (long long)kc->shape[2]);
+  if (out->shape[0] != T || out->shape[1] != Hq || out->shape[2] != kMlaDv)
+    return fail(PA_ERR_INVALID_ARG, "out must be [T, Hq, 512]");
+  if (Hq > (1 << 20) || T > (int64_t(1) << 30) || NB > (int64_t(1) << 31) - 1 || MB > (1 << 28))
+    return fail(PA_ERR_UNSUPPORTED, "tensor extents too large");
+  if (sl->shape[0] != B) return fail(PA_ERR_INVALID_ARG, "seq_lens has %lld entries, block_tables %lld rows", (long long)sl->shape[0], (long long)B);
+  if (B * MB > (int64_t(1) << 31)) return fail(PA_ERR_UNSUPPORTED, "block table too large");
+  if (lse->data && (lse->shape[0] != T || lse->shape[1] != Hq)) return fail(PA_ERR_INVALID_ARG, "lse shape must be [T, Hq]");
+  if (B == 0 || T == 0) return PA_OK;
+  if (qsl->data) {
+    if (qsl->shape[0] != B + 1) return fail(PA_ERR_INVALID_ARG, "query_start_loc must have B+1 entries");
+    if (qsl->stride[0] != 1) return fail(PA_ERR_INVALID_ARG, "query_start_loc must be contiguous");
+    if (T < B || T > B * static_cast<int64_t>(max_qlen))
+      return fail(PA_ERR_INVALID_ARG, "T = %lld query tokens is outside [B, B * max_query_len]", (long long)T);
+  } else {
+    if (T != B) return fail(PA_ERR_INVALID_ARG, "without query_start_loc, q needs one token per sequence (T == B)");
+    if (max_qlen != 1) return fail(PA_ERR_INVALID_ARG, "max_query_len must be 1 without query_start_loc");
+  }
+  if (sl->stride[0] != 1) return fail(PA_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (bt->stride[1] != 1) return fail(PA_ERR_INVALID_ARG, "block_tables rows must be contiguous");
+  if (q->stride[2] != 1 || q->stride[1] != kMlaDqk)
+    return fail(PA_ERR_INVALID_ARG, "q must have contiguous heads (stride[1] == 576, stride[2] == 1)");
+  if ((q->stride[0] * 2) % 16 != 0 || !aligned(q->data, 16)) return fail(PA_ERR_INVALID_ARG, "q rows must be 16-byte aligned");
+  if (out->stride[2] != 1 || (out->stride[1] % 4) != 0 || (out->stride[0] % 4) != 0 || !aligned(out->data, 8))
+    return fail(PA_ERR_INVALID_ARG, "out must have a contiguous last dim, strides multiple of 4 elements, 8-byte alignment");
+  const int esz = kc->dtype == PA_FP8_E4M3 ? 1 : 2;
+  if (kc->stride[2] != 1) return fail(PA_ERR_INVALID_ARG, "kv_cache last dim must be contiguous");
+  for (int d = 0; d < 2; ++d)
+    if ((kc->stride[d] * esz) % 16 != 0) return fail(PA_ERR_INVALID_ARG, "kv_cache strides must be multiples of 16 bytes");
+  if (!aligned(kc->data, 16)) return fail(PA_ERR_INVALID_ARG, "kv_cache data must be 16-byte aligned");
+  if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return fail(PA_ERR_INVALID_ARG, "scale and kv_scale must be finite");
+  if ((st = check_mla_shape(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq), kc->dtype,
+                            max_qlen, opts)) != PA_OK)
+    return st;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  MlaPlan pl;
+  if ((st = make_mla_plan(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq), kc->dtype,
+                          max_qlen, opts, ds->num_sms, ds->smem_optin, &pl)) != PA_OK)
+    return st;
+  void* ws = nullptr;
+  if (opts && opts->workspace) {
+    if (opts->workspace_bytes < pl.ws_bytes)
+      return fail(PA_ERR_WORKSPACE, "caller workspace %zu bytes < %zu needed", opts->workspace_bytes, pl.ws_bytes);
+    if (!aligned(opts->workspace, 256)) return fail(PA_ERR_INVALID_ARG, "caller workspace must be 256-byte aligned");
+    ws = opts->workspace;
+  } else {
+    if (ds->ws_bytes < pl.ws_bytes) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+      if (cs != cudaStreamCaptureStatusNone)
+        return fail(PA_ERR_WORKSPACE, "workspace must grow to %zu bytes, which is not allowed during stream capture; "
+                    "call paged_attn_mla_reserve first", pl.ws_bytes);
+      if (ds->ws) {
+        if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+        ds->ws = nullptr;
+        ds->ws_bytes = 0;
+      }
+      if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      ds->ws_bytes = pl.ws_bytes;
+    }
+    ws = ds->ws;
+  }
+  CUtensorMap tm;
+  if ((st = encode_mla_map(&tm, kc, esz, NB)) != PA_OK) return st;
+
+  const float kLog2e = 1.4426950408889634f;
+  pa::SplitParams sp = {};
+  sp.q = static_cast<const uint16_t*>(q->data);
+  sp.q_stride_t = q->stride[0];
+  sp.out = static_cast<uint16_t*>(out->data);
+  sp.out_stride_t = out->stride[0];
+  sp.out_stride_h = out->stride[1];
+  sp.lse = static_cast<float*>(lse->data);
+  sp.lse_stride_t = lse->data ? lse->stride[0] : 0;
+  sp.lse_stride_h = lse->data ? lse->stride[1] : 0;
+  sp.block_tables = static_cast<const int32_t*>(bt->data);
+  sp.bt_stride = bt->stride[0];
+  sp.seq_lens = static_cast<const int32_t*>(sl->data);
+  sp.qsl = static_cast<const int32_t*>(qsl->data);
+  sp.num_seqs = static_cast<int32_t>(B);
+  sp.num_tokens = static_cast<int32_t>(T);
+  sp.Hq = static_cast<int32_t>(Hq);
+  sp.Hkv = 1;
+  sp.G = pl.Gc;
+  sp.max_qlen = max_qlen;
+  sp.num_pages = static_cast<int32_t>(NB);
+  sp.max_blocks = static_cast<int32_t>(MB);
+  sp.HC = 1;
+  sp.NC = pl.NC;
+  sp.MT = pl.RT;
+  sp.R_max = pl.R_max;
+  sp.nstage = pl.nstage;
+  sp.min_pages = pl.min_pages;
+  sp.scale_log2 = scale * (esz == 1 ? kv_scale : 1.0f) * kLog2e;
+  sp.v_scale = esz == 1 ? kv_scale : 1.0f;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  sp.ws_unit = reinterpret_cast<int4*>(wsb + pl.ws_unit);
+  sp.ws_ml = reinterpret_cast<float2*>(wsb + pl.ws_ml);
+  sp.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
+  sp.err = ds->status;
+  sp.off_prefix = pl.off_prefix;
+  sp.off_bar = pl.off_bar;
+  sp.off_q = pl.off_q;
+  sp.q_slot_bytes = pl.q_slot_bytes;
+  sp.off_stage = pl.off_stage;
+  sp.stage_bytes = pl.stage_bytes;
+  sp.kv_bytes = pl.stage_bytes;
+  sp.off_xchg = pl.off_xchg;
+  sp.team_bytes = pl.team_bytes;
+
+  pa::MergeParams mp = {};
+  mp.out = sp.out;
+  mp.out_stride_t = sp.out_stride_t;
+  mp.out_stride_h = sp.out_stride_h;
+  mp.lse = sp.lse;
+  mp.lse_stride_t = sp.lse_stride_t;
+  mp.lse_stride_h = sp.lse_stride_h;
+  mp.seq_lens = sp.seq_lens;
+  mp.qsl = sp.qsl;
+  mp.num_seqs = sp.num_seqs;
+  mp.num_tokens = sp.num_tokens;
+  mp.G = pl.Gc;
+  mp.HC = 1;
+  mp.NC = pl.NC;
+  mp.R_max = pl.R_max;
+  mp.max_qlen = max_qlen;
+  mp.split_grid = pl.grid * pl.nteam;
+  mp.v_scale = sp.v_scale;
+  mp.ws_unit = sp.ws_unit;
+  mp.ws_ml = sp.ws_ml;
+  mp.ws_o = sp.ws_o;
+  mp.err = sp.err;
+
+  cudaEvent_t ev0 = opts ? static_cast<cudaEvent_t>(opts->split_start_event) : nullptr;
+  cudaEvent_t ev1 = opts ? static_cast<cudaEvent_t>(opts->split_stop_event) : nullptr;
+  const bool pdl = !(opts && opts->disable_pdl);
+  cudaError_t e;
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (ev0 || ev1) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
+  if (ev0 && (e = cudaEventRecordWithFlags(ev0, stream, rec_flags)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(start)");
+  if ((e = pa::launch_mla(esz == 1, pl.RT, tm, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream)) !=
+      cudaSuccess)
+    return cuda_fail(e, "MLA split kernel launch");
+  if (ev1 && (e = cudaEventRecordWithFlags(ev1, stream, rec_flags)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(stop)");
+  if ((e = pa::launch_merge_mla(mp, static_cast<int>(B) * pl.NC, pl.R_max, pdl && !ev1, stream)) != cudaSuccess)
+    return cuda_fail(e, "MLA merge kernel launch");
+  return PA_OK;
+}
+
 }  // namespace
 
 namespace pa {
@@ -747,6 +1028,83 @@ int paged_attn_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_hea
   Plan pl;
   if ((st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, nullptr, ds->num_sms,
                       ds->smem_optin, &pl)) != PA_OK)
+    return st;
+  if (ds->ws_bytes >= pl.ws_bytes) return PA_OK;
+  cudaError_t e;
+  if (ds->ws) {
+    if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    ds->ws = nullptr;
+    ds->ws_bytes = 0;
+  }
+  if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+  ds->ws_bytes = pl.ws_bytes;
+  return PA_OK;
+}
+
+int paged_attn_mla_decode_ex(const pa_tensor_t* q, const pa_tensor_t* kv_cache, const pa_tensor_t* block_tables,
+                             const pa_tensor_t* seq_lens, const pa_tensor_t* query_start_loc, int32_t max_query_len,
+                             float scale, float kv_scale, const pa_tensor_t* out, const pa_tensor_t* lse,
+                             const pa_options_t* opts, pa_stream_t stream) {
+  t_last_error.clear();
+  return mla_decode_impl(q, kv_cache, block_tables, seq_lens, query_start_loc, max_query_len, scale, kv_scale, out, lse,
+                         opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int paged_attn_mla_decode(const pa_tensor_t* q, const pa_tensor_t* kv_cache, const pa_tensor_t* block_tables,
+                          const pa_tensor_t* seq_lens, const pa_tensor_t* query_start_loc, int32_t max_query_len,
+                          float scale, float kv_scale, const pa_tensor_t* out, const pa_tensor_t* lse,
+                          pa_stream_t stream) {
+  return paged_attn_mla_decode_ex(q, kv_cache, block_tables, seq_lens, query_start_loc, max_query_len, scale, kv_scale,
+                                  out, lse, nullptr, stream);
+}
+
+int paged_attn_mla_plan(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype, int32_t max_query_len,
+                        const pa_options_t* opts, pa_plan_t* plan) {
+  t_last_error.clear();
+  if (plan == nullptr) return fail(PA_ERR_INVALID_ARG, "plan pointer is NULL");
+  int st = check_mla_shape(num_seqs, num_q_heads, kv_dtype, max_query_len, opts);
+  if (st != PA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  MlaPlan pl;
+  if ((st = make_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len, opts, ds->num_sms, ds->smem_optin, &pl)) !=
+      PA_OK)
+    return st;
+  plan->num_ctas = pl.grid;
+  plan->heads_per_cta = pl.Gc;
+  plan->row_tiles = pl.RT;
+  plan->num_stages = pl.nstage;
+  plan->threads_per_cta = pl.threads;
+  plan->smem_bytes = static_cast<int32_t>(pl.smem);
+  plan->min_pages_per_cta = pl.min_pages;
+  plan->merge_rows = pl.R_max;
+  plan->page_pairing = 0;
+  plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
+  plan->variant = 2;
+  plan->block_pages = 1;
+  return PA_OK;
+}
+
+int paged_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype, int32_t max_query_len,
+                                  size_t* bytes) {
+  if (bytes == nullptr) return fail(PA_ERR_INVALID_ARG, "bytes pointer is NULL");
+  pa_plan_t plan;
+  const int st = paged_attn_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len, nullptr, &plan);
+  if (st == PA_OK) *bytes = static_cast<size_t>(plan.workspace_bytes);
+  return st;
+}
+
+int paged_attn_mla_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype, int32_t max_query_len) {
+  t_last_error.clear();
+  int st = check_mla_shape(num_seqs, num_q_heads, kv_dtype, max_query_len, nullptr);
+  if (st != PA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
+  MlaPlan pl;
+  if ((st = make_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len, nullptr, ds->num_sms, ds->smem_optin,
+                          &pl)) != PA_OK)
     return st;
   if (ds->ws_bytes >= pl.ws_bytes) return PA_OK;
   cudaError_t e;

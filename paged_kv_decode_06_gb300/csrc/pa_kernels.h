@@ -60,6 +60,8 @@ struct SplitParams {
   const float* v_tok;
   int64_t tok_stride_page;  // floats between pages of the scale tensors
   uint32_t tok_bytes;       // HC * 16 * 4: one tensor's scales of one page
+  // MLA kernel: bytes between the shared-memory regions of a CTA's teams
+  uint32_t team_bytes;
 };
 
 struct MergeParams {
@@ -120,6 +122,16 @@ cudaError_t launch_merge(int head_dim, const MergeParams& p, int units, int rows
 cudaError_t launch_split_tc(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                             int grid, int smem, bool pdl, cudaStream_t stream);
 cudaError_t set_split_smem_limits_tc(int smem);
+// MLA decode over a latent cache [NB, 16, 576] (value = first 512 columns);
+// rt = 16-row tiles of a head chunk (1 or 2).  A CTA runs mla_teams(rt)
+// independent teams in mla_threads(rt) threads; p.HC = 1, p.G = heads per chunk.
+cudaError_t launch_mla(bool fp8, int rt, const CUtensorMap& tm, const SplitParams& p, int grid, int smem, bool pdl,
+                       cudaStream_t stream);
+int mla_threads(int rt);
+int mla_teams(int rt);
+cudaError_t set_mla_smem_limits(int smem);
+// LSE merge of MLA partials (512 value columns): one warp per (unit, row).
+cudaError_t launch_merge_mla(const MergeParams& p, int units, int rows, bool pdl, cudaStream_t stream);
 cudaError_t set_split_smem_limits_bf16(int smem);
 cudaError_t set_split_smem_limits_fp8(int smem);
 

@@ -224,6 +224,75 @@ __global__ void __launch_bounds__(kWideThreads) pa_merge_wide_kernel(const Merge
   if (pg == 0) write_merged(p, m, dq, acc, l, mx, dq == 0);
 }
 
+// MLA: 512 value columns per row (the latent width); one warp per (unit,
+// row), lane l holding columns 4 l + 128 j (j < 4); two partials' loads are
+// issued before either is combined.
+__device__ __forceinline__ void lse_acc4(float& mx, float& l, float4 (&acc)[4], float2 ml, const float4 (&o)[4]) {
+  if (ml.x == -INFINITY) return;
+  const float nm = fmaxf(mx, ml.x);
+  const float a = fast_exp2(mx - nm);
+  const float b = fast_exp2(ml.x - nm);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc[j].x = acc[j].x * a + o[j].x * b;
+    acc[j].y = acc[j].y * a + o[j].y * b;
+    acc[j].z = acc[j].z * a + o[j].z * b;
+    acc[j].w = acc[j].w * a + o[j].w * b;
+  }
+  l = l * a + ml.y * b;
+  mx = nm;
+}
+
+__global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const MergeParams p) {
+  constexpr int D = 512;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const MergeRow m = merge_row<D>(p, blockIdx.x, blockIdx.y * kMergeWarps + warp, lane);
+  if (!m.work) return;
+  float mx = -INFINITY, l = 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 1 < m.nparts; s += 2) {
+    const int64_t sa = slot_row(p, m, s), sb = slot_row(p, m, s + 1);
+    const float2 ma = p.ws_ml[sa], mb = p.ws_ml[sb];
+    float4 oa[4], ob[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      oa[j] = *reinterpret_cast<const float4*>(p.ws_o + sa * D + 4 * lane + 128 * j);
+      ob[j] = *reinterpret_cast<const float4*>(p.ws_o + sb * D + 4 * lane + 128 * j);
+    }
+    lse_acc4(mx, l, acc, ma, oa);
+    lse_acc4(mx, l, acc, mb, ob);
+  }
+  if (s < m.nparts) {
+    const int64_t sa = slot_row(p, m, s);
+    const float2 ma = p.ws_ml[sa];
+    float4 oa[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) oa[j] = *reinterpret_cast<const float4*>(p.ws_o + sa * D + 4 * lane + 128 * j);
+    lse_acc4(mx, l, acc, ma, oa);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) write_merged(p, m, lane + 32 * j, acc[j], l, mx, lane == 0 && j == 0);
+}
+
+cudaError_t launch_merge_mla(const MergeParams& p, int units, int rows, bool pdl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units), static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps), 1);
+  cfg.blockDim = dim3(32 * kMergeWarps, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pa_merge_mla_kernel, p);
+}
+
 cudaError_t launch_merge(int head_dim, const MergeParams& p, int units, int rows, bool wide, bool pdl,
                          cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};

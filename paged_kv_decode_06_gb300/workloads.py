@@ -199,16 +199,19 @@ def _fill_normal(t: torch.Tensor, gen: torch.Generator, divisor: float, fp8: boo
             flat[s:e] = x.to(torch.bfloat16)
 
 
-def make_workload(spec: WorkloadSpec, device: str = "cpu", seed: Optional[int] = None) -> Workload:
+def make_workload(spec: WorkloadSpec, device: str = "cpu", seed: Optional[int] = None,
+                  content_seed: Optional[int] = None) -> Workload:
     """Build one seeded batch.  Metadata comes from numpy's PCG64 with
-    ``seed``; tensor contents from torch's generator on ``device`` with the
-    same seed (so CPU and CUDA draws differ, but each is reproducible)."""
+    ``seed``; tensor contents from torch's generator on ``device`` with
+    ``content_seed`` (default: the same seed; CPU and CUDA draws differ, but
+    each is reproducible).  Batches that differ only in ``content_seed`` share
+    lengths, block tables and pool size."""
     seed = spec.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     seq_lens, query_lens, qsl, block_tables, pool = draw_metadata(spec, rng)
     T = int(query_lens.sum())
     gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
+    gen.manual_seed(seed if content_seed is None else content_seed)
     fp8 = spec.kv_dtype == "fp8"
     q = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=device)
     _fill_normal(q, gen, 1.0, False)
@@ -355,16 +358,19 @@ class MlaWorkload:
         return int(self.seq_lens.astype(np.int64).sum()) * self.spec.head_dim * self.kv_elem_bytes
 
 
-def make_mla_workload(spec: MlaSpec, device: str = "cpu", seed: Optional[int] = None) -> MlaWorkload:
-    """One seeded MLA batch: metadata from numpy's PCG64, tensor contents from
-    torch's generator on ``device`` (q and cache rows N(0,1); fp8 codes
-    e4m3(N(0,1) / fp8_source_scale))."""
+def make_mla_workload(spec: MlaSpec, device: str = "cpu", seed: Optional[int] = None,
+                      content_seed: Optional[int] = None) -> MlaWorkload:
+    """One seeded MLA batch: metadata from numpy's PCG64 with ``seed``, tensor
+    contents from torch's generator on ``device`` with ``content_seed``
+    (default: ``seed``): q and cache rows N(0,1); fp8 codes
+    e4m3(N(0,1) / fp8_source_scale).  Batches that differ only in
+    ``content_seed`` share lengths, block tables and pool size."""
     seed = spec.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     seq_lens, query_lens, qsl, block_tables, pool = draw_metadata(spec, rng)
     T = int(query_lens.sum())
     gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
+    gen.manual_seed(seed if content_seed is None else content_seed)
     fp8 = spec.kv_dtype == "fp8"
     q = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=device)
     _fill_normal(q, gen, 1.0, False)

@@ -251,3 +251,71 @@ def test_per_token_cache_write_arguments(lib):
     assert lib.paged_attn_cache_write_per_token(*[ctypes.byref(x) for x in d], None, None) == binding.PA_ERR_INVALID_ARG
     if not torch.cuda.is_available():
         assert _cwt_call(lib, a, ok, ok) == binding.PA_ERR_CUDA
+
+
+# ------------------------------------------------------------------ MLA decode
+
+def _mla_args(T=3, Hq=16, NB=10, B=3, MB=4, kv=torch.bfloat16, Dqk=576, Dv=512):
+    return dict(q=torch.zeros(T, Hq, Dqk, dtype=torch.bfloat16), c=torch.zeros(NB, 16, Dqk, dtype=kv),
+                bt=torch.zeros(B, MB, dtype=torch.int32), sl=torch.ones(B, dtype=torch.int32), qsl=None,
+                out=torch.zeros(T, Hq, Dv, dtype=torch.bfloat16), lse=torch.zeros(T, Hq, dtype=torch.float32),
+                max_qlen=1, opts=None)
+
+
+def _mla_call(lib, a, scale=0.07):
+    descs = [binding.tensor_desc(a[n]) for n in ("q", "c", "bt", "sl", "qsl", "out", "lse")]
+    refs = [ctypes.byref(d) for d in descs]
+    if a["opts"] is None:
+        return lib.paged_attn_mla_decode(*refs[:5], a["max_qlen"], scale, 1.0, refs[5], refs[6], None)
+    return lib.paged_attn_mla_decode_ex(*refs[:5], a["max_qlen"], scale, 1.0, refs[5], refs[6],
+                                        ctypes.byref(a["opts"]), None)
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: a.update(q=a["q"].float()), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(out=torch.zeros(3, 16, 576, dtype=torch.bfloat16)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(c=torch.zeros(10, 16, 1, 576, dtype=torch.bfloat16)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(q=torch.zeros(3, 16, 512, dtype=torch.bfloat16),
+                        c=torch.zeros(10, 16, 512, dtype=torch.bfloat16)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(c=torch.zeros(10, 8, 576, dtype=torch.bfloat16)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(c=torch.zeros(10, 16, 576, dtype=torch.float32)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(q=torch.zeros(3, 16, 1152, dtype=torch.bfloat16)[:, :, :576]), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(c=torch.zeros(10, 16, 580, dtype=torch.bfloat16)[:, :, :576]), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(max_qlen=2), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(q=torch.zeros(33 * 3, 16, 576, dtype=torch.bfloat16),
+                        out=torch.zeros(33 * 3, 16, 512, dtype=torch.bfloat16), lse=None,
+                        qsl=torch.arange(0, 100, 33, dtype=torch.int32), max_qlen=33), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(opts=binding.make_options(sliding_window=8)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(opts=binding.make_options(heads_per_cta=2)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(opts=binding.make_options(use_tcgen05=2)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(lse=torch.zeros(3, 8, dtype=torch.float32)), binding.PA_ERR_INVALID_ARG),
+])
+def test_mla_invalid_arguments_rejected_on_host(lib, mutate, expect):
+    a = _mla_args()
+    mutate(a)
+    assert _mla_call(lib, a) == expect, binding.paged_attn_last_error_message()
+    assert binding.paged_attn_last_error_message() != ""
+
+
+def test_mla_non_finite_scale_rejected(lib):
+    assert _mla_call(lib, _mla_args(), scale=float("inf")) == binding.PA_ERR_INVALID_ARG
+
+
+def test_mla_valid_arguments_without_gpu_report_cuda_error(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _mla_call(lib, _mla_args()) == binding.PA_ERR_CUDA
+    a = _mla_args(kv=torch.float8_e4m3fn, T=6)
+    a.update(qsl=torch.tensor([0, 1, 3, 6], dtype=torch.int32), max_qlen=3)
+    assert _mla_call(lib, a) == binding.PA_ERR_CUDA
+
+
+def test_mla_plan_rejects_bad_shapes_without_device(lib):
+    for args, status in (((0, 16), binding.PA_ERR_UNSUPPORTED), ((4, 0), binding.PA_ERR_INVALID_ARG),
+                         ((4, 16, 7), binding.PA_ERR_INVALID_ARG), ((4, 16, binding.PA_BF16, 33), binding.PA_ERR_UNSUPPORTED)):
+        with pytest.raises(binding.PagedAttnError) as e:
+            binding.paged_attn_mla_plan(*args)
+        assert e.value.status == status
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.paged_attn_mla_reserve(4, 16, binding.PA_BF16, 0)
+    assert e.value.status == binding.PA_ERR_INVALID_ARG

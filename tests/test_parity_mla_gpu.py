@@ -1,0 +1,183 @@
+"""MLA decode on the GPU vs the float64 MLA oracle, element by element, through
+the C ABI (paged_attn_mla_decode).
+
+Tolerances (max absolute error): out 1e-2 for bf16 caches, 2e-2 for fp8
+caches; lse 1e-3.  Small cases are compared in full; the full-size MLA
+workloads on sampled sequences, in the launch configuration the benchmark
+times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_06_gb300 import binding
+from paged_kv_decode_06_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = {"bf16": 1e-2, "fp8": 2e-2}
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    binding.paged_attn_device_status(clear=True)
+    yield
+
+
+def _rows_of(w, seqs):
+    qsl = w.query_start_loc if w.query_start_loc is not None else np.arange(w.spec.num_seqs + 1)
+    return np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seqs])
+
+
+def check(w, seqs=None, options=None, ref=None):
+    out, lse = binding.mla_decode_workload(w, options=options)
+    torch.cuda.synchronize()
+    status = binding.paged_attn_device_status(clear=True)
+    assert status == 0, f"device status {status:#x}"
+    if ref is None:
+        ref = oracle.run_mla_workload(w, seqs=seqs)
+    rows = _rows_of(w, range(w.spec.num_seqs) if seqs is None else seqs)
+    o = out.float().cpu().numpy()[rows]
+    l = lse.cpu().numpy()[rows]
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    err_o = np.abs(o - ref[0][rows]).max()
+    err_l = np.abs(l - ref[1][rows]).max()
+    tol = TOL_OUT[w.spec.kv_dtype]
+    assert err_o <= tol, f"max|out - oracle| = {err_o:.3e} > {tol}"
+    assert err_l <= TOL_LSE, f"max|lse - oracle| = {err_l:.3e} > {TOL_LSE}"
+    return out, lse, err_o, err_l
+
+
+def _spec(kv="bf16", Hq=16, seq_lens=(1, 15, 16, 17, 31, 32, 33, 100), qlens=(1,), seed=5, pool=None):
+    fp8 = kv == "fp8"
+    return wl.custom_mla_spec(num_q_heads=Hq, kv_dtype=kv, seq_lens=seq_lens, query_len_choices=qlens,
+                              pool_pages=pool, kv_scale=0.05 if fp8 else 1.0, fp8_source_scale=0.05 if fp8 else 1.0,
+                              seed=seed)
+
+
+def test_mla_tiny_config_full():
+    check(wl.make_mla_workload(wl.MLA_CONFIGS["mla_tiny"], device="cuda"))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_mla_page_boundaries_and_ragged_tails(kv):
+    check(wl.make_mla_workload(_spec(kv=kv), device="cuda"))
+
+
+# heads x query lengths: 1 row tile (two teams a CTA), 2 row tiles, several head chunks
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("Hq,qlens", [(16, (1,)), (8, (1,)), (1, (1,)), (16, (4,)), (16, (2, 3, 4)), (32, (1,)),
+                                      (128, (1,)), (16, (3,)), (4, (1, 5, 8)), (2, (16,))])
+def test_mla_heads_and_verification_runs(kv, Hq, qlens):
+    w = wl.make_mla_workload(_spec(kv=kv, Hq=Hq, qlens=qlens, seq_lens=(16, 17, 40, 64, 130), seed=Hq + len(qlens)),
+                             device="cuda")
+    check(w)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 152])
+@pytest.mark.parametrize("kv,Hq,qlens", [("bf16", 16, (1,)), ("fp8", 16, (4,))])
+def test_mla_forced_split_counts_exercise_the_merge(num_ctas, kv, Hq, qlens):
+    w = wl.make_mla_workload(_spec(kv=kv, Hq=Hq, qlens=qlens, seq_lens=(3, 50, 300, 17, 1000), seed=num_ctas),
+                             device="cuda")
+    ref = oracle.run_mla_workload(w)
+    check(w, ref=ref, options=binding.make_options(num_ctas=num_ctas, min_pages_per_cta=1))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_mla_non_finite_tail_slots_and_unused_pages_do_not_leak(kv):
+    w = wl.make_mla_workload(_spec(kv=kv, seq_lens=(3, 17, 40, 1)), device="cuda")
+    ref = oracle.run_mla_workload(w)
+    nan_code = torch.tensor(float("nan")).to(torch.bfloat16) if kv == "bf16" else torch.tensor(0x7F, dtype=torch.uint8)
+    used = set()
+    for i, L in enumerate(w.seq_lens):
+        n = (int(L) + 15) // 16
+        used.update(int(x) for x in w.block_tables[i, :n])
+        last = int(w.block_tables[i, n - 1])
+        w.kv_cache[last, int(L) - 16 * (n - 1):] = nan_code
+    for p in range(w.num_pages):
+        if p not in used:
+            w.kv_cache[p] = nan_code
+    check(w, ref=ref)
+
+
+def test_mla_strided_cache_and_lse_optional():
+    w = wl.make_mla_workload(_spec(seq_lens=(20, 90, 33)), device="cuda")
+    ref = oracle.run_mla_workload(w)
+    # the latent cache as one half of a [NB, 16, 2, 576] allocation (page and slot strides grow)
+    big = torch.zeros((w.num_pages, 16, 2, 576), dtype=w.kv_cache.dtype, device="cuda")
+    big[:, :, 0] = w.kv_cache
+    w.kv_cache = big[:, :, 0]
+    assert not w.kv_cache.is_contiguous()
+    check(w, ref=ref)
+    out, lse = binding.mla_decode_workload(w, want_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None and np.abs(out.float().cpu().numpy() - ref[0]).max() <= TOL_OUT["bf16"]
+
+
+def test_mla_caller_workspace_and_deterministic_results():
+    w = wl.make_mla_workload(_spec(qlens=(1, 2), seq_lens=(500, 33, 1200)), device="cuda")
+    n = binding.paged_attn_mla_workspace_size(w.spec.num_seqs, w.spec.num_q_heads, binding.PA_BF16, 2)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    o1, l1, _, _ = check(w, options=binding.make_options(workspace=ws.data_ptr(), workspace_bytes=n))
+    o2, l2 = binding.mla_decode_workload(w)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.mla_decode_workload(w, options=binding.make_options(workspace=ws.data_ptr(), workspace_bytes=64))
+    assert e.value.status == binding.PA_ERR_WORKSPACE
+
+
+def test_mla_out_of_range_page_id_is_reported():
+    w = wl.make_mla_workload(_spec(seq_lens=(40, 20)), device="cuda")
+    w.block_tables = w.block_tables.copy()
+    w.block_tables[0, 1] = w.num_pages + 5
+    binding.mla_decode_workload(w)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) & binding.STATUS_PAGE_RANGE
+
+
+def test_mla_cuda_graph_capture_and_replay_with_new_metadata():
+    w = wl.make_mla_workload(_spec(seq_lens=(100, 300, 17, 64), pool=200), device="cuda")
+    s = w.spec
+    binding.paged_attn_mla_reserve(s.num_seqs, s.num_q_heads, binding.PA_BF16, 1)
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    out = torch.empty((w.q.shape[0], s.num_q_heads, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.q.shape[:2], dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    binding.paged_attn_mla_decode(w.q, w.kv_cache, bt, sl, None, 1, s.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        binding.paged_attn_mla_decode(w.q, w.kv_cache, bt, sl, None, 1, s.scale, out=out, lse=lse, stream=stream)
+    rng = np.random.default_rng(6)
+    for _ in range(3):
+        new_lens = rng.integers(1, 301, size=s.num_seqs).astype(np.int32)
+        n = (new_lens + 15) // 16
+        perm = rng.permutation(w.num_pages)
+        new_bt = np.full_like(w.block_tables, -1)
+        cur = 0
+        for i in range(s.num_seqs):
+            new_bt[i, :n[i]] = perm[cur:cur + n[i]]
+            cur += n[i]
+        bt.copy_(torch.from_numpy(new_bt))
+        sl.copy_(torch.from_numpy(new_lens))
+        w.q.normal_()
+        g.replay()
+        torch.cuda.synchronize()
+        w.block_tables, w.seq_lens = new_bt, new_lens
+        ref = oracle.run_mla_workload(w)
+        assert np.abs(out.float().cpu().numpy() - ref[0]).max() <= TOL_OUT["bf16"]
+        assert np.abs(lse.cpu().numpy() - ref[1]).max() <= TOL_LSE
+    assert binding.paged_attn_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("name", ["mla_tp8", "mla_mtp_fp8"])
+def test_mla_full_size_configs_sampled(name):
+    w = wl.make_mla_workload(wl.MLA_CONFIGS[name], device="cuda")
+    rng = np.random.default_rng(len(name))
+    seqs = set(rng.choice(w.spec.num_seqs, size=5, replace=False).tolist())
+    seqs.update({int(np.argmax(w.seq_lens)), int(np.argmin(w.seq_lens))})
+    _, _, eo, el = check(w, seqs=sorted(seqs))
+    print(f"{name}: sampled seqs {sorted(seqs)}: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
