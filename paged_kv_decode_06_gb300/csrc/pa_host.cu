@@ -562,7 +562,7 @@ constexpr int kMlaMaxRows = 32;   // query rows of one head chunk (2 tiles of 16
 
 struct MlaPlan {
   int B, Hq, max_qlen, esz;
-  int Gc, NC, R_max, RT, nteam, threads, grid, min_pages, nstage;
+  int Gc, NC, R_max, RT, nteam, threads, grid, min_pages, nstage, q_slots, pair;
   uint32_t stage_bytes, q_slot_bytes, off_stage, off_q, off_xchg, off_bar, team_bytes, off_prefix, smem;
   size_t ws_unit, ws_ml, ws_o, ws_bytes;
 };
@@ -574,9 +574,9 @@ int check_mla_options(const pa_options_t* opts) {
   if (opts->page_pairing < 0 || opts->page_pairing > 2)
     return fail(PA_ERR_INVALID_ARG, "page_pairing %d not in {0, 1, 2}", opts->page_pairing);
   if (opts->heads_per_cta != 0 || opts->sliding_window > 0 || opts->sinks != nullptr || opts->use_tcgen05 == 2 ||
-      opts->page_pairing == 2 || has_token_scales(opts))
+      has_token_scales(opts))
     return fail(PA_ERR_UNSUPPORTED, "MLA decode takes none of heads_per_cta, sliding_window, sinks, use_tcgen05 = 2, "
-                "page_pairing = 2, token scales");
+                "token scales");
   return PA_OK;
 }
 
@@ -612,16 +612,22 @@ int make_mla_plan(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t*
   p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
   p.stage_bytes = static_cast<uint32_t>(kPageSize * kMlaDqk * p.esz);
   p.q_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(max_qlen) * p.Gc * kMlaDqk * 2, 1024));
-  const uint32_t xchg = 8192u * static_cast<uint32_t>(p.RT);
+  // One query slot a team: the next segment's rows are fetched once the
+  // consumers hold the current ones in registers, and the room goes to the ring.
+  p.q_slots = 1;
+  const uint32_t xchg = 16384u * static_cast<uint32_t>(p.RT);   // 2 steps x 4 quarters x 2 KB a row tile
   const uint32_t bars = static_cast<uint32_t>(align_up(8u * (2 * kMaxStages + 4 + 2 * p.RT), 128));
   const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));
   const int64_t room = (static_cast<int64_t>(smem_optin) - 1024 - prefix_bytes) / p.nteam / 1024 * 1024;
-  const int64_t fixed = 2 * static_cast<int64_t>(p.q_slot_bytes) + xchg + bars;
+  const int64_t fixed = static_cast<int64_t>(p.q_slots) * p.q_slot_bytes + xchg + bars;
   p.nstage = room > fixed ? static_cast<int>(std::min<int64_t>(kMaxStages, (room - fixed) / p.stage_bytes)) : 0;
   if (p.nstage < 2) return fail(PA_ERR_UNSUPPORTED, "no MLA launch configuration fits %d bytes of shared memory", smem_optin);
   p.off_stage = 0;
   p.off_q = p.off_stage + p.nstage * p.stage_bytes;
-  p.off_xchg = p.off_q + 2 * p.q_slot_bytes;
+  p.off_xchg = p.off_q + static_cast<uint32_t>(p.q_slots) * p.q_slot_bytes;
+  // Page pairs (a consumer step holds two stages) when the ring keeps two more in flight.
+  const int pairing = opts ? opts->page_pairing : 0;
+  p.pair = pairing == 2 ? 1 : (pairing == 1 ? 0 : (p.nstage >= 4 ? 1 : 0));
   p.off_bar = p.off_xchg + xchg;
   p.team_bytes = static_cast<uint32_t>(align_up(p.off_bar + bars, 1024));
   p.off_prefix = p.team_bytes * static_cast<uint32_t>(p.nteam);
@@ -787,6 +793,8 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
   sp.kv_bytes = pl.stage_bytes;
   sp.off_xchg = pl.off_xchg;
   sp.team_bytes = pl.team_bytes;
+  sp.q_slots = pl.q_slots;
+  sp.pair_pages = pl.pair;
 
   pa::MergeParams mp = {};
   mp.out = sp.out;
@@ -1079,10 +1087,10 @@ int paged_attn_mla_plan(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype,
   plan->smem_bytes = static_cast<int32_t>(pl.smem);
   plan->min_pages_per_cta = pl.min_pages;
   plan->merge_rows = pl.R_max;
-  plan->page_pairing = 0;
+  plan->page_pairing = pl.pair;
   plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
   plan->variant = 2;
-  plan->block_pages = 1;
+  plan->block_pages = pl.pair ? 2 : 1;
   return PA_OK;
 }
 

@@ -60,8 +60,10 @@ struct SplitParams {
   const float* v_tok;
   int64_t tok_stride_page;  // floats between pages of the scale tensors
   uint32_t tok_bytes;       // HC * 16 * 4: one tensor's scales of one page
-  // MLA kernel: bytes between the shared-memory regions of a CTA's teams
+  // MLA kernel: bytes between the shared-memory regions of a CTA's teams,
+  // query slots per team (1 or 2)
   uint32_t team_bytes;
+  int32_t q_slots;
 };
 
 struct MergeParams {

@@ -140,74 +140,83 @@ struct MlaWarp {
   }
 };
 
-// One page for one consumer warp.  st: the page's stage; xbuf: this step's
-// exchange buffer of the row tile (4 quarters x 1 KB) and xbar / xpar its
-// mbarrier (4 arrivals) and phase parity; tb: first token of the page;
-// lim0 / lim1: last key rows g / g+8 may see.  Returns false if the exchange
-// wait timed out.
-template <bool FP8>
-__device__ __forceinline__ bool mla_page(MlaWarp<FP8>& ws, uint32_t st, uint32_t xbuf, uint32_t xbar, uint32_t xpar,
-                                         int cq, int tb, int L, int min_lim, int lim0, int lim1, float scale_log2,
-                                         int lane) {
+// NP consecutive pages of a segment for one consumer warp.  st[pg]: page
+// pg's stage; xbuf: this step's exchange buffer of the row tile (4 quarters x
+// NP KB) and xbar / xpar its mbarrier (4 arrivals) and phase parity; tb: first
+// token of the first page; lim0 / lim1: last key rows g / g+8 may see.
+// Returns false if the exchange wait timed out.
+template <bool FP8, int NP>
+__device__ __forceinline__ bool mla_pages(MlaWarp<FP8>& ws, const uint32_t (&st)[NP], uint32_t xbuf, uint32_t xbar,
+                                          uint32_t xpar, int cq, int tb, int L, int min_lim, int lim0, int lim1,
+                                          float scale_log2, int lane) {
   const int tig = lane & 3, mi = lane >> 3, rr = lane & 7;
   // ---- partial scores over this quarter's 144 features ----
-  float S[2][4];
+  float S[2 * NP][4];
 #pragma unroll
-  for (int n = 0; n < 2; ++n) S[n][0] = S[n][1] = S[n][2] = S[n][3] = 0.f;
+  for (int n = 0; n < 2 * NP; ++n) S[n][0] = S[n][1] = S[n][2] = S[n][3] = 0.f;
   if constexpr (FP8) {
 #pragma unroll
     for (int kk = 0; kk < kMlaKs - 1; kk += 2) {
       const int ks = kMlaKs * cq + kk;
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4(st + mla_off<FP8>(rr + 8 * (mi & 1), ks + (mi >> 1)), r0, r1, r2, r3);
-      mma_f16(S[0], ws.Qf[kk], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
-      mma_f16(S[1], ws.Qf[kk], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
-      mma_f16(S[0], ws.Qf[kk + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
-      mma_f16(S[1], ws.Qf[kk + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(st[pg] + mla_off<FP8>(rr + 8 * (mi & 1), ks + (mi >> 1)), r0, r1, r2, r3);
+        mma_f16(S[2 * pg], ws.Qf[kk], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
+        mma_f16(S[2 * pg + 1], ws.Qf[kk], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+        mma_f16(S[2 * pg], ws.Qf[kk + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
+        mma_f16(S[2 * pg + 1], ws.Qf[kk + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+      }
     }
-    {
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
       uint32_t r0, r1;   // the quarter's ninth k-step: keys 0-7 and 8-15 of one 16-feature chunk
-      ldsm_x2(st + mla_off<FP8>(rr + 8 * (mi & 1), kMlaKs * cq + kMlaKs - 1), r0, r1);
-      mma_f16(S[0], ws.Qf[kMlaKs - 1], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
-      mma_f16(S[1], ws.Qf[kMlaKs - 1], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+      ldsm_x2(st[pg] + mla_off<FP8>(rr + 8 * (mi & 1), kMlaKs * cq + kMlaKs - 1), r0, r1);
+      mma_f16(S[2 * pg], ws.Qf[kMlaKs - 1], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
+      mma_f16(S[2 * pg + 1], ws.Qf[kMlaKs - 1], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
     }
   } else {
 #pragma unroll
     for (int kk = 0; kk < kMlaKs; ++kk) {
       const int ks = kMlaKs * cq + kk;
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4(st + mla_off<FP8>(rr + 8 * (mi >> 1), 2 * ks + (mi & 1)), r0, r1, r2, r3);
-      mma_bf16(S[0], ws.Qf[kk], r0, r1);
-      mma_bf16(S[1], ws.Qf[kk], r2, r3);
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(st[pg] + mla_off<FP8>(rr + 8 * (mi >> 1), 2 * ks + (mi & 1)), r0, r1, r2, r3);
+        mma_bf16(S[2 * pg], ws.Qf[kk], r0, r1);
+        mma_bf16(S[2 * pg + 1], ws.Qf[kk], r2, r3);
+      }
     }
   }
   // ---- the four quarters' partials meet in shared memory ----
-  const uint32_t mine = xbuf + static_cast<uint32_t>(cq) * 1024u + 16u * lane;
-  sts_f4(mine, S[0][0], S[0][1], S[0][2], S[0][3]);
-  sts_f4(mine + 512u, S[1][0], S[1][1], S[1][2], S[1][3]);
+  const uint32_t mine = xbuf + static_cast<uint32_t>(cq) * (1024u * NP) + 16u * lane;
+#pragma unroll
+  for (int n = 0; n < 2 * NP; ++n) sts_f4(mine + 512u * n, S[n][0], S[n][1], S[n][2], S[n][3]);
   __syncwarp();
   if (lane == 0) mbar_arrive(xbar);
   if (!mbar_wait(xbar, xpar)) return false;
-  float x[2][4];
-  {
-    const float4 a0 = lds_f4(xbuf + 16u * lane), a1 = lds_f4(xbuf + 512u + 16u * lane);
-    x[0][0] = a0.x; x[0][1] = a0.y; x[0][2] = a0.z; x[0][3] = a0.w;
-    x[1][0] = a1.x; x[1][1] = a1.y; x[1][2] = a1.z; x[1][3] = a1.w;
+  float x[2 * NP][4];
+#pragma unroll
+  for (int n = 0; n < 2 * NP; ++n) {
+    const float4 a = lds_f4(xbuf + 512u * n + 16u * lane);
+    x[n][0] = a.x; x[n][1] = a.y; x[n][2] = a.z; x[n][3] = a.w;
   }
 #pragma unroll
   for (int q = 1; q < 4; ++q) {   // same order in every quarter: identical sums
-    const float4 a0 = lds_f4(xbuf + q * 1024u + 16u * lane), a1 = lds_f4(xbuf + q * 1024u + 512u + 16u * lane);
-    x[0][0] += a0.x; x[0][1] += a0.y; x[0][2] += a0.z; x[0][3] += a0.w;
-    x[1][0] += a1.x; x[1][1] += a1.y; x[1][2] += a1.z; x[1][3] += a1.w;
+#pragma unroll
+    for (int n = 0; n < 2 * NP; ++n) {
+      const float4 a = lds_f4(xbuf + q * (1024u * NP) + 512u * n + 16u * lane);
+      x[n][0] += a.x; x[n][1] += a.y; x[n][2] += a.z; x[n][3] += a.w;
+    }
   }
 #pragma unroll
-  for (int n = 0; n < 2; ++n)
+  for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) x[n][e] *= scale_log2;
   // ---- causal run / context tail mask ----
-  if (tb + kPage - 1 > min_lim) {
+  if (tb + kPage * NP - 1 > min_lim) {
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int tok = tb + 8 * n + 2 * tig + e;
@@ -216,8 +225,13 @@ __device__ __forceinline__ bool mla_page(MlaWarp<FP8>& ws, uint32_t st, uint32_t
       }
   }
   // ---- online softmax (exp2 domain) ----
-  float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-  float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+  float mx0 = fmaxf(x[0][0], x[0][1]);
+  float mx1 = fmaxf(x[0][2], x[0][3]);
+#pragma unroll
+  for (int n = 1; n < 2 * NP; ++n) {
+    mx0 = fmaxf(mx0, fmaxf(x[n][0], x[n][1]));
+    mx1 = fmaxf(mx1, fmaxf(x[n][2], x[n][3]));
+  }
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -232,7 +246,7 @@ __device__ __forceinline__ bool mla_page(MlaWarp<FP8>& ws, uint32_t st, uint32_t
   ws.m1 = mn1;
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int n = 0; n < 2; ++n) {
+  for (int n = 0; n < 2 * NP; ++n) {
     x[n][0] = fast_exp2(x[n][0] - base0);
     x[n][1] = fast_exp2(x[n][1] - base0);
     x[n][2] = fast_exp2(x[n][2] - base1);
@@ -251,67 +265,70 @@ __device__ __forceinline__ bool mla_page(MlaWarp<FP8>& ws, uint32_t st, uint32_t
       ws.O[J][3] *= a1;
     }
   }
-  uint32_t Pa[4];
-  if constexpr (FP8) {
-    Pa[0] = pack_f16(x[0][0], x[0][1]);
-    Pa[1] = pack_f16(x[0][2], x[0][3]);
-    Pa[2] = pack_f16(x[1][0], x[1][1]);
-    Pa[3] = pack_f16(x[1][2], x[1][3]);
-  } else {
-    Pa[0] = pack_bf16(x[0][0], x[0][1]);
-    Pa[1] = pack_bf16(x[0][2], x[0][3]);
-    Pa[2] = pack_bf16(x[1][0], x[1][1]);
-    Pa[3] = pack_bf16(x[1][2], x[1][3]);
-  }
   // ---- P V over this quarter's 128 value columns; rows at or past the
   // sequence end are zeroed (stale, even non-finite, tail slots) ----
-  const int vt = L - tb;
-  const bool tail = vt < kPage;
-  const uint32_t mb0 = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
-  const uint32_t mb1 = (2 * tig + 8 < vt ? 0x0000ffffu : 0u) | (2 * tig + 9 < vt ? 0xffff0000u : 0u);
-  if constexpr (FP8) {
 #pragma unroll
-    for (int c = 0; c < 8; c += 2) {
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_t(st + mla_off<FP8>(rr + 8 * (mi & 1), 8 * cq + c + (mi >> 1)), r0, r1, r2, r3);
-      const uint32_t u0 = prmt(r0, 0u, 0x3120u), u1 = prmt(r1, 0u, 0x3120u);
-      const uint32_t u2 = prmt(r2, 0u, 0x3120u), u3 = prmt(r3, 0u, 0x3120u);
-      uint32_t b[8] = {e4m3x2_to_f16x2(u0), e4m3x2_to_f16x2(u1), e4m3x2_to_f16x2(u0 >> 16),
-                       e4m3x2_to_f16x2(u1 >> 16), e4m3x2_to_f16x2(u2), e4m3x2_to_f16x2(u3),
-                       e4m3x2_to_f16x2(u2 >> 16), e4m3x2_to_f16x2(u3 >> 16)};
-      if (tail) {
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          b[e] &= mb0;
-          b[e + 1] &= mb1;
-        }
-      }
-      mma_f16(ws.O[2 * c], Pa, b[0], b[1]);
-      mma_f16(ws.O[2 * c + 1], Pa, b[2], b[3]);
-      mma_f16(ws.O[2 * c + 2], Pa, b[4], b[5]);
-      mma_f16(ws.O[2 * c + 3], Pa, b[6], b[7]);
+  for (int pg = 0; pg < NP; ++pg) {
+    uint32_t Pa[4];
+    if constexpr (FP8) {
+      Pa[0] = pack_f16(x[2 * pg][0], x[2 * pg][1]);
+      Pa[1] = pack_f16(x[2 * pg][2], x[2 * pg][3]);
+      Pa[2] = pack_f16(x[2 * pg + 1][0], x[2 * pg + 1][1]);
+      Pa[3] = pack_f16(x[2 * pg + 1][2], x[2 * pg + 1][3]);
+    } else {
+      Pa[0] = pack_bf16(x[2 * pg][0], x[2 * pg][1]);
+      Pa[1] = pack_bf16(x[2 * pg][2], x[2 * pg][3]);
+      Pa[2] = pack_bf16(x[2 * pg + 1][0], x[2 * pg + 1][1]);
+      Pa[3] = pack_bf16(x[2 * pg + 1][2], x[2 * pg + 1][3]);
     }
-  } else {
+    const int vt = L - tb - kPage * pg;
+    const bool tail = vt < kPage;
+    const uint32_t mb0 = (2 * tig < vt ? 0x0000ffffu : 0u) | (2 * tig + 1 < vt ? 0xffff0000u : 0u);
+    const uint32_t mb1 = (2 * tig + 8 < vt ? 0x0000ffffu : 0u) | (2 * tig + 9 < vt ? 0xffff0000u : 0u);
+    if constexpr (FP8) {
 #pragma unroll
-    for (int J = 0; J < 16; J += 2) {
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_t(st + mla_off<FP8>(rr + 8 * (mi & 1), 16 * cq + J + (mi >> 1)), r0, r1, r2, r3);
-      if (tail) {
-        r0 &= mb0;
-        r1 &= mb1;
-        r2 &= mb0;
-        r3 &= mb1;
+      for (int c = 0; c < 8; c += 2) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(st[pg] + mla_off<FP8>(rr + 8 * (mi & 1), 8 * cq + c + (mi >> 1)), r0, r1, r2, r3);
+        const uint32_t u0 = prmt(r0, 0u, 0x3120u), u1 = prmt(r1, 0u, 0x3120u);
+        const uint32_t u2 = prmt(r2, 0u, 0x3120u), u3 = prmt(r3, 0u, 0x3120u);
+        uint32_t b[8] = {e4m3x2_to_f16x2(u0), e4m3x2_to_f16x2(u1), e4m3x2_to_f16x2(u0 >> 16),
+                         e4m3x2_to_f16x2(u1 >> 16), e4m3x2_to_f16x2(u2), e4m3x2_to_f16x2(u3),
+                         e4m3x2_to_f16x2(u2 >> 16), e4m3x2_to_f16x2(u3 >> 16)};
+        if (tail) {
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            b[e] &= mb0;
+            b[e + 1] &= mb1;
+          }
+        }
+        mma_f16(ws.O[2 * c], Pa, b[0], b[1]);
+        mma_f16(ws.O[2 * c + 1], Pa, b[2], b[3]);
+        mma_f16(ws.O[2 * c + 2], Pa, b[4], b[5]);
+        mma_f16(ws.O[2 * c + 3], Pa, b[6], b[7]);
       }
-      mma_bf16(ws.O[J], Pa, r0, r1);
-      mma_bf16(ws.O[J + 1], Pa, r2, r3);
+    } else {
+#pragma unroll
+      for (int J = 0; J < 16; J += 2) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(st[pg] + mla_off<FP8>(rr + 8 * (mi & 1), 16 * cq + J + (mi >> 1)), r0, r1, r2, r3);
+        if (tail) {
+          r0 &= mb0;
+          r1 &= mb1;
+          r2 &= mb0;
+          r3 &= mb1;
+        }
+        mma_bf16(ws.O[J], Pa, r0, r1);
+        mma_bf16(ws.O[J + 1], Pa, r2, r3);
+      }
     }
   }
   return true;
 }
 
 // Team layout in shared memory, from the team's base (team t at
-// base + t * team_bytes): ring stages at off_stage, two query slots at off_q,
-// exchange buffers at off_xchg (2 steps x RT row tiles x 4 quarters x 1 KB),
+// base + t * team_bytes): ring stages at off_stage, q_slots query slots at off_q,
+// exchange buffers at off_xchg (2 steps x RT row tiles x 4 quarters x 2 KB),
 // barriers at off_bar (full[nstage], empty[nstage], qfull[2], qempty[2],
 // xfull[2][RT]: the exchange of step parity b of row tile rt).  The
 // sequence metadata (page prefix, lengths, query starts) is shared by the CTA
@@ -399,9 +416,9 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
         }
       }
       if (k == 0 || cu.j == 0) {
-        const int qs = qseg & 1;
-        if (qseg >= 2) {
-          if (!mbar_wait(qempty_bar(qs), static_cast<uint32_t>((qseg >> 1) - 1) & 1u)) {
+        const int qs = qseg % p.q_slots;
+        if (qseg >= p.q_slots) {
+          if (!mbar_wait(qempty_bar(qs), static_cast<uint32_t>(qseg / p.q_slots - 1) & 1u)) {
             if (lane == 0) atomicOr(p.err, kErrTimeout);
             break;
           }
@@ -443,7 +460,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
   const int tig = lane & 3;
   const int rho0 = 16 * rt + gq;
   const int rho1 = rho0 + 8;
-  const uint32_t xbase = tbase + p.off_xchg + static_cast<uint32_t>(rt) * 4096u;
+  const uint32_t xbase = tbase + p.off_xchg + static_cast<uint32_t>(rt) * 8192u;
 
   Cursor cu = locate(s_pre, B, NC, start);
   int qseg = 0;
@@ -458,7 +475,8 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
 
   int stage = 0;
   uint32_t round = 0;
-  for (int64_t k = 0; k < count; ++k) {
+  int64_t k = 0;
+  while (k < count) {
     if (!mbar_wait(full_bar(stage), round & 1u)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
@@ -468,8 +486,8 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       si = seq_info(p, s_len, s_qsl, cu.i, lane == 0 && cw == 0, 0);
       seg_k0 = k;
       seg_j0 = cu.j;
-      const int qs = qseg & 1;
-      if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg >> 1) & 1u)) {
+      const int qs = qseg % p.q_slots;
+      if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg / p.q_slots) & 1u)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
@@ -495,23 +513,51 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       ++qseg;
       ws.reset();
     }
+    // Two consecutive pages of the segment are taken together when the ring
+    // is deep enough (one exchange and one softmax reduction per 32 keys).
+    int stage2 = stage + 1;
+    uint32_t round2 = round;
+    if (stage2 == nstage) {
+      stage2 = 0;
+      ++round2;
+    }
+    const bool pair = p.pair_pages && (k + 1 < count) && (cu.j + 1 < cu.n);
+    if (pair && !mbar_wait(full_bar(stage2), round2 & 1u)) {
+      if (lane == 0) atomicOr(p.err, kErrTimeout);
+      break;
+    }
     const int tb = kPage * cu.j;
     if (active) {
       // exchange buffer b = step parity is used for the (step >> 1)-th time
       const int b = static_cast<int>(step & 1u);
-      if (!mla_page<FP8>(ws, tbase + p.off_stage + static_cast<uint32_t>(stage) * GG::STAGE,
-                         xbase + static_cast<uint32_t>(b * RT) * 4096u, xfull_bar(b, rt), (step >> 1) & 1u, cq, tb,
-                         si.L, si.L - si.qn, lim0, lim1, p.scale_log2, lane)) {
+      const uint32_t xb = xbase + static_cast<uint32_t>(b * RT) * 8192u;
+      const uint32_t s0 = tbase + p.off_stage + static_cast<uint32_t>(stage) * GG::STAGE;
+      bool ok;
+      if (pair) {
+        const uint32_t sts[2] = {s0, tbase + p.off_stage + static_cast<uint32_t>(stage2) * GG::STAGE};
+        ok = mla_pages<FP8, 2>(ws, sts, xb, xfull_bar(b, rt), (step >> 1) & 1u, cq, tb, si.L, si.L - si.qn, lim0,
+                               lim1, p.scale_log2, lane);
+      } else {
+        const uint32_t sts[1] = {s0};
+        ok = mla_pages<FP8, 1>(ws, sts, xb, xfull_bar(b, rt), (step >> 1) & 1u, cq, tb, si.L, si.L - si.qn, lim0,
+                               lim1, p.scale_log2, lane);
+      }
+      if (!ok) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
       ++step;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar(stage));
-    const bool seg_last = (k + 1 == count) || (cu.j == cu.n - 1);
+    if (lane == 0) {
+      mbar_arrive(empty_bar(stage));
+      if (pair) mbar_arrive(empty_bar(stage2));
+    }
+    const int np = pair ? 2 : 1;
+    const int j_last = cu.j + np - 1;
+    const bool seg_last = (k + np == count) || (j_last == cu.n - 1);
     if (seg_last && active) {
-      const bool complete = (seg_j0 == 0) && (cu.j == cu.n - 1);
+      const bool complete = (seg_j0 == 0) && (j_last == cu.n - 1);
       float lt0 = ws.l0 + __shfl_xor_sync(0xffffffffu, ws.l0, 1);
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
       float lt1 = ws.l1 + __shfl_xor_sync(0xffffffffu, ws.l1, 1);
@@ -569,11 +615,14 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
         }
       }
     }
-    advance(cu, s_pre, B, NC);
-    if (++stage == nstage) {
-      stage = 0;
-      ++round;
+    for (int t = 0; t < np; ++t) {
+      advance(cu, s_pre, B, NC);
+      if (++stage == nstage) {
+        stage = 0;
+        ++round;
+      }
     }
+    k += np;
   }
 }
 
