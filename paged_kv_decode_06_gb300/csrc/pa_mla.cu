@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
   if (g >= NG || X == 0) return;
   const int64_t start = static_cast<int64_t>(g) * X / NG;
   const int64_t end = static_cast<int64_t>(g + 1) * X / NG;
-  const int64_t count = end - start;
+  const int count = static_cast<int>(end - start);   // pages of this worker (X / NG < 2^31)
   if (count <= 0) return;
   const uint32_t qrow_bytes = static_cast<uint32_t>(G * kMlaDqk * 2);   // one query token of a head chunk
 
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
     BlockTableCache btc;
     int stage = 0;
     uint32_t round = 0;
-    for (int64_t k = 0; k < count; ++k) {
+    for (int k = 0; k < count; ++k) {
       if (round > 0) {
         if (!mbar_wait(empty_bar(stage), (round - 1) & 1u)) {
           if (lane == 0) atomicOr(p.err, kErrTimeout);
@@ -453,6 +453,16 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
   }
 
   // ============================== consumers ================================
+  // g, NG and X are needed only at segment boundaries: recomputed there from
+  // shared memory and launch constants instead of staying live in registers.
+  auto worker = [&]() { return team * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x); };
+  auto total_pages = [&]() { return static_cast<int64_t>(p.NC) * s_pre[p.num_seqs]; };
+  auto workers = [&](int64_t x) {
+    int64_t n = (x + p.min_pages - 1) / p.min_pages;
+    if (n < 1) n = 1;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * TT::NTEAM;
+    return static_cast<int>(n < nw ? n : nw);
+  };
   const int cw = wt - 1;
   const int rt = cw >> 2;            // 16-row tile
   const int cq = cw & 3;             // column quarter
@@ -464,7 +474,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
 
   Cursor cu = locate(s_pre, B, NC, start);
   int qseg = 0;
-  int64_t seg_k0 = 0;
+  bool seg_first_page = false;      // the segment starts at this worker's first page
   int seg_j0 = 0;
   SeqInfo si = {0, 0, 0, 0};
   bool active = false, ok0 = false, ok1 = false;
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
 
   int stage = 0;
   uint32_t round = 0;
-  int64_t k = 0;
+  int k = 0;
   while (k < count) {
     if (!mbar_wait(full_bar(stage), round & 1u)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
     if (k == 0 || cu.j == 0) {
       // ---- new segment: query rows into registers, state reset ----
       si = seq_info(p, s_len, s_qsl, cu.i, lane == 0 && cw == 0, 0);
-      seg_k0 = k;
+      seg_first_page = k == 0;
       seg_j0 = cu.j;
       const int qs = qseg % p.q_slots;
       if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg / p.q_slots) & 1u)) {
@@ -493,10 +503,12 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       }
       if (seg_j0 == 0 && cw == 0 && lane == 0) {
         // This worker holds the unit's first page: describe the unit for the merge.
-        const int64_t a = static_cast<int64_t>(NC) * s_pre[cu.i] + static_cast<int64_t>(cu.c) * cu.n;
-        const int last = static_cast<int>(((a + cu.n) * NG - 1) / X);
-        p.ws_unit[static_cast<int64_t>(cu.i) * NC + cu.c] =
-            make_int4(g, (last - g + 1) | (k != 0 ? (1 << 30) : 0), si.t0, si.qn);
+        const int64_t xt = total_pages();
+        const int gw = worker();
+        const int64_t a = static_cast<int64_t>(p.NC) * s_pre[cu.i] + static_cast<int64_t>(cu.c) * cu.n;
+        const int last = static_cast<int>(((a + cu.n) * workers(xt) - 1) / xt);
+        p.ws_unit[static_cast<int64_t>(cu.i) * p.NC + cu.c] =
+            make_int4(gw, (last - gw + 1) | (k != 0 ? (1 << 30) : 0), si.t0, si.qn);
       }
       const int R = G * si.qn;
       active = 16 * rt < R;
@@ -593,8 +605,8 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
           }
         }
       } else {
-        const int which = (seg_k0 == 0) ? 0 : 1;
-        const int64_t rowbase = static_cast<int64_t>(2 * g + which) * p.R_max;
+        const int which = seg_first_page ? 0 : 1;
+        const int64_t rowbase = static_cast<int64_t>(2 * worker() + which) * p.R_max;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const bool ok = half ? ok1 : ok0;
