@@ -152,7 +152,10 @@ for i in seq_iter:
                                  fp8_source_scale=spec.fp8_source_scale, seed=nseq)
         w = wl.make_mla_workload(sub)
         t0 = time.perf_counter()
-        oracle.run_mla_workload(w)
+        if impl == "c":
+            c_oracle.run_mla_workload(w, threads=used)
+        else:
+            oracle.run_mla_workload(w)
         t_used += time.perf_counter() - t0
         done_bytes += w.kv_bytes(); nseq += 1; ntok += L
         if t_used >= budget:
@@ -178,16 +181,14 @@ print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": nto
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env.pop(k, None)
-    if impl == "numpy" or config.startswith("mla"):
+    if impl == "numpy":
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             env[k] = "1"
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    if config.startswith("mla"):
-        d["threads"] = 1
-    what = (f"plain-C float64 oracle, {d['threads']} OpenMP thread(s)" if impl == "c" and not config.startswith("mla")
+    what = (f"plain-C float64 oracle, {d['threads']} OpenMP thread(s)" if impl == "c"
             else "float64 NumPy oracle, single-threaded BLAS")
     sample = (f"{what}, {d['seqs']} whole sequences ({d['tokens']} cached tokens) drawn from the {config} "
               f"workload's length mix, {d['seconds']:.1f} s of oracle time")
@@ -197,11 +198,7 @@ print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": nto
 def cpu_baseline(config: str, budget_s: float):
     """The ``cpu_baseline`` object: the C oracle on all host cores (value), on
     one core, and the NumPy oracle on one core, each on its own bounded sample
-    (MLA workloads: the NumPy MLA oracle on one core)."""
-    if config.startswith("mla"):
-        g, cores, sample = cpu_oracle_sample(config, budget_s=budget_s, threads=1, impl="numpy")
-        return {"value": g, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
-                "host_cores": os.cpu_count(), "host_cpu": _cpu_model()}
+    (MLA workloads: the MLA oracles)."""
     gbs, cores, sample = cpu_oracle_sample(config, budget_s=0.4 * budget_s, threads=0, impl="c")
     g1, _, s1 = cpu_oracle_sample(config, budget_s=0.3 * budget_s, threads=1, impl="c")
     gn, _, sn = cpu_oracle_sample(config, budget_s=0.3 * budget_s, threads=1, impl="numpy")

@@ -45,6 +45,10 @@ def load():
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                                          ctypes.c_float, ctypes.c_float, P, P, ctypes.c_int, P, P, P, P,
                                          ctypes.c_int]
+        lib.pa_oracle_mla_decode.restype = ctypes.c_int
+        lib.pa_oracle_mla_decode.argtypes = [P, P, ctypes.c_int, P, ctypes.c_int64, P, P, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                             ctypes.c_float, P, P, P, ctypes.c_int]
         lib.pa_oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -100,3 +104,40 @@ def run_workload(w, seqs=None, sliding_window=0, sinks=None, threads=0):
     return paged_decode_attention(q_bits, k, v, w.block_tables, w.seq_lens, w.query_start_loc, s.scale, s.k_scale,
                                   s.v_scale, s.kv_dtype, seqs=seqs, sliding_window=sliding_window, sinks=sinks,
                                   k_token_scales=ks, v_token_scales=vs, threads=threads)
+
+
+def mla_decode(q_bits, cache, block_tables, seq_lens, query_start_loc, scale, kv_scale=1.0, kv_dtype="bf16",
+               kv_lora_rank=512, seqs=None, threads=0):
+    """Same arguments and results as ``oracle.mla_decode`` (plus ``threads``);
+    rows outside ``seqs`` are NaN."""
+    lib = load()
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    fp8 = kv_dtype == "fp8"
+    c = np.ascontiguousarray(cache, dtype=np.uint8 if fp8 else np.uint16)
+    T, Hq, Dqk = q.shape
+    NB = c.shape[0]
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = len(sl)
+    qsl = None if query_start_loc is None else np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    mask = None
+    if seqs is not None:
+        mask = np.zeros(B, dtype=np.uint8)
+        mask[list(seqs)] = 1
+    out = np.full((T, Hq, kv_lora_rank), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    st = lib.pa_oracle_mla_decode(_ptr(q), _ptr(c), int(fp8), _ptr(bt), bt.shape[1], _ptr(sl), _ptr(qsl), B, T, Hq,
+                                  Dqk, int(kv_lora_rank), NB, float(scale), float(kv_scale), _ptr(out), _ptr(lse),
+                                  _ptr(mask), int(threads))
+    if st != 0:
+        raise ValueError("C oracle rejected the inputs")
+    return out, lse
+
+
+def run_mla_workload(w, seqs=None, threads=0):
+    """C-oracle outputs for a ``paged_kv_decode_06_gb300.workloads.MlaWorkload``."""
+    from paged_kv_decode_06_gb300.workloads import host_mla_arrays
+    q_bits, c = host_mla_arrays(w)
+    s = w.spec
+    return mla_decode(q_bits, c, w.block_tables, w.seq_lens, w.query_start_loc, s.scale, s.kv_scale, s.kv_dtype,
+                      s.kv_lora_rank, seqs=seqs, threads=threads)

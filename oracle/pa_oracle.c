@@ -170,6 +170,91 @@ int pa_oracle_decode(const uint16_t* q_bits, const void* k, const void* v, int k
   return bad ? -1 : 0;
 }
 
+/*
+ * MLA decode over a paged latent cache (the NumPy oracle's oracle/mla.py,
+ * restated loop by loop; ATOM model-operations guide, "Multi-head latent
+ * attention"): every cached token is one row C_j of Dqk values (latent part
+ * first, kv_lora_rank values, then the rotary part) shared by all query heads;
+ * s_j = scale * <q[t, h], C_j> for j <= p, out = sum_j exp(s_j - lse) C_j[0:Dv].
+ * Sequence by sequence: the rows are decoded once (OpenMP over rows), then
+ * OpenMP over (query row, head) pairs.
+ *
+ * q_bits   uint16 [T, Hq, Dqk]; cache [NB, 16, Dqk] contiguous, uint16 bf16 patterns
+ *          (kv_fp8 = 0) or uint8 e4m3fn codes (value = code * kv_scale)
+ * out      double [T, Hq, Dv]; lse double [T, Hq]; other arguments as pa_oracle_decode.
+ * Returns 0, or -1 on an invalid argument.
+ */
+int pa_oracle_mla_decode(const uint16_t* q_bits, const void* cache, int kv_fp8, const int32_t* block_tables,
+                         int64_t bt_stride, const int32_t* seq_lens, const int32_t* qsl, int B, int T, int Hq,
+                         int Dqk, int Dv, int64_t NB, float scale, float kv_scale, double* out, double* lse,
+                         const uint8_t* seq_mask, int threads) {
+  if (B < 0 || T < 0 || Hq <= 0 || Dqk <= 0 || Dv <= 0 || Dv > Dqk) return -1;
+  const double sc = (double)scale, ks = (double)kv_scale;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  for (int i = 0; i < B; ++i) {
+    if (seq_mask && !seq_mask[i]) continue;
+    const int L = seq_lens[i];
+    const int t0 = qsl ? qsl[i] : i;
+    const int qn = qsl ? qsl[i + 1] - qsl[i] : 1;
+    if (L < 1 || qn < 1 || qn > L || t0 < 0 || t0 + qn > T) return -1;
+    for (int j = 0; j < L; j += PA_PAGE) {
+      const int64_t page = block_tables[(int64_t)i * bt_stride + j / PA_PAGE];
+      if (page < 0 || page >= NB) return -1;
+    }
+    /* the sequence's decoded rows, gathered through the block table (once for all heads) */
+    double* C = (double*)malloc(sizeof(double) * (size_t)L * Dqk);
+    if (!C) return -1;
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < L; ++j) {
+      const int64_t page = block_tables[(int64_t)i * bt_stride + j / PA_PAGE];
+      const int64_t row = (page * PA_PAGE + j % PA_PAGE) * (int64_t)Dqk;
+      for (int d = 0; d < Dqk; ++d)
+        C[(size_t)j * Dqk + d] = kv_fp8 ? e4m3fn_value(((const uint8_t*)cache)[row + d]) * ks
+                                        : bf16_value(((const uint16_t*)cache)[row + d]);
+    }
+    int bad = 0;
+    /* one task per (query row, head) */
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int rh = 0; rh < qn * Hq; ++rh) {
+      const int r = rh / Hq, h = rh % Hq;
+      const int p = L - qn + r;
+      const uint16_t* qrow = q_bits + ((int64_t)(t0 + r) * Hq + h) * Dqk;
+      double* s = (double*)malloc(sizeof(double) * (size_t)(p + 1));
+      if (!s) {
+        bad = 1;
+        continue;
+      }
+      /* pass 1: scores of keys 0..p and their maximum */
+      double m = -INFINITY;
+      for (int j = 0; j <= p; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < Dqk; ++d) dot += bf16_value(qrow[d]) * C[(size_t)j * Dqk + d];
+        s[j] = sc * dot;
+        if (s[j] > m) m = s[j];
+      }
+      /* pass 2: normaliser and the weighted sum of the latent parts */
+      double sum = 0.0;
+      for (int j = 0; j <= p; ++j) sum += exp(s[j] - m);
+      const double l = m + log(sum);
+      double* orow = out + ((int64_t)(t0 + r) * Hq + h) * Dv;
+      for (int d = 0; d < Dv; ++d) orow[d] = 0.0;
+      for (int j = 0; j <= p; ++j) {
+        const double w = exp(s[j] - l);
+        for (int d = 0; d < Dv; ++d) orow[d] += w * C[(size_t)j * Dqk + d];
+      }
+      lse[(int64_t)(t0 + r) * Hq + h] = l;
+      free(s);
+    }
+    free(C);
+    if (bad) return -1;
+  }
+  return 0;
+}
+
 /* Threads OpenMP would use by default (1 without OpenMP). */
 int pa_oracle_max_threads(void) {
 #ifdef _OPENMP

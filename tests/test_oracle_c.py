@@ -54,3 +54,19 @@ def test_c_oracle_sampled_sequences_and_thread_counts():
     assert np.isnan(a[0][0]).all() and np.isfinite(a[0][1]).all()
     ref = oracle.run_workload(w, seqs=[1, 3])
     assert np.abs(a[0][[1, 3]] - ref[0][[1, 3]]).max() < 1e-11
+
+
+# ------------------------------------------------------------------ MLA
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("qlens", [(1,), (2, 3, 4)])
+def test_c_mla_oracle_matches_numpy_oracle(kv, qlens):
+    fp8 = kv == "fp8"
+    w = wl.make_mla_workload(wl.custom_mla_spec(num_q_heads=4, kv_dtype=kv, seq_lens=(1, 16, 17, 60),
+                                                query_len_choices=qlens, kv_scale=0.05 if fp8 else 1.0,
+                                                fp8_source_scale=0.05 if fp8 else 1.0, seed=len(qlens) + 3))
+    a = oracle.run_mla_workload(w)
+    b = c_oracle.run_mla_workload(w)
+    assert np.abs(a[0] - b[0]).max() < 1e-11 and np.abs(a[1] - b[1]).max() < 1e-11
+    c = c_oracle.run_mla_workload(w, threads=1)
+    assert np.array_equal(b[0], c[0]) and np.array_equal(b[1], c[1])
