@@ -636,7 +636,7 @@ int make_mla_plan(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t*
   p.ws_unit = 0;
   p.ws_ml = align_up(p.ws_unit + static_cast<size_t>(16) * B * p.NC, 256);
   p.ws_o = align_up(p.ws_ml + rows * 8, 256);
-  p.ws_bytes = align_up(p.ws_o + rows * kMlaDv * 4, 256);
+  p.ws_bytes = align_up(p.ws_o + rows * kMlaDv * 2, 256);   // f16 normalised partial outputs
   *out = p;
   return PA_OK;
 }

@@ -132,7 +132,8 @@ cudaError_t launch_mla(bool fp8, int rt, const CUtensorMap& tm, const SplitParam
 int mla_threads(int rt);
 int mla_teams(int rt);
 cudaError_t set_mla_smem_limits(int smem);
-// LSE merge of MLA partials (512 value columns): one warp per (unit, row).
+// LSE merge of MLA partials (512 value columns; the split kernel writes each
+// piece's normalised output in f16 into ws_o): one warp per (unit, row).
 cudaError_t launch_merge_mla(const MergeParams& p, int units, int rows, bool pdl, cudaStream_t stream);
 cudaError_t set_split_smem_limits_bf16(int smem);
 cudaError_t set_split_smem_limits_fp8(int smem);

@@ -11,6 +11,8 @@
 //   out = v_scale * sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
 //   lse = ln 2 * (M + log2 sum_s 2^(m_s - M) l_s)
 // accumulated online (running max), so each partial is loaded once.
+#include <cuda_fp16.h>
+
 #include "pa_device.cuh"
 #include "pa_kernels.h"
 
@@ -224,22 +226,33 @@ __global__ void __launch_bounds__(kWideThreads) pa_merge_wide_kernel(const Merge
   if (pg == 0) write_merged(p, m, dq, acc, l, mx, dq == 0);
 }
 
-// MLA: 512 value columns per row (the latent width); one warp per (unit,
-// row), lane l holding columns 4 l + 128 j (j < 4); two partials' loads are
-// issued before either is combined.
-__device__ __forceinline__ void lse_acc4(float& mx, float& l, float4 (&acc)[4], float2 ml, const float4 (&o)[4]) {
-  if (ml.x == -INFINITY) return;
+// MLA: 512 value columns per row (the latent width); the split kernel leaves
+// each piece's normalised output O_s / l_s in f16 (p.ws_o read as f16) with
+// (m_s, l_s), so a piece weighs 2^(m_s - M) l_s.  One warp per (unit, row),
+// lane l holding columns 4 l + 128 j (j < 4); two partials' loads are issued
+// before either is combined.
+__device__ __forceinline__ float4 f16x4_to_float4(uint2 v) {
+  const __half2 a = *reinterpret_cast<const __half2*>(&v.x);
+  const __half2 b = *reinterpret_cast<const __half2*>(&v.y);
+  const float2 fa = __half22float2(a), fb = __half22float2(b);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+__device__ __forceinline__ void lse_acc4(float& mx, float& l, float4 (&acc)[4], float2 ml, const uint2 (&o)[4]) {
+  if (ml.x == -INFINITY || !(ml.y > 0.f)) return;
   const float nm = fmaxf(mx, ml.x);
   const float a = fast_exp2(mx - nm);
   const float b = fast_exp2(ml.x - nm);
+  const float bw = b * ml.y;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    acc[j].x = acc[j].x * a + o[j].x * b;
-    acc[j].y = acc[j].y * a + o[j].y * b;
-    acc[j].z = acc[j].z * a + o[j].z * b;
-    acc[j].w = acc[j].w * a + o[j].w * b;
+    const float4 v = f16x4_to_float4(o[j]);
+    acc[j].x = acc[j].x * a + v.x * bw;
+    acc[j].y = acc[j].y * a + v.y * bw;
+    acc[j].z = acc[j].z * a + v.z * bw;
+    acc[j].w = acc[j].w * a + v.w * bw;
   }
-  l = l * a + ml.y * b;
+  l = l * a + bw;
   mx = nm;
 }
 
@@ -251,6 +264,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const Me
   const int lane = threadIdx.x & 31;
   const MergeRow m = merge_row<D>(p, blockIdx.x, blockIdx.y * kMergeWarps + warp, lane);
   if (!m.work) return;
+  const uint16_t* ws = reinterpret_cast<const uint16_t*>(p.ws_o);
   float mx = -INFINITY, l = 0.f;
   float4 acc[4];
 #pragma unroll
@@ -259,11 +273,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const Me
   for (; s + 1 < m.nparts; s += 2) {
     const int64_t sa = slot_row(p, m, s), sb = slot_row(p, m, s + 1);
     const float2 ma = p.ws_ml[sa], mb = p.ws_ml[sb];
-    float4 oa[4], ob[4];
+    uint2 oa[4], ob[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      oa[j] = *reinterpret_cast<const float4*>(p.ws_o + sa * D + 4 * lane + 128 * j);
-      ob[j] = *reinterpret_cast<const float4*>(p.ws_o + sb * D + 4 * lane + 128 * j);
+      oa[j] = *reinterpret_cast<const uint2*>(ws + sa * D + 4 * lane + 128 * j);
+      ob[j] = *reinterpret_cast<const uint2*>(ws + sb * D + 4 * lane + 128 * j);
     }
     lse_acc4(mx, l, acc, ma, oa);
     lse_acc4(mx, l, acc, mb, ob);
@@ -271,9 +285,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const Me
   if (s < m.nparts) {
     const int64_t sa = slot_row(p, m, s);
     const float2 ma = p.ws_ml[sa];
-    float4 oa[4];
+    uint2 oa[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) oa[j] = *reinterpret_cast<const float4*>(p.ws_o + sa * D + 4 * lane + 128 * j);
+    for (int j = 0; j < 4; ++j) oa[j] = *reinterpret_cast<const uint2*>(ws + sa * D + 4 * lane + 128 * j);
     lse_acc4(mx, l, acc, ma, oa);
   }
 #pragma unroll

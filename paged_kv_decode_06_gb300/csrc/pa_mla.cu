@@ -612,7 +612,12 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
           const bool ok = half ? ok1 : ok0;
           if (!ok) continue;
           const int rho = half ? rho1 : rho0;
-          float* orow = p.ws_o + (rowbase + rho) * kMlaDv + 128 * cq;
+          // the piece's normalised output O / l in f16 (values are weighted
+          // averages of cached rows: within f16 range, 2^-11 relative error);
+          // the merge weighs it back with l
+          const float lt = half ? lt1 : lt0;
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.ws_o) + (rowbase + rho) * kMlaDv + 128 * cq;
 #pragma unroll
           for (int J = 0; J < 16; J += 2) {
 #pragma unroll
@@ -620,7 +625,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
               float va, vb;
               int d;
               ws.pair_at(J, jj, half, tig, va, vb, d);
-              *reinterpret_cast<float2*>(orow + d) = make_float2(va, vb);
+              *reinterpret_cast<uint32_t*>(orow + d) = pack_f16(va * inv, vb * inv);
             }
           }
           if (cq == 0 && tig == 0) p.ws_ml[rowbase + rho] = make_float2(half ? ws.m1 : ws.m0, half ? lt1 : lt0);
