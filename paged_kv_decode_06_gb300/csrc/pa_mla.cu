@@ -9,19 +9,21 @@
 //
 // Work decomposition: that of the grouped-query split kernel (units
 // (sequence, chunk of query heads) laid end to end in page order, every
-// worker a contiguous page range, cut units leaving fp32 partials for the LSE
-// merge), with "worker" = team: a CTA holds one or two independent teams, each
-// one producer warp and 4 * RT consumer warps (RT = 16-row tiles of a chunk,
-// at most 2), with its own ring, query slots and barriers.
+// worker a contiguous page range, cut units leaving partials for the LSE
+// merge: the normalised output in f16 with the fp32 running max and sum), with
+// "worker" = team: a CTA holds one or two independent teams, each one producer
+// warp and 4 * RT consumer warps (RT = 16-row tiles of a chunk, at most 2),
+// with its own ring, query slot and barriers.
 //
 // The value part of a row is 512 wide, too wide for one warp's accumulator
 // (16 rows x 512 fp32 = 256 registers a lane), so the four consumer warps of a
 // row tile split the columns: warp quarter cq owns value columns
-// [128 cq, 128 cq + 128) and Q K^T features [144 cq, 144 cq + 144).  Per page
-// each warp computes its partial 16 x 16 score tile with mma.sync, the four
-// partials meet in shared memory (one named barrier per page), every warp sums
-// them in the same order (so all four hold identical scores, maxima and sums),
-// runs the online softmax and accumulates P V for its own columns.
+// [128 cq, 128 cq + 128) and Q K^T features [144 cq, 144 cq + 144).  Per step
+// (one page, or two consecutive pages of a segment) each warp computes its
+// partial 16-row score tile with mma.sync, the four partials meet in shared
+// memory behind an mbarrier (four arrivals, bounded wait), every warp sums them
+// in the same order (so all four hold identical scores, maxima and sums), runs
+// the online softmax and accumulates P V for its own columns.
 //
 // Ring stage = one page: the whole [16, 576] row block in one TMA box
 // (64 features x 16 slots x 9 column blocks), which lands as 9 blocks of 16
