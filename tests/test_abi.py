@@ -319,3 +319,4 @@ def test_mla_plan_rejects_bad_shapes_without_device(lib):
     with pytest.raises(binding.PagedAttnError) as e:
         binding.paged_attn_mla_reserve(4, 16, binding.PA_BF16, 0)
     assert e.value.status == binding.PA_ERR_INVALID_ARG
+

@@ -181,3 +181,40 @@ def test_mla_full_size_configs_sampled(name):
     seqs.update({int(np.argmax(w.seq_lens)), int(np.argmin(w.seq_lens))})
     _, _, eo, el = check(w, seqs=sorted(seqs))
     print(f"{name}: sampled seqs {sorted(seqs)}: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
+
+
+def test_mla_padded_query_output_and_lse_strides():
+    w = wl.make_mla_workload(_spec(qlens=(1, 3), seq_lens=(40, 7, 130)), device="cuda")
+    ref = oracle.run_mla_workload(w)
+    T, Hq = w.q.shape[:2]
+    qbig = torch.zeros((T, Hq + 2, 576), dtype=torch.bfloat16, device="cuda")   # token stride (Hq + 2) * 576
+    qbig[:, :Hq] = w.q
+    w.q = qbig[:, :Hq]
+    obig = torch.full((T, Hq + 1, 520), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = obig[:, :Hq, :512]
+    lbig = torch.full((Hq, T + 3), float("nan"), dtype=torch.float32, device="cuda")
+    lse = lbig[:, :T].t()
+    binding.mla_decode_workload(w, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    assert np.abs(out.float().cpu().numpy() - ref[0]).max() <= TOL_OUT["bf16"]
+    assert np.abs(lse.cpu().numpy() - ref[1]).max() <= TOL_LSE
+    assert torch.isnan(obig[:, Hq:]).all() and torch.isnan(obig[:, :, 512:]).all()   # nothing written outside
+
+
+def test_mla_context_shorter_than_its_query_run_is_reported():
+    w = wl.make_mla_workload(_spec(qlens=(3,), seq_lens=(40, 20)), device="cuda")
+    w.seq_lens = w.seq_lens.copy()
+    w.seq_lens[1] = 2          # fewer cached tokens than the run's 3 query tokens
+    binding.mla_decode_workload(w)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) & binding.STATUS_SEQ_LEN
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_mla_single_token_contexts_and_long_runs(kv):
+    # L = q (every row sees a prefix of its own run), and runs of 16 tokens
+    w = wl.make_mla_workload(_spec(kv=kv, Hq=2, qlens=(16,), seq_lens=(16, 17, 31, 33)), device="cuda")
+    check(w)
+    w = wl.make_mla_workload(_spec(kv=kv, Hq=16, seq_lens=(1, 1, 2, 1)), device="cuda")
+    check(w)
