@@ -220,6 +220,23 @@ def _cpu_model() -> str:
     return platform.machine()
 
 
+def _packed_views(parts, device):
+    """One buffer holding several tensors back to back (each 16-byte aligned):
+    returns (buffer, [views]).  parts = [(shape, dtype)]."""
+    import torch
+    offs, off = [], 0
+    for shape, dtype in parts:
+        n = int(math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        offs.append((off, n))
+        off += (n + 15) // 16 * 16
+    if device == "pinned":
+        buf = torch.empty(max(off, 16), dtype=torch.uint8).pin_memory()
+    else:
+        buf = torch.empty(max(off, 16), dtype=torch.uint8, device=device)
+    views = [buf[o:o + n].view(dtype).view(shape) for (o, n), (shape, dtype) in zip(offs, parts)]
+    return buf, views
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -379,26 +396,36 @@ def run_ours(args, world, rank, local):
     direct_ms = d0.elapsed_time(d1) / args.steps
     ms = max_over_ranks(ms, world, device=dev)
 
-    # end-to-end through the public API: pinned host inputs in, results out, every step
-    h_q = [w.q.cpu().pin_memory() for w in works]
-    h_bt = torch.from_numpy(base.block_tables).pin_memory()
-    h_sl = torch.from_numpy(base.seq_lens).pin_memory()
-    h_qsl = torch.from_numpy(base.query_start_loc).pin_memory() if qsl is not None else None
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q = torch.empty_like(base.q)
+    # end-to-end through the public API: every step copies its inputs (q, block
+    # table, lengths, query starts) from pinned host memory and reads out / lse
+    # back; each direction is one copy of one packed buffer whose views are the
+    # tensors the call takes
+    in_parts = [(tuple(base.q.shape), base.q.dtype), (tuple(base.block_tables.shape), torch.int32),
+                (tuple(base.seq_lens.shape), torch.int32)]
+    if qsl is not None:
+        in_parts.append((tuple(base.query_start_loc.shape), torch.int32))
+    out_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
+    d_in, d_views = _packed_views(in_parts, dev)
+    d_outbuf, (e_out, e_lse) = _packed_views(out_parts, dev)
+    h_outbuf, _ = _packed_views(out_parts, "pinned")
+    h_ins = []
+    for w in works:
+        h_in, hv = _packed_views(in_parts, "pinned")
+        hv[0].copy_(w.q.cpu())
+        hv[1].copy_(torch.from_numpy(base.block_tables))
+        hv[2].copy_(torch.from_numpy(base.seq_lens))
+        if qsl is not None:
+            hv[3].copy_(torch.from_numpy(base.query_start_loc))
+        h_ins.append(h_in)
+    e_q, e_bt, e_sl = d_views[0], d_views[1], d_views[2]
+    e_qsl = d_views[3] if qsl is not None else None
 
     def e2e_step(k):
         w = works[k % pools]
-        d_q.copy_(h_q[k % pools], non_blocking=True)
-        bt.copy_(h_bt, non_blocking=True)
-        sl.copy_(h_sl, non_blocking=True)
-        if qsl is not None:
-            qsl.copy_(h_qsl, non_blocking=True)
-        binding.paged_attn_decode(d_q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
-                                  spec.v_scale, out=out, lse=lse, options=pool_opts[k % pools])
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        d_in.copy_(h_ins[k % pools], non_blocking=True)
+        binding.paged_attn_decode(e_q, w.k_cache, w.v_cache, e_bt, e_sl, e_qsl, mq, spec.scale, spec.k_scale,
+                                  spec.v_scale, out=e_out, lse=e_lse, options=pool_opts[k % pools])
+        h_outbuf.copy_(d_outbuf, non_blocking=True)
 
     for k in range(args.warmup):
         e2e_step(k)
@@ -411,8 +438,8 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    h2d = d_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4 + (h_qsl.numel() * 4 if h_qsl is not None else 0)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    h2d = d_in.numel()
+    d2h = d_outbuf.numel()
     status = binding.paged_attn_device_status(clear=True)
 
     if rank != 0:
@@ -445,7 +472,9 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
                      "per_launch_bytes": step_bytes},
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "per step: one copy of the packed inputs from pinned host memory, the API call from "
+                        "Python, one copy of the packed out / lse back"},
         "direct_call": {"value": step_bytes * world / (direct_ms * 1e-3) / 1e9, "unit": "GB/s",
                         "ms_per_step": direct_ms,
                         "note": "paged_attn_decode called from Python each step (no CUDA graph)"},
@@ -560,24 +589,34 @@ def run_mla(args, world, rank, local):
     torch.cuda.synchronize()
     direct_ms = d0.elapsed_time(d1) / args.steps
     ms = max_over_ranks(ms, world, device=dev)
-    # end to end through the public API: pinned host inputs in, results out, every step
-    h_q = [w.q.cpu().pin_memory() for w in works]
-    h_bt = torch.from_numpy(base.block_tables).pin_memory()
-    h_sl = torch.from_numpy(base.seq_lens).pin_memory()
-    h_qsl = torch.from_numpy(base.query_start_loc).pin_memory() if qsl is not None else None
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q = torch.empty_like(base.q)
+    # end to end through the public API: per step one packed copy of the inputs
+    # from pinned host memory and one of out / lse back (as in run_ours)
+    in_parts = [(tuple(base.q.shape), base.q.dtype), (tuple(base.block_tables.shape), torch.int32),
+                (tuple(base.seq_lens.shape), torch.int32)]
+    if qsl is not None:
+        in_parts.append((tuple(base.query_start_loc.shape), torch.int32))
+    out_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
+    d_in, d_views = _packed_views(in_parts, dev)
+    d_outbuf, (e_out, e_lse) = _packed_views(out_parts, dev)
+    h_outbuf, _ = _packed_views(out_parts, "pinned")
+    h_ins = []
+    for w in works:
+        h_in, hv = _packed_views(in_parts, "pinned")
+        hv[0].copy_(w.q.cpu())
+        hv[1].copy_(torch.from_numpy(base.block_tables))
+        hv[2].copy_(torch.from_numpy(base.seq_lens))
+        if qsl is not None:
+            hv[3].copy_(torch.from_numpy(base.query_start_loc))
+        h_ins.append(h_in)
+    e_q, e_bt, e_sl = d_views[0], d_views[1], d_views[2]
+    e_qsl = d_views[3] if qsl is not None else None
 
     def e2e_step(k):
-        d_q.copy_(h_q[k % pools], non_blocking=True)
-        bt.copy_(h_bt, non_blocking=True)
-        sl.copy_(h_sl, non_blocking=True)
-        if qsl is not None:
-            qsl.copy_(h_qsl, non_blocking=True)
-        step(k, q=d_q)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        w = works[k % pools]
+        d_in.copy_(h_ins[k % pools], non_blocking=True)
+        binding.paged_attn_mla_decode(e_q, w.kv_cache, e_bt, e_sl, e_qsl, mq, spec.scale, spec.kv_scale, out=e_out,
+                                      lse=e_lse)
+        h_outbuf.copy_(d_outbuf, non_blocking=True)
 
     for k in range(args.warmup):
         e2e_step(k)
@@ -590,8 +629,8 @@ def run_mla(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    h2d = d_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4 + (h_qsl.numel() * 4 if h_qsl is not None else 0)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    h2d = d_in.numel()
+    d2h = d_outbuf.numel()
     status = binding.paged_attn_device_status(clear=True)
     if rank != 0:
         if world > 1:
@@ -623,7 +662,9 @@ def run_mla(args, world, rank, local):
                      "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
                      "per_launch_bytes": step_bytes, "tensor_tflops": flops / (split_mean * 1e-3) / 1e12},
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "per step: one copy of the packed inputs from pinned host memory, the API call from "
+                        "Python, one copy of the packed out / lse back"},
         "direct_call": {"value": step_bytes * world / (direct_ms * 1e-3) / 1e9, "unit": "GB/s",
                         "ms_per_step": direct_ms,
                         "note": "paged_attn_mla_decode called from Python each step (no CUDA graph)"},

@@ -116,7 +116,29 @@ def _dtype_code(t: torch.Tensor) -> int:
     return 0          # not a pa_dtype: the library rejects it with PA_ERR_INVALID_ARG
 
 
+_DESC_CACHE = {}
+_DESC_CACHE_MAX = 1024
+
+
 def tensor_desc(t: Optional[torch.Tensor]) -> PaTensor:
+    """The pa_tensor_t of a tensor.  Descriptors hold only (pointer, dtype,
+    shape, strides), so one built for a key serves every later tensor with the
+    same key: they are cached (a per-call decode then costs a few dictionary
+    lookups instead of ctypes field assignments).  Treat the result as
+    read-only."""
+    if t is None:
+        return _new_desc(None)
+    key = (t.data_ptr(), t.dtype, t.shape, t.stride())
+    d = _DESC_CACHE.get(key)
+    if d is None:
+        d = _new_desc(t)
+        if len(_DESC_CACHE) >= _DESC_CACHE_MAX:
+            _DESC_CACHE.clear()
+        _DESC_CACHE[key] = d
+    return d
+
+
+def _new_desc(t: Optional[torch.Tensor]) -> PaTensor:
     d = PaTensor()
     if t is None:
         d.data = None
