@@ -54,6 +54,34 @@
 
 namespace pa {
 
+// max of three floats in one instruction (the three-input max of sm_100+)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of v[0..N) by a tree of three-input maxima (about N/2 instructions
+// instead of N - 1); v is overwritten.
+template <int N>
+struct Max3Tree {
+  static __device__ __forceinline__ float run(float* v) {
+    constexpr int M = (N + 2) / 3;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const int a = 3 * i;
+      if (a + 2 < N) v[i] = fmax3(v[a], v[a + 1], v[a + 2]);
+      else if (a + 1 < N) v[i] = fmaxf(v[a], v[a + 1]);
+      else v[i] = v[a];
+    }
+    return Max3Tree<M>::run(v);
+  }
+};
+template <>
+struct Max3Tree<1> {
+  static __device__ __forceinline__ float run(float* v) { return v[0]; }
+};
+
 constexpr int kTcProducers = 2;
 constexpr int kTcPvWarp = 2;
 constexpr int kTcMmaWarp = 3;
@@ -507,20 +535,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (WINDOW && window > 0) interior = interior && tb > si.L - 1 - window;
         float mb;
         if (interior) {
-          float mx[16];
+          float mx[16 * NP4];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            mx[e] = sv[0][e];
+          for (int k = 0; k < NP4; ++k)
 #pragma unroll
-            for (int k = 1; k < NP4; ++k) mx[e] = fmaxf(mx[e], sv[k][e]);
-          }
-#pragma unroll
-          for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-            for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
-          mb = mx[0] * c;
+            for (int e = 0; e < 16; ++e) mx[16 * k + e] = sv[k][e];
+          mb = Max3Tree<16 * NP4>::run(mx) * c;
         } else {
-          mb = -INFINITY;
+          float mx[16 * NP4];
 #pragma unroll
           for (int k = 0; k < NP4; ++k)
 #pragma unroll
@@ -530,8 +552,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (WINDOW && window > 0) vis = vis && tok > lim - window;
               const float x = vis ? sv[k][e] * c : -INFINITY;
               sv[k][e] = x;
-              mb = fmaxf(mb, x);
+              mx[16 * k + e] = x;
             }
+          mb = Max3Tree<16 * NP4>::run(mx);
         }
         const float m_new = fmaxf(m, mb);
         const bool grow = m_new > m + 8.f;   // also true when m = -inf and m_new is finite
