@@ -61,6 +61,27 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Packed fp32 pairs (the f32x2 arithmetic of sm_100+): one instruction
+// operates on both halves of a 64-bit register pair.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Maximum of v[0..N) by a tree of three-input maxima (about N/2 instructions
 // instead of N - 1); v is overwritten.
 template <int N>
@@ -599,22 +620,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float mult = interior ? c : 1.f;   // masked scores are already scaled
           const uint32_t tP = tSP + kTmemPhi;
           const uint32_t tPlo = tSP + kTmemPlo;
-          float lsum = 0.f;
+          // pairs of scores through packed fp32 arithmetic: exponent argument
+          // (one FMA for two), residue a - bf16(a) (one FMA for two), running sum
+          const uint64_t mult2 = f2_pack(mult, mult), mneg2 = f2_pack(mneg, mneg);
+          const uint64_t minus1 = f2_pack(-1.f, -1.f);
+          uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < NP4; ++k) {
             uint32_t w[8], wl[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const float a0 = fast_exp2(fmaf(sv[k][2 * e], mult, mneg));
-              const float a1 = fast_exp2(fmaf(sv[k][2 * e + 1], mult, mneg));
+              float x0, x1;
+              f2_unpack(ffma2(f2_pack(sv[k][2 * e], sv[k][2 * e + 1]), mult2, mneg2), x0, x1);
+              const float a0 = fast_exp2(x0);
+              const float a1 = fast_exp2(x1);
               w[e] = pack_bf16(a0, a1);
-              wl[e] = pack_bf16(a0 - bf16_lo(w[e]), a1 - bf16_hi(w[e]));   // exact residues, rounded once
-              lsum += a0 + a1;
+              const uint64_t a2 = f2_pack(a0, a1);
+              float r0, r1;   // exact residues a - bf16(a), rounded once below
+              f2_unpack(ffma2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), minus1, a2), r0, r1);
+              wl[e] = pack_bf16(r0, r1);
+              lsum2 = fadd2(lsum2, a2);
             }
             tmem_st8(tP + 8u * k, w);
             tmem_st8(tPlo + 8u * k, wl);
           }
-          l += lsum;
+          {
+            float s0, s1;
+            f2_unpack(lsum2, s0, s1);
+            l += s0 + s1;
+          }
           tmem_wait_st();
         }
         tc_fence_before();
