@@ -32,6 +32,7 @@
 // from HBM once.  fp8 codes are converted to f16 in registers (exact), with the
 // query in f16; kv_scale is folded into the logit scale and the output.
 // Every wait is bounded (kErrTimeout).
+#include "pa_pack.cuh"
 #include "pa_split.cuh"
 
 namespace pa {
@@ -71,6 +72,10 @@ __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r
 
 __device__ __forceinline__ void sts_f4(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+__device__ __forceinline__ void lds_u64x2(uint32_t addr, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr) : "memory");
 }
 
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
@@ -197,24 +202,36 @@ __device__ __forceinline__ bool mla_pages(MlaWarp<FP8>& ws, const uint32_t (&st)
   __syncwarp();
   if (lane == 0) mbar_arrive(xbar);
   if (!mbar_wait(xbar, xpar)) return false;
-  float x[2 * NP][4];
+  // sums of the four partials as packed pairs (row g's two columns, row g+8's)
+  uint64_t X[2 * NP][2];
 #pragma unroll
-  for (int n = 0; n < 2 * NP; ++n) {
-    const float4 a = lds_f4(xbuf + 512u * n + 16u * lane);
-    x[n][0] = a.x; x[n][1] = a.y; x[n][2] = a.z; x[n][3] = a.w;
-  }
+  for (int n = 0; n < 2 * NP; ++n) lds_u64x2(xbuf + 512u * n + 16u * lane, X[n][0], X[n][1]);
 #pragma unroll
   for (int q = 1; q < 4; ++q) {   // same order in every quarter: identical sums
 #pragma unroll
     for (int n = 0; n < 2 * NP; ++n) {
-      const float4 a = lds_f4(xbuf + q * (1024u * NP) + 512u * n + 16u * lane);
-      x[n][0] += a.x; x[n][1] += a.y; x[n][2] += a.z; x[n][3] += a.w;
+      uint64_t a, b;
+      lds_u64x2(xbuf + q * (1024u * NP) + 512u * n + 16u * lane, a, b);
+      X[n][0] = fadd2(X[n][0], a);
+      X[n][1] = fadd2(X[n][1], b);
     }
   }
+  float x[2 * NP][4];
 #pragma unroll
-  for (int n = 0; n < 2 * NP; ++n)
+  for (int n = 0; n < 2 * NP; ++n) {
+    f2_unpack(X[n][0], x[n][0], x[n][1]);
+    f2_unpack(X[n][1], x[n][2], x[n][3]);
+  }
+  // With a positive scale the maximum is taken over the raw scores and the
+  // scale is folded into the exponent's FMA; otherwise the scores are scaled first.
+  const bool fold = scale_log2 > 0.f;
+  if (!fold) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[n][e] *= scale_log2;
+    for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] *= scale_log2;
+  }
+  const float cs = fold ? scale_log2 : 1.f;
   // ---- causal run / context tail mask ----
   if (tb + kPage * NP - 1 > min_lim) {
 #pragma unroll
@@ -231,13 +248,15 @@ __device__ __forceinline__ bool mla_pages(MlaWarp<FP8>& ws, const uint32_t (&st)
   float mx1 = fmaxf(x[0][2], x[0][3]);
 #pragma unroll
   for (int n = 1; n < 2 * NP; ++n) {
-    mx0 = fmaxf(mx0, fmaxf(x[n][0], x[n][1]));
-    mx1 = fmaxf(mx1, fmaxf(x[n][2], x[n][3]));
+    mx0 = fmax3(mx0, x[n][0], x[n][1]);
+    mx1 = fmax3(mx1, x[n][2], x[n][3]);
   }
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  mx0 *= cs;
+  mx1 *= cs;
   const float mn0 = fmaxf(ws.m0, mx0);
   const float mn1 = fmaxf(ws.m1, mx1);
   const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
@@ -246,18 +265,23 @@ __device__ __forceinline__ bool mla_pages(MlaWarp<FP8>& ws, const uint32_t (&st)
   const float a1 = fast_exp2(ws.m1 - base1);
   ws.m0 = mn0;
   ws.m1 = mn1;
-  float s0 = 0.f, s1 = 0.f;
+  const uint64_t cs2 = f2_pack(cs, cs);
+  const uint64_t nb0 = f2_pack(-base0, -base0), nb1 = f2_pack(-base1, -base1);
+  uint64_t s0 = f2_pack(0.f, 0.f), s1 = s0;
 #pragma unroll
   for (int n = 0; n < 2 * NP; ++n) {
-    x[n][0] = fast_exp2(x[n][0] - base0);
-    x[n][1] = fast_exp2(x[n][1] - base0);
-    x[n][2] = fast_exp2(x[n][2] - base1);
-    x[n][3] = fast_exp2(x[n][3] - base1);
-    s0 += x[n][0] + x[n][1];
-    s1 += x[n][2] + x[n][3];
+    f2_unpack(ffma2(f2_pack(x[n][0], x[n][1]), cs2, nb0), x[n][0], x[n][1]);
+    f2_unpack(ffma2(f2_pack(x[n][2], x[n][3]), cs2, nb1), x[n][2], x[n][3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[n][e] = fast_exp2(x[n][e]);
+    s0 = fadd2(s0, f2_pack(x[n][0], x[n][1]));
+    s1 = fadd2(s1, f2_pack(x[n][2], x[n][3]));
   }
-  ws.l0 = ws.l0 * a0 + s0;
-  ws.l1 = ws.l1 * a1 + s1;
+  float s0a, s0b, s1a, s1b;
+  f2_unpack(s0, s0a, s0b);
+  f2_unpack(s1, s1a, s1b);
+  ws.l0 = ws.l0 * a0 + (s0a + s0b);
+  ws.l1 = ws.l1 * a1 + (s1a + s1b);
   if (__any_sync(0xffffffffu, (a0 != 1.f) || (a1 != 1.f))) {
 #pragma unroll
     for (int J = 0; J < 16; ++J) {
