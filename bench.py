@@ -804,8 +804,8 @@ def _spec_for(args):
 def kernel_source_sha256(kernel):
     """Hash of the sources a split kernel is compiled from (stamps ncu figures)."""
     import hashlib
-    names = ["pa_split.cuh", "pa_device.cuh"] + (["pa_split_tc.cuh", "pa_pack.cuh"] if kernel == "pa_split_tc_kernel"
-                                                 else []) + (["pa_mla.cu", "pa_pack.cuh"] if kernel == "pa_mla_kernel" else [])
+    names = ["pa_split.cuh", "pa_device.cuh", "pa_pack.cuh"] + \
+        (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else []) + (["pa_mla.cu"] if kernel == "pa_mla_kernel" else [])
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:

@@ -36,6 +36,7 @@
 
 #include "pa_device.cuh"
 #include "pa_kernels.h"
+#include "pa_pack.cuh"
 
 namespace pa {
 
@@ -394,6 +395,13 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
     }
   }
   float x[2 * NP][4];
+  // fp8 caches (whose consumers are issue-bound): with a positive scale and no
+  // per-key scales the maximum is taken over the raw scores and the scale is
+  // folded into the exponent's FMA, and the softmax arithmetic runs on packed
+  // f32x2 pairs.  bf16 caches keep scalar arithmetic (there the packed form
+  // costs registers and measured slower).
+  constexpr bool kPacked = FP8;
+  const bool fold = kPacked && !TOKS && scale_log2 > 0.f;
   if constexpr (TOKS) {
     // key token 8n + 2*tig + e of the block: the logit takes that key's scale
 #pragma unroll
@@ -401,19 +409,24 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
 #pragma unroll
       for (int h8 = 0; h8 < 2; ++h8) {
         const float2 ks = lds_f2(ts[pg] + 32u * h8 + 8u * tig);
-        const float c0 = scale_log2 * ks.x, c1 = scale_log2 * ks.y;
-        x[2 * pg + h8][0] = S[2 * pg + h8][0] * c0;
-        x[2 * pg + h8][1] = S[2 * pg + h8][1] * c1;
-        x[2 * pg + h8][2] = S[2 * pg + h8][2] * c0;
-        x[2 * pg + h8][3] = S[2 * pg + h8][3] * c1;
+        const uint64_t c2 = f2_pack(scale_log2 * ks.x, scale_log2 * ks.y);
+        const int n = 2 * pg + h8;
+        f2_unpack(fmul2(f2_pack(S[n][0], S[n][1]), c2), x[n][0], x[n][1]);
+        f2_unpack(fmul2(f2_pack(S[n][2], S[n][3]), c2), x[n][2], x[n][3]);
       }
     }
+  } else if (fold) {
+#pragma unroll
+    for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] = S[n][e];
   } else {
 #pragma unroll
     for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[n][e] = S[n][e] * scale_log2;
   }
+  const float csc = fold ? scale_log2 : 1.f;   // scale still to apply in the exponent
   // keys allowed for a row: lim - W < token <= lim (causal run end; sliding
   // window start when W > 0, whose largest start is L - W for the last row)
   if (tb + kPage * NP - 1 > min_lim || (window > 0 && tb < L - window)) {
@@ -432,13 +445,20 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
   float mx1 = fmaxf(x[0][2], x[0][3]);
 #pragma unroll
   for (int n = 1; n < 2 * NP; ++n) {
-    mx0 = fmaxf(mx0, fmaxf(x[n][0], x[n][1]));
-    mx1 = fmaxf(mx1, fmaxf(x[n][2], x[n][3]));
+    if constexpr (kPacked) {
+      mx0 = fmax3(mx0, x[n][0], x[n][1]);
+      mx1 = fmax3(mx1, x[n][2], x[n][3]);
+    } else {
+      mx0 = fmaxf(mx0, fmaxf(x[n][0], x[n][1]));
+      mx1 = fmaxf(mx1, fmaxf(x[n][2], x[n][3]));
+    }
   }
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  mx0 *= csc;
+  mx1 *= csc;
   const float mn0 = fmaxf(cs.m0, mx0);
   const float mn1 = fmaxf(cs.m1, mx1);
   const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
@@ -447,26 +467,58 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
   const float a1 = fast_exp2(cs.m1 - base1);
   cs.m0 = mn0;
   cs.m1 = mn1;
-  float s0 = 0.f, s1 = 0.f;
+  if constexpr (!kPacked) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < 2 * NP; ++n) {
+      x[n][0] = fast_exp2(x[n][0] - base0);
+      x[n][1] = fast_exp2(x[n][1] - base0);
+      x[n][2] = fast_exp2(x[n][2] - base1);
+      x[n][3] = fast_exp2(x[n][3] - base1);
+      s0 += x[n][0] + x[n][1];
+      s1 += x[n][2] + x[n][3];
+    }
+    cs.l0 = cs.l0 * a0 + s0;
+    cs.l1 = cs.l1 * a1 + s1;
+    if (__any_sync(0xffffffffu, (a0 != 1.f) || (a1 != 1.f))) {
+#pragma unroll
+      for (int J = 0; J < GG::NT; ++J) {
+        cs.O[J][0] *= a0;
+        cs.O[J][1] *= a0;
+        cs.O[J][2] *= a1;
+        cs.O[J][3] *= a1;
+      }
+    }
+  } else {
+  // exponent arguments, exponentials' row sums and the O rescale as packed
+  // pairs (the mma accumulator quads hold row g's two columns, then row g+8's)
+  const uint64_t csc2 = f2_pack(csc, csc);
+  const uint64_t nb0 = f2_pack(-base0, -base0), nb1 = f2_pack(-base1, -base1);
+  uint64_t s0p = f2_pack(0.f, 0.f), s1p = s0p;
 #pragma unroll
   for (int n = 0; n < 2 * NP; ++n) {
-    x[n][0] = fast_exp2(x[n][0] - base0);
-    x[n][1] = fast_exp2(x[n][1] - base0);
-    x[n][2] = fast_exp2(x[n][2] - base1);
-    x[n][3] = fast_exp2(x[n][3] - base1);
-    s0 += x[n][0] + x[n][1];
-    s1 += x[n][2] + x[n][3];
+    f2_unpack(ffma2(f2_pack(x[n][0], x[n][1]), csc2, nb0), x[n][0], x[n][1]);
+    f2_unpack(ffma2(f2_pack(x[n][2], x[n][3]), csc2, nb1), x[n][2], x[n][3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[n][e] = fast_exp2(x[n][e]);
+    s0p = fadd2(s0p, f2_pack(x[n][0], x[n][1]));
+    s1p = fadd2(s1p, f2_pack(x[n][2], x[n][3]));
   }
-  cs.l0 = cs.l0 * a0 + s0;
-  cs.l1 = cs.l1 * a1 + s1;
+  {
+    float u0, u1, v0, v1;
+    f2_unpack(s0p, u0, u1);
+    f2_unpack(s1p, v0, v1);
+    cs.l0 = cs.l0 * a0 + (u0 + u1);
+    cs.l1 = cs.l1 * a1 + (v0 + v1);
+  }
   if (__any_sync(0xffffffffu, (a0 != 1.f) || (a1 != 1.f))) {
+    const uint64_t a00 = f2_pack(a0, a0), a11 = f2_pack(a1, a1);
 #pragma unroll
     for (int J = 0; J < GG::NT; ++J) {
-      cs.O[J][0] *= a0;
-      cs.O[J][1] *= a0;
-      cs.O[J][2] *= a1;
-      cs.O[J][3] *= a1;
+      f2_unpack(fmul2(f2_pack(cs.O[J][0], cs.O[J][1]), a00), cs.O[J][0], cs.O[J][1]);
+      f2_unpack(fmul2(f2_pack(cs.O[J][2], cs.O[J][3]), a11), cs.O[J][2], cs.O[J][3]);
     }
+  }
   }
   if constexpr (TOKS) {
     // P V with per-token value scales: each weight takes its value row's scale
@@ -485,10 +537,10 @@ __device__ __forceinline__ void consume_pages(ConsumerState<D, FP8>& cs, const u
           c0 = t0 < vt ? c0 : 0.f;
           c1 = t0 + 1 < vt ? c1 : 0.f;
         }
-        x[2 * pg + h8][0] *= c0;
-        x[2 * pg + h8][1] *= c1;
-        x[2 * pg + h8][2] *= c0;
-        x[2 * pg + h8][3] *= c1;
+        const uint64_t c2 = f2_pack(c0, c1);
+        const int n = 2 * pg + h8;
+        f2_unpack(fmul2(f2_pack(x[n][0], x[n][1]), c2), x[n][0], x[n][1]);
+        f2_unpack(fmul2(f2_pack(x[n][2], x[n][3]), c2), x[n][2], x[n][3]);
       }
     }
   }
