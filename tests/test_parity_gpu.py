@@ -289,3 +289,13 @@ def test_split_timing_events_direct_and_captured():
     assert a.elapsed_time(b) > 0.0
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("kv,qlens", [("bf16", (1,)), ("fp8", (1, 2, 3, 4)), ("bf16", (2, 3, 4))])
+def test_batch_of_512_sequences(kv, qlens):
+    # the engine's max_num_seqs: the device-side page prefix spans two scan passes
+    rng = np.random.default_rng(513)
+    lens = tuple(int(x) for x in rng.integers(4, 400, size=512))
+    w = wl.make_workload(_spec(kv=kv, G=4, Hkv=8, qlens=qlens, seq_lens=lens, seed=513), device="cuda")
+    seqs = sorted(set(rng.choice(512, size=16, replace=False).tolist()) | {0, 255, 256, 511})
+    check(w, seqs=seqs)

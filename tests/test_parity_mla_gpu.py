@@ -75,7 +75,7 @@ def test_mla_heads_and_verification_runs(kv, Hq, qlens):
     check(w)
 
 
-@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 152])
+@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 152, 300])
 @pytest.mark.parametrize("kv,Hq,qlens", [("bf16", 16, (1,)), ("fp8", 16, (4,))])
 def test_mla_forced_split_counts_exercise_the_merge(num_ctas, kv, Hq, qlens):
     w = wl.make_mla_workload(_spec(kv=kv, Hq=Hq, qlens=qlens, seq_lens=(3, 50, 300, 17, 1000), seed=num_ctas),
@@ -218,3 +218,13 @@ def test_mla_single_token_contexts_and_long_runs(kv):
     check(w)
     w = wl.make_mla_workload(_spec(kv=kv, Hq=16, seq_lens=(1, 1, 2, 1)), device="cuda")
     check(w)
+
+
+@pytest.mark.parametrize("kv,qlens", [("bf16", (1,)), ("fp8", (1, 2, 3, 4))])
+def test_mla_batch_of_512_sequences(kv, qlens):
+    # the engine's max_num_seqs: lengths 1..300, sampled rows checked against the oracle
+    rng = np.random.default_rng(512)
+    lens = tuple(int(x) for x in rng.integers(4, 301, size=512))
+    w = wl.make_mla_workload(_spec(kv=kv, Hq=16, qlens=qlens, seq_lens=lens, seed=512), device="cuda")
+    seqs = sorted(set(rng.choice(512, size=12, replace=False).tolist()) | {0, 511})
+    check(w, seqs=seqs)
