@@ -120,7 +120,7 @@ typedef struct pa_plan_t {
   int32_t merge_rows;        /* rows per merge unit (heads_per_cta * G * max_query_len) */
   int32_t page_pairing;      /* 1 if consumer warps take two pages of a sequence at once */
   int64_t workspace_bytes;   /* split workspace the call needs                          */
-  int32_t variant;           /* 0: mma.sync warps; 1: tcgen05 / tensor-memory kernel    */
+  int32_t variant;           /* 0: mma.sync warps; 1: tcgen05 / tensor-memory kernel; 2: MLA */
   int32_t block_pages;       /* pages a consumer step takes (1, 2 paired, 4 tcgen05)    */
 } pa_plan_t;
 
@@ -285,6 +285,9 @@ int paged_attn_cache_write_per_token(const pa_tensor_t* key, const pa_tensor_t* 
  *
  * Errors, device status bits, workspace and graph-capture rules as for
  * paged_attn_decode (paged_attn_mla_workspace_size gives the workspace a shape needs).
+ * The pieces of a sequence cut across CTAs meet in f16 (their normalised outputs):
+ * cached values must lie within the f16 range (|v| <= 65504; any fp8 cache does);
+ * an overflow sets status bit 4 and the affected rows are undefined.
  */
 int paged_attn_mla_decode(const pa_tensor_t* q, const pa_tensor_t* kv_cache, const pa_tensor_t* block_tables,
                           const pa_tensor_t* seq_lens, const pa_tensor_t* query_start_loc,
@@ -334,7 +337,7 @@ int paged_attn_release(void);
 /* Read the device status word of the current device into *flags (bit 0: page id out of
  * range; bit 1: seq_len < query length; bit 2: query length outside [1, max_query_len]
  * or query_start_loc inconsistent; bit 3: a pipeline wait timed out; bit 4: a query value
- * overflowed the f16 range on the fp8 path).  clear != 0 resets it to 0.  Synchronises
+ * overflowed the f16 range on the fp8 path, or an MLA partial output did).  clear != 0 resets it to 0.  Synchronises
  * the device: a debugging aid, not for the hot path. */
 int paged_attn_device_status(uint32_t* flags, int32_t clear);
 

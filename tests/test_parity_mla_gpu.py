@@ -228,3 +228,14 @@ def test_mla_batch_of_512_sequences(kv, qlens):
     w = wl.make_mla_workload(_spec(kv=kv, Hq=16, qlens=qlens, seq_lens=lens, seed=512), device="cuda")
     seqs = sorted(set(rng.choice(512, size=12, replace=False).tolist()) | {0, 511})
     check(w, seqs=seqs)
+
+
+def test_mla_partial_outputs_beyond_f16_range_are_reported():
+    # a bf16 latent value of 1e6 in a sequence cut across CTAs: the pieces meet in
+    # f16, which cannot hold it, and the status word says so
+    w = wl.make_mla_workload(_spec(seq_lens=(300, 40)), device="cuda")
+    page = int(w.block_tables[0, 3])
+    w.kv_cache[page, :, :512] = 1.0e6
+    binding.mla_decode_workload(w, options=binding.make_options(num_ctas=8, min_pages_per_cta=1))
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) & binding.STATUS_F16_RANGE
