@@ -237,6 +237,133 @@ def _packed_views(parts, device):
     return buf, views
 
 
+def _timed_passes(step, ev_opts_for, pools, args, world, local, dev):
+    """Warm-up, CUDA-graph capture and the three timed passes of a decode
+    benchmark.  step(k, opts=None, stream_=None) enqueues step k (pool k % pools)
+    on stream_ (None: the current stream); ev_opts_for(pidx, ev_a, ev_b) gives
+    pool pidx's options with the split kernel's start / stop events.
+
+    The decode step runs as an engine runs it: captured in CUDA graphs and
+    replayed, so the device time is not hidden behind Python's per-call
+    marshalling.  A graph holds GSTEP consecutive steps (rotating the KV pools),
+    so the programmatic-dependent-launch overlap between steps survives inside
+    it; single-step graphs cover a remainder.  Pass 1 (value): K whole steps back
+    to back, bracketed by barrier + synchronize; pass 2 (roofline): the split
+    kernel's own duration, step by step, from external event records; pass 3:
+    the same K steps as direct calls through the binding (no graph).
+    Returns (ms per step, max over ranks; split-kernel ms list; direct ms; clocks)."""
+    import torch
+
+    from paged_kv_decode_06_gb300 import binding
+    stream = torch.cuda.current_stream()
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    cap = torch.cuda.Stream()
+    gstep = pools * max(1, 8 // pools)
+
+    def capture(first, n, opts=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for j in range(n):
+                step(first + j, opts=opts, stream_=cap)
+        return g
+
+    big = capture(0, gstep)
+    singles = [capture(pidx, 1) for pidx in range(pools)]
+
+    def run_steps(count):
+        k = 0
+        while k + gstep <= count:
+            big.replay()
+            k += gstep
+        while k < count:
+            singles[k % pools].replay()
+            k += 1
+    ev_a = torch.cuda.Event(enable_timing=True)
+    ev_b = torch.cuda.Event(enable_timing=True)
+    ev_a.record(stream); ev_b.record(stream)     # torch times only events it has recorded once itself
+    torch.cuda.synchronize()
+    rgraphs = [capture(pidx, 1, opts=ev_opts_for(pidx, ev_a, ev_b)) for pidx in range(pools)]
+    run_steps(max(args.warmup, gstep))
+    torch.cuda.synchronize()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t_begin.record(stream)
+        run_steps(args.steps)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        split_ms = []
+        for k in range(args.steps):
+            rgraphs[k % pools].replay()
+            ev_b.synchronize()
+            split_ms.append(ev_a.elapsed_time(ev_b))
+    ms = t_begin.elapsed_time(t_end) / args.steps
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    direct_ms = d0.elapsed_time(d1) / args.steps
+    return max_over_ranks(ms, world, device=dev), split_ms, direct_ms, clk.summary()
+
+
+def _packed_e2e(base, works, out, lse, dev, call, args):
+    """End to end through the public API: every step copies its inputs (q,
+    block table, lengths, query starts) from pinned host memory and reads out /
+    lse back; each direction is one copy of one packed buffer whose views are the
+    tensors the call takes.  call(k, q, bt, sl, qsl, out, lse) makes step k's API
+    call on the device views.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    import torch
+    has_qsl = base.query_start_loc is not None
+    in_parts = [(tuple(base.q.shape), base.q.dtype), (tuple(base.block_tables.shape), torch.int32),
+                (tuple(base.seq_lens.shape), torch.int32)]
+    if has_qsl:
+        in_parts.append((tuple(base.query_start_loc.shape), torch.int32))
+    out_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
+    d_in, d_views = _packed_views(in_parts, dev)
+    d_outbuf, (e_out, e_lse) = _packed_views(out_parts, dev)
+    h_outbuf, _ = _packed_views(out_parts, "pinned")
+    h_ins = []
+    for w in works:
+        h_in, hv = _packed_views(in_parts, "pinned")
+        hv[0].copy_(w.q.cpu())
+        hv[1].copy_(torch.from_numpy(base.block_tables))
+        hv[2].copy_(torch.from_numpy(base.seq_lens))
+        if has_qsl:
+            hv[3].copy_(torch.from_numpy(base.query_start_loc))
+        h_ins.append(h_in)
+    e_qsl = d_views[3] if has_qsl else None
+    pools = len(works)
+
+    def e2e_step(k):
+        d_in.copy_(h_ins[k % pools], non_blocking=True)
+        call(k, d_views[0], d_views[1], d_views[2], e_qsl, e_out, e_lse)
+        h_outbuf.copy_(d_outbuf, non_blocking=True)
+
+    stream = torch.cuda.current_stream()
+    for k in range(args.warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / args.steps, d_in.numel(), d_outbuf.numel()
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -315,7 +442,6 @@ def run_ours(args, world, rank, local):
     mq = spec.max_query_len if qsl is not None else 1
     out = torch.empty_like(base.q)
     lse = torch.empty(base.q.shape[:2], dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
 
     def step(k, opts=None, stream_=None):
         w = works[k % pools]
@@ -324,122 +450,16 @@ def run_ours(args, world, rank, local):
         binding.paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
                                   spec.v_scale, out=out, lse=lse, options=opts, stream=stream_)
 
-    for k in range(args.warmup):
-        step(k)
-    torch.cuda.synchronize()
-    assert binding.paged_attn_device_status(clear=True) == 0
+    ms, split_ms, direct_ms, clocks = _timed_passes(
+        step, lambda pidx, ea, eb: pool_options(works[pidx], split_start_event=ea, split_stop_event=eb), pools, args,
+        world, local, dev)
 
-    # The decode step as an engine runs it: captured in CUDA graphs and replayed,
-    # so the device time is not hidden behind Python's per-call marshalling.
-    # A graph holds GSTEP consecutive steps (rotating the KV pools), so the
-    # programmatic-dependent-launch overlap between steps survives inside it;
-    # single-step graphs cover a remainder.  (Direct calls are timed below too.)
-    cap = torch.cuda.Stream()
-    gstep = pools * max(1, 8 // pools)
-
-    def capture(first, n, opts=None):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            for j in range(n):
-                step(first + j, opts=opts, stream_=cap)
-        return g
-
-    big = capture(0, gstep)
-    singles = [capture(pidx, 1) for pidx in range(pools)]
-
-    def run_steps(count):
-        k = 0
-        while k + gstep <= count:
-            big.replay()
-            k += gstep
-        while k < count:
-            singles[k % pools].replay()
-            k += 1
-    # roofline graphs: external event records around the split kernel
-    ev_a = torch.cuda.Event(enable_timing=True)
-    ev_b = torch.cuda.Event(enable_timing=True)
-    ev_a.record(stream); ev_b.record(stream)     # torch times only events it has recorded once itself
-    torch.cuda.synchronize()
-    ev_opts = [pool_options(w, split_start_event=ev_a, split_stop_event=ev_b) for w in works]
-    rgraphs = [capture(pidx, 1, opts=ev_opts[pidx]) for pidx in range(pools)]
-    run_steps(max(args.warmup, gstep))
-    torch.cuda.synchronize()
-
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        # pass 1 (value): K whole steps back to back, bracketed by barrier + sync
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        t_begin.record(stream)
-        run_steps(args.steps)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        # pass 2 (roofline): the split kernel's own duration, step by step
-        split_ms = []
-        for k in range(args.steps):
-            rgraphs[k % pools].replay()
-            ev_b.synchronize()
-            split_ms.append(ev_a.elapsed_time(ev_b))
-    ms = t_begin.elapsed_time(t_end) / args.steps
-    # pass 3: the same K steps as direct calls through the binding (no graph)
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for k in range(args.steps):
-        step(k)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    direct_ms = d0.elapsed_time(d1) / args.steps
-    ms = max_over_ranks(ms, world, device=dev)
-
-    # end-to-end through the public API: every step copies its inputs (q, block
-    # table, lengths, query starts) from pinned host memory and reads out / lse
-    # back; each direction is one copy of one packed buffer whose views are the
-    # tensors the call takes
-    in_parts = [(tuple(base.q.shape), base.q.dtype), (tuple(base.block_tables.shape), torch.int32),
-                (tuple(base.seq_lens.shape), torch.int32)]
-    if qsl is not None:
-        in_parts.append((tuple(base.query_start_loc.shape), torch.int32))
-    out_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
-    d_in, d_views = _packed_views(in_parts, dev)
-    d_outbuf, (e_out, e_lse) = _packed_views(out_parts, dev)
-    h_outbuf, _ = _packed_views(out_parts, "pinned")
-    h_ins = []
-    for w in works:
-        h_in, hv = _packed_views(in_parts, "pinned")
-        hv[0].copy_(w.q.cpu())
-        hv[1].copy_(torch.from_numpy(base.block_tables))
-        hv[2].copy_(torch.from_numpy(base.seq_lens))
-        if qsl is not None:
-            hv[3].copy_(torch.from_numpy(base.query_start_loc))
-        h_ins.append(h_in)
-    e_q, e_bt, e_sl = d_views[0], d_views[1], d_views[2]
-    e_qsl = d_views[3] if qsl is not None else None
-
-    def e2e_step(k):
+    def e2e_call(k, q, bt_, sl_, qsl_, out_, lse_):
         w = works[k % pools]
-        d_in.copy_(h_ins[k % pools], non_blocking=True)
-        binding.paged_attn_decode(e_q, w.k_cache, w.v_cache, e_bt, e_sl, e_qsl, mq, spec.scale, spec.k_scale,
-                                  spec.v_scale, out=e_out, lse=e_lse, options=pool_opts[k % pools])
-        h_outbuf.copy_(d_outbuf, non_blocking=True)
+        binding.paged_attn_decode(q, w.k_cache, w.v_cache, bt_, sl_, qsl_, mq, spec.scale, spec.k_scale,
+                                  spec.v_scale, out=out_, lse=lse_, options=pool_opts[k % pools])
 
-    for k in range(args.warmup):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        e2e_step(k)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    h2d = d_in.numel()
-    d2h = d_outbuf.numel()
+    e2e_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
     status = binding.paged_attn_device_status(clear=True)
 
     if rank != 0:
@@ -479,7 +499,7 @@ def run_ours(args, world, rank, local):
                         "ms_per_step": direct_ms,
                         "note": "paged_attn_decode called from Python each step (no CUDA graph)"},
         "gpu_launches": 2 * args.steps,   # split + merge per timed step
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "device_status": status,
     }
     if not args.no_cpu_baseline and not args.batch:
@@ -522,115 +542,27 @@ def run_mla(args, world, rank, local):
     T = base.q.shape[0]
     out = torch.empty((T, spec.num_q_heads, spec.kv_lora_rank), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, spec.num_q_heads), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
 
-    def step(k, opts=None, stream_=None, q=None):
+    def step(k, opts=None, stream_=None):
         w = works[k % pools]
-        binding.paged_attn_mla_decode(w.q if q is None else q, w.kv_cache, bt, sl, qsl, mq, spec.scale, spec.kv_scale,
-                                      out=out, lse=lse, options=opts, stream=stream_)
+        binding.paged_attn_mla_decode(w.q, w.kv_cache, bt, sl, qsl, mq, spec.scale, spec.kv_scale, out=out, lse=lse,
+                                      options=opts, stream=stream_)
 
-    for k in range(args.warmup):
-        step(k)
-    torch.cuda.synchronize()
-    assert binding.paged_attn_device_status(clear=True) == 0
-    cap = torch.cuda.Stream()
-    gstep = pools * max(1, 8 // pools)
+    ev_opt = {}
 
-    def capture(first, n, opts=None):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            for j in range(n):
-                step(first + j, opts=opts, stream_=cap)
-        return g
+    def ev_opts_for(pidx, ea, eb):
+        if "o" not in ev_opt:
+            ev_opt["o"] = binding.make_options(split_start_event=ea, split_stop_event=eb)
+        return ev_opt["o"]
 
-    big = capture(0, gstep)
-    singles = [capture(pidx, 1) for pidx in range(pools)]
+    ms, split_ms, direct_ms, clocks = _timed_passes(step, ev_opts_for, pools, args, world, local, dev)
 
-    def run_steps(count):
-        k = 0
-        while k + gstep <= count:
-            big.replay()
-            k += gstep
-        while k < count:
-            singles[k % pools].replay()
-            k += 1
-    ev_a = torch.cuda.Event(enable_timing=True)
-    ev_b = torch.cuda.Event(enable_timing=True)
-    ev_a.record(stream); ev_b.record(stream)
-    torch.cuda.synchronize()
-    ev_opt = binding.make_options(split_start_event=ev_a, split_stop_event=ev_b)
-    rgraphs = [capture(pidx, 1, opts=ev_opt) for pidx in range(pools)]
-    run_steps(max(args.warmup, gstep))
-    torch.cuda.synchronize()
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        t_begin.record(stream)
-        run_steps(args.steps)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        split_ms = []
-        for k in range(args.steps):
-            rgraphs[k % pools].replay()
-            ev_b.synchronize()
-            split_ms.append(ev_a.elapsed_time(ev_b))
-    ms = t_begin.elapsed_time(t_end) / args.steps
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for k in range(args.steps):
-        step(k)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    direct_ms = d0.elapsed_time(d1) / args.steps
-    ms = max_over_ranks(ms, world, device=dev)
-    # end to end through the public API: per step one packed copy of the inputs
-    # from pinned host memory and one of out / lse back (as in run_ours)
-    in_parts = [(tuple(base.q.shape), base.q.dtype), (tuple(base.block_tables.shape), torch.int32),
-                (tuple(base.seq_lens.shape), torch.int32)]
-    if qsl is not None:
-        in_parts.append((tuple(base.query_start_loc.shape), torch.int32))
-    out_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
-    d_in, d_views = _packed_views(in_parts, dev)
-    d_outbuf, (e_out, e_lse) = _packed_views(out_parts, dev)
-    h_outbuf, _ = _packed_views(out_parts, "pinned")
-    h_ins = []
-    for w in works:
-        h_in, hv = _packed_views(in_parts, "pinned")
-        hv[0].copy_(w.q.cpu())
-        hv[1].copy_(torch.from_numpy(base.block_tables))
-        hv[2].copy_(torch.from_numpy(base.seq_lens))
-        if qsl is not None:
-            hv[3].copy_(torch.from_numpy(base.query_start_loc))
-        h_ins.append(h_in)
-    e_q, e_bt, e_sl = d_views[0], d_views[1], d_views[2]
-    e_qsl = d_views[3] if qsl is not None else None
-
-    def e2e_step(k):
+    def e2e_call(k, q, bt_, sl_, qsl_, out_, lse_):
         w = works[k % pools]
-        d_in.copy_(h_ins[k % pools], non_blocking=True)
-        binding.paged_attn_mla_decode(e_q, w.kv_cache, e_bt, e_sl, e_qsl, mq, spec.scale, spec.kv_scale, out=e_out,
-                                      lse=e_lse)
-        h_outbuf.copy_(d_outbuf, non_blocking=True)
+        binding.paged_attn_mla_decode(q, w.kv_cache, bt_, sl_, qsl_, mq, spec.scale, spec.kv_scale, out=out_,
+                                      lse=lse_)
 
-    for k in range(args.warmup):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        e2e_step(k)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    h2d = d_in.numel()
-    d2h = d_outbuf.numel()
+    e2e_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
     status = binding.paged_attn_device_status(clear=True)
     if rank != 0:
         if world > 1:
@@ -669,7 +601,7 @@ def run_mla(args, world, rank, local):
                         "ms_per_step": direct_ms,
                         "note": "paged_attn_mla_decode called from Python each step (no CUDA graph)"},
         "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "device_status": status,
     }
     if not args.no_cpu_baseline and not args.batch:

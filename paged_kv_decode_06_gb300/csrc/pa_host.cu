@@ -317,6 +317,48 @@ int encode_cache_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int D, int
   return PA_OK;
 }
 
+// Grow the library-owned workspace of a device to at least `bytes` (a free and
+// a fresh allocation; the old contents need not survive).  Caller holds g_mu.
+int grow_workspace(DeviceState* ds, size_t bytes) {
+  if (ds->ws_bytes >= bytes) return PA_OK;
+  cudaError_t e;
+  if (ds->ws) {
+    if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    ds->ws = nullptr;
+    ds->ws_bytes = 0;
+  }
+  if ((e = cudaMalloc(&ds->ws, bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+  ds->ws_bytes = bytes;
+  return PA_OK;
+}
+
+// The split workspace of a call: the caller's (checked for size and
+// alignment), or the library-owned one of the device, grown outside stream
+// capture (during capture an undersized workspace is an error: the caller
+// reserves it first with `reserve_fn`).  Caller holds g_mu.
+int acquire_workspace(DeviceState* ds, const pa_options_t* opts, size_t bytes, cudaStream_t stream,
+                      const char* reserve_fn, void** ws) {
+  if (opts && opts->workspace) {
+    if (opts->workspace_bytes < bytes)
+      return fail(PA_ERR_WORKSPACE, "caller workspace %zu bytes < %zu needed", opts->workspace_bytes, bytes);
+    if (!aligned(opts->workspace, 256)) return fail(PA_ERR_INVALID_ARG, "caller workspace must be 256-byte aligned");
+    *ws = opts->workspace;
+    return PA_OK;
+  }
+  if (ds->ws_bytes < bytes) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(PA_ERR_WORKSPACE, "workspace must grow to %zu bytes, which is not allowed during stream capture; "
+                  "call %s first", bytes, reserve_fn);
+    const int st = grow_workspace(ds, bytes);
+    if (st != PA_OK) return st;
+  }
+  *ws = ds->ws;
+  return PA_OK;
+}
+
 int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* vc, const pa_tensor_t* bt,
                 const pa_tensor_t* sl, const pa_tensor_t* qsl, int32_t max_qlen, float scale, float k_scale,
                 float v_scale, const pa_tensor_t* out, const pa_tensor_t* lse, const pa_options_t* opts,
@@ -408,31 +450,8 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
                       kc->dtype, max_qlen, opts, ds->num_sms, ds->smem_optin, &pl)) != PA_OK)
     return st;
 
-  // workspace
   void* ws = nullptr;
-  if (opts && opts->workspace) {
-    if (opts->workspace_bytes < pl.ws_bytes)
-      return fail(PA_ERR_WORKSPACE, "caller workspace %zu bytes < %zu needed", opts->workspace_bytes, pl.ws_bytes);
-    if (!aligned(opts->workspace, 256)) return fail(PA_ERR_INVALID_ARG, "caller workspace must be 256-byte aligned");
-    ws = opts->workspace;
-  } else {
-    if (ds->ws_bytes < pl.ws_bytes) {
-      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-      if (cs != cudaStreamCaptureStatusNone)
-        return fail(PA_ERR_WORKSPACE, "workspace must grow to %zu bytes, which is not allowed during stream capture; "
-                    "call paged_attn_reserve first", pl.ws_bytes);
-      if (ds->ws) {
-        if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-        ds->ws = nullptr;
-        ds->ws_bytes = 0;
-      }
-      if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-      ds->ws_bytes = pl.ws_bytes;
-    }
-    ws = ds->ws;
-  }
+  if ((st = acquire_workspace(ds, opts, pl.ws_bytes, stream, "paged_attn_reserve", &ws)) != PA_OK) return st;
 
   CUtensorMap tk, tv;
   if ((st = encode_cache_map(&tk, kc, esz, static_cast<int>(D), static_cast<int>(Hkv), pl.HC, NB)) != PA_OK) return st;
@@ -723,29 +742,7 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
                           max_qlen, opts, ds->num_sms, ds->smem_optin, &pl)) != PA_OK)
     return st;
   void* ws = nullptr;
-  if (opts && opts->workspace) {
-    if (opts->workspace_bytes < pl.ws_bytes)
-      return fail(PA_ERR_WORKSPACE, "caller workspace %zu bytes < %zu needed", opts->workspace_bytes, pl.ws_bytes);
-    if (!aligned(opts->workspace, 256)) return fail(PA_ERR_INVALID_ARG, "caller workspace must be 256-byte aligned");
-    ws = opts->workspace;
-  } else {
-    if (ds->ws_bytes < pl.ws_bytes) {
-      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-      if (cs != cudaStreamCaptureStatusNone)
-        return fail(PA_ERR_WORKSPACE, "workspace must grow to %zu bytes, which is not allowed during stream capture; "
-                    "call paged_attn_mla_reserve first", pl.ws_bytes);
-      if (ds->ws) {
-        if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-        ds->ws = nullptr;
-        ds->ws_bytes = 0;
-      }
-      if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-      ds->ws_bytes = pl.ws_bytes;
-    }
-    ws = ds->ws;
-  }
+  if ((st = acquire_workspace(ds, opts, pl.ws_bytes, stream, "paged_attn_mla_reserve", &ws)) != PA_OK) return st;
   CUtensorMap tm;
   if ((st = encode_mla_map(&tm, kc, esz, NB)) != PA_OK) return st;
 
@@ -1037,16 +1034,7 @@ int paged_attn_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_hea
   if ((st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, nullptr, ds->num_sms,
                       ds->smem_optin, &pl)) != PA_OK)
     return st;
-  if (ds->ws_bytes >= pl.ws_bytes) return PA_OK;
-  cudaError_t e;
-  if (ds->ws) {
-    if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-    ds->ws = nullptr;
-    ds->ws_bytes = 0;
-  }
-  if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-  ds->ws_bytes = pl.ws_bytes;
-  return PA_OK;
+  return grow_workspace(ds, pl.ws_bytes);
 }
 
 int paged_attn_mla_decode_ex(const pa_tensor_t* q, const pa_tensor_t* kv_cache, const pa_tensor_t* block_tables,
@@ -1114,16 +1102,7 @@ int paged_attn_mla_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dty
   if ((st = make_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len, nullptr, ds->num_sms, ds->smem_optin,
                           &pl)) != PA_OK)
     return st;
-  if (ds->ws_bytes >= pl.ws_bytes) return PA_OK;
-  cudaError_t e;
-  if (ds->ws) {
-    if ((e = cudaFree(ds->ws)) != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-    ds->ws = nullptr;
-    ds->ws_bytes = 0;
-  }
-  if ((e = cudaMalloc(&ds->ws, pl.ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-  ds->ws_bytes = pl.ws_bytes;
-  return PA_OK;
+  return grow_workspace(ds, pl.ws_bytes);
 }
 
 int paged_attn_release(void) {

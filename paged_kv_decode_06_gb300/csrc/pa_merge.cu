@@ -238,8 +238,17 @@ __device__ __forceinline__ float4 f16x4_to_float4(uint2 v) {
   return make_float4(fa.x, fa.y, fb.x, fb.y);
 }
 
-__device__ __forceinline__ void lse_acc4(float& mx, float& l, float4 (&acc)[4], float2 ml, const uint2 (&o)[4]) {
+// true if one of the four f16 values is infinite or NaN (exponent all ones)
+__device__ __forceinline__ bool f16x4_overflow(uint2 v) {
+  return ((v.x & 0x7C00u) == 0x7C00u) || ((v.x & 0x7C000000u) == 0x7C000000u) || ((v.y & 0x7C00u) == 0x7C00u) ||
+         ((v.y & 0x7C000000u) == 0x7C000000u);
+}
+
+__device__ __forceinline__ void lse_acc4(float& mx, float& l, float4 (&acc)[4], float2 ml, const uint2 (&o)[4],
+                                         bool& overflow) {
   if (ml.x == -INFINITY || !(ml.y > 0.f)) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) overflow |= f16x4_overflow(o[j]);
   const float nm = fmaxf(mx, ml.x);
   const float a = fast_exp2(mx - nm);
   const float b = fast_exp2(ml.x - nm);
@@ -266,6 +275,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const Me
   if (!m.work) return;
   const uint16_t* ws = reinterpret_cast<const uint16_t*>(p.ws_o);
   float mx = -INFINITY, l = 0.f;
+  bool overflow = false;   // a piece's f16 output beyond the f16 range
   float4 acc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -279,8 +289,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const Me
       oa[j] = *reinterpret_cast<const uint2*>(ws + sa * D + 4 * lane + 128 * j);
       ob[j] = *reinterpret_cast<const uint2*>(ws + sb * D + 4 * lane + 128 * j);
     }
-    lse_acc4(mx, l, acc, ma, oa);
-    lse_acc4(mx, l, acc, mb, ob);
+    lse_acc4(mx, l, acc, ma, oa, overflow);
+    lse_acc4(mx, l, acc, mb, ob, overflow);
   }
   if (s < m.nparts) {
     const int64_t sa = slot_row(p, m, s);
@@ -288,8 +298,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps) pa_merge_mla_kernel(const Me
     uint2 oa[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) oa[j] = *reinterpret_cast<const uint2*>(ws + sa * D + 4 * lane + 128 * j);
-    lse_acc4(mx, l, acc, ma, oa);
+    lse_acc4(mx, l, acc, ma, oa, overflow);
   }
+  if (overflow) atomicOr(p.err, kErrF16Range);
 #pragma unroll
   for (int j = 0; j < 4; ++j) write_merged(p, m, lane + 32 * j, acc[j], l, mx, lane == 0 && j == 0);
 }

@@ -640,12 +640,11 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
           const int rho = half ? rho1 : rho0;
           // the piece's normalised output O / l in f16 (a weighted average of
           // cached rows, 2^-11 relative error); the merge weighs it back with
-          // l.  A cached value beyond the f16 range (|v| > 65504, possible only
-          // in a bf16 cache) would overflow here: reported as kErrF16Range.
+          // l and reports a value beyond the f16 range (|v| > 65504, possible
+          // only in a bf16 cache) as kErrF16Range.
           const float lt = half ? lt1 : lt0;
           const float inv = lt > 0.f ? 1.f / lt : 0.f;
           uint16_t* orow = reinterpret_cast<uint16_t*>(p.ws_o) + (rowbase + rho) * kMlaDv + 128 * cq;
-          bool fits = true;
 #pragma unroll
           for (int J = 0; J < 16; J += 2) {
 #pragma unroll
@@ -653,12 +652,9 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
               float va, vb;
               int d;
               ws.pair_at(J, jj, half, tig, va, vb, d);
-              const uint32_t h2 = pack_f16(va * inv, vb * inv);
-              fits &= ((h2 & 0x7C00u) != 0x7C00u) && ((h2 & 0x7C000000u) != 0x7C000000u);
-              *reinterpret_cast<uint32_t*>(orow + d) = h2;
+              *reinterpret_cast<uint32_t*>(orow + d) = pack_f16(va * inv, vb * inv);
             }
           }
-          if (!fits) atomicOr(p.err, kErrF16Range);
           if (cq == 0 && tig == 0) p.ws_ml[rowbase + rho] = make_float2(half ? ws.m1 : ws.m0, half ? lt1 : lt0);
         }
       }
