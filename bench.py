@@ -704,17 +704,19 @@ def run_cache_write(args, world, rank, local):
     e2e_ms = e0.elapsed_time(e1) / max(1, args.steps // 10)
     peak, peak_kind = _peaks()
     value = step_bytes / (ms * 1e-3) / 1e9
+    workload = f"cache_write_T{T}_{args.kv_dtype}" + ("_per_token" if per_token else "")
+    kernel = "pa_cache_write_tok_kernel" if per_token else "pa_cache_write_kernel"
     line = {
         "metric": "paged KV cache write GB/s (rows read + written), 1 GPU", "value": value, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f8e4m3" if fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": f"cache_write_T{T}_{args.kv_dtype}" + ("_per_token" if per_token else ""),
+        "config": {"workload": workload,
                    "tokens": T, "kv_heads": Hkv, "head_dim": D,
                    "bytes_per_step": step_bytes, "pools_rotated": pools,
                    "step_mode": "CUDA graph replay of paged_attn_cache_write"},
         "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
-                     "traffic": None, "kernel": "pa_cache_write_tok_kernel" if per_token else "pa_cache_write_kernel",
+                     "traffic": _traffic_from_profiles(workload, kernel), "kernel": kernel,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * key.numel() * 2, "d2h_bytes_per_step": 0},
@@ -734,10 +736,14 @@ def _spec_for(args):
 
 
 def kernel_source_sha256(kernel):
-    """Hash of the sources a split kernel is compiled from (stamps ncu figures)."""
+    """Hash of the sources a kernel is compiled from (stamps ncu figures)."""
     import hashlib
-    names = ["pa_split.cuh", "pa_device.cuh", "pa_pack.cuh"] + \
-        (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else []) + (["pa_mla.cu"] if kernel == "pa_mla_kernel" else [])
+    if kernel.startswith("pa_cache_write"):
+        names = ["pa_cache_write.cu", "pa_device.cuh", "pa_pack.cuh"]
+    else:
+        names = ["pa_split.cuh", "pa_device.cuh", "pa_pack.cuh"] + \
+            (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else []) + \
+            (["pa_mla.cu"] if kernel == "pa_mla_kernel" else [])
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:
@@ -746,8 +752,8 @@ def kernel_source_sha256(kernel):
 
 
 def _traffic_from_profiles(config, kernel):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary,
-    when it was taken on the current kernel source (else None)."""
+    """DRAM bytes per launch of a kernel from the committed ncu summary, when it
+    was taken on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None

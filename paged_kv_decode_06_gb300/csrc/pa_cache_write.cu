@@ -6,11 +6,12 @@
 // fp32 on the host; round to nearest even, saturating to +-448).
 //
 // One thread moves 8 consecutive features (16 bytes of bf16 input) of one
-// (token, head) row; the grid strides over all tokens x heads x 8-feature
-// chunks.  A token's rows of all heads are one contiguous run in the cache, so
+// (token, head) row; a grid of one wave of resident blocks strides over all
+// tokens x heads x 8-feature chunks.  A token's rows of all heads are one contiguous run in the cache, so
 // the stores of a warp are contiguous.
 #include "pa_device.cuh"
 #include "pa_kernels.h"
+#include "pa_pack.cuh"
 
 namespace pa {
 
@@ -20,151 +21,244 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   return r;
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWriteParams p) {
-  const int chunks_per_head = p.head_dim / 8;
-  const int64_t chunks_per_token = static_cast<int64_t>(p.num_kv_heads) * chunks_per_head;
-  const int64_t total = static_cast<int64_t>(p.num_tokens) * chunks_per_token;
-  const int64_t num_slots = static_cast<int64_t>(p.num_pages) * kPage;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = idx / chunks_per_token;
-    const int64_t rem = idx - t * chunks_per_token;
-    const int h = static_cast<int>(rem / chunks_per_head);
-    const int d0 = static_cast<int>(rem - static_cast<int64_t>(h) * chunks_per_head) * 8;
-    const int64_t slot = p.slot_mapping[t];
-    if (slot < 0) continue;                       // padding token
-    if (slot >= num_slots) {
-      if (d0 == 0 && h == 0) atomicOr(p.err, kErrPageRange);
-      continue;
-    }
-    const int64_t page = slot / kPage;
-    const int64_t off = slot - page * kPage;
-#pragma unroll
-    for (int tensor = 0; tensor < 2; ++tensor) {
-      const uint16_t* src = (tensor ? p.value : p.key) + t * (tensor ? p.v_stride_t : p.k_stride_t) +
-                            static_cast<int64_t>(h) * (tensor ? p.v_stride_h : p.k_stride_h) + d0;
-      const int64_t dst_elem = page * (tensor ? p.vc_stride_page : p.kc_stride_page) +
-                               off * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
-                               static_cast<int64_t>(h) * (tensor ? p.vc_stride_head : p.kc_stride_head) + d0;
-      const uint4 x = *reinterpret_cast<const uint4*>(src);
-      if constexpr (FP8) {
-        const float r = tensor ? p.v_rscale : p.k_rscale;
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t q[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          q[e] = e4m3x2_from_f32(bf16_lo(w[e]) * r, bf16_hi(w[e]) * r);
-        uint2 out;
-        out.x = q[0] | (q[1] << 16);
-        out.y = q[2] | (q[3] << 16);
-        uint8_t* dst = (tensor ? p.v_cache : p.k_cache) + dst_elem;
-        *reinterpret_cast<uint2*>(dst) = out;
-      } else {
-        uint8_t* dst = (tensor ? p.v_cache : p.k_cache) + dst_elem * 2;
-        *reinterpret_cast<uint4*>(dst) = x;
-      }
-    }
-  }
+// Integer quotient of an index by a per-call divisor: 32-bit when the index
+// range fits (every practical call), 64-bit otherwise (a uniform branch).
+__device__ __forceinline__ int64_t cw_div(int64_t a, int64_t b, bool narrow) {
+  return narrow ? static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b)) : a / b;
 }
 
-// Per-token fp8 write (the pages' reshape_and_cache_with_pertoken_quant): the
-// D / 8 threads of one (token, head) row sit on consecutive lanes of a warp
-// (a row starts at a multiple of D / 8 in the flattened index, and D / 8
-// divides 32), so the row's max |x| is an xor-shuffle reduction inside that
-// lane group.  scale = amax / 448 and r = 448 / amax are IEEE fp32 divisions;
-// codes = e4m3fn(x * r), round to nearest even, saturating; a zero row stores
-// scale 0 and zero codes.  Every lane of a warp runs the same number of loop
-// trips (the trip test is on the block's first index), so the shuffles see
-// full warps.  A trip takes two index groups a grid apart and issues all four
-// row loads (K and V of each) before the reductions.
-__global__ void __launch_bounds__(256) pa_cache_write_tok_kernel(const CacheWriteParams p) {
-  constexpr int U = 2;              // index groups per trip, all loads issued before any reduction
-  const int cph = p.head_dim / 8;   // chunks per head (8 or 16)
-  const int64_t chunks_per_token = static_cast<int64_t>(p.num_kv_heads) * cph;
-  const int64_t total = static_cast<int64_t>(p.num_tokens) * chunks_per_token;
+// Per-tensor scales (or a bf16 copy).  A trip takes U chunk indices a grid
+// apart; every row load is issued before any slot is looked at (a padding
+// token's row is read and dropped), so a trip waits for one memory latency,
+// not a slot lookup followed by the row loads.
+template <bool FP8, int U>
+__global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWriteParams p) {
+  const int cph = p.head_dim / 8;
+  const int64_t cpt = static_cast<int64_t>(p.num_kv_heads) * cph;   // chunks per token
+  const int64_t total = static_cast<int64_t>(p.num_tokens) * cpt;
+  const bool narrow = total <= 0xFFFFFFFFll;
   const int64_t num_slots = static_cast<int64_t>(p.num_pages) * kPage;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; i0 < total; i0 += U * stride) {
-    int64_t t[U], page[U], off[U];
-    int h[U], d0[U];
-    bool live[U];
-    uint4 xs[U][2];
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total; i0 += U * stride) {
+    int64_t t[U];
+    int h[U], d0[U], slot[U];
+    uint4 x[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t idx = i0 + u * stride + threadIdx.x;
+      const int64_t idx = i0 + u * stride;
       const bool in = idx < total;
-      t[u] = in ? idx / chunks_per_token : 0;
-      const int64_t rem = idx - t[u] * chunks_per_token;
-      h[u] = in ? static_cast<int>(rem / cph) : 0;
-      d0[u] = in ? static_cast<int>(rem - static_cast<int64_t>(h[u]) * cph) * 8 : 0;
-      const int64_t slot = in ? p.slot_mapping[t[u]] : -1;
-      if (in && slot >= num_slots && d0[u] == 0 && h[u] == 0) atomicOr(p.err, kErrPageRange);
-      live[u] = in && slot >= 0 && slot < num_slots;
-      page[u] = live[u] ? slot / kPage : 0;
-      off[u] = live[u] ? slot - page[u] * kPage : 0;
-      xs[u][0] = xs[u][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (live[u]) {
-        xs[u][0] = *reinterpret_cast<const uint4*>(p.key + t[u] * p.k_stride_t +
-                                                   static_cast<int64_t>(h[u]) * p.k_stride_h + d0[u]);
-        xs[u][1] = *reinterpret_cast<const uint4*>(p.value + t[u] * p.v_stride_t +
-                                                   static_cast<int64_t>(h[u]) * p.v_stride_h + d0[u]);
+      t[u] = in ? cw_div(idx, cpt, narrow) : 0;
+      const int rem = static_cast<int>(idx - t[u] * cpt);
+      h[u] = in ? rem / cph : 0;
+      d0[u] = in ? (rem - h[u] * cph) * 8 : 0;
+      slot[u] = in ? p.slot_mapping[t[u]] : -1;
+      x[u][0] = x[u][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (in) {
+        x[u][0] = *reinterpret_cast<const uint4*>(p.key + t[u] * p.k_stride_t + h[u] * p.k_stride_h + d0[u]);
+        x[u][1] = *reinterpret_cast<const uint4*>(p.value + t[u] * p.v_stride_t + h[u] * p.v_stride_h + d0[u]);
       }
     }
-    float amax[U][2];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int tensor = 0; tensor < 2; ++tensor) {
-        const uint4 x = xs[u][tensor];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
-        amax[u][tensor] = a;
-      }
-    for (int o = 1; o < cph; o <<= 1)
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int tensor = 0; tensor < 2; ++tensor)
-          amax[u][tensor] = fmaxf(amax[u][tensor], __shfl_xor_sync(0xffffffffu, amax[u][tensor], o));
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (!live[u]) continue;
+      if (slot[u] < 0) continue;                   // padding token (or past the end)
+      if (slot[u] >= num_slots) {
+        if (d0[u] == 0 && h[u] == 0) atomicOr(p.err, kErrPageRange);
+        continue;
+      }
+      const int64_t page = slot[u] / kPage;
+      const int64_t off = slot[u] - page * kPage;
 #pragma unroll
       for (int tensor = 0; tensor < 2; ++tensor) {
-        const uint4 x = xs[u][tensor];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        const float a = amax[u][tensor];
-        const float r = a > 0.f ? __fdiv_rn(448.f, a) : 0.f;
-        uint32_t q[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) q[e] = e4m3x2_from_f32(bf16_lo(w[e]) * r, bf16_hi(w[e]) * r);
-        const int64_t dst_elem = page[u] * (tensor ? p.vc_stride_page : p.kc_stride_page) +
-                                 off[u] * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
+        const int64_t dst_elem = page * (tensor ? p.vc_stride_page : p.kc_stride_page) +
+                                 off * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
                                  static_cast<int64_t>(h[u]) * (tensor ? p.vc_stride_head : p.kc_stride_head) + d0[u];
-        *reinterpret_cast<uint2*>((tensor ? p.v_cache : p.k_cache) + dst_elem) =
-            make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-        if (d0[u] == 0) {
-          float* sc = tensor ? p.v_tok : p.k_tok;
-          sc[page[u] * (tensor ? p.vs_stride_page : p.ks_stride_page) +
-             static_cast<int64_t>(h[u]) * (tensor ? p.vs_stride_head : p.ks_stride_head) +
-             off[u] * (tensor ? p.vs_stride_slot : p.ks_stride_slot)] = __fdiv_rn(a, 448.f);
+        if constexpr (FP8) {
+          const float r = tensor ? p.v_rscale : p.k_rscale;
+          const uint64_t r2 = f2_pack(r, r);
+          const uint32_t w[4] = {x[u][tensor].x, x[u][tensor].y, x[u][tensor].z, x[u][tensor].w};
+          uint32_t q[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float lo, hi;
+            f2_unpack(fmul2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), r2), lo, hi);
+            q[e] = e4m3x2_from_f32(lo, hi);
+          }
+          *reinterpret_cast<uint2*>((tensor ? p.v_cache : p.k_cache) + dst_elem) =
+              make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        } else {
+          *reinterpret_cast<uint4*>((tensor ? p.v_cache : p.k_cache) + dst_elem * 2) = x[u][tensor];
         }
       }
     }
   }
 }
 
-cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int grid, cudaStream_t stream) {
-  if (p.k_tok != nullptr) {
-    pa_cache_write_tok_kernel<<<grid, 256, 0, stream>>>(p);
-  } else if (fp8) {
-    pa_cache_write_kernel<true><<<grid, 256, 0, stream>>>(p);
-  } else {
-    pa_cache_write_kernel<false><<<grid, 256, 0, stream>>>(p);
+// Largest of two pairs of 16-bit unsigned integers, half by half.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Per-token fp8 write (the pages' reshape_and_cache_with_pertoken_quant).  A
+// (token, head) row of D / 8 16-byte chunks belongs to a group of G lanes of
+// one warp, each lane taking CPL chunks c0, c0 + G, ... (G = the power of two
+// with CPL * G covering the row, at most 32; chunks past the row's end idle), so the
+// row's max |x| is an xor-shuffle reduction inside the group.  For finite bf16
+// values the bit patterns with the sign cleared order like |x|, so the maxima
+// are 16-bit integer maxima (exact), K's and V's carried in one 32-bit word.
+// scale = amax / 448 and r = 448 / amax are IEEE fp32 divisions; codes =
+// e4m3fn(x * r), round to nearest even, saturating; a zero row stores scale 0
+// and zero codes.  The trip test is on the warp's first row, so every lane of a
+// warp runs the same trips and the shuffles see full warps.  A trip takes U rows
+// per group, a grid apart, and issues all their loads (K and V) together with
+// the slot lookups.
+template <int CPL, int U>
+__global__ void __launch_bounds__(256) pa_cache_write_tok_kernel(const CacheWriteParams p, int G) {
+  const int lane = threadIdx.x & 31;
+  const int c0 = lane & (G - 1);
+  const int rpw = 32 / G;                                   // rows per warp per index group
+  const int64_t rows = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads;
+  const bool narrow = rows <= 0xFFFFFFFFll;
+  const int64_t num_slots = static_cast<int64_t>(p.num_pages) * kPage;
+  const int64_t wpass = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32) * rpw;   // rows per grid pass
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * rpw;
+  for (int64_t rb = w0; rb < rows; rb += U * wpass) {
+    int64_t t[U];
+    int h[U], slot[U];
+    uint4 x[U][CPL][2];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t r = rb + u * wpass + lane / G;
+      const bool in = r < rows;
+      t[u] = in ? cw_div(r, p.num_kv_heads, narrow) : 0;
+      h[u] = in ? static_cast<int>(r - t[u] * p.num_kv_heads) : 0;
+      slot[u] = in ? p.slot_mapping[t[u]] : -1;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int d0 = (c0 + k * G) * 8;
+        x[u][k][0] = x[u][k][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (in && d0 < p.head_dim) {
+          x[u][k][0] = *reinterpret_cast<const uint4*>(p.key + t[u] * p.k_stride_t + h[u] * p.k_stride_h + d0);
+          x[u][k][1] = *reinterpret_cast<const uint4*>(p.value + t[u] * p.v_stride_t + h[u] * p.v_stride_h + d0);
+        }
+      }
+    }
+    uint32_t m[U];   // |x| maxima as bf16 bits: K's in the low half, V's in the high half
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint32_t mk = 0u, mv = 0u;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const uint4 a = x[u][k][0], b = x[u][k][1];
+        mk = max_u16x2(mk, max_u16x2(max_u16x2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                     max_u16x2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+        mv = max_u16x2(mv, max_u16x2(max_u16x2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
+                                     max_u16x2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
+      }
+      m[u] = max_u16x2(__byte_perm(mk, mv, 0x5410), __byte_perm(mk, mv, 0x7632));
+    }
+    for (int o = 1; o < G; o <<= 1)
+#pragma unroll
+      for (int u = 0; u < U; ++u) m[u] = max_u16x2(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (slot[u] < 0) continue;
+      if (slot[u] >= num_slots) {
+        if (c0 == 0 && h[u] == 0) atomicOr(p.err, kErrPageRange);
+        continue;
+      }
+      const int64_t page = slot[u] / kPage;
+      const int64_t off = slot[u] - page * kPage;
+      const float amax[2] = {__uint_as_float(m[u] << 16), __uint_as_float(m[u] & 0xFFFF0000u)};
+#pragma unroll
+      for (int tensor = 0; tensor < 2; ++tensor) {
+        const float r = amax[tensor] > 0.f ? __fdiv_rn(448.f, amax[tensor]) : 0.f;
+        const uint64_t r2 = f2_pack(r, r);
+        uint8_t* row = (tensor ? p.v_cache : p.k_cache) + page * (tensor ? p.vc_stride_page : p.kc_stride_page) +
+                       off * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
+                       static_cast<int64_t>(h[u]) * (tensor ? p.vc_stride_head : p.kc_stride_head);
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+          const int d0 = (c0 + k * G) * 8;
+          if (d0 >= p.head_dim) continue;
+          const uint4 v = x[u][k][tensor];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t q[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float lo, hi;
+            f2_unpack(fmul2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), r2), lo, hi);
+            q[e] = e4m3x2_from_f32(lo, hi);
+          }
+          *reinterpret_cast<uint2*>(row + d0) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        }
+      }
+      // the row's two scales: lane c0 = 0 stores K's and c0 = 1 V's (one lane
+      // both when G = 1), so the division issues once per group
+      for (int j = c0; j < 2; j += G) {
+        float* sc = j ? p.v_tok : p.k_tok;
+        sc[page * (j ? p.vs_stride_page : p.ks_stride_page) +
+           static_cast<int64_t>(h[u]) * (j ? p.vs_stride_head : p.ks_stride_head) +
+           off * (j ? p.vs_stride_slot : p.ks_stride_slot)] = __fdiv_rn(j ? amax[1] : amax[0], 448.f);
+      }
+    }
   }
+}
+
+namespace {
+
+int g_occ[3] = {1, 1, 1};   // resident 256-thread blocks per SM of each write kernel
+
+template <typename K>
+int resident_blocks(K kernel) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = 1;
+  }
+  return n;
+}
+
+int grid_for(int64_t need, int num_sms, int occ) {
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, int64_t(num_sms) * occ)));
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Chosen by timing the 16384-token chunk (8 KV heads, D128) over chunks per
+// lane x index groups per trip: more rows in flight per thread cost occupancy
+// and gained nothing; four chunks per lane share one row's reduction, divisions
+// and address arithmetic.
+constexpr int kU = 1;          // per-tensor write: index groups per trip
+constexpr int kCpl = 4;        // per-token write: chunks of a row per lane (kCpl * 32 * 8 >= 512 features)
+constexpr int kUTok = 1;       // per-token write: rows per lane group per trip
+
+}  // namespace
+
+void init_cache_write_occupancy() {
+  g_occ[0] = resident_blocks(pa_cache_write_kernel<false, kU>);
+  g_occ[1] = resident_blocks(pa_cache_write_kernel<true, kU>);
+  g_occ[2] = resident_blocks(pa_cache_write_tok_kernel<kCpl, kUTok>);
+}
+
+// Grid: the blocks that fit on the device at once (one wave), fewer when the
+// call has less work than one trip of each thread.
+cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int num_sms, cudaStream_t stream) {
+  const int cph = p.head_dim / 8;
+  if (p.k_tok != nullptr) {
+    int G = 1;
+    while (kCpl * G < cph && G < 32) G <<= 1;
+    const int64_t rows = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads;
+    pa_cache_write_tok_kernel<kCpl, kUTok>
+        <<<grid_for(ceil_div(rows, int64_t(8) * (32 / G) * kUTok), num_sms, g_occ[2]), 256, 0, stream>>>(p, G);
+    return cudaGetLastError();
+  }
+  const int64_t need = ceil_div(static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * cph, int64_t(256) * kU);
+  if (fp8)
+    pa_cache_write_kernel<true, kU><<<grid_for(need, num_sms, g_occ[1]), 256, 0, stream>>>(p);
+  else
+    pa_cache_write_kernel<false, kU><<<grid_for(need, num_sms, g_occ[0]), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,7 @@ int device_state(DeviceState** out, int* dev_out) {
       return cuda_fail(e, "cudaFuncSetAttribute(split tcgen05)");
     if ((e = pa::set_mla_smem_limits(s.smem_optin)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(MLA)");
+    pa::init_cache_write_occupancy();
     void* ptr = nullptr;
     if ((e = cudaGetSymbolAddress(&ptr, g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
@@ -956,10 +957,7 @@ static int cache_write_impl(const pa_tensor_t* key, const pa_tensor_t* value, co
     p.vs_stride_slot = vts->stride[2];
   }
   p.err = ds->status;
-  const int64_t work = T * Hkv * (D / 8);
-  const int64_t blocks = (work + 255) / 256;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(blocks, int64_t(ds->num_sms) * 8)));
-  cudaError_t e = pa::launch_cache_write(esz == 1, p, grid, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = pa::launch_cache_write(esz == 1, p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cache write kernel launch");
   return PA_OK;
 }

@@ -103,7 +103,10 @@ struct CacheWriteParams {
   int64_t vs_stride_page, vs_stride_head, vs_stride_slot;
 };
 
-cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int grid, cudaStream_t stream);
+// Grid sized to one wave of resident blocks on num_sms SMs (occupancy taken
+// once by init_cache_write_occupancy, outside any stream capture).
+cudaError_t launch_cache_write(bool fp8, const CacheWriteParams& p, int num_sms, cudaStream_t stream);
+void init_cache_write_occupancy();
 
 // Launchers (one translation unit per cache dtype).  `pdl` requests
 // programmatic dependent launch for the merge kernel.

@@ -29,7 +29,9 @@ def _lib(cuda_lib):
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
-@pytest.mark.parametrize("T,Hkv,D,NB", [(1, 1, 64, 2), (37, 2, 128, 9), (1000, 8, 128, 80), (513, 8, 64, 40)])
+@pytest.mark.parametrize("T,Hkv,D,NB", [(1, 1, 64, 2), (37, 2, 128, 9), (1000, 8, 128, 80), (513, 8, 64, 40),
+                                        (77, 3, 16, 6), (150, 3, 96, 12), (45, 3, 512, 4),
+                                        (16384, 8, 128, 1088)])   # the benchmarked chunk: several trips
 def test_cache_write_bit_exact(kv, T, Hkv, D, NB):
     g = torch.Generator(device="cuda").manual_seed(T + Hkv + D)
     scale = 4.0 if kv == "fp8" else 1.0

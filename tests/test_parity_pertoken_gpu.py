@@ -144,7 +144,11 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("T,Hkv,D,NB", [(1, 1, 64, 2), (37, 2, 128, 9), (1000, 8, 128, 80), (513, 8, 64, 40)])
+# head dims whose rows fill a power-of-two lane group (64, 128, 256), leave lanes
+# of the group idle (16 -> two lanes, 96 -> 12 of 16) or give a lane two chunks (512)
+@pytest.mark.parametrize("T,Hkv,D,NB", [(1, 1, 64, 2), (37, 2, 128, 9), (1000, 8, 128, 80), (513, 8, 64, 40),
+                                        (77, 3, 16, 6), (150, 3, 96, 12), (61, 2, 256, 5), (45, 3, 512, 4),
+                                        (16384, 8, 128, 1088)])   # the benchmarked chunk: several trips
 def test_per_token_cache_write_bit_exact(T, Hkv, D, NB):
     g = torch.Generator(device="cuda").manual_seed(T * 7 + D)
     mag = torch.exp(torch.randn(T, Hkv, 1, device="cuda", generator=g) * 3)
