@@ -105,3 +105,51 @@ def test_write_then_decode_matches_oracle(kv):
     tol = 2e-2 if fp8 else 1e-2
     assert np.abs(out.float().cpu().numpy() - ref_out).max() <= tol
     assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 1e-3
+
+
+def _padded_rows(T, Hkv, D, g, scale):
+    """bf16 [T, Hkv, D] as a view of wider rows: padded head and token strides,
+    a 16-byte offset."""
+    big = (torch.randn(T, Hkv + 1, D + 24, device="cuda", generator=g) * scale).to(torch.bfloat16)
+    return big[:, 1:, 8:8 + D]
+
+
+def _padded_cache(NB, Hkv, D, kv, g):
+    """A cache [NB, 16, Hkv, D] as a view of rows 32 elements wider (16 before,
+    16 after), filled with random bytes that must survive the write."""
+    if kv == "fp8":
+        big = torch.randint(0, 256, (NB, 16, Hkv, D + 32), dtype=torch.uint8, device="cuda", generator=g)
+    else:
+        big = torch.randn(NB, 16, Hkv, D + 32, device="cuda", generator=g).to(torch.bfloat16)
+    return big, big[..., 16:16 + D]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("D", [64, 96])
+def test_padded_strides_then_all_padding_slots(kv, D):
+    T, Hkv, NB = 300, 3, 24
+    g = torch.Generator(device="cuda").manual_seed(D + (kv == "fp8"))
+    key = _padded_rows(T, Hkv, D, g, 4.0)
+    val = _padded_rows(T, Hkv, D, g, 4.0)
+    kbig, kc = _padded_cache(NB, Hkv, D, kv, g)
+    vbig, vc = _padded_cache(NB, Hkv, D, kv, g)
+    rng = np.random.default_rng(D)
+    slots = rng.permutation(NB * 16)[:T].astype(np.int32)
+    slots[rng.random(T) < 0.2] = -1
+    kb0, vb0 = _host_cache(kbig), _host_cache(vbig)
+    binding.paged_attn_cache_write(key, val, torch.from_numpy(slots).cuda(), kc, vc, 0.05, 0.07)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    ek, ev = oracle.cache_write(_bits(key), _bits(val), slots, kb0[..., 16:16 + D], vb0[..., 16:16 + D], 0.05, 0.07,
+                                kv)
+    for got, before, e in ((kbig, kb0, ek), (vbig, vb0, ev)):
+        expect = before.copy()
+        expect[..., 16:16 + D] = e
+        assert np.array_equal(_host_cache(got), expect)          # the padding columns are untouched
+    # every slot padding: nothing is written
+    kb1, vb1 = _host_cache(kbig), _host_cache(vbig)
+    binding.paged_attn_cache_write(key, val, torch.full((T,), -1, dtype=torch.int32, device="cuda"), kc, vc,
+                                   0.05, 0.07)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    assert np.array_equal(_host_cache(kbig), kb1) and np.array_equal(_host_cache(vbig), vb1)

@@ -221,3 +221,36 @@ def test_write_then_decode_per_token():
                                                                      v_token_scales=w.v_token_scales))
     torch.cuda.synchronize()
     assert np.abs(out.float().cpu().numpy() - ref_bf16[0]).max() < 0.25   # e4m3 keeps ~2 significant digits
+
+
+@pytest.mark.parametrize("D", [96, 128])
+def test_per_token_cache_write_padded_strides_and_second_chunk_maxima(D):
+    """Key/value rows and caches as views with padded strides; the row maxima
+    sit in a lane's later chunks (the reduction must cover every chunk a lane
+    holds, not only its first)."""
+    T, Hkv, NB = 200, 3, 16
+    g = torch.Generator(device="cuda").manual_seed(D)
+    bigk = torch.randn(T, Hkv + 1, D + 24, device="cuda", generator=g).to(torch.bfloat16)
+    bigv = torch.randn(T, Hkv + 1, D + 24, device="cuda", generator=g).to(torch.bfloat16)
+    key, val = bigk[:, 1:, 8:8 + D], bigv[:, 1:, 8:8 + D]
+    key[:, :, D - 3] = 50.0                  # the last chunk holds each key row's max
+    val[:, :, D // 2 + 1] = -70.0            # a middle chunk holds each value row's max (negative)
+    kbig = torch.randint(0, 256, (NB, 16, Hkv, D + 32), dtype=torch.uint8, device="cuda", generator=g)
+    vbig = torch.randint(0, 256, (NB, 16, Hkv, D + 32), dtype=torch.uint8, device="cuda", generator=g)
+    kc, vc = kbig[..., 16:16 + D], vbig[..., 16:16 + D]
+    ks = torch.rand(NB, Hkv, 16, device="cuda", generator=g)
+    vs = torch.rand(NB, Hkv, 16, device="cuda", generator=g)
+    slots = np.random.default_rng(D).permutation(NB * 16)[:T].astype(np.int32)
+    kb0, vb0 = kbig.cpu().numpy(), vbig.cpu().numpy()
+    host = [kb0[..., 16:16 + D], vb0[..., 16:16 + D], ks.cpu().numpy(), vs.cpu().numpy()]
+    binding.paged_attn_cache_write_per_token(key, val, torch.from_numpy(slots).cuda(), kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    ek, ev, eks, evs = oracle.cache_write_per_token(_bits(key), _bits(val), slots, *host)
+    for got, before, e in ((kbig, kb0, ek), (vbig, vb0, ev)):
+        expect = before.copy()
+        expect[..., 16:16 + D] = e
+        assert np.array_equal(got.cpu().numpy(), expect)
+    assert np.array_equal(ks.cpu().numpy(), eks) and np.array_equal(vs.cpu().numpy(), evs)
+    written = eks[slots // 16, :, slots % 16]
+    assert np.allclose(written, np.float32(50.0) / np.float32(448.0))   # the planted maxima decided the scales
