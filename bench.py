@@ -121,12 +121,16 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
-def cpu_oracle_sample(config: str, budget_s: float = 15.0, threads: int = 1, impl: str = "c"):
-    """Time a float64 oracle on a bounded sample of the workload (whole
-    sequences, added until ~budget_s of oracle time) in a child process.
-    impl "c": the plain-C oracle with ``threads`` OpenMP threads (0 = all host
-    cores); impl "numpy": the NumPy oracle, single-threaded BLAS.  Returns
-    (GB/s of KV processed, threads used, sample text)."""
+def cpu_oracle_steps(config: str, budgets, threads: int = 1, impl: str = "c"):
+    """Time a float64 oracle on bounded samples of the workload, one sample per
+    entry of ``budgets`` (seconds of oracle time; whole sequences are added until
+    the budget is spent, at least one per sample), all in one child process.
+    Sequences are taken in a fixed random order of the workload's length mix and
+    each sample continues where the previous one stopped (cycling); a sequence's
+    synthetic contents are generated once and reused.  impl "c": the plain-C
+    oracle with ``threads`` OpenMP threads (0 = all host cores); impl "numpy": the
+    NumPy oracle, single-threaded BLAS.  Returns (list of per-sample dicts with
+    gbs / seqs / tokens / seconds, threads used, description)."""
     code = f"""
 import json, os, sys, time
 sys.path.insert(0, {ROOT!r})
@@ -141,42 +145,50 @@ sl, ql, qsl, bt, pool = wl.draw_metadata(spec, rng)
 order = np.random.default_rng(123).permutation(spec.num_seqs)
 impl, threads = {impl!r}, {threads}
 used = c_oracle.max_threads() if (impl == "c" and threads <= 0) else (threads if impl == "c" else 1)
-budget = {budget_s}
-done_bytes = 0; t_used = 0.0; nseq = 0; ntok = 0
-seq_iter = (int(i) for _ in range(1000) for i in order)
-for i in seq_iter:
+cache, cached_bytes = {{}}, 0
+
+def sequence(k):
+    # the k-th sequence of the order, in a private pool holding only its pages
+    # (same shapes and value distribution as the workload)
+    global cached_bytes
+    if k in cache:
+        return cache[k]
+    i = int(order[k % len(order)])
     L = int(sl[i]); q = int(ql[i]); n = (L + 15) // 16
     if mla:
         sub = wl.custom_mla_spec(num_q_heads=spec.num_q_heads, kv_dtype=spec.kv_dtype, seq_lens=(L,),
                                  query_len_choices=(q,), pool_pages=n, kv_scale=spec.kv_scale,
-                                 fp8_source_scale=spec.fp8_source_scale, seed=nseq)
+                                 fp8_source_scale=spec.fp8_source_scale, seed=k)
         w = wl.make_mla_workload(sub)
-        t0 = time.perf_counter()
-        if impl == "c":
-            c_oracle.run_mla_workload(w, threads=used)
-        else:
-            oracle.run_mla_workload(w)
-        t_used += time.perf_counter() - t0
-        done_bytes += w.kv_bytes(); nseq += 1; ntok += L
-        if t_used >= budget:
-            break
-        continue
-    # a private pool holding only this sequence's pages (same shapes and value distribution)
-    sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
-                         kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
-                         k_scale=spec.k_scale, v_scale=spec.v_scale, fp8_source_scale=spec.fp8_source_scale,
-                         seed=nseq, token_scale_range=spec.token_scale_range)
-    w = wl.make_workload(sub)
-    t0 = time.perf_counter()
-    if impl == "c":
-        c_oracle.run_workload(w, threads=used)
     else:
-        oracle.run_workload(w)
-    t_used += time.perf_counter() - t0
-    done_bytes += w.kv_bytes(); nseq += 1; ntok += L
-    if t_used >= budget:
-        break
-print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": ntok, "seconds": t_used, "threads": used}}))
+        sub = wl.custom_spec(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                             kv_dtype=spec.kv_dtype, seq_lens=(L,), query_len_choices=(q,), pool_pages=n,
+                             k_scale=spec.k_scale, v_scale=spec.v_scale, fp8_source_scale=spec.fp8_source_scale,
+                             seed=k, token_scale_range=spec.token_scale_range)
+        w = wl.make_workload(sub)
+    if cached_bytes + w.kv_bytes() <= (2 << 30):
+        cache[k] = (w, L)
+        cached_bytes += w.kv_bytes()
+    return w, L
+
+def run(w):
+    if mla:
+        c_oracle.run_mla_workload(w, threads=used) if impl == "c" else oracle.run_mla_workload(w)
+    else:
+        c_oracle.run_workload(w, threads=used) if impl == "c" else oracle.run_workload(w)
+
+k = 0
+out = []
+for budget in {list(budgets)!r}:
+    done_bytes = 0; t_used = 0.0; nseq = 0; ntok = 0
+    while nseq == 0 or t_used < budget:
+        w, L = sequence(k % len(order))
+        t0 = time.perf_counter()
+        run(w)
+        t_used += time.perf_counter() - t0
+        done_bytes += w.kv_bytes(); nseq += 1; ntok += L; k += 1
+    out.append({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": ntok, "seconds": t_used}})
+print(json.dumps({{"steps": out, "threads": used}}))
 """
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -184,15 +196,24 @@ print(json.dumps({{"gbs": done_bytes / t_used / 1e9, "seqs": nseq, "tokens": nto
     if impl == "numpy":
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             env[k] = "1"
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=600 + 3 * sum(budgets))
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
     what = (f"plain-C float64 oracle, {d['threads']} OpenMP thread(s)" if impl == "c"
             else "float64 NumPy oracle, single-threaded BLAS")
+    return d["steps"], d["threads"], what
+
+
+def cpu_oracle_sample(config: str, budget_s: float = 15.0, threads: int = 1, impl: str = "c"):
+    """One bounded sample (``cpu_oracle_steps`` with one budget).  Returns (GB/s
+    of KV processed, threads used, sample text)."""
+    steps, used, what = cpu_oracle_steps(config, [budget_s], threads, impl)
+    d = steps[0]
     sample = (f"{what}, {d['seqs']} whole sequences ({d['tokens']} cached tokens) drawn from the {config} "
               f"workload's length mix, {d['seconds']:.1f} s of oracle time")
-    return d["gbs"], d["threads"], sample
+    return d["gbs"], used, sample
 
 
 def cpu_baseline(config: str, budget_s: float):
@@ -367,14 +388,16 @@ def _packed_e2e(base, works, out, lse, dev, call, args):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    vals = []
-    sample = ""
-    cores = 1
-    for _ in range(max(1, args.warmup)):
-        cpu_oracle_sample(args.config, budget_s=1.0, threads=0, impl="c")
-    for _ in range(args.steps):
-        gbs, cores, sample = cpu_oracle_sample(args.config, budget_s=args.ref_budget, threads=0, impl="c")
-        vals.append(gbs)
+    # every step one bounded sample, the whole run about --ref-total seconds of
+    # oracle time (at most --ref-budget a step, at least one whole sequence)
+    per_step = min(args.ref_budget, max(0.02, args.ref_total / (args.steps + args.warmup)))
+    steps, cores, what = cpu_oracle_steps(args.config, [per_step] * (args.warmup + args.steps), threads=0, impl="c")
+    timed = steps[args.warmup:]
+    vals = [d["gbs"] for d in timed]
+    sample = (f"{what}; {args.steps} timed samples after {args.warmup} warm-up ones, each about {per_step:.2f} s "
+              f"of oracle time over whole sequences drawn from the {args.config} workload's length mix "
+              f"(median {statistics.median([d['seqs'] for d in timed]):.0f} sequences, "
+              f"{sum(d['tokens'] for d in timed)} cached tokens in all); value = median GB/s")
     from paged_kv_decode_06_gb300 import workloads as wl
     import numpy as np
     mla = args.config in wl.MLA_CONFIGS
@@ -783,7 +806,9 @@ def main():
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
     ap.add_argument("--per-token", action="store_true", help="cache_write: fp8 with one scale per row")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--ref-budget", type=float, default=8.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="reference arm: most oracle seconds a step")
+    ap.add_argument("--ref-total", type=float, default=120.0,
+                    help="reference arm: oracle seconds of the whole run (split over warm-up and timed steps)")
     args = ap.parse_args()
     world, rank, local = _dist_env()
     if args.impl == "reference":
