@@ -446,7 +446,7 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
-  Plan pl;
+  Plan pl{};
   if ((st = make_plan(static_cast<int>(B), static_cast<int>(Hq), static_cast<int>(Hkv), static_cast<int>(D),
                       kc->dtype, max_qlen, opts, ds->num_sms, ds->smem_optin, &pl)) != PA_OK)
     return st;
@@ -738,7 +738,7 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
-  MlaPlan pl;
+  MlaPlan pl{};
   if ((st = make_mla_plan(static_cast<int>(std::min<int64_t>(B, kMaxSeqs + 1)), static_cast<int>(Hq), kc->dtype,
                           max_qlen, opts, ds->num_sms, ds->smem_optin, &pl)) != PA_OK)
     return st;
@@ -992,7 +992,7 @@ int paged_attn_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
-  Plan pl;
+  Plan pl{};
   if ((st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, opts, ds->num_sms,
                       ds->smem_optin, &pl)) != PA_OK)
     return st;
@@ -1028,7 +1028,7 @@ int paged_attn_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_hea
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
-  Plan pl;
+  Plan pl{};
   if ((st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype, max_query_len, nullptr, ds->num_sms,
                       ds->smem_optin, &pl)) != PA_OK)
     return st;
@@ -1061,7 +1061,7 @@ int paged_attn_mla_plan(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype,
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
-  MlaPlan pl;
+  MlaPlan pl{};
   if ((st = make_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len, opts, ds->num_sms, ds->smem_optin, &pl)) !=
       PA_OK)
     return st;
@@ -1096,7 +1096,7 @@ int paged_attn_mla_reserve(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dty
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != PA_OK) return st;
-  MlaPlan pl;
+  MlaPlan pl{};
   if ((st = make_mla_plan(num_seqs, num_q_heads, kv_dtype, max_query_len, nullptr, ds->num_sms, ds->smem_optin,
                           &pl)) != PA_OK)
     return st;
