@@ -206,8 +206,12 @@ int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_
  *                   nothing; an entry >= 16 * NB writes nothing and sets bit 0 of the
  *                   device status word.  Two tokens with the same slot: which one
  *                   lands is unspecified.
- *   k_cache, v_cache bf16 or fp8e4m3 [NB, 16, Hkv, D], same rules as for
- *                   paged_attn_decode.
+ *   k_cache, v_cache bf16 or fp8e4m3 [NB, 16, Hkv, D]: stride[3] == 1, other
+ *                   strides multiples of 16 bytes, data 16-byte aligned.  D is any
+ *                   multiple of 8 up to 512 (of 16 for fp8 caches, by the stride
+ *                   rule), Hkv at most 4096, T at most 2^30, NB below 2^31
+ *                   (else PA_ERR_UNSUPPORTED).  The decode entry points read
+ *                   D = 64 and 128.
  *   k_scale, v_scale fp8 caches only: the stored code is e4m3fn(x * r) with
  *                   r = 1.0f / scale rounded once to fp32; round to nearest even,
  *                   finite magnitudes above 448 and infinities saturate to +-448.
