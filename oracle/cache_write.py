@@ -6,25 +6,24 @@ and FP8 KV cache write; model-operations guide, token_layout/slots.py:
 with slot s = slot_mapping[t] >= 0 stores its key and value rows of every KV
 head at physical page s // 16, slot s % 16 of the caches; tokens with a
 negative slot (padding) write nothing.  bf16 caches take the bf16 rows
-unchanged; fp8 caches take e4m3fn codes of ``float32(x) * r`` with
-``r = float32(1) / float32(scale)`` (one fp32 scale per tensor, its reciprocal
-rounded once to fp32).
+unchanged; fp8 caches take e4m3fn codes of ``float32(x) / float32(scale)``,
+one IEEE fp32 division by the tensor's one fp32 scale: a cached value is
+read back as code * scale, so the code is the value divided by the scale.
 
 Per-token quantisation (the pages' ``reshape_and_cache_with_pertoken_quant``,
 FP8 KV cache write of MHA layers): every written (token, KV head) row gets its
-own scale.  Readings adopted: the row's scale is ``float32(amax) / 448`` with
-``amax = max_d |x_d|`` (448 = the largest finite e4m3fn magnitude), one IEEE
-fp32 division; the codes are ``e4m3fn(float32(x) * r)`` with
-``r = float32(448) / float32(amax)`` (one fp32 division, so the largest element
-lands on +-448 up to one rounding); an all-zero row stores scale 0 and zero
-codes.  Scales are stored ``[num_pages, num_kv_heads, 16]`` float32.
+own scale.  Readings adopted: the row's scale is ``s = float32(amax) / 448``
+with ``amax = max_d |x_d|`` (448 = the largest finite e4m3fn magnitude), one
+IEEE fp32 division; the codes are ``e4m3fn(float32(x) / s)``, again one IEEE
+fp32 division by the stored scale (a row is read back as code * s, the same
+rule as the per-tensor write), so the largest element lands on +-448 up to one
+rounding; an all-zero row stores scale 0 and zero codes.  Scales are stored
+``[num_pages, num_kv_heads, 16]`` float32.
 
-Readings adopted where the pages are silent: the scale is applied as one fp32
-multiplication by its fp32 reciprocal (it differs from an IEEE division only
-when x / scale falls within one fp32 ulp of an e4m3 rounding boundary); the
-e4m3fn encoding rounds to nearest, ties to even, and saturates finite
-magnitudes above 448 (and infinities) to +-448 (the "satfinite" convention);
-a slot at or past the end of the pool is an error and writes nothing.
+Readings adopted where the pages are silent: the e4m3fn encoding rounds to
+nearest, ties to even, and saturates finite magnitudes above 448 (and
+infinities) to +-448 (the "satfinite" convention); a slot at or past the end
+of the pool is an error and writes nothing.
 """
 from __future__ import annotations
 
@@ -58,10 +57,10 @@ def e4m3fn_encode(x: np.ndarray) -> np.ndarray:
 
 
 def quantize_rows(bits: np.ndarray, scale: float) -> np.ndarray:
-    """bf16 rows -> e4m3fn codes of float32(x) * (float32(1) / float32(scale))."""
+    """bf16 rows -> e4m3fn codes of float32(x) / float32(scale) (IEEE fp32 division)."""
     x32 = bf16_bits_to_float64(bits).astype(np.float32)
-    r32 = np.float32(1.0) / np.float32(scale)
-    y32 = x32 * r32
+    with np.errstate(over="ignore"):           # a quotient past the fp32 range saturates below
+        y32 = x32 / np.float32(scale)
     return e4m3fn_encode(y32.astype(np.float64))
 
 
@@ -95,15 +94,14 @@ def quantize_rows_per_token(bits: np.ndarray):
     """bf16 rows [..., D] -> (e4m3fn codes [..., D], float32 scales [...]).
 
     amax = max_d |x_d|; scale = float32(amax) / float32(448);
-    codes = e4m3fn(float32(x) * (float32(448) / float32(amax))), or zeros with
+    codes = e4m3fn(float32(x) / scale) (IEEE fp32 division), or zeros with
     scale 0 when amax == 0."""
     x32 = bf16_bits_to_float64(bits).astype(np.float32)
     amax = np.abs(x32).max(axis=-1)
     scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
-    with np.errstate(divide="ignore"):
-        r = np.where(amax > 0, np.float32(E4M3_MAX) / np.where(amax > 0, amax, np.float32(1)), np.float32(0))
-    y32 = (x32 * r.astype(np.float32)[..., None]).astype(np.float32)
-    return e4m3fn_encode(y32.astype(np.float64)), scale
+    nonzero = scale > 0
+    y32 = np.where(nonzero[..., None], x32 / np.where(nonzero, scale, np.float32(1))[..., None], np.float32(0))
+    return e4m3fn_encode(y32.astype(np.float32).astype(np.float64)), scale
 
 
 def cache_write_per_token(key_bits, value_bits, slot_mapping, k_cache, v_cache, k_scales, v_scales):

@@ -40,15 +40,34 @@ def test_saturation_and_special_points(x, code):
     assert oracle.e4m3fn_encode(np.array([x]))[0] == code
 
 
-def test_quantize_multiplies_by_the_fp32_reciprocal():
+def _torch_quantize(x_bf16, scale):
+    """torch's own fp32 division and e4m3fn cast (NaN for quotients past 448
+    in torch, so callers keep inside the finite range)."""
+    return (x_bf16.float() / torch.tensor(scale, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_quantize_divides_by_the_scale():
     bits = torch.tensor([0.3, -7.5, 15.0, 0.0123]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle.quantize_rows(bits, 0.05)
-    r = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(0.05, dtype=torch.float32)
-    y = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float() * r
-    assert np.array_equal(got, y.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    assert np.array_equal(got, _torch_quantize(x, 0.05))
     # 100 / 0.05 = 2000 is beyond the e4m3fn range: saturates (torch's cast would give NaN)
     big = torch.tensor([100.0, -100.0]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert oracle.quantize_rows(big, 0.05).tolist() == [0x7E, 0xFE]
+
+
+def test_quantize_is_a_division_not_a_reciprocal_product():
+    # x = 0.000732421875 * 2^k (exact in bf16) over the fp32 scale 0.03: the
+    # quotient lands exactly on a midpoint of the e4m3fn grid (0.0244140625 =
+    # 2^-6 * (1 + 4.5/8) for k = 0) and rounds to the even code, while x times
+    # the fp32 reciprocal of 0.03 lands one fp32 ulp above it and rounds up
+    x = torch.tensor([0.000732421875 * 2.0 ** k for k in range(4)] + [-0.00146484375]).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    got = oracle.quantize_rows(bits, 0.03)
+    expect = _torch_quantize(x, 0.03)
+    assert np.array_equal(got, expect)
+    recip = (x.float() * (torch.tensor(1.0) / torch.tensor(0.03))).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (expect != recip).all()                                  # the case tells the two forms apart
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
@@ -72,11 +91,8 @@ def test_scatter_against_page_offset_arithmetic(kv_dtype):
         if kv_dtype == "bf16":
             flat_k[slots[t]], flat_v[slots[t]] = kb[t], vb[t]
         else:
-            rk = torch.tensor(1.0) / torch.tensor(0.05)
-            rv = torch.tensor(1.0) / torch.tensor(0.07)
-            kq = (torch.from_numpy(kb[t].view(np.int16)).view(torch.bfloat16).float() * rk).to(torch.float8_e4m3fn)
-            vq = (torch.from_numpy(vb[t].view(np.int16)).view(torch.bfloat16).float() * rv).to(torch.float8_e4m3fn)
-            flat_k[slots[t]], flat_v[slots[t]] = kq.view(torch.uint8).numpy(), vq.view(torch.uint8).numpy()
+            flat_k[slots[t]] = _torch_quantize(torch.from_numpy(kb[t].view(np.int16)).view(torch.bfloat16), 0.05)
+            flat_v[slots[t]] = _torch_quantize(torch.from_numpy(vb[t].view(np.int16)).view(torch.bfloat16), 0.07)
     assert np.array_equal(k2, flat_k.reshape(kc.shape)) and np.array_equal(v2, flat_v.reshape(vc.shape))
 
 
@@ -101,10 +117,25 @@ def test_per_token_quantize_matches_torch_ops():
     xt = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float()
     amax = xt.abs().amax(dim=-1)
     ref_scale = amax / 448.0
-    r = torch.tensor(448.0) / amax
-    ref_codes = (xt * r[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref_codes = (xt / ref_scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(scales, ref_scale.numpy())
     assert np.array_equal(codes, ref_codes)
+
+
+def test_per_token_codes_divide_by_the_stored_scale():
+    # a row with max |x| = 0.78515625 (bf16 0x3F49): x = 1.1980533599853516e-05
+    # over its scale 0.78515625 / 448 (fp32) is 0.0068359375, a midpoint of the
+    # e4m3fn grid (7 * 2^-10, between the subnormal codes 3 and 4) that rounds to
+    # the even code; x times the fp32 reciprocal 448 / 0.78515625 lands one fp32
+    # ulp below it and rounds down instead
+    x = torch.tensor([[0.78515625, 1.1980533599853516e-05, -1.1980533599853516e-05, 0.5]]).to(torch.bfloat16)
+    codes, scales = oracle.quantize_rows_per_token(_bf16_bits(x.float()))
+    s = x.float().abs().amax(dim=-1) / 448.0
+    expect = (x.float() / s[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, expect) and scales[0] == s.item()
+    recip = (x.float() * (torch.tensor(448.0) / x.float().abs().amax(dim=-1))[..., None])
+    recip = recip.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (expect[0, 1:3] != recip[0, 1:3]).all()                 # the case tells the two forms apart
 
 
 def test_per_token_row_max_lands_on_the_top_code():
@@ -163,7 +194,7 @@ def test_per_token_scatter_against_page_offset_arithmetic():
             xv = torch.from_numpy(vb[t, h].view(np.int16)).view(torch.bfloat16).float()
             for x, fc, fs in ((xk, fk, fks), (xv, fv, fvs)):
                 amax = x.abs().max()
-                fc[slots[t], h] = (x * (torch.tensor(448.0) / amax)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                fc[slots[t], h] = (x / (amax / 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
                 fs[slots[t], h] = (amax / 448.0).item()
     assert np.array_equal(k2, fk.reshape(kc.shape)) and np.array_equal(v2, fv.reshape(vc.shape))
     assert np.array_equal(ks2, fks.reshape(NB, 16, Hkv).transpose(0, 2, 1))
@@ -183,7 +214,8 @@ _real_cw = _il.import_module("oracle.cache_write")   # the module (the package r
 _CW_MUTANTS = {
     "ties_away_from_zero": ("(d_lo == d_hi) & (lo % 2 == 0)", "(d_lo == d_hi) & False"),
     "no_saturation": ("np.minimum(a, _VALUES[-1])", "np.minimum(a, _VALUES[-2])"),
-    "multiply_by_scale": ("y32 = x32 * r32", "y32 = x32 * np.float32(scale)"),
+    "multiply_by_scale": ("y32 = x32 / np.float32(scale)", "y32 = x32 * np.float32(scale)"),
+    "multiply_by_reciprocal": ("y32 = x32 / np.float32(scale)", "y32 = x32 * (np.float32(1) / np.float32(scale))"),
     "slot_offset_swapped": ("page, off = int(s) // PAGE_SIZE, int(s) % PAGE_SIZE",
                             "off, page = int(s) // PAGE_SIZE, int(s) % PAGE_SIZE"),
     "sign_dropped": ("code = np.where(np.signbit(x), code | 0x80, code)", "code = np.where(np.signbit(x), code, code)"),
@@ -194,8 +226,10 @@ _CW_MUTANTS = {
     "pt_scale_inverted": ("scale = (amax / np.float32(E4M3_MAX))", "scale = (np.float32(E4M3_MAX) / amax)"),
     "pt_scale_slot_head_swapped": ("ks_out[page, :, off], vs_out[page, :, off] = ksc, vsc",
                                    "ks_out[page, off % ks_out.shape[1], :ksc.shape[0]], vs_out[page, off % vs_out.shape[1], :vsc.shape[0]] = ksc, vsc"),
-    "pt_reciprocal_of_scale": ("np.float32(E4M3_MAX) / np.where(amax > 0, amax, np.float32(1))",
-                               "np.float32(1) / (np.where(amax > 0, amax, np.float32(1)) / np.float32(E4M3_MAX))"),
+    "pt_multiply_by_reciprocal": ("x32 / np.where(nonzero, scale, np.float32(1))[..., None]",
+                                  "x32 * (np.float32(E4M3_MAX) / np.where(nonzero, amax, np.float32(1)))[..., None]"),
+    "pt_multiply_by_scale": ("x32 / np.where(nonzero, scale, np.float32(1))[..., None]",
+                             "x32 * np.where(nonzero, scale, np.float32(1))[..., None]"),
 }
 
 
@@ -216,11 +250,13 @@ def test_cache_write_pins_catch_mutant(name):
                                          e4m3fn_to_float64=oracle.e4m3fn_to_float64,
                                          bf16_bits_to_float64=oracle.bf16_bits_to_float64)
     calls = [(pins.test_encoder_matches_torch_inside_the_finite_range, ()), (pins.test_every_grid_value_and_midpoint, ()),
-             (pins.test_quantize_multiplies_by_the_fp32_reciprocal, ()), (pins.test_out_of_range_slots_write_nothing, ())]
+             (pins.test_quantize_divides_by_the_scale, ()), (pins.test_quantize_is_a_division_not_a_reciprocal_product, ()),
+             (pins.test_out_of_range_slots_write_nothing, ())]
     calls += [(pins.test_saturation_and_special_points, args) for args in
               [(448.0, 0x7E), (1e30, 0x7E), (-500.0, 0xFE), (-0.0, 0x80)]]
     calls += [(pins.test_scatter_against_page_offset_arithmetic, (k,)) for k in ("bf16", "fp8")]
     calls += [(pins.test_per_token_quantize_matches_torch_ops, ()), (pins.test_per_token_row_max_lands_on_the_top_code, ()),
+              (pins.test_per_token_codes_divide_by_the_stored_scale, ()),
               (pins.test_per_token_zero_row_and_power_of_two_rows, ()), (pins.test_per_token_round_trip_error_bound, ()),
               (pins.test_per_token_scatter_against_page_offset_arithmetic, ())]
     caught = 0
