@@ -17,7 +17,8 @@ with ``amax = max_d |x_d|`` (448 = the largest finite e4m3fn magnitude), one
 IEEE fp32 division; the codes are ``e4m3fn(float32(x) / s)``, again one IEEE
 fp32 division by the stored scale (a row is read back as code * s, the same
 rule as the per-tensor write), so the largest element lands on +-448 up to one
-rounding; an all-zero row stores scale 0 and zero codes.  Scales are stored
+rounding; an all-zero row stores scale 0 and the code 0x00 throughout (its
+-0 elements too: x / 0 has no value to take a sign from).  Scales are stored
 ``[num_pages, num_kv_heads, 16]`` float32.
 
 Readings adopted where the pages are silent: the e4m3fn encoding rounds to

@@ -148,7 +148,7 @@ def test_per_token_row_max_lands_on_the_top_code():
 
 
 def test_per_token_zero_row_and_power_of_two_rows():
-    zero = np.zeros((1, 8), dtype=np.uint16)
+    zero = np.array([[0, 0x8000] * 4], dtype=np.uint16)          # +0 and -0
     codes, scales = oracle.quantize_rows_per_token(zero)
     assert scales[0] == 0.0 and not codes.any()
     rng = np.random.default_rng(9)
