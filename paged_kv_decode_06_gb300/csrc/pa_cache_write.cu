@@ -2,8 +2,8 @@
 // and FP8 KV cache writes; token_layout/slots.py: slot_mapping): every new token
 // with slot s >= 0 stores its key and value rows of all KV heads at page s / 16,
 // slot s % 16 of the paged caches.  bf16 caches take the rows as they are; fp8
-// caches take e4m3fn codes of x * (1 / scale) (the reciprocal rounded once to
-// fp32 on the host; round to nearest even, saturating to +-448).
+// caches take e4m3fn codes of x / scale (a cached value reads back as code *
+// scale): one IEEE fp32 division, round to nearest even, saturating to +-448.
 //
 // One thread moves 8 consecutive features (16 bytes of bf16 input) of one
 // (token, head) row; a grid of one wave of resident blocks strides over all
@@ -19,6 +19,16 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   unsigned short r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Four e4m3fn code pairs of eight bf16 values (one 16-byte chunk) divided by s:
+// every quotient an IEEE round-to-nearest fp32 division.
+__device__ __forceinline__ uint2 e4m3x8_div(const uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t q[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) q[e] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[e]), s), __fdiv_rn(bf16_hi(w[e]), s));
+  return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
 }
 
 // Integer quotient of an index by a per-call divisor: 32-bit when the index
@@ -73,18 +83,8 @@ __global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWritePar
                                  off * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
                                  static_cast<int64_t>(h[u]) * (tensor ? p.vc_stride_head : p.kc_stride_head) + d0[u];
         if constexpr (FP8) {
-          const float r = tensor ? p.v_rscale : p.k_rscale;
-          const uint64_t r2 = f2_pack(r, r);
-          const uint32_t w[4] = {x[u][tensor].x, x[u][tensor].y, x[u][tensor].z, x[u][tensor].w};
-          uint32_t q[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float lo, hi;
-            f2_unpack(fmul2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), r2), lo, hi);
-            q[e] = e4m3x2_from_f32(lo, hi);
-          }
           *reinterpret_cast<uint2*>((tensor ? p.v_cache : p.k_cache) + dst_elem) =
-              make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+              e4m3x8_div(x[u][tensor], tensor ? p.v_scale : p.k_scale);
         } else {
           *reinterpret_cast<uint4*>((tensor ? p.v_cache : p.k_cache) + dst_elem * 2) = x[u][tensor];
         }
@@ -107,9 +107,9 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // row's max |x| is an xor-shuffle reduction inside the group.  For finite bf16
 // values the bit patterns with the sign cleared order like |x|, so the maxima
 // are 16-bit integer maxima (exact), K's and V's carried in one 32-bit word.
-// scale = amax / 448 and r = 448 / amax are IEEE fp32 divisions; codes =
-// e4m3fn(x * r), round to nearest even, saturating; a zero row stores scale 0
-// and zero codes.  The trip test is on the warp's first row, so every lane of a
+// scale = amax / 448 and the codes e4m3fn(x / scale) are IEEE fp32 divisions
+// (round to nearest even, saturating); a zero row stores scale 0 and zero
+// codes.  The trip test is on the warp's first row, so every lane of a
 // warp runs the same trips and the shuffles see full warps.  A trip takes U rows
 // per group, a grid apart, and issues all their loads (K and V) together with
 // the slot lookups.
@@ -170,11 +170,12 @@ __global__ void __launch_bounds__(256) pa_cache_write_tok_kernel(const CacheWrit
       }
       const int64_t page = slot[u] / kPage;
       const int64_t off = slot[u] - page * kPage;
-      const float amax[2] = {__uint_as_float(m[u] << 16), __uint_as_float(m[u] & 0xFFFF0000u)};
+      // every lane of the group forms the row's two scales (the same IEEE
+      // quotients), so no broadcast is needed; an all-zero row's scale is 0
+      const float sc[2] = {__fdiv_rn(__uint_as_float(m[u] << 16), 448.f),
+                           __fdiv_rn(__uint_as_float(m[u] & 0xFFFF0000u), 448.f)};
 #pragma unroll
       for (int tensor = 0; tensor < 2; ++tensor) {
-        const float r = amax[tensor] > 0.f ? __fdiv_rn(448.f, amax[tensor]) : 0.f;
-        const uint64_t r2 = f2_pack(r, r);
         uint8_t* row = (tensor ? p.v_cache : p.k_cache) + page * (tensor ? p.vc_stride_page : p.kc_stride_page) +
                        off * (tensor ? p.vc_stride_slot : p.kc_stride_slot) +
                        static_cast<int64_t>(h[u]) * (tensor ? p.vc_stride_head : p.kc_stride_head);
@@ -182,25 +183,18 @@ __global__ void __launch_bounds__(256) pa_cache_write_tok_kernel(const CacheWrit
         for (int k = 0; k < CPL; ++k) {
           const int d0 = (c0 + k * G) * 8;
           if (d0 >= p.head_dim) continue;
-          const uint4 v = x[u][k][tensor];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t q[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float lo, hi;
-            f2_unpack(fmul2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), r2), lo, hi);
-            q[e] = e4m3x2_from_f32(lo, hi);
-          }
-          *reinterpret_cast<uint2*>(row + d0) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+          // an all-zero row (its elements +0 or -0) stores the code 0x00 throughout
+          *reinterpret_cast<uint2*>(row + d0) =
+              sc[tensor] > 0.f ? e4m3x8_div(x[u][k][tensor], sc[tensor]) : make_uint2(0u, 0u);
         }
       }
       // the row's two scales: lane c0 = 0 stores K's and c0 = 1 V's (one lane
-      // both when G = 1), so the division issues once per group
+      // both when G = 1)
       for (int j = c0; j < 2; j += G) {
-        float* sc = j ? p.v_tok : p.k_tok;
-        sc[page * (j ? p.vs_stride_page : p.ks_stride_page) +
-           static_cast<int64_t>(h[u]) * (j ? p.vs_stride_head : p.ks_stride_head) +
-           off * (j ? p.vs_stride_slot : p.ks_stride_slot)] = __fdiv_rn(j ? amax[1] : amax[0], 448.f);
+        float* dst = j ? p.v_tok : p.k_tok;
+        dst[page * (j ? p.vs_stride_page : p.ks_stride_page) +
+            static_cast<int64_t>(h[u]) * (j ? p.vs_stride_head : p.ks_stride_head) +
+            off * (j ? p.vs_stride_slot : p.ks_stride_slot)] = sc[j];
       }
     }
   }

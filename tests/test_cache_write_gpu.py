@@ -153,3 +153,37 @@ def test_padded_strides_then_all_padding_slots(kv, D):
     torch.cuda.synchronize()
     assert binding.paged_attn_device_status(clear=True) == 0
     assert np.array_equal(_host_cache(kbig), kb1) and np.array_equal(_host_cache(vbig), vb1)
+
+
+def test_fp8_writes_divide_by_the_scale():
+    """Inputs whose quotient by the scale sits exactly on a midpoint of the
+    e4m3fn grid, where an fp32 division and a product with the fp32 reciprocal
+    round to different codes; tiny rows whose scale is an fp32 subnormal; rows
+    of +0 and -0."""
+    D = 16
+    # per-tensor, scale 0.03: x = 0.000732421875 * 2^k lands on midpoints
+    row = [0.000732421875 * 2.0 ** k for k in range(4)] + [-0.00146484375, 1.0, -3.0, 0.25]
+    x = torch.tensor([[row * 2]], device="cuda").to(torch.bfloat16)
+    kc = torch.zeros(1, 16, 1, D, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    binding.paged_attn_cache_write(x, x, torch.tensor([7], dtype=torch.int32, device="cuda"), kc, vc, 0.03, 0.03)
+    torch.cuda.synchronize()
+    assert np.array_equal(kc[0, 7].cpu().numpy(), oracle.quantize_rows(_bits(x)[0], 0.03))
+    # per-token: max |x| = 0.78515625 puts 1.1980533599853516e-05 / scale on a midpoint;
+    # a row of max 1e-39 (subnormal in bf16 and fp32); a row of +0 / -0
+    rows = torch.tensor([[0.78515625, 1.1980533599853516e-05, -1.1980533599853516e-05, 0.5] * 4,
+                         [1e-39, -3e-40, 5e-41, 0.0] * 4,
+                         [0.0, -0.0, 0.0, -0.0] * 4], device="cuda").to(torch.bfloat16)[:, None, :]
+    kc = torch.full((1, 16, 1, D), 0x55, dtype=torch.uint8, device="cuda")
+    vc = torch.full_like(kc, 0x55)
+    ks = torch.full((1, 1, 16), 7.0, device="cuda")
+    vs = torch.full_like(ks, 7.0)
+    host = [_host_cache(kc), _host_cache(vc), ks.cpu().numpy(), vs.cpu().numpy()]
+    slots = np.array([2, 9, 12], dtype=np.int32)
+    binding.paged_attn_cache_write_per_token(rows, rows, torch.from_numpy(slots).cuda(), kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    ek, ev, eks, evs = oracle.cache_write_per_token(_bits(rows), _bits(rows), slots, *host)
+    assert np.array_equal(_host_cache(kc), ek) and np.array_equal(_host_cache(vc), ev)
+    assert np.array_equal(ks.cpu().numpy(), eks) and np.array_equal(vs.cpu().numpy(), evs)
+    assert eks[0, 0, 9] > 0 and not ek[0, 12].any()
