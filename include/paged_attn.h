@@ -33,6 +33,11 @@
  *   - Functions return a pa_status (PA_OK = 0); nothing throws across the
  *     ABI.  paged_attn_last_error_message() gives a human-readable detail of
  *     the last failure on the calling thread.
+ *   - The first call of any entry point on a device sets that device up once
+ *     (attributes, kernel limits, the device addresses of the status word and
+ *     of the no-allocation scratch array).  The library keeps that state for
+ *     the life of the process and does not survive cudaDeviceReset: after a
+ *     reset, every later call on that device is undefined.
  */
 #ifndef PAGED_ATTN_H
 #define PAGED_ATTN_H
@@ -105,6 +110,14 @@ typedef struct pa_options_t {
                                   Requires v_token_scales too and an fp8 cache; entries of slots
                                   past a sequence's end may hold anything, even non-finite values */
   const struct pa_tensor_t* v_token_scales;  /* the same for V (value = code * v_scale * scale) */
+  int32_t wait_limit_us;       /* >0: every pipeline wait inside the decode kernels gives up after this
+                                  many microseconds (status bit 3, the kernel returns); 0 = 2 seconds */
+  int32_t test_starve_cta;     /* testing aid for the give-up path, 0 = off.  k > 0: the producer warp
+                                  of split CTA k-1 issues no copies, so that CTA's consumer warps wait
+                                  out wait_limit_us, set status bit 3 and return; the call's results
+                                  are then undefined (the affected rows keep stale partials).  The
+                                  mma.sync split kernel only (PA_ERR_UNSUPPORTED for the tcgen05 and
+                                  MLA kernels) */
 } pa_options_t;
 
 /* Launch plan the library picks for a problem shape (for tests, tuning and
@@ -120,7 +133,8 @@ typedef struct pa_plan_t {
   int32_t merge_rows;        /* rows per merge unit (heads_per_cta * G * max_query_len) */
   int32_t page_pairing;      /* 1 if consumer warps take two pages of a sequence at once */
   int64_t workspace_bytes;   /* split workspace the call needs                          */
-  int32_t variant;           /* 0: mma.sync warps; 1: tcgen05 / tensor-memory kernel; 2: MLA */
+  int32_t variant;           /* 0: mma.sync warps; 1: tcgen05 / tensor-memory kernel; 2: MLA on
+                                mma.sync warps; 3: MLA on tcgen05 / tensor memory           */
   int32_t block_pages;       /* pages a consumer step takes (1, 2 paired, 4 tcgen05)    */
 } pa_plan_t;
 
@@ -177,10 +191,13 @@ int paged_attn_decode_ex(const pa_tensor_t* q, const pa_tensor_t* k_cache, const
  * the library's device code, so the call never calls cudaMalloc/cudaFree or any
  * other allocating routine.  It serves callers whose memory is owned by a pool
  * or allocator they must not bypass, or that run where allocation is not
- * allowed.  Every GPU on which the library's kernels are loaded holds that
- * array until the process exits.
- *   - The first call on a device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ * allowed.
+ *   - The library's per-device set-up (the first call of ANY entry point on a
+ *     device, with that device current) looks up the array's device address,
+ *     which also loads it under CUDA's lazy module loading; from then on that
+ *     GPU holds the 16 MiB until the process exits.  Make one call on each
+ *     device before a memory pool takes the device's free memory, and before
+ *     any stream capture.
  *   - A shape needing more scratch than 16 MiB (see paged_attn_workspace_size)
  *     is rejected with PA_ERR_WORKSPACE before anything is enqueued.
  *   - All calls share the one array and it keeps the last call's contents (no
@@ -212,10 +229,10 @@ int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_
  *                   rule), Hkv at most 4096, T at most 2^30, NB below 2^31
  *                   (else PA_ERR_UNSUPPORTED).  The decode entry points read
  *                   D = 64 and 128.
- *   k_scale, v_scale fp8 caches only: the stored code is e4m3fn(x * r) with
- *                   r = 1.0f / scale rounded once to fp32; round to nearest even,
- *                   finite magnitudes above 448 and infinities saturate to +-448.
- *                   bf16 caches store x unchanged.
+ *   k_scale, v_scale fp8 caches only: the stored code is e4m3fn(x / scale), one
+ *                   IEEE fp32 division (a cached value reads back as code * scale);
+ *                   round to nearest even, finite magnitudes above 448 and
+ *                   infinities saturate to +-448.  bf16 caches store x unchanged.
  *   stream          stream the work is enqueued on.
  *
  * Errors as for paged_attn_decode.  Asynchronous; allocates nothing.
@@ -235,10 +252,10 @@ int paged_attn_cache_write(const pa_tensor_t* key, const pa_tensor_t* value, con
  *   k_token_scales, v_token_scales  f32 [NB, Hkv, 16], any non-negative strides,
  *                   4-byte aligned: entry [page][head][slot] receives the row's scale.
  *   For every written (token, head) row x (bf16, D values): amax = max_d |x_d|;
- *   scale = amax / 448 and r = 448 / amax (IEEE fp32 divisions); code_d =
- *   e4m3fn(x_d * r), round to nearest even, saturating to +-448; an all-zero row
- *   stores scale 0 and zero codes.  Rows must be finite with amax either 0 or at
- *   least 448 / FLT_MAX (else r overflows and the codes are undefined).
+ *   scale = amax / 448 and code_d = e4m3fn(x_d / scale), both IEEE fp32
+ *   divisions (the row reads back as code * scale), round to nearest even,
+ *   saturating to +-448; an all-zero row (+0 or -0 elements) stores scale 0 and
+ *   the code 0x00 throughout.  Rows must be finite.
  *   paged_attn_decode_ex reads such a cache with pa_options_t.k_token_scales /
  *   v_token_scales and k_scale = v_scale = 1.
  *
@@ -283,9 +300,11 @@ int paged_attn_cache_write_per_token(const pa_tensor_t* key, const pa_tensor_t* 
  *   out             bf16 [T, Hq, 512]; stride[2] == 1, other strides multiples of 4.
  *   lse             f32 [T, Hq] or data == NULL.
  *   opts            (the _ex form) num_ctas, min_pages_per_cta, disable_pdl,
- *                   workspace / workspace_bytes and the split events apply; the
- *                   grouped-query options (heads_per_cta, sliding_window, sinks,
- *                   use_tcgen05 = 2, token scales) are rejected with PA_ERR_UNSUPPORTED.
+ *                   workspace / workspace_bytes, wait_limit_us and the split events
+ *                   apply; use_tcgen05 picks the split kernel (0 or 1: the mma.sync
+ *                   kernel, 2: the tensor-memory kernel); the grouped-query
+ *                   options (heads_per_cta, sliding_window, sinks, token scales,
+ *                   test_starve_cta) are rejected with PA_ERR_UNSUPPORTED.
  *
  * Errors, device status bits, workspace and graph-capture rules as for
  * paged_attn_decode (paged_attn_mla_workspace_size gives the workspace a shape needs).

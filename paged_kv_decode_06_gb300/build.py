@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libpagedattn.so")
 SOURCES = ["pa_host.cu", "pa_split_bf16.cu", "pa_split_fp8.cu", "pa_split_fp8_tok.cu", "pa_merge.cu", "pa_static_ws.cu", "pa_cache_write.cu",
-           "pa_split_tc.cu", "pa_mla.cu"]
+           "pa_split_tc.cu", "pa_mla.cu", "pa_mla_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

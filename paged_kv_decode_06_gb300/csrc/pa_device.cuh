@@ -16,7 +16,8 @@ constexpr uint32_t kErrQueryLen = 4u;
 constexpr uint32_t kErrTimeout = 8u;
 constexpr uint32_t kErrF16Range = 16u;
 
-// A pipeline wait gives up after this long (nanoseconds of %globaltimer).
+// A pipeline wait gives up after this long (nanoseconds of %globaltimer)
+// unless the call sets its own limit.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 constexpr int kPage = 16;
@@ -62,14 +63,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// the caller reports kErrTimeout) if it has not completed within
-// kWaitTimeoutNs; never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// the caller reports kErrTimeout) if it has not completed within limit_ns
+// nanoseconds; never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0u && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if ((it & 31u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -33,6 +33,13 @@ constexpr int kMaxRowsMma = 64;      // query rows per KV head of the mma.sync k
 constexpr int kMaxRowsTc = 128;      // ... and of the tensor-memory kernel (bf16 caches)
 constexpr int kTcBlockPages = 4;
 constexpr int kTcThreads = 384;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // pipeline wait limit without wait_limit_us
+
+// Wait limit and starved CTA of a call (pa_options_t.wait_limit_us, test_starve_cta).
+uint64_t wait_limit_ns(const pa_options_t* opts) {
+  return (opts && opts->wait_limit_us > 0) ? static_cast<uint64_t>(opts->wait_limit_us) * 1000ull : kDefaultWaitNs;
+}
+int starved_cta(const pa_options_t* opts) { return (opts && opts->test_starve_cta > 0) ? opts->test_starve_cta - 1 : -1; }
 
 thread_local std::string t_last_error;
 
@@ -97,11 +104,16 @@ int device_state(DeviceState** out, int* dev_out) {
       return cuda_fail(e, "cudaFuncSetAttribute(split tcgen05)");
     if ((e = pa::set_mla_smem_limits(s.smem_optin)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(MLA)");
+    if ((e = pa::set_mla_tc_smem_limits(s.smem_optin)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(MLA, tcgen05)");
     pa::init_cache_write_occupancy();
     void* ptr = nullptr;
     if ((e = cudaGetSymbolAddress(&ptr, g_status_word)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
     s.status = static_cast<uint32_t*>(ptr);
+    // the no-allocation entry point's scratch array: its address (and module)
+    // now, before a caller's pool may take the device's free memory
+    if (pa::static_scratch_setup() != PA_OK) return PA_ERR_CUDA;
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -417,6 +429,8 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
   if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return fail(PA_ERR_INVALID_ARG, "scale, k_scale and v_scale must be finite");
   if (opts && opts->sinks && !aligned(opts->sinks, 4)) return fail(PA_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
+  if (opts && (opts->wait_limit_us < 0 || opts->test_starve_cta < 0))
+    return fail(PA_ERR_INVALID_ARG, "wait_limit_us and test_starve_cta must not be negative");
   const bool tok = has_token_scales(opts);
   if (tok) {
     if (kc->dtype != PA_FP8_E4M3) return fail(PA_ERR_INVALID_ARG, "per-token scales need an fp8 cache");
@@ -511,6 +525,10 @@ int decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor_t* 
     sp.tok_stride_page = opts->k_token_scales->stride[0];
     sp.tok_bytes = pl.tok_bytes;
   }
+  sp.wait_ns = wait_limit_ns(opts);
+  sp.starve_cta = starved_cta(opts);
+  if (sp.starve_cta >= 0 && pl.tc)
+    return fail(PA_ERR_UNSUPPORTED, "test_starve_cta applies to the mma.sync split kernel only");
 
   pa::MergeParams mp = {};
   mp.out = sp.out;
@@ -583,7 +601,9 @@ constexpr int kMlaMaxRows = 32;   // query rows of one head chunk (2 tiles of 16
 struct MlaPlan {
   int B, Hq, max_qlen, esz;
   int Gc, NC, R_max, RT, nteam, threads, grid, min_pages, nstage, q_slots, pair;
-  uint32_t stage_bytes, q_slot_bytes, off_stage, off_q, off_xchg, off_bar, team_bytes, off_prefix, smem;
+  bool tc;     // tensor-memory kernel
+  int rpad;    // tc: rows of a unit padded to 16 or 32 (the P V product's N)
+  uint32_t stage_bytes, q_slot_bytes, off_stage, off_q, off_xchg, off_bar, team_bytes, off_prefix, smem, off_buf;
   size_t ws_unit, ws_ml, ws_o, ws_bytes;
 };
 
@@ -593,10 +613,11 @@ int check_mla_options(const pa_options_t* opts) {
     return fail(PA_ERR_INVALID_ARG, "use_tcgen05 %d not in {0, 1, 2}", opts->use_tcgen05);
   if (opts->page_pairing < 0 || opts->page_pairing > 2)
     return fail(PA_ERR_INVALID_ARG, "page_pairing %d not in {0, 1, 2}", opts->page_pairing);
-  if (opts->heads_per_cta != 0 || opts->sliding_window > 0 || opts->sinks != nullptr || opts->use_tcgen05 == 2 ||
-      has_token_scales(opts))
-    return fail(PA_ERR_UNSUPPORTED, "MLA decode takes none of heads_per_cta, sliding_window, sinks, use_tcgen05 = 2, "
-                "token scales");
+  if (opts->wait_limit_us < 0) return fail(PA_ERR_INVALID_ARG, "wait_limit_us %d is negative", opts->wait_limit_us);
+  if (opts->heads_per_cta != 0 || opts->sliding_window > 0 || opts->sinks != nullptr || has_token_scales(opts) ||
+      opts->test_starve_cta != 0)
+    return fail(PA_ERR_UNSUPPORTED, "MLA decode takes none of heads_per_cta, sliding_window, sinks, token scales, "
+                "test_starve_cta");
   return PA_OK;
 }
 
@@ -626,10 +647,49 @@ int make_mla_plan(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t*
   p.NC = Hq / p.Gc;
   p.R_max = p.Gc * max_qlen;
   p.RT = (p.R_max + 15) / 16;
-  p.nteam = pa::mla_teams(p.RT);
-  p.threads = pa::mla_threads(p.RT);
   p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
   p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
+  // The tensor-memory kernel when the caller asks for it (use_tcgen05 = 2); a
+  // unit's rows (at most 32) always fit it.
+  p.tc = opts && opts->use_tcgen05 == 2;
+  if (p.tc) {
+    // one worker a CTA; shared memory: the two block buffers (4 pages of rows
+    // in the MMA layout), the P buffers, a ring of raw page slots, barriers, the
+    // softmax exchange, sequence metadata
+    p.rpad = p.R_max <= 16 ? 16 : 32;
+    p.nteam = 1;
+    p.threads = pa::mla_tc_threads();
+    p.q_slots = 1;
+    p.pair = 0;
+    const uint32_t buf_bytes = 2u * 9u * 4u * 2048u;
+    const uint32_t p_bytes = 2u * (p.esz == 1 ? 1u : 2u) * static_cast<uint32_t>(p.rpad) * 128u;
+    p.stage_bytes = static_cast<uint32_t>(kPageSize * kMlaDqk * p.esz);
+    const uint32_t bars = static_cast<uint32_t>(align_up(8u * (2 * kMaxStages + 16), 128));
+    const uint32_t xchg = 4096;
+    const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));
+    p.off_buf = 0;
+    p.off_q = buf_bytes;
+    p.off_stage = p.off_q + p_bytes;
+    const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - p.off_stage - bars - xchg - prefix_bytes;
+    p.nstage = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / p.stage_bytes)) : 0;
+    if (p.nstage < 2)
+      return fail(PA_ERR_UNSUPPORTED, "no tcgen05 MLA launch configuration fits %d bytes of shared memory", smem_optin);
+    p.off_bar = p.off_stage + static_cast<uint32_t>(p.nstage) * p.stage_bytes;
+    p.off_xchg = p.off_bar + bars;
+    p.off_prefix = p.off_xchg + xchg;
+    p.team_bytes = 0;
+    p.q_slot_bytes = 0;
+    p.smem = 1024 + p.off_prefix + prefix_bytes;
+    const size_t rows = static_cast<size_t>(2) * p.grid * p.R_max;
+    p.ws_unit = 0;
+    p.ws_ml = align_up(p.ws_unit + static_cast<size_t>(16) * B * p.NC, 256);
+    p.ws_o = align_up(p.ws_ml + rows * 8, 256);
+    p.ws_bytes = align_up(p.ws_o + rows * kMlaDv * 2, 256);   // f16 normalised partial outputs
+    *out = p;
+    return PA_OK;
+  }
+  p.nteam = pa::mla_teams(p.RT);
+  p.threads = pa::mla_threads(p.RT);
   p.stage_bytes = static_cast<uint32_t>(kPageSize * kMlaDqk * p.esz);
   p.q_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(max_qlen) * p.Gc * kMlaDqk * 2, 1024));
   // One query slot a team: the next segment's rows are fetched once the
@@ -792,7 +852,10 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
   sp.off_xchg = pl.off_xchg;
   sp.team_bytes = pl.team_bytes;
   sp.q_slots = pl.q_slots;
+  sp.wait_ns = wait_limit_ns(opts);
+  sp.starve_cta = -1;
   sp.pair_pages = pl.pair;
+  sp.off_buf = pl.off_buf;
 
   pa::MergeParams mp = {};
   mp.out = sp.out;
@@ -829,9 +892,11 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
   }
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, stream, rec_flags)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(start)");
-  if ((e = pa::launch_mla(esz == 1, pl.RT, tm, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream)) !=
-      cudaSuccess)
-    return cuda_fail(e, "MLA split kernel launch");
+  if (pl.tc)
+    e = pa::launch_mla_tc(esz == 1, pl.rpad, tm, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
+  else
+    e = pa::launch_mla(esz == 1, pl.RT, tm, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "MLA split kernel launch");
   if (ev1 && (e = cudaEventRecordWithFlags(ev1, stream, rec_flags)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(stop)");
   if ((e = pa::launch_merge_mla(mp, static_cast<int>(B) * pl.NC, pl.R_max, pdl && !ev1, stream)) != cudaSuccess)
@@ -944,8 +1009,8 @@ static int cache_write_impl(const pa_tensor_t* key, const pa_tensor_t* value, co
   p.num_kv_heads = static_cast<int32_t>(Hkv);
   p.head_dim = static_cast<int32_t>(D);
   p.num_pages = static_cast<int32_t>(k_cache->shape[0]);
-  p.k_rscale = tok ? 0.f : 1.0f / k_scale;   // fp32 reciprocal, rounded once
-  p.v_rscale = tok ? 0.f : 1.0f / v_scale;
+  p.k_scale = tok ? 0.f : k_scale;
+  p.v_scale = tok ? 0.f : v_scale;
   if (tok) {
     p.k_tok = static_cast<float*>(kts->data);
     p.v_tok = static_cast<float*>(vts->data);
@@ -1075,8 +1140,8 @@ int paged_attn_mla_plan(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype,
   plan->merge_rows = pl.R_max;
   plan->page_pairing = pl.pair;
   plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
-  plan->variant = 2;
-  plan->block_pages = pl.pair ? 2 : 1;
+  plan->variant = pl.tc ? 3 : 2;
+  plan->block_pages = pl.tc ? 4 : (pl.pair ? 2 : 1);
   return PA_OK;
 }
 

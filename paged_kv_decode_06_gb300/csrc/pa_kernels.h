@@ -64,6 +64,13 @@ struct SplitParams {
   // query slots per team (1 or 2)
   uint32_t team_bytes;
   int32_t q_slots;
+  // tensor-memory MLA kernel: the two block buffers (rows in the MMA layout)
+  uint32_t off_buf;
+  // pipeline waits give up after wait_ns nanoseconds (status bit 3)
+  uint64_t wait_ns;
+  // testing aid (mma.sync kernel): the producer of split CTA starve_cta issues
+  // no copies, so that CTA's consumers run into the wait limit; -1 = none
+  int32_t starve_cta;
 };
 
 struct MergeParams {
@@ -93,7 +100,7 @@ struct CacheWriteParams {
   int64_t kc_stride_page, kc_stride_slot, kc_stride_head;   // elements of the cache dtype
   int64_t vc_stride_page, vc_stride_slot, vc_stride_head;
   int32_t num_tokens, num_kv_heads, head_dim, num_pages;
-  float k_rscale, v_rscale; // fp8 only: code = e4m3(x * rscale), rscale = fp32(1 / scale)
+  float k_scale, v_scale;   // fp8 only: code = e4m3(x / scale), one IEEE fp32 division
   uint32_t* err;
   // per-token quantisation (fp8 only): row scale = amax / 448 stored at
   // [page, head, slot] of f32 [NB, Hkv, 16] tensors; nullptr = per-tensor scales
@@ -135,10 +142,21 @@ cudaError_t launch_mla(bool fp8, int rt, const CUtensorMap& tm, const SplitParam
 int mla_threads(int rt);
 int mla_teams(int rt);
 cudaError_t set_mla_smem_limits(int smem);
+// Tensor-memory (tcgen05) MLA decode: one head chunk of at most rpad (16 or
+// 32) query rows per unit, mla_tc_threads() threads a CTA; shared-memory
+// layout in p.off_buf (block buffers), p.off_q (P buffers), p.off_stage (raw
+// page ring of p.nstage slots), p.off_bar, p.off_xchg, p.off_prefix.
+cudaError_t launch_mla_tc(bool fp8, int rpad, const CUtensorMap& tm, const SplitParams& p, int grid, int smem,
+                          bool pdl, cudaStream_t stream);
+int mla_tc_threads();
+cudaError_t set_mla_tc_smem_limits(int smem);
 // LSE merge of MLA partials (512 value columns; the split kernel writes each
 // piece's normalised output in f16 into ws_o): one warp per (unit, row).
 cudaError_t launch_merge_mla(const MergeParams& p, int units, int rows, bool pdl, cudaStream_t stream);
 cudaError_t set_split_smem_limits_bf16(int smem);
+// Resolve the no-allocation entry point's static scratch on the current device
+// (once per device; part of the per-device set-up).  Returns a pa_status.
+int static_scratch_setup();
 cudaError_t set_split_smem_limits_fp8(int smem);
 
 }  // namespace pa

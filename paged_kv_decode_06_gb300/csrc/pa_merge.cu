@@ -68,6 +68,11 @@ __device__ __forceinline__ MergeRow merge_row(const MergeParams& p, int u, int r
   m.nparts = d.y & 0x3fffffff;
   m.first_is_tail = (d.y >> 30) & 1;
   const int t0 = d.z, qn = d.w;
+  // A descriptor this call's split kernel did not write (its CTA gave up on a
+  // timed-out wait) may hold anything: one that would index outside the
+  // workspace or the outputs is skipped, so a failed call stays in bounds.
+  if (m.gf < 0 || m.nparts > p.split_grid - m.gf || t0 < 0 || qn < 1 || qn > p.max_qlen || t0 > p.num_tokens - qn)
+    return m;
   if (m.nparts <= 1 || m.rho >= p.G * qn) return m;
   const int t = t0 + m.rho / p.G;
   const int hq = (c * p.HC + m.hh) * p.G + m.rho % p.G;

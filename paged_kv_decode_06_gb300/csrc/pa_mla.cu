@@ -155,7 +155,7 @@ struct MlaWarp {
 template <bool FP8, int NP>
 __device__ __forceinline__ bool mla_pages(MlaWarp<FP8>& ws, const uint32_t (&st)[NP], uint32_t xbuf, uint32_t xbar,
                                           uint32_t xpar, int cq, int tb, int L, int min_lim, int lim0, int lim1,
-                                          float scale_log2, int lane) {
+                                          float scale_log2, int lane, uint64_t wait_ns) {
   const int tig = lane & 3, mi = lane >> 3, rr = lane & 7;
   // ---- partial scores over this quarter's 144 features ----
   float S[2 * NP][4];
@@ -201,7 +201,7 @@ __device__ __forceinline__ bool mla_pages(MlaWarp<FP8>& ws, const uint32_t (&st)
   for (int n = 0; n < 2 * NP; ++n) sts_f4(mine + 512u * n, S[n][0], S[n][1], S[n][2], S[n][3]);
   __syncwarp();
   if (lane == 0) mbar_arrive(xbar);
-  if (!mbar_wait(xbar, xpar)) return false;
+  if (!mbar_wait(xbar, xpar, wait_ns)) return false;
   // sums of the four partials as packed pairs (row g's two columns, row g+8's)
   uint64_t X[2 * NP][2];
 #pragma unroll
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
     uint32_t round = 0;
     for (int k = 0; k < count; ++k) {
       if (round > 0) {
-        if (!mbar_wait(empty_bar(stage), (round - 1) & 1u)) {
+        if (!mbar_wait(empty_bar(stage), (round - 1) & 1u, p.wait_ns)) {
           if (lane == 0) atomicOr(p.err, kErrTimeout);
           break;
         }
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       if (k == 0 || cu.j == 0) {
         const int qs = qseg % p.q_slots;
         if (qseg >= p.q_slots) {
-          if (!mbar_wait(qempty_bar(qs), static_cast<uint32_t>(qseg / p.q_slots - 1) & 1u)) {
+          if (!mbar_wait(qempty_bar(qs), static_cast<uint32_t>(qseg / p.q_slots - 1) & 1u, p.wait_ns)) {
             if (lane == 0) atomicOr(p.err, kErrTimeout);
             break;
           }
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
   uint32_t round = 0;
   int k = 0;
   while (k < count) {
-    if (!mbar_wait(full_bar(stage), round & 1u)) {
+    if (!mbar_wait(full_bar(stage), round & 1u, p.wait_ns)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       seg_first_page = k == 0;
       seg_j0 = cu.j;
       const int qs = qseg % p.q_slots;
-      if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg / p.q_slots) & 1u)) {
+      if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg / p.q_slots) & 1u, p.wait_ns)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       ++round2;
     }
     const bool pair = p.pair_pages && (k + 1 < count) && (cu.j + 1 < cu.n);
-    if (pair && !mbar_wait(full_bar(stage2), round2 & 1u)) {
+    if (pair && !mbar_wait(full_bar(stage2), round2 & 1u, p.wait_ns)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
@@ -574,11 +574,11 @@ __global__ void __launch_bounds__(MlaTeams<RT>::THREADS, 1)
       if (pair) {
         const uint32_t sts[2] = {s0, tbase + p.off_stage + static_cast<uint32_t>(stage2) * GG::STAGE};
         ok = mla_pages<FP8, 2>(ws, sts, xb, xfull_bar(b, rt), (step >> 1) & 1u, cq, tb, si.L, si.L - si.qn, lim0,
-                               lim1, p.scale_log2, lane);
+                               lim1, p.scale_log2, lane, p.wait_ns);
       } else {
         const uint32_t sts[1] = {s0};
         ok = mla_pages<FP8, 1>(ws, sts, xb, xfull_bar(b, rt), (step >> 1) & 1u, cq, tb, si.L, si.L - si.qn, lim0,
-                               lim1, p.scale_log2, lane);
+                               lim1, p.scale_log2, lane, p.wait_ns);
       }
       if (!ok) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);

@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 
   if (warp == 0) {
     // ============================ producer =================================
+    if (g == p.starve_cta) return;   // testing aid: this CTA's pages never arrive
     Cursor cu = locate(s_pre, B, NC, start);
     int qseg = 0;
     BlockTableCache btc;
@@ -662,7 +663,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     uint32_t round = 0;    // k / nstage
     for (int64_t k = 0; k < count; ++k) {
       if (round > 0) {
-        if (!mbar_wait(empty_bar(stage), (round - 1) & 1u)) {
+        if (!mbar_wait(empty_bar(stage), (round - 1) & 1u, p.wait_ns)) {
           if (lane == 0) atomicOr(p.err, kErrTimeout);
           break;
         }
@@ -670,7 +671,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       if (k == 0 || cu.j == 0) {
         const int qs = qseg & 1;
         if (qseg >= 2) {
-          if (!mbar_wait(qempty_bar(qs), static_cast<uint32_t>((qseg >> 1) - 1) & 1u)) {
+          if (!mbar_wait(qempty_bar(qs), static_cast<uint32_t>((qseg >> 1) - 1) & 1u, p.wait_ns)) {
             if (lane == 0) atomicOr(p.err, kErrTimeout);
             break;
           }
@@ -753,7 +754,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
   uint32_t round = 0;              // k / nstage for the page at `stage`
   int64_t k = 0;
   while (k < count) {
-    if (!mbar_wait(full_bar(stage), round & 1u)) {
+    if (!mbar_wait(full_bar(stage), round & 1u, p.wait_ns)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
@@ -763,7 +764,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       seg_k0 = k;
       seg_j0 = cu.j;
       const int qs = qseg & 1;
-      if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg >> 1) & 1u)) {
+      if (!mbar_wait(qfull_bar(qs), static_cast<uint32_t>(qseg >> 1) & 1u, p.wait_ns)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
@@ -814,7 +815,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
       ++round2;
     }
     const bool pair = p.pair_pages && (k + 1 < count) && (cu.j + 1 < cu.n);
-    if (pair && !mbar_wait(full_bar(stage2), round2 & 1u)) {
+    if (pair && !mbar_wait(full_bar(stage2), round2 & 1u, p.wait_ns)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }

@@ -48,6 +48,16 @@
 // metadata: Q lives in TMEM, as the A operand of a TS-MMA.
 // Every wait is bounded (kErrTimeout); the CTA drains its MMAs before it frees
 // tensor memory.
+//
+// Parity waits: mbarrier.try_wait.parity cannot tell "the wanted phase has
+// completed" from "the barrier is still one phase behind it" (the phase before
+// has the same parity), so each wait below is made only when the waiter knows
+// the barrier's previous phase is complete.  The per-group "P V done" barrier
+// is the delicate one: Q K^T of block b is issued only after P V(b-2) is done,
+// so a softmax group that has seen S(b) knows P V(b-2) is complete before it
+// waits for P V(b) (segment end) or P V(b-2) (rescale); letting Q K^T run
+// further ahead (three S/P buffers) breaks this and lets the segment-end wait
+// pass while P V(b-2) is still accumulating.
 #pragma once
 
 #include "pa_pack.cuh"
@@ -134,8 +144,8 @@ struct BlockWalker {
 };
 
 // Warp-uniform bounded wait: true only if every lane saw the phase complete.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
 }
 
 template <int D>
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t round = 0;
     while (wk.more()) {
       const TcBlock t = wk.next(s_pre, B, NC);
-      if (round > 0 && !warp_wait(empty_bar(stage), (round - 1) & 1u)) {
+      if (round > 0 && !warp_wait(empty_bar(stage), (round - 1) & 1u, p.wait_ns)) {
         if (lane == 0) atomicOr(p.err, kErrTimeout);
         break;
       }
@@ -309,9 +319,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (t.first) ++seg;
       // S(b) goes where P(b-2), the same group's previous block, was: its P V
       // must be done (the group read S(b-2) before it wrote P(b-2)).
-      if (!warp_wait(full_bar(stage), round & 1u) ||
-          (b >= 2 && !warp_wait(odone_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u)) ||
-          (t.first && !warp_wait(qfull_bar(seg & 1), static_cast<uint32_t>(seg >> 1) & 1u))) {
+      if (!warp_wait(full_bar(stage), round & 1u, p.wait_ns) ||
+          (b >= 2 && !warp_wait(odone_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u, p.wait_ns)) ||
+          (t.first && !warp_wait(qfull_bar(seg & 1), static_cast<uint32_t>(seg >> 1) & 1u, p.wait_ns))) {
         ok = false;
         break;
       }
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Every MMA this warp issued must be complete before tensor memory is freed.
     if (lane == 0) umma_commit(drain_bar);
     __syncwarp();
-    if (!warp_wait(drain_bar, 0u) && lane == 0) atomicOr(p.err, kErrTimeout);
+    if (!warp_wait(drain_bar, 0u, p.wait_ns) && lane == 0) atomicOr(p.err, kErrTimeout);
   } else if (warp == kTcPvWarp) {
     // ============================ P V issuer ===============================
     // Runs beside the Q K^T issuer, so the two MMA streams do not wait on
@@ -360,10 +370,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool ofirst = b - b0 < 2;
       // full(stage) has completed before P(b) exists; waiting on it here makes
       // the stage's TMA data visible to this warp directly.
-      if (!warp_wait(pfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u) ||
-          !warp_wait(full_bar(stage), round & 1u) ||
+      if (!warp_wait(pfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u, p.wait_ns) ||
+          !warp_wait(full_bar(stage), round & 1u, p.wait_ns) ||
           // the previous segment's epilogue must have read both O accumulators
-          (ofirst && seg >= 1 && !warp_wait(ofree_bar, static_cast<uint32_t>(seg - 1) & 1u))) {
+          (ofirst && seg >= 1 && !warp_wait(ofree_bar, static_cast<uint32_t>(seg - 1) & 1u, p.wait_ns))) {
         ok = false;
         break;
       }
@@ -411,7 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
     if (lane == 0) umma_commit(drain2_bar);
     __syncwarp();
-    if (!warp_wait(drain2_bar, 0u) && lane == 0) atomicOr(p.err, kErrTimeout);
+    if (!warp_wait(drain2_bar, 0u, p.wait_ns) && lane == 0) atomicOr(p.err, kErrTimeout);
   } else {
     // ============================ softmax ==================================
     // Two groups of four warps; group gi = (warp - 4) / 4 takes the blocks b
@@ -498,7 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if ((b & 1) == gi) {
         // ---- the block's S row ----------------------------------------------
-        if (!warp_wait(sfull_bar(gi), static_cast<uint32_t>(b >> 1) & 1u)) {
+        if (!warp_wait(sfull_bar(gi), static_cast<uint32_t>(b >> 1) & 1u, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -560,7 +570,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         } else if (__any_sync(0xffffffffu, grow)) {
           // O must hold P V of the group's previous block before it is rescaled.
-          if (!warp_wait(odone_bar(gi), static_cast<uint32_t>((b >> 1) - 1) & 1u)) {
+          if (!warp_wait(odone_bar(gi), static_cast<uint32_t>((b >> 1) - 1) & 1u, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -641,7 +651,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         xstat[(seg & 1) * 256 + gi * 128 + rho] = make_float2(m, l);
         __syncwarp();
         if (lane == 0) mbar_arrive(xstat_bar(q4));
-        if (!warp_wait(xstat_bar(q4), static_cast<uint32_t>(seg) & 1u)) {
+        if (!warp_wait(xstat_bar(q4), static_cast<uint32_t>(seg) & 1u, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -658,8 +668,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int bl0 = (b & 1) == 0 ? b : b - 1;
         const int bl1 = (b & 1) == 1 ? b : b - 1;
         const bool has0 = bl0 >= b0, has1 = bl1 >= b0;
-        if ((has0 && !warp_wait(odone_bar(0), static_cast<uint32_t>(bl0 >> 1) & 1u)) ||
-            (has1 && !warp_wait(odone_bar(1), static_cast<uint32_t>(bl1 >> 1) & 1u))) {
+        if ((has0 && !warp_wait(odone_bar(0), static_cast<uint32_t>(bl0 >> 1) & 1u, p.wait_ns)) ||
+            (has1 && !warp_wait(odone_bar(1), static_cast<uint32_t>(bl1 >> 1) & 1u, p.wait_ns))) {
           ok = false;
           break;
         }

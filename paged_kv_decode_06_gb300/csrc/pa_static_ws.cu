@@ -7,13 +7,15 @@
 // that has no handle on an allocator at all.  The split kernel needs scratch
 // for its partial results, so this entry point takes it from one file-scope
 // device array instead of the per-device workspace the library would otherwise
-// cudaMalloc.  The array is part of the library's device code, so every GPU on
-// which the library's kernels are loaded holds its 16 MiB until the process
-// exits.
+// cudaMalloc.
 //
 // The array name is only a host-side stand-in; its device address comes from
-// cudaGetSymbolAddress, taken once per device (with that device current) on the
-// first call there.  Make that first call before any stream capture.
+// cudaGetSymbolAddress, taken once per device with that device current.  The
+// library's per-device set-up (the first call of any entry point on a device)
+// takes it, which also loads the array's module under CUDA's lazy module
+// loading: from then on that GPU holds the 16 MiB until the process exits.  So
+// make one call of any entry point on each device before a memory pool takes
+// the device's free memory, and before any stream capture.
 //
 // Every call uses the same array.  Nothing in it has to start at zero (each
 // call writes every scratch value before it reads it), but the array keeps the
@@ -67,6 +69,15 @@ int scratch_for_current_device(void** out) {
 }
 
 }  // namespace
+
+namespace pa {
+// Per-device set-up hook (called with the device current): resolves the
+// scratch array's address now, so its module is loaded early.
+int static_scratch_setup() {
+  void* unused = nullptr;
+  return scratch_for_current_device(&unused);
+}
+}  // namespace pa
 
 extern "C" int paged_attn_decode_static_scratch(const pa_tensor_t* q, const pa_tensor_t* k_cache,
                                                 const pa_tensor_t* v_cache, const pa_tensor_t* block_tables,

@@ -287,7 +287,9 @@ def _mla_call(lib, a, scale=0.07):
                         qsl=torch.arange(0, 100, 33, dtype=torch.int32), max_qlen=33), binding.PA_ERR_UNSUPPORTED),
     (lambda a: a.update(opts=binding.make_options(sliding_window=8)), binding.PA_ERR_UNSUPPORTED),
     (lambda a: a.update(opts=binding.make_options(heads_per_cta=2)), binding.PA_ERR_UNSUPPORTED),
-    (lambda a: a.update(opts=binding.make_options(use_tcgen05=2)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(opts=binding.make_options(use_tcgen05=3)), binding.PA_ERR_INVALID_ARG),
+    (lambda a: a.update(opts=binding.make_options(test_starve_cta=1)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(opts=binding.make_options(wait_limit_us=-1)), binding.PA_ERR_INVALID_ARG),
     (lambda a: a.update(lse=torch.zeros(3, 8, dtype=torch.float32)), binding.PA_ERR_INVALID_ARG),
 ])
 def test_mla_invalid_arguments_rejected_on_host(lib, mutate, expect):
@@ -320,3 +322,20 @@ def test_mla_plan_rejects_bad_shapes_without_device(lib):
         binding.paged_attn_mla_reserve(4, 16, binding.PA_BF16, 0)
     assert e.value.status == binding.PA_ERR_INVALID_ARG
 
+
+
+def _opt_call(lib, opts):
+    a = _good_args()
+    descs = [binding.tensor_desc(a[n]) for n in ("q", "k", "v", "bt", "sl", "qsl", "out", "lse")]
+    refs = [ctypes.byref(d) for d in descs]
+    return lib.paged_attn_decode_ex(*refs[:6], a["max_qlen"], 0.1, 1.0, 1.0, refs[6], refs[7], ctypes.byref(opts),
+                                    None)
+
+
+def test_wait_limit_and_starve_options_checked_on_the_host(lib):
+    for bad in (binding.make_options(wait_limit_us=-5), binding.make_options(test_starve_cta=-1)):
+        assert _opt_call(lib, bad) == binding.PA_ERR_INVALID_ARG
+        assert "negative" in binding.paged_attn_last_error_message()
+    if not torch.cuda.is_available():
+        # valid values pass every host check; the call then fails at device set-up
+        assert _opt_call(lib, binding.make_options(wait_limit_us=1000, test_starve_cta=3)) == binding.PA_ERR_CUDA

@@ -3,13 +3,16 @@ the C ABI (paged_attn_mla_decode).
 
 Tolerances (max absolute error): out 1e-2 for bf16 caches, 2e-2 for fp8
 caches; lse 1e-3.  Small cases are compared in full; the full-size MLA
-workloads on sampled sequences, in the launch configuration the benchmark
-times."""
+workloads on every row against the plain-C oracle and on sampled sequences
+against the NumPy oracle, in the launch configuration the benchmark times.
+The main cases run on both split kernels: the mma.sync kernel (the default)
+and the tensor-memory (tcgen05) kernel (use_tcgen05 = 2)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
+from oracle import c_oracle
 from paged_kv_decode_06_gb300 import binding
 from paged_kv_decode_06_gb300 import workloads as wl
 
@@ -30,7 +33,17 @@ def _rows_of(w, seqs):
     return np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seqs])
 
 
-def check(w, seqs=None, options=None, ref=None):
+KERNELS = {"tc": 2, "mma": 0}
+
+
+def _opts(kernel, **kw):
+    return binding.make_options(use_tcgen05=KERNELS[kernel], **kw)
+
+
+def check(w, seqs=None, options=None, ref=None, kernel=None):
+    if kernel is not None:
+        assert options is None
+        options = _opts(kernel)
     out, lse = binding.mla_decode_workload(w, options=options)
     torch.cuda.synchronize()
     status = binding.paged_attn_device_status(clear=True)
@@ -56,36 +69,48 @@ def _spec(kv="bf16", Hq=16, seq_lens=(1, 15, 16, 17, 31, 32, 33, 100), qlens=(1,
                               seed=seed)
 
 
-def test_mla_tiny_config_full():
-    check(wl.make_mla_workload(wl.MLA_CONFIGS["mla_tiny"], device="cuda"))
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+def test_mla_tiny_config_full(kernel):
+    check(wl.make_mla_workload(wl.MLA_CONFIGS["mla_tiny"], device="cuda"), kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_mla_page_boundaries_and_ragged_tails(kv, kernel):
+    check(wl.make_mla_workload(_spec(kv=kv), device="cuda"), kernel=kernel)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
-def test_mla_page_boundaries_and_ragged_tails(kv):
-    check(wl.make_mla_workload(_spec(kv=kv), device="cuda"))
+def test_mla_plan_variants(kv):
+    code = binding.PA_FP8_E4M3 if kv == "fp8" else binding.PA_BF16
+    assert binding.paged_attn_mla_plan(32, 16, code, 4)["variant"] == 2
+    assert binding.paged_attn_mla_plan(32, 16, code, 4, options=_opts("tc"))["variant"] == 3
 
 
 # heads x query lengths: 1 row tile (two teams a CTA), 2 row tiles, several head chunks
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("Hq,qlens", [(16, (1,)), (8, (1,)), (1, (1,)), (16, (4,)), (16, (2, 3, 4)), (32, (1,)),
                                       (128, (1,)), (16, (3,)), (4, (1, 5, 8)), (2, (16,))])
-def test_mla_heads_and_verification_runs(kv, Hq, qlens):
+def test_mla_heads_and_verification_runs(kv, Hq, qlens, kernel):
     w = wl.make_mla_workload(_spec(kv=kv, Hq=Hq, qlens=qlens, seq_lens=(16, 17, 40, 64, 130), seed=Hq + len(qlens)),
                              device="cuda")
-    check(w)
+    check(w, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 152, 300])
 @pytest.mark.parametrize("kv,Hq,qlens", [("bf16", 16, (1,)), ("fp8", 16, (4,))])
-def test_mla_forced_split_counts_exercise_the_merge(num_ctas, kv, Hq, qlens):
+def test_mla_forced_split_counts_exercise_the_merge(num_ctas, kv, Hq, qlens, kernel):
     w = wl.make_mla_workload(_spec(kv=kv, Hq=Hq, qlens=qlens, seq_lens=(3, 50, 300, 17, 1000), seed=num_ctas),
                              device="cuda")
     ref = oracle.run_mla_workload(w)
-    check(w, ref=ref, options=binding.make_options(num_ctas=num_ctas, min_pages_per_cta=1))
+    check(w, ref=ref, options=_opts(kernel, num_ctas=num_ctas, min_pages_per_cta=1))
 
 
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
-def test_mla_non_finite_tail_slots_and_unused_pages_do_not_leak(kv):
+def test_mla_non_finite_tail_slots_and_unused_pages_do_not_leak(kv, kernel):
     w = wl.make_mla_workload(_spec(kv=kv, seq_lens=(3, 17, 40, 1)), device="cuda")
     ref = oracle.run_mla_workload(w)
     nan_code = torch.tensor(float("nan")).to(torch.bfloat16) if kv == "bf16" else torch.tensor(0x7F, dtype=torch.uint8)
@@ -98,7 +123,7 @@ def test_mla_non_finite_tail_slots_and_unused_pages_do_not_leak(kv):
     for p in range(w.num_pages):
         if p not in used:
             w.kv_cache[p] = nan_code
-    check(w, ref=ref)
+    check(w, ref=ref, kernel=kernel)
 
 
 def test_mla_strided_cache_and_lse_optional():
@@ -173,14 +198,18 @@ def test_mla_cuda_graph_capture_and_replay_with_new_metadata():
     assert binding.paged_attn_device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
 @pytest.mark.parametrize("name", ["mla_tp8", "mla_mtp_fp8"])
-def test_mla_full_size_configs_sampled(name):
+def test_mla_full_size_configs_every_row(name, kernel):
+    """Every query row against the C oracle; sampled sequences against the
+    NumPy oracle too."""
     w = wl.make_mla_workload(wl.MLA_CONFIGS[name], device="cuda")
+    _, _, eo, el = check(w, ref=c_oracle.run_mla_workload(w), kernel=kernel)
     rng = np.random.default_rng(len(name))
-    seqs = set(rng.choice(w.spec.num_seqs, size=5, replace=False).tolist())
+    seqs = set(rng.choice(w.spec.num_seqs, size=3, replace=False).tolist())
     seqs.update({int(np.argmax(w.seq_lens)), int(np.argmin(w.seq_lens))})
-    _, _, eo, el = check(w, seqs=sorted(seqs))
-    print(f"{name}: sampled seqs {sorted(seqs)}: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
+    check(w, seqs=sorted(seqs), kernel=kernel)
+    print(f"{name}: all {w.q.shape[0]} query tokens: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
 
 
 def test_mla_padded_query_output_and_lse_strides():
