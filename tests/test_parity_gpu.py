@@ -1,14 +1,17 @@
 """CUDA path vs the float64 oracle, element by element, through the C ABI.
 
 Tolerances (max absolute error): out 1e-2 for bf16 caches, 2e-2 for fp8
-caches; lse 1e-3.  Small cases are compared in full; the full-size workloads
-are compared on sampled sequences, in the launch configuration the benchmark
-times (the library's default plan)."""
+caches; lse 1e-3.  Small cases are compared in full.  The full-size workloads
+are compared on every query row against the plain-C float64 oracle (pinned to
+the NumPy oracle to 1e-11; all host cores), and on sampled sequences against
+the NumPy oracle as well, in the launch configuration the benchmark times (the
+library's default plan)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
+from oracle import c_oracle
 from paged_kv_decode_06_gb300 import binding
 from paged_kv_decode_06_gb300 import workloads as wl
 
@@ -194,7 +197,7 @@ def test_cuda_graph_capture_and_replay_with_new_metadata():
     assert binding.paged_attn_device_status(clear=True) == 0
 
 
-# ------------------------------------------------ full-size workloads (sampled)
+# ------------------------------------------------ full-size workloads (every row)
 
 def _sample_seqs(w, k, seed):
     rng = np.random.default_rng(seed)
@@ -205,12 +208,20 @@ def _sample_seqs(w, k, seed):
     return sorted(idx)
 
 
+def check_every_row(w, **kw):
+    """Every query row against the C oracle, then sampled sequences against
+    the NumPy oracle (each on its own GPU call)."""
+    _, _, eo, el = check(w, ref=c_oracle.run_workload(w), **kw)
+    seqs = _sample_seqs(w, 3, seed=w.spec.seed)
+    check(w, seqs=seqs, **kw)
+    return eo, el
+
+
 @pytest.mark.parametrize("name", ["llama3_8b", "batch1_32k", "fp8", "mtp"])
-def test_full_size_configs_sampled(name):
+def test_full_size_configs_every_row(name):
     w = wl.make_workload(wl.CONFIGS[name], device="cuda")
-    seqs = _sample_seqs(w, 6, seed=wl.CONFIG_ORDER.index(name))
-    _, _, eo, el = check(w, seqs=seqs)
-    print(f"{name}: sampled seqs {seqs}: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
+    eo, el = check_every_row(w)
+    print(f"{name}: all {w.q.shape[0]} query tokens: max|out err| {eo:.3e}, max|lse err| {el:.3e}")
 
 
 # ------------------------------------------------ sliding window and attention sinks

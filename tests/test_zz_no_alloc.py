@@ -5,9 +5,12 @@ not allowed, so the library must not cudaMalloc its split scratch on their
 behalf.  This entry point takes the scratch from a fixed 16 MiB device array
 inside the library.  The test calls it through the C ABI twice in a row (the
 second call finds the first call's data in the shared array) and checks each
-result against paged_attn_decode on the same inputs, with the parity
-tolerances (out 1e-2 bf16 / 2e-2 fp8, lse 1e-3).  It also checks that a shape
-needing more than 16 MiB is refused on the host.
+result against the float64 oracle and against paged_attn_decode on the same
+inputs, with the parity tolerances (out 1e-2 bf16 / 2e-2 fp8, lse 1e-3).  With
+the library's own workspace released first, it checks that the calls left that
+workspace empty: an ordinary call under stream capture, which may not allocate,
+still finds no workspace.  It also checks that a shape needing more than 16 MiB
+is refused on the host.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test."""
@@ -17,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_decode_06_gb300 import binding
 from paged_kv_decode_06_gb300 import workloads as wl
 
@@ -58,19 +62,45 @@ def test_static_scratch_matches_paged_attn_decode_on_two_calls_in_a_row(cuda_lib
     ]
     works = [wl.make_workload(s, device="cuda") for s in specs]
     args = [_device_args(w) for w in works]
+    oracle_ref = [oracle.run_workload(w) for w in works]
     binding.paged_attn_device_status(clear=True)
+    binding.paged_attn_release()          # the library's own workspace: none from here on
     # two calls in a row through the static-scratch entry point
     got = [_call(lib, "paged_attn_decode_static_scratch", w, *a) for w, a in zip(works, args)]
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    _assert_no_library_workspace(lib, works[0], *args[0])
     # the same inputs through the ordinary entry point
     ref = [_call(lib, "paged_attn_decode", w, *a) for w, a in zip(works, args)]
     torch.cuda.synchronize()
     assert binding.paged_attn_device_status(clear=True) == 0
-    for w, (o, l), (ro, rl) in zip(works, got, ref):
+    for w, (o, l), (ro, rl), (oo, ol) in zip(works, got, ref, oracle_ref):
         assert torch.isfinite(o.float()).all() and torch.isfinite(l).all()
+        tol = TOL_OUT[w.spec.kv_dtype]
+        err_o = np.abs(o.float().cpu().numpy() - oo).max()
+        err_l = np.abs(l.cpu().numpy() - ol).max()
+        assert err_o <= tol, f"static scratch vs oracle: max|out| error {err_o:.3e}"
+        assert err_l <= TOL_LSE, f"static scratch vs oracle: max|lse| error {err_l:.3e}"
         err_o = (o.float() - ro.float()).abs().max().item()
         err_l = (l - rl).abs().max().item()
-        assert err_o <= TOL_OUT[w.spec.kv_dtype], err_o
+        assert err_o <= tol, err_o
         assert err_l <= TOL_LSE, err_l
+
+
+def _assert_no_library_workspace(lib, w, bt, sl, qsl, mq):
+    """paged_attn_decode never allocates during stream capture: with no
+    library workspace it returns PA_ERR_WORKSPACE before enqueueing anything."""
+    s = w.spec
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:2], dtype=torch.float32, device=w.q.device)
+    descs = [binding.tensor_desc(t) for t in (w.q, w.k_cache, w.v_cache, bt, sl, qsl, out, lse)]
+    refs = [ctypes.byref(d) for d in descs]
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        st = lib.paged_attn_decode(*refs[:6], mq, s.scale, s.k_scale, s.v_scale, refs[6], refs[7],
+                                   stream.cuda_stream)
+    assert st == binding.PA_ERR_WORKSPACE, (st, lib.paged_attn_last_error_message().decode())
 
 
 def test_static_scratch_refuses_shapes_beyond_16_mib(cuda_lib):
