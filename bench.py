@@ -229,16 +229,45 @@ def cpu_baseline(config: str, budget_s: float):
             "numpy_single_core": {"value": gn, "unit": "GB/s", "cores": 1, "sample": sn}}
 
 
+# Arm "CPU part" ids (/proc/cpuinfo) of the server cores an Arm host may have.
+_ARM_PARTS = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2", "0xd4f": "Neoverse-V2",
+              "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+
+
 def _cpu_model() -> str:
+    """The host CPU's model name: lscpu's "Model name" (with its vendor),
+    else /proc/cpuinfo's "model name", else the Arm part id mapped to its core
+    name (Arm hosts list only the part id there); the part id is appended."""
+    name, part = None, None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        fields = {}
+        for line in r.stdout.splitlines():
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+        if fields.get("Model name", "-") != "-":
+            vendor = fields.get("Vendor ID", "")
+            name = fields["Model name"] if vendor in ("", "-") or vendor in fields["Model name"] else \
+                f"{vendor} {fields['Model name']}"
+    except (OSError, subprocess.SubprocessError):
+        pass
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu part", "hardware")):
-                    return line.split(":", 1)[1].strip()
+                key = line.split(":", 1)[0].strip().lower()
+                if key == "model name" and name is None:
+                    name = line.split(":", 1)[1].strip()
+                elif key == "cpu part" and part is None:
+                    part = line.split(":", 1)[1].strip().lower()
     except OSError:
         pass
-    import platform
-    return platform.machine()
+    if name is None and part is not None:
+        name = _ARM_PARTS.get(part, "Arm core")
+    if name is None:
+        import platform
+        name = platform.machine()
+    return f"{name} (CPU part {part})" if part else name
 
 
 def _packed_views(parts, device):
@@ -259,20 +288,23 @@ def _packed_views(parts, device):
 
 
 def _timed_passes(step, ev_opts_for, pools, args, world, local, dev):
-    """Warm-up, CUDA-graph capture and the three timed passes of a decode
-    benchmark.  step(k, opts=None, stream_=None) enqueues step k (pool k % pools)
-    on stream_ (None: the current stream); ev_opts_for(pidx, ev_a, ev_b) gives
+    """Warm-up, CUDA-graph capture and the timed passes of a decode benchmark.
+    step(k, opts=None, stream_=None) enqueues step k (pool k % pools) on
+    stream_ (None: the current stream); ev_opts_for(pidx, ev_a, ev_b) gives
     pool pidx's options with the split kernel's start / stop events.
 
     The decode step runs as an engine runs it: captured in CUDA graphs and
     replayed, so the device time is not hidden behind Python's per-call
     marshalling.  A graph holds GSTEP consecutive steps (rotating the KV pools),
     so the programmatic-dependent-launch overlap between steps survives inside
-    it; single-step graphs cover a remainder.  Pass 1 (value): K whole steps back
-    to back, bracketed by barrier + synchronize; pass 2 (roofline): the split
-    kernel's own duration, step by step, from external event records; pass 3:
-    the same K steps as direct calls through the binding (no graph).
-    Returns (ms per step, max over ranks; split-kernel ms list; direct ms; clocks)."""
+    it; single-step graphs cover a remainder.  Pass 1 (value): a timed window of
+    exactly K steps back to back, bracketed by barrier + synchronize, repeated
+    until the windows add up to at least --min-seconds (the same repeat count on
+    every rank); ms per step = the median window.  Pass 2 (roofline): the split
+    kernel's own duration, step by step, from external event records (at least
+    200 steps).  Pass 3: K steps as direct calls through the binding (no graph).
+    The clock sampler runs across passes 1 and 2.  Returns (ms per step, max
+    over ranks; split-kernel ms list; direct ms; clocks; repeat count)."""
     import torch
 
     from paged_kv_decode_06_gb300 import binding
@@ -307,26 +339,36 @@ def _timed_passes(step, ev_opts_for, pools, args, world, local, dev):
     ev_a.record(stream); ev_b.record(stream)     # torch times only events it has recorded once itself
     torch.cuda.synchronize()
     rgraphs = [capture(pidx, 1, opts=ev_opts_for(pidx, ev_a, ev_b)) for pidx in range(pools)]
-    run_steps(max(args.warmup, gstep))
-    torch.cuda.synchronize()
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # graph warm-up, which also sizes the repeat count
+    n_est = max(args.warmup, 4 * gstep)
+    t_begin.record(stream)
+    run_steps(n_est)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    est_ms = t_begin.elapsed_time(t_end) / n_est
+    repeats = max(1, math.ceil(args.min_seconds * 1e3 / max(1e-6, args.steps * est_ms)))
+    repeats = int(max_over_ranks(float(min(repeats, 100000)), world, device=dev))
+    windows = []
     with ClockSampler(local) as clk:
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        t_begin.record(stream)
-        run_steps(args.steps)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
+        for _ in range(repeats):
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            t_begin.record(stream)
+            run_steps(args.steps)
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            windows.append(t_begin.elapsed_time(t_end) / args.steps)
         split_ms = []
-        for k in range(args.steps):
+        for k in range(max(args.steps, 200)):
             rgraphs[k % pools].replay()
             ev_b.synchronize()
             split_ms.append(ev_a.elapsed_time(ev_b))
-    ms = t_begin.elapsed_time(t_end) / args.steps
+    ms = statistics.median(windows)
     d0 = torch.cuda.Event(enable_timing=True)
     d1 = torch.cuda.Event(enable_timing=True)
     d0.record(stream)
@@ -335,7 +377,7 @@ def _timed_passes(step, ev_opts_for, pools, args, world, local, dev):
     d1.record(stream)
     torch.cuda.synchronize()
     direct_ms = d0.elapsed_time(d1) / args.steps
-    return max_over_ranks(ms, world, device=dev), split_ms, direct_ms, clk.summary()
+    return max_over_ranks(ms, world, device=dev), split_ms, direct_ms, clk.summary(), repeats
 
 
 def _packed_e2e(base, works, out, lse, dev, call, args):
@@ -421,30 +463,37 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
+def _setup_rank(local, world):
+    import torch
+
+    from paged_kv_decode_06_gb300 import binding
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl")
+    binding.load()
+    return dev
+
+
+def measure_decode(spec, args, world, local, dev, window=0, sinks=False, tc=0):
+    """Every timed pass of one grouped-query decode workload (see
+    _timed_passes and _packed_e2e) plus the figures the JSON line reports."""
     import numpy as np
     import torch
 
     from paged_kv_decode_06_gb300 import binding
     from paged_kv_decode_06_gb300 import workloads as wl
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    binding.load()
-    spec = _spec_for(args)
     base = wl.make_workload(spec, device=str(dev))
     step_bytes = base.kv_bytes()
     sinks_t = None
-    if args.window > 0:
+    if window > 0:
         # algorithmic bytes with a sliding window: the union of the query rows'
         # windows, min(L, W + q - 1) keys per sequence
         eb = 1 if spec.kv_dtype == "fp8" else 2
-        seen = np.minimum(base.seq_lens.astype(np.int64), args.window + base.query_lens.astype(np.int64) - 1)
+        seen = np.minimum(base.seq_lens.astype(np.int64), window + base.query_lens.astype(np.int64) - 1)
         step_bytes = int(seen.sum()) * spec.num_kv_heads * spec.head_dim * 2 * eb
-    if args.sinks:
+    if sinks:
         sinks_t = torch.randn(spec.num_q_heads, generator=torch.Generator().manual_seed(3)).to(dev)
     pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
     # every pool shares the first one's metadata (lengths, page ids); only the contents differ
@@ -453,12 +502,11 @@ def run_ours(args, world, rank, local):
 
     def pool_options(w, **extra):
         # per-token fp8 scales belong to each pool's cache
-        if args.window > 0 or args.sinks or args.tc or w.k_token_scales is not None or extra:
-            return binding.make_options(sliding_window=args.window, sinks=sinks_t, use_tcgen05=args.tc,
+        if window > 0 or sinks or tc or w.k_token_scales is not None or extra:
+            return binding.make_options(sliding_window=window, sinks=sinks_t, use_tcgen05=tc,
                                         k_token_scales=w.k_token_scales, v_token_scales=w.v_token_scales, **extra)
         return None
     pool_opts = [pool_options(w) for w in works]
-    # every pool shares the metadata of the first (same lengths, same page ids)
     bt = torch.from_numpy(base.block_tables).to(dev)
     sl = torch.from_numpy(base.seq_lens).to(dev)
     qsl = torch.from_numpy(base.query_start_loc).to(dev) if base.query_start_loc is not None else None
@@ -473,7 +521,7 @@ def run_ours(args, world, rank, local):
         binding.paged_attn_decode(w.q, w.k_cache, w.v_cache, bt, sl, qsl, mq, spec.scale, spec.k_scale,
                                   spec.v_scale, out=out, lse=lse, options=opts, stream=stream_)
 
-    ms, split_ms, direct_ms, clocks = _timed_passes(
+    ms, split_ms, direct_ms, clocks, repeats = _timed_passes(
         step, lambda pidx, ea, eb: pool_options(works[pidx], split_start_event=ea, split_stop_event=eb), pools, args,
         world, local, dev)
 
@@ -484,78 +532,29 @@ def run_ours(args, world, rank, local):
 
     e2e_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
     status = binding.paged_attn_device_status(clear=True)
-
-    if rank != 0:
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return
-    peak, peak_kind = _peaks()
-    split_mean = statistics.mean(split_ms)
-    achieved = step_bytes / (split_mean * 1e-3) / 1e9
     plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                                    binding.kv_dtype_code(spec.kv_dtype), mq,
-                                   options=binding.make_options(use_tcgen05=args.tc))
+                                   options=binding.make_options(use_tcgen05=tc))
     kernel = "pa_split_tc_kernel" if plan["variant"] == 1 else "pa_split_kernel"
-    traffic = _traffic_from_profiles(spec.name, kernel)
-    value = job_throughput_gbs(step_bytes, world, ms)
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
-        "frac_of_hbm_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f8e4m3" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
-        "config": {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
-                   "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_dtype": spec.kv_dtype,
-                   "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
-                   "sliding_window": args.window, "sinks": bool(args.sinks), "use_tcgen05": args.tc,
-                   "l2": "no flush; each step reads >= 2x L2 of KV (pools rotated when one is smaller)",
-                   "step_mode": "CUDA graph replay; a step = one paged_attn_decode call (split + merge)",
-                   "plan": plan},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
-                     "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
-                     "per_launch_bytes": step_bytes},
-        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "note": "per step: one copy of the packed inputs from pinned host memory, the API call from "
-                        "Python, one copy of the packed out / lse back"},
-        "direct_call": {"value": step_bytes * world / (direct_ms * 1e-3) / 1e9, "unit": "GB/s",
-                        "ms_per_step": direct_ms,
-                        "note": "paged_attn_decode called from Python each step (no CUDA graph)"},
-        "gpu_launches": 2 * args.steps,   # split + merge per timed step
-        "clocks": clocks,
-        "device_status": status,
-    }
-    if not args.no_cpu_baseline and not args.batch:
-        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    del works, base, out, lse
+    torch.cuda.empty_cache()
+    return dict(spec=spec, step_bytes=step_bytes, pools=pools, ms=ms, split_ms=split_ms, direct_ms=direct_ms,
+                clocks=clocks, repeats=repeats, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, status=status, plan=plan,
+                kernel=kernel, traffic=_traffic_from_profiles(spec.name, kernel), flops=None)
 
 
-def run_mla(args, world, rank, local):
-    """MLA decode (paged_attn_mla_decode): the same measurement as run_ours,
-    on a latent cache [NB, 16, 576] (every cached row read once per step)."""
-    import dataclasses
-
+def measure_mla(spec, args, world, local, dev):
+    """measure_decode for MLA decode (paged_attn_mla_decode) on a latent cache
+    [NB, 16, 576]: every cached row is read once per step."""
     import numpy as np
     import torch
 
     from paged_kv_decode_06_gb300 import binding
     from paged_kv_decode_06_gb300 import workloads as wl
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    binding.load()
-    spec = wl.MLA_CONFIGS[args.config]
-    if args.batch:
-        spec = dataclasses.replace(spec, num_seqs=args.batch, name=f"{spec.name}_b{args.batch}")
     base = wl.make_mla_workload(spec, device=str(dev))
     step_bytes = base.kv_bytes()
     pools = min(16, max(1, math.ceil(2 * L2_BYTES / step_bytes)))
-    # every pool shares the first one's metadata (lengths, page ids); only the contents differ
     works = [base] + [wl.make_mla_workload(spec, device=str(dev), content_seed=spec.seed + 100 * k)
                       for k in range(1, pools)]
     bt = torch.from_numpy(base.block_tables).to(dev)
@@ -578,7 +577,7 @@ def run_mla(args, world, rank, local):
             ev_opt["o"] = binding.make_options(split_start_event=ea, split_stop_event=eb)
         return ev_opt["o"]
 
-    ms, split_ms, direct_ms, clocks = _timed_passes(step, ev_opts_for, pools, args, world, local, dev)
+    ms, split_ms, direct_ms, clocks, repeats = _timed_passes(step, ev_opts_for, pools, args, world, local, dev)
 
     def e2e_call(k, q, bt_, sl_, qsl_, out_, lse_):
         w = works[k % pools]
@@ -587,49 +586,112 @@ def run_mla(args, world, rank, local):
 
     e2e_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
     status = binding.paged_attn_device_status(clear=True)
-    if rank != 0:
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return
-    peak, peak_kind = _peaks()
-    split_mean = statistics.mean(split_ms)
-    achieved = step_bytes / (split_mean * 1e-3) / 1e9
     plan = binding.paged_attn_mla_plan(spec.num_seqs, spec.num_q_heads, binding.kv_dtype_code(spec.kv_dtype), mq)
-    kernel = "pa_mla_kernel"
-    value = job_throughput_gbs(step_bytes, world, ms)
     # tensor work per step: 2 * rows * (576 + 512) flops per cached token of each row's sequence
     rows_tokens = int((base.seq_lens.astype(np.int64) * base.query_lens.astype(np.int64)).sum()) * spec.num_q_heads
     flops = 2 * rows_tokens * (spec.head_dim + spec.kv_lora_rank)
-    line = {
+    del works, base, out, lse
+    torch.cuda.empty_cache()
+    return dict(spec=spec, step_bytes=step_bytes, pools=pools, ms=ms, split_ms=split_ms, direct_ms=direct_ms,
+                clocks=clocks, repeats=repeats, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, status=status, plan=plan,
+                kernel="pa_mla_kernel", traffic=_traffic_from_profiles(spec.name, "pa_mla_kernel"), flops=flops)
+
+
+def _line(r, args, world, window=0, sinks=False, tc=0):
+    """The JSON line of one measured workload (measure_decode / measure_mla)."""
+    spec = r["spec"]
+    peak, peak_kind = _peaks()
+    split_mean = statistics.mean(r["split_ms"])
+    achieved = r["step_bytes"] / (split_mean * 1e-3) / 1e9
+    value = job_throughput_gbs(r["step_bytes"], world, r["ms"])
+    mla = r["kernel"] == "pa_mla_kernel"
+    config = {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads}
+    if mla:
+        config.update(kv_lora_rank=spec.kv_lora_rank, rope_dim=spec.rope_dim, kv_dtype=spec.kv_dtype,
+                      max_query_len=spec.max_query_len, flops_per_step=r["flops"])
+    else:
+        config.update(kv_heads=spec.num_kv_heads, head_dim=spec.head_dim, kv_dtype=spec.kv_dtype,
+                      max_query_len=spec.max_query_len, sliding_window=window, sinks=bool(sinks), use_tcgen05=tc)
+    api = "paged_attn_mla_decode" if mla else "paged_attn_decode"
+    config.update({"kv_bytes_per_step": r["step_bytes"], "kv_pools_rotated": r["pools"],
+                   "l2": "no flush; each step reads >= 2x L2 of KV (pools rotated when one is smaller)",
+                   "step_mode": f"CUDA graph replay; a step = one {api} call (split + merge)",
+                   "timed_windows": f"{r['repeats']} windows of exactly {args.steps} steps; value from the median "
+                                    f"window",
+                   "plan": r["plan"]})
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": r["traffic"], "kernel": r["kernel"], "peak_source": f"{peak_kind} hbm_gbs",
+            "split_kernel_us_mean": split_mean * 1e3, "split_kernel_us_median": statistics.median(r["split_ms"]) * 1e3,
+            "per_launch_bytes": r["step_bytes"]}
+    if mla:
+        roof["tensor_tflops"] = r["flops"] / (split_mean * 1e-3) / 1e12
+    return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
+        "warmup": args.warmup, "ms_per_step": r["ms"], "us_per_step": r["ms"] * 1e3,
         "frac_of_hbm_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f8e4m3" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
-        "config": {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
-                   "kv_lora_rank": spec.kv_lora_rank, "rope_dim": spec.rope_dim, "kv_dtype": spec.kv_dtype,
-                   "max_query_len": spec.max_query_len, "kv_bytes_per_step": step_bytes, "kv_pools_rotated": pools,
-                   "flops_per_step": flops,
-                   "l2": "no flush; each step reads >= 2x L2 of latent cache (pools rotated when one is smaller)",
-                   "step_mode": "CUDA graph replay; a step = one paged_attn_mla_decode call (split + merge)",
-                   "plan": plan},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic_from_profiles(spec.name, kernel), "kernel": kernel,
-                     "peak_source": f"{peak_kind} hbm_gbs", "split_kernel_us_mean": split_mean * 1e3,
-                     "per_launch_bytes": step_bytes, "tensor_tflops": flops / (split_mean * 1e-3) / 1e12},
-        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+        "config": config, "roofline": roof,
+        "e2e": {"value": r["step_bytes"] / (r["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
                 "note": "per step: one copy of the packed inputs from pinned host memory, the API call from "
                         "Python, one copy of the packed out / lse back"},
-        "direct_call": {"value": step_bytes * world / (direct_ms * 1e-3) / 1e9, "unit": "GB/s",
-                        "ms_per_step": direct_ms,
-                        "note": "paged_attn_mla_decode called from Python each step (no CUDA graph)"},
-        "gpu_launches": 2 * args.steps,
-        "clocks": clocks,
-        "device_status": status,
+        "direct_call": {"value": r["step_bytes"] * world / (r["direct_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                        "ms_per_step": r["direct_ms"],
+                        "note": f"{api} called from Python each step (no CUDA graph)"},
+        "gpu_launches": 2 * args.steps * r["repeats"],   # split + merge per timed step
+        "clocks": r["clocks"],
+        "device_status": r["status"],
     }
-    if not args.no_cpu_baseline and not args.batch:
-        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
-    print(json.dumps(line), flush=True)
+
+
+# Workloads measured beside the headline one in the same process (their
+# `per_config` entries): the other decode configurations, then the extensions.
+PER_CONFIG = ["tiny", "batch1_32k", "fp8", "mtp", "verify8", "fp8_pertoken", "mla_tp8", "mla_mtp_fp8"]
+
+
+def _per_config_entry(r, args, world):
+    ln = _line(r, args, world)
+    roof = ln["roofline"]
+    return {"us_per_step": ln["us_per_step"], "kv_gbs": ln["value"], "frac": ln["frac_of_hbm_peak"],
+            "split_kernel_us": roof["split_kernel_us_mean"], "split_kernel_frac": roof["frac"],
+            "traffic": roof["traffic"], "kernel": roof["kernel"], "kv_bytes_per_step": r["step_bytes"],
+            "e2e_gbs": ln["e2e"]["value"], "timed_windows": r["repeats"], "clocks": ln["clocks"],
+            "device_status": r["status"], "dtype": ln["dtype"]}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from paged_kv_decode_06_gb300 import workloads as wl
+    dev = _setup_rank(local, world)
+    mla = args.config in wl.MLA_CONFIGS
+    if mla:
+        spec = wl.MLA_CONFIGS[args.config]
+        if args.batch:
+            import dataclasses
+            spec = dataclasses.replace(spec, num_seqs=args.batch, name=f"{spec.name}_b{args.batch}")
+        r = measure_mla(spec, args, world, local, dev)
+    else:
+        spec = _spec_for(args)
+        r = measure_decode(spec, args, world, local, dev, window=args.window, sinks=args.sinks, tc=args.tc)
+    per_config = {}
+    if not args.no_per_config and not args.batch and args.window == 0 and not args.sinks and args.tc == 0:
+        for name in PER_CONFIG:
+            if name == args.config:
+                continue
+            if name in wl.MLA_CONFIGS:
+                pr = measure_mla(wl.MLA_CONFIGS[name], args, world, local, dev)
+            else:
+                pr = measure_decode(wl.CONFIGS[name], args, world, local, dev)
+            per_config[name] = _per_config_entry(pr, args, world)
+    if rank == 0:
+        line = _line(r, args, world, window=args.window, sinks=args.sinks, tc=args.tc)
+        if per_config:
+            line["per_config"] = per_config
+            line["gpu_launches"] += sum(2 * args.steps * e["timed_windows"] for e in per_config.values())
+        if not args.no_cpu_baseline and not args.batch:
+            line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
+        print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -806,6 +868,10 @@ def main():
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
     ap.add_argument("--per-token", action="store_true", help="cache_write: fp8 with one scale per row")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="decode: repeat the K-step timed window until the windows add up to this long")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="decode: measure only --config (no per_config entries for the other workloads)")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="reference arm: most oracle seconds a step")
     ap.add_argument("--ref-total", type=float, default=120.0,
                     help="reference arm: oracle seconds of the whole run (split over warm-up and timed steps)")
@@ -815,8 +881,6 @@ def main():
         run_reference(args, world, rank)
     elif args.op == "cache_write":
         run_cache_write(args, world, rank, local)
-    elif args.config.startswith("mla"):
-        run_mla(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 
