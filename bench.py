@@ -543,7 +543,7 @@ def measure_decode(spec, args, world, local, dev, window=0, sinks=False, tc=0):
                 kernel=kernel, traffic=_traffic_from_profiles(spec.name, kernel), flops=None)
 
 
-def measure_mla(spec, args, world, local, dev):
+def measure_mla(spec, args, world, local, dev, tc=0):
     """measure_decode for MLA decode (paged_attn_mla_decode) on a latent cache
     [NB, 16, 576]: every cached row is read once per step."""
     import numpy as np
@@ -565,16 +565,18 @@ def measure_mla(spec, args, world, local, dev):
     out = torch.empty((T, spec.num_q_heads, spec.kv_lora_rank), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, spec.num_q_heads), dtype=torch.float32, device=dev)
 
+    kopts = binding.make_options(use_tcgen05=tc) if tc else None
+
     def step(k, opts=None, stream_=None):
         w = works[k % pools]
         binding.paged_attn_mla_decode(w.q, w.kv_cache, bt, sl, qsl, mq, spec.scale, spec.kv_scale, out=out, lse=lse,
-                                      options=opts, stream=stream_)
+                                      options=opts if opts is not None else kopts, stream=stream_)
 
     ev_opt = {}
 
     def ev_opts_for(pidx, ea, eb):
         if "o" not in ev_opt:
-            ev_opt["o"] = binding.make_options(split_start_event=ea, split_stop_event=eb)
+            ev_opt["o"] = binding.make_options(split_start_event=ea, split_stop_event=eb, use_tcgen05=tc)
         return ev_opt["o"]
 
     ms, split_ms, direct_ms, clocks, repeats = _timed_passes(step, ev_opts_for, pools, args, world, local, dev)
@@ -582,19 +584,21 @@ def measure_mla(spec, args, world, local, dev):
     def e2e_call(k, q, bt_, sl_, qsl_, out_, lse_):
         w = works[k % pools]
         binding.paged_attn_mla_decode(q, w.kv_cache, bt_, sl_, qsl_, mq, spec.scale, spec.kv_scale, out=out_,
-                                      lse=lse_)
+                                      lse=lse_, options=kopts)
 
     e2e_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
     status = binding.paged_attn_device_status(clear=True)
-    plan = binding.paged_attn_mla_plan(spec.num_seqs, spec.num_q_heads, binding.kv_dtype_code(spec.kv_dtype), mq)
+    plan = binding.paged_attn_mla_plan(spec.num_seqs, spec.num_q_heads, binding.kv_dtype_code(spec.kv_dtype), mq,
+                                       options=binding.make_options(use_tcgen05=tc))
     # tensor work per step: 2 * rows * (576 + 512) flops per cached token of each row's sequence
     rows_tokens = int((base.seq_lens.astype(np.int64) * base.query_lens.astype(np.int64)).sum()) * spec.num_q_heads
     flops = 2 * rows_tokens * (spec.head_dim + spec.kv_lora_rank)
     del works, base, out, lse
     torch.cuda.empty_cache()
+    kernel = "pa_mla_tc_kernel" if plan["variant"] == 3 else "pa_mla_kernel"
     return dict(spec=spec, step_bytes=step_bytes, pools=pools, ms=ms, split_ms=split_ms, direct_ms=direct_ms,
                 clocks=clocks, repeats=repeats, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, status=status, plan=plan,
-                kernel="pa_mla_kernel", traffic=_traffic_from_profiles(spec.name, "pa_mla_kernel"), flops=flops)
+                kernel=kernel, traffic=_traffic_from_profiles(spec.name, kernel), flops=flops)
 
 
 def _line(r, args, world, window=0, sinks=False, tc=0):
@@ -604,7 +608,7 @@ def _line(r, args, world, window=0, sinks=False, tc=0):
     split_mean = statistics.mean(r["split_ms"])
     achieved = r["step_bytes"] / (split_mean * 1e-3) / 1e9
     value = job_throughput_gbs(r["step_bytes"], world, r["ms"])
-    mla = r["kernel"] == "pa_mla_kernel"
+    mla = r["kernel"] in ("pa_mla_kernel", "pa_mla_tc_kernel")
     config = {"workload": spec.name, "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads}
     if mla:
         config.update(kv_lora_rank=spec.kv_lora_rank, rope_dim=spec.rope_dim, kv_dtype=spec.kv_dtype,
@@ -670,7 +674,7 @@ def run_ours(args, world, rank, local):
         if args.batch:
             import dataclasses
             spec = dataclasses.replace(spec, num_seqs=args.batch, name=f"{spec.name}_b{args.batch}")
-        r = measure_mla(spec, args, world, local, dev)
+        r = measure_mla(spec, args, world, local, dev, tc=args.tc)
     else:
         spec = _spec_for(args)
         r = measure_decode(spec, args, world, local, dev, window=args.window, sinks=args.sinks, tc=args.tc)
@@ -828,7 +832,8 @@ def kernel_source_sha256(kernel):
     else:
         names = ["pa_split.cuh", "pa_device.cuh", "pa_pack.cuh"] + \
             (["pa_split_tc.cuh"] if kernel == "pa_split_tc_kernel" else []) + \
-            (["pa_mla.cu"] if kernel == "pa_mla_kernel" else [])
+            (["pa_mla.cu"] if kernel == "pa_mla_kernel" else []) + \
+            (["pa_split_tc.cuh", "pa_mla_tc.cu"] if kernel == "pa_mla_tc_kernel" else [])
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(ROOT, "paged_kv_decode_06_gb300", "csrc", name), "rb") as f:
@@ -863,7 +868,7 @@ def main():
     ap.add_argument("--window", type=int, default=0, help="decode: sliding window of W keys (0 = off)")
     ap.add_argument("--sinks", action="store_true", help="decode: per-query-head attention sinks")
     ap.add_argument("--tc", type=int, default=0, choices=[0, 1, 2],
-                    help="decode split kernel: 0 planner's choice, 1 mma.sync, 2 tcgen05 (bf16)")
+                    help="split kernel: 0 planner's choice, 1 mma.sync, 2 tcgen05 (grouped-query: bf16 caches)")
     ap.add_argument("--tokens", type=int, default=16384, help="cache_write: tokens written per step")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"], help="cache_write: cache dtype")
     ap.add_argument("--per-token", action="store_true", help="cache_write: fp8 with one scale per row")

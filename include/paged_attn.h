@@ -118,6 +118,12 @@ typedef struct pa_options_t {
                                   are then undefined (the affected rows keep stale partials).  The
                                   mma.sync split kernel only (PA_ERR_UNSUPPORTED for the tcgen05 and
                                   MLA kernels) */
+  int32_t segment_cost_pages;  /* tensor-memory MLA kernel: the work split charges
+                                  every unit (sequence, head chunk) a CTA starts this many pages on
+                                  top of its pages, so CTAs that open more units get fewer pages
+                                  (a unit costs a Q staging and an epilogue).  0 = the planner's
+                                  value for the shape; < 0 = an equal page split.  Ignored by the
+                                  other kernels */
 } pa_options_t;
 
 /* Launch plan the library picks for a problem shape (for tests, tuning and
@@ -301,8 +307,12 @@ int paged_attn_cache_write_per_token(const pa_tensor_t* key, const pa_tensor_t* 
  *   lse             f32 [T, Hq] or data == NULL.
  *   opts            (the _ex form) num_ctas, min_pages_per_cta, disable_pdl,
  *                   workspace / workspace_bytes, wait_limit_us and the split events
- *                   apply; use_tcgen05 picks the split kernel (0 or 1: the mma.sync
- *                   kernel, 2: the tensor-memory kernel); the grouped-query
+ *                   apply; use_tcgen05 picks the split kernel (0: the planner's
+ *                   choice, the tensor-memory kernel for fp8 caches or units of
+ *                   more than 16 rows, else the mma.sync kernel; 1: always the
+ *                   mma.sync kernel; 2: always the tensor-memory kernel);
+ *                   segment_cost_pages tunes the tensor-memory kernel's work
+ *                   split; the grouped-query
  *                   options (heads_per_cta, sliding_window, sinks, token scales,
  *                   test_starve_cta) are rejected with PA_ERR_UNSUPPORTED.
  *

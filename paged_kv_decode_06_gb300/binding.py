@@ -35,7 +35,8 @@ class PaOptions(ctypes.Structure):
                 ("split_start_event", ctypes.c_void_p), ("split_stop_event", ctypes.c_void_p),
                 ("use_tcgen05", ctypes.c_int32),
                 ("k_token_scales", ctypes.POINTER(PaTensor)), ("v_token_scales", ctypes.POINTER(PaTensor)),
-                ("wait_limit_us", ctypes.c_int32), ("test_starve_cta", ctypes.c_int32)]
+                ("wait_limit_us", ctypes.c_int32), ("test_starve_cta", ctypes.c_int32),
+                ("segment_cost_pages", ctypes.c_int32)]
 
 
 class PaPlan(ctypes.Structure):
@@ -170,13 +171,16 @@ def _stream_handle(stream) -> int:
 def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=False, workspace=None,
                  workspace_bytes=0, split_start_event=None, split_stop_event=None, page_pairing=0,
                  sliding_window=0, sinks=None, use_tcgen05=0, k_token_scales=None,
-                 v_token_scales=None, wait_limit_us=0, test_starve_cta=0) -> PaOptions:
+                 v_token_scales=None, wait_limit_us=0, test_starve_cta=0,
+                 segment_cost_pages=0) -> PaOptions:
     """Options for paged_attn_decode_ex.  sinks: CUDA float32 tensor [Hq] (kept
     alive by the caller) or None.  use_tcgen05: 0 planner's choice, 1 never,
     2 always (bf16 caches).  k_token_scales / v_token_scales: CUDA float32
     [NB, Hkv, 16] per-token scales of an fp8 cache (kept alive by the caller).
     wait_limit_us: pipeline wait limit (0 = 2 s).  test_starve_cta: testing aid,
-    k > 0 makes split CTA k-1 receive no pages (its waits run out)."""
+    k > 0 makes split CTA k-1 receive no pages (its waits run out).
+    segment_cost_pages: tensor-memory MLA work split, pages charged per unit a
+    CTA starts (0 planner's value, < 0 equal page split)."""
     o = PaOptions()
     o.num_ctas = num_ctas
     o.min_pages_per_cta = min_pages_per_cta
@@ -187,6 +191,7 @@ def make_options(num_ctas=0, min_pages_per_cta=0, heads_per_cta=0, disable_pdl=F
     o.use_tcgen05 = use_tcgen05
     o.wait_limit_us = wait_limit_us
     o.test_starve_cta = test_starve_cta
+    o.segment_cost_pages = segment_cost_pages
     if sinks is not None:
         if sinks.dtype != torch.float32 or not sinks.is_contiguous():
             raise TypeError("sinks must be a contiguous float32 tensor")

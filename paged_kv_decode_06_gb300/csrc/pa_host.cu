@@ -28,6 +28,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxSeqs = 8192;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxStages = 32;
+constexpr int kMaxSegCost = 1 << 20;           // segment_cost_pages bound (keeps the split's cost prefix in range)
+constexpr int kMlaTcSegCostBf16 = 12, kMlaTcSegCostFp8 = 36;
 constexpr int kDefaultMinPages = 4;
 constexpr int kMaxRowsMma = 64;      // query rows per KV head of the mma.sync kernel
 constexpr int kMaxRowsTc = 128;      // ... and of the tensor-memory kernel (bf16 caches)
@@ -604,6 +606,8 @@ struct MlaPlan {
   bool tc;     // tensor-memory kernel
   int rpad;    // tc: rows of a unit padded to 16 or 32 (the P V product's N)
   uint32_t stage_bytes, q_slot_bytes, off_stage, off_q, off_xchg, off_bar, team_bytes, off_prefix, smem, off_buf;
+  uint32_t off_qring;   // tc: the Q staging ring
+  int seg_cost;         // tc: pages the work split charges per unit a CTA starts
   size_t ws_unit, ws_ml, ws_o, ws_bytes;
 };
 
@@ -614,6 +618,8 @@ int check_mla_options(const pa_options_t* opts) {
   if (opts->page_pairing < 0 || opts->page_pairing > 2)
     return fail(PA_ERR_INVALID_ARG, "page_pairing %d not in {0, 1, 2}", opts->page_pairing);
   if (opts->wait_limit_us < 0) return fail(PA_ERR_INVALID_ARG, "wait_limit_us %d is negative", opts->wait_limit_us);
+  if (opts->segment_cost_pages > kMaxSegCost)
+    return fail(PA_ERR_INVALID_ARG, "segment_cost_pages %d > %d", opts->segment_cost_pages, kMaxSegCost);
   if (opts->heads_per_cta != 0 || opts->sliding_window > 0 || opts->sinks != nullptr || has_token_scales(opts) ||
       opts->test_starve_cta != 0)
     return fail(PA_ERR_UNSUPPORTED, "MLA decode takes none of heads_per_cta, sliding_window, sinks, token scales, "
@@ -649,32 +655,61 @@ int make_mla_plan(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t*
   p.RT = (p.R_max + 15) / 16;
   p.min_pages = (opts && opts->min_pages_per_cta > 0) ? opts->min_pages_per_cta : kDefaultMinPages;
   p.grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : num_sms;
-  // The tensor-memory kernel when the caller asks for it (use_tcgen05 = 2); a
-  // unit's rows (at most 32) always fit it.
-  p.tc = opts && opts->use_tcgen05 == 2;
+  // The tensor-memory kernel when the caller asks for it (use_tcgen05 = 2) or,
+  // by default, where it measured faster: fp8 caches (the converter warps
+  // feed the tensor cores f16 rows once a page, where the mma.sync kernel
+  // converts per fragment) and units of more than 16 rows (one M = 128 Q K^T
+  // covers 32 rows as cheaply as 16).  A unit's rows (at most 32) always fit.
+  const int tcsel = opts ? opts->use_tcgen05 : 0;
+  p.tc = tcsel == 2 || (tcsel == 0 && (p.esz == 1 || p.R_max > 16));
   if (p.tc) {
-    // one worker a CTA; shared memory: the two block buffers (4 pages of rows
-    // in the MMA layout), the P buffers, a ring of raw page slots, barriers, the
-    // softmax exchange, sequence metadata
+    // one worker a CTA; shared memory: the three block buffers (3 pages of
+    // rows in the MMA layout), the P buffers, a ring of raw page slots, the Q
+    // staging ring, barriers, the softmax exchange, sequence metadata
     p.rpad = p.R_max <= 16 ? 16 : 32;
+    // a unit a CTA starts costs about a Q staging, an epilogue and a pipeline
+    // refill: measured, near 4 blocks of 3 pages (bf16) and 12 (fp8)
+    const int sc = opts ? opts->segment_cost_pages : 0;
+    p.seg_cost = sc < 0 ? 0 : (sc > 0 ? sc : (p.esz == 1 ? kMlaTcSegCostFp8 : kMlaTcSegCostBf16));
     p.nteam = 1;
     p.threads = pa::mla_tc_threads();
-    p.q_slots = 1;
     p.pair = 0;
-    const uint32_t buf_bytes = 2u * 9u * 4u * 2048u;
-    const uint32_t p_bytes = 2u * (p.esz == 1 ? 1u : 2u) * static_cast<uint32_t>(p.rpad) * 128u;
+    // three block buffers of 3 pages in the MMA layout; fp8 caches add a ring
+    // of raw page slots for the converters (bf16 boxes land in the buffers)
+    const uint32_t buf_bytes = 3u * 9u * 3u * 2048u;
+    const uint32_t p_bytes = 2u * static_cast<uint32_t>(p.rpad) * 128u;
     p.stage_bytes = static_cast<uint32_t>(kPageSize * kMlaDqk * p.esz);
-    const uint32_t bars = static_cast<uint32_t>(align_up(8u * (2 * kMaxStages + 16), 128));
-    const uint32_t xchg = 4096;
+    const uint32_t xchg = 3328;   // alpha [4][32] f32, flags [4][4], row factors [32] f32, row outputs [32] pointers
     const uint32_t prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));
+    const uint32_t qslot = static_cast<uint32_t>(p.rpad) * 208u;   // one 192-byte slice of every Q row
     p.off_buf = 0;
     p.off_q = buf_bytes;
     p.off_stage = p.off_q + p_bytes;
-    const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - p.off_stage - bars - xchg - prefix_bytes;
-    p.nstage = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / p.stage_bytes)) : 0;
-    if (p.nstage < 2)
+    // A Q ring of 6 slots (a whole Q in flight) if it fits beside an fp8 raw
+    // ring of at least 4 page slots, else 2 slots; then the deepest raw ring
+    // whose barriers (2 a slot + 19 + 1 a Q slot) still fit
+    uint32_t bars = 0;
+    bool placed = false;
+    for (const int qr : {6, 2}) {
+      const int min_stages = p.esz == 1 ? (qr == 6 ? 4 : 2) : 0;
+      for (p.nstage = p.esz == 1 ? kMaxStages : 0; p.nstage >= min_stages; --p.nstage) {
+        bars = static_cast<uint32_t>(align_up(8u * (2 * p.nstage + 19 + qr), 128));
+        if (1024 + static_cast<int64_t>(p.off_stage) + static_cast<int64_t>(p.nstage) * p.stage_bytes +
+                static_cast<int64_t>(qr) * qslot + bars + xchg + prefix_bytes <=
+            smem_optin) {
+          placed = true;
+          break;
+        }
+      }
+      if (placed) {
+        p.q_slots = qr;
+        break;
+      }
+    }
+    if (!placed)
       return fail(PA_ERR_UNSUPPORTED, "no tcgen05 MLA launch configuration fits %d bytes of shared memory", smem_optin);
-    p.off_bar = p.off_stage + static_cast<uint32_t>(p.nstage) * p.stage_bytes;
+    p.off_qring = p.off_stage + static_cast<uint32_t>(p.nstage) * p.stage_bytes;
+    p.off_bar = p.off_qring + static_cast<uint32_t>(p.q_slots) * qslot;
     p.off_xchg = p.off_bar + bars;
     p.off_prefix = p.off_xchg + xchg;
     p.team_bytes = 0;
@@ -723,13 +758,14 @@ int make_mla_plan(int B, int Hq, int kv_dtype, int max_qlen, const pa_options_t*
 
 // TMA map over a latent cache [NB, 16, 576] with dimensions (feature within a
 // 64-feature block, slot, block, page): one box = a whole page, landing as 9
-// column blocks of 16 swizzled rows.
-int encode_mla_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int64_t NB) {
+// column blocks of 16 swizzled rows (box_blocks = 9), or one column block of
+// one page (box_blocks = 1).
+int encode_mla_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int64_t NB, int box_blocks) {
   cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(kPageSize), static_cast<cuuint64_t>(kMlaDqk / 64),
                         static_cast<cuuint64_t>(NB)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->stride[1]) * esz, static_cast<cuuint64_t>(64 * esz),
                            static_cast<cuuint64_t>(t->stride[0]) * esz};
-  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(kPageSize), static_cast<cuuint32_t>(kMlaDqk / 64), 1u};
+  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(kPageSize), static_cast<cuuint32_t>(box_blocks), 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUresult r = g_encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                               t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -804,8 +840,9 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
     return st;
   void* ws = nullptr;
   if ((st = acquire_workspace(ds, opts, pl.ws_bytes, stream, "paged_attn_mla_reserve", &ws)) != PA_OK) return st;
-  CUtensorMap tm;
-  if ((st = encode_mla_map(&tm, kc, esz, NB)) != PA_OK) return st;
+  CUtensorMap tm, tb;
+  if ((st = encode_mla_map(&tm, kc, esz, NB, kMlaDqk / 64)) != PA_OK) return st;
+  if ((st = encode_mla_map(&tb, kc, esz, NB, 1)) != PA_OK) return st;
 
   const float kLog2e = 1.4426950408889634f;
   pa::SplitParams sp = {};
@@ -856,6 +893,8 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
   sp.starve_cta = -1;
   sp.pair_pages = pl.pair;
   sp.off_buf = pl.off_buf;
+  sp.off_qring = pl.off_qring;
+  sp.seg_cost = pl.tc ? pl.seg_cost : 0;
 
   pa::MergeParams mp = {};
   mp.out = sp.out;
@@ -893,7 +932,7 @@ int mla_decode_impl(const pa_tensor_t* q, const pa_tensor_t* kc, const pa_tensor
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, stream, rec_flags)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(start)");
   if (pl.tc)
-    e = pa::launch_mla_tc(esz == 1, pl.rpad, tm, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
+    e = pa::launch_mla_tc(esz == 1, pl.rpad, tm, tb, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
   else
     e = pa::launch_mla(esz == 1, pl.RT, tm, sp, pl.grid, static_cast<int>(pl.smem), pdl && !ev0, stream);
   if (e != cudaSuccess) return cuda_fail(e, "MLA split kernel launch");
@@ -1141,7 +1180,7 @@ int paged_attn_mla_plan(int32_t num_seqs, int32_t num_q_heads, int32_t kv_dtype,
   plan->page_pairing = pl.pair;
   plan->workspace_bytes = static_cast<int64_t>(pl.ws_bytes);
   plan->variant = pl.tc ? 3 : 2;
-  plan->block_pages = pl.tc ? 4 : (pl.pair ? 2 : 1);
+  plan->block_pages = pl.tc ? 3 : (pl.pair ? 2 : 1);
   return PA_OK;
 }
 

@@ -61,16 +61,21 @@ struct SplitParams {
   int64_t tok_stride_page;  // floats between pages of the scale tensors
   uint32_t tok_bytes;       // HC * 16 * 4: one tensor's scales of one page
   // MLA kernel: bytes between the shared-memory regions of a CTA's teams,
-  // query slots per team (1 or 2)
+  // query slots per team (1 or 2); tensor-memory MLA kernel: slots of the Q
+  // staging ring
   uint32_t team_bytes;
   int32_t q_slots;
-  // tensor-memory MLA kernel: the two block buffers (rows in the MMA layout)
+  // tensor-memory MLA kernel: the three block buffers (rows in the MMA layout)
   uint32_t off_buf;
   // pipeline waits give up after wait_ns nanoseconds (status bit 3)
   uint64_t wait_ns;
   // testing aid (mma.sync kernel): the producer of split CTA starve_cta issues
   // no copies, so that CTA's consumers run into the wait limit; -1 = none
   int32_t starve_cta;
+  // tensor-memory MLA kernel: the Q staging ring; pages the work split
+  // charges for every unit a CTA starts (0: an equal page split)
+  uint32_t off_qring;
+  int32_t seg_cost;
 };
 
 struct MergeParams {
@@ -144,10 +149,12 @@ int mla_teams(int rt);
 cudaError_t set_mla_smem_limits(int smem);
 // Tensor-memory (tcgen05) MLA decode: one head chunk of at most rpad (16 or
 // 32) query rows per unit, mla_tc_threads() threads a CTA; shared-memory
-// layout in p.off_buf (block buffers), p.off_q (P buffers), p.off_stage (raw
-// page ring of p.nstage slots), p.off_bar, p.off_xchg, p.off_prefix.
-cudaError_t launch_mla_tc(bool fp8, int rpad, const CUtensorMap& tm, const SplitParams& p, int grid, int smem,
-                          bool pdl, cudaStream_t stream);
+// layout in p.off_buf (block buffers), p.off_q (P buffers), p.off_stage (fp8:
+// raw page ring of p.nstage slots), p.off_bar, p.off_xchg, p.off_prefix.  tm:
+// a whole page per box (fp8), tb: one 64-feature column block of a page per
+// box (bf16).
+cudaError_t launch_mla_tc(bool fp8, int rpad, const CUtensorMap& tm, const CUtensorMap& tb, const SplitParams& p,
+                          int grid, int smem, bool pdl, cudaStream_t stream);
 int mla_tc_threads();
 cudaError_t set_mla_tc_smem_limits(int smem);
 // LSE merge of MLA partials (512 value columns; the split kernel writes each

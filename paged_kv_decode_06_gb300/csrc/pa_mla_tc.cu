@@ -19,21 +19,29 @@
 // query rows on the tensor-memory lanes (the padded rows past R are never read),
 // so the softmax is a thread per row that owns all of a block's keys.
 //
-// A block is up to 4 pages (64 keys) of one segment.  Per block:
+// A block is up to 3 pages (48 keys) of one segment.  Per block:
 //   S[128 x 16np]     = Q[128 x 576] K^T        36 TS-MMAs (Q in tensor memory)
-//   O^T[vb][128 x R]  += V^T[vb] P^T            4 SS-MMAs a page (bf16 caches: twice,
-//                                                P carried as bf16 hi + lo terms)
-// Tensor memory (512 columns): O^T [0, 4 R_pad), S [128, 192), Q [192, 480).
+//   O^T[vb][128 x R]  += V^T[vb] P^T            4 SS-MMAs a page (P in f16 for fp8
+//                                                caches, bf16 for bf16 caches, as the
+//                                                mma.sync MLA kernel carries it)
+// Tensor memory (512 columns): O^T [0, 4 R_pad), S [4 R_pad, +64) (two S
+// buffers [64, 192) for R_pad = 16), Q [192, 480).
 //
+// A block's rows sit in one of three block buffers in the MMA layout
+// ([column block][page][16 rows x 128 B], 128-byte swizzle), so the rows of the
+// next two blocks arrive while a block is computed.
 // Roles (352 threads):
-//   warp 0      producer: block-table lookups, one TMA box per page (the whole
-//               16 x 576 row block) into a ring of raw page slots;
+//   bf16 caches: warps 0, 3, 8-10 producers: block-table lookups and one TMA
+//               box (16 rows x 64 features) per page and column block, straight
+//               into the block's buffer, the boxes dealt one a lane over the five
+//               warps;
+//   fp8 caches: warp 0 producer: one TMA box per page (the whole 16 x 576 row
+//               block) into a ring of raw page slots; warps 3, 8-10 converters:
+//               each raw page into the block's buffer, codes to f16 (exact),
+//               rows past the sequence end zeroed;
 //   warp 1      Q K^T issuer, owner of the tensor-memory allocation;
-//   warp 2      P V issuer;
-//   warps 3, 8-10 converters: each raw page into the MMA layout of the block's
-//               buffer ([column block][page][16 rows x 128 B], 128-byte
-//               swizzle): bf16 rows are copied, fp8 codes become f16 (exact);
-//               value rows past the sequence end are zeroed;
+//   warp 2      P V issuer (bf16 caches: zeroes the value rows past the
+//               sequence end first);
 //   warps 4-7   softmax, thread = query row = tensor-memory lane: S row, mask,
 //               block max, exponentials into the P buffer (shared memory, the
 //               B operand of P V), lazy O rescale, segment epilogue.
@@ -51,18 +59,36 @@ namespace {
 constexpr int kMtcDqk = 576;
 constexpr int kMtcDv = 512;
 constexpr int kMtcCb = kMtcDqk / 64;             // 64-feature column blocks of a row
-constexpr int kMtcBlockPages = 4;
+constexpr int kMtcBlockPages = 3;
+constexpr int kMtcNbuf = 3;                       // block buffers
 constexpr uint32_t kMtcTile = 2048;               // MMA layout: one page of one column block, 16 x 128 B
 constexpr uint32_t kMtcCbStride = kMtcBlockPages * kMtcTile;
-constexpr uint32_t kMtcBuf = kMtcCb * kMtcCbStride;   // one block's rows in the MMA layout (72 KB)
+constexpr uint32_t kMtcBuf = kMtcCb * kMtcCbStride;   // one block's rows in the MMA layout (54 KB)
 constexpr int kMtcThreads = 352;
 constexpr int kMtcProducer = 0, kMtcQkWarp = 1, kMtcPvWarp = 2, kMtcSoftmax0 = 4;
-constexpr int kMtcConverters = 4;                 // warps 3, 8, 9, 10
+constexpr int kMtcConverters = 4;                 // fp8: warps 3, 8, 9, 10
+constexpr int kMtcBoxProducers = 5;               // bf16: warps 0, 3, 8, 9, 10
 constexpr uint32_t kMtcCols = 512;
-constexpr uint32_t kMtcTmemO = 0, kMtcTmemS = 128, kMtcTmemQ = 192;
+constexpr uint32_t kMtcTmemO = 0, kMtcTmemQ = 192;   // S: see mtc_tmem_s
 constexpr int kMtcQsteps = kMtcDqk / 16;          // k-steps of Q K^T
+// Q staging ring: a slot holds one 96-feature slice (192 B) of every row, rows
+// 208 B apart (odd multiple of 16 B: the 16-byte reads of 8 lanes hit
+// distinct banks)
+constexpr int kMtcQslices = 6;
+constexpr uint32_t kMtcQsliceBytes = kMtcDqk * 2 / kMtcQslices;
+constexpr uint32_t kMtcQrow = kMtcQsliceBytes + 16;
+static_assert(kMtcQsliceBytes % 64 == 0, "a slice is whole groups of 16 tensor-memory columns");
 
 __device__ __forceinline__ int converter_index(int warp) { return warp == 3 ? 0 : warp - 7; }
+__device__ __forceinline__ int box_producer_index(int warp) { return warp == 0 ? 0 : (warp == 3 ? 1 : warp - 6); }
+
+// S buffers: two when a unit has at most 16 rows (O^T then needs only 64
+// columns), so Q K^T of the next block runs while the softmax reads this one;
+// one for 32 rows.  Tensor-memory column of S buffer x.
+template <int RP>
+__device__ __forceinline__ constexpr uint32_t mtc_tmem_s(int x) {
+  return RP == 16 ? 64u + 64u * static_cast<uint32_t>(x) : 128u;
+}
 
 // Instruction descriptor of kind::f16 (fp32 accumulator): A and B both bf16 or
 // both f16; `a_mn` / `b_mn` select the MN-major (transposed) operand layout.
@@ -76,20 +102,114 @@ __device__ __forceinline__ uint32_t mtc_idesc(int M, int N, bool bf16, bool a_mn
   return d;
 }
 
+// 16 bytes global -> shared without a register round trip (L2 only); this
+// thread's copies complete in commit-group order.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+// An arrival on `bar` once every earlier copy of this thread has landed (the
+// barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Has the phase with the given parity completed?  Never suspends the thread.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// f16x2 -> its two floats (exact).
+__device__ __forceinline__ void f16x2_unpack(uint32_t x, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
+
+// mbarrier.try_wait with a suspend-time hint: a thread whose phase is not
+// complete may sleep up to hint_ns (it resumes when the phase completes), so
+// waiting warps leave the issue slots of their SM sub-partition to the warps
+// that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
 }
 
-// Named-barrier-free bounded wait of all lanes of a warp.
+// Bounded wait of all lanes of a warp (kErrTimeout after limit_ns).
 __device__ __forceinline__ bool mtc_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
+  bool done = mbar_try_wait_sleep(bar, parity, 4096u);
+  if (!done) {
+    const uint64_t t0 = global_timer_ns();
+    while (!(done = mbar_try_wait_sleep(bar, parity, 4096u)))
+      if (global_timer_ns() - t0 > limit_ns) break;
+  }
+  return __all_sync(0xffffffffu, done);
+}
+
+// Work split.  The flattened positions (sequence, head chunk, page) are cut
+// into contiguous ranges, one a CTA, of equal cost: a position costs one
+// page, and every unit (sequence, head chunk) but the first adds W just
+// before its first page, since a CTA pays for every unit it opens (a Q
+// staging, an epilogue, a pipeline refill).  Cost prefix of x: the positions
+// before x plus W for each unit after the first that starts at or before x.
+// Inside a unit the prefix grows by one a page, so (with at most one CTA a
+// page of cost) the CTAs holding a unit's pages are consecutive and none of
+// them is empty.  Units of sequences without pages count too, which keeps
+// the prefix a plain non-decreasing function of the position.
+__device__ __forceinline__ int64_t split_cost(const int32_t* pre, int B, int NC, int64_t W, int64_t x, int64_t X) {
+  if (x >= X) return X + W * (static_cast<int64_t>(NC) * B - 1);
+  const Cursor cu = locate(pre, B, NC, x);
+  return x + W * (static_cast<int64_t>(NC) * cu.i + cu.c);
+}
+
+// First position x in [0, X] whose cost prefix reaches gi / NG of the total
+// (a 32-way search by one warp; every lane returns it).
+__device__ int64_t split_point(const int32_t* pre, int B, int NC, int64_t W, int64_t X, int NG, int gi, int lane) {
+  const int64_t target = static_cast<int64_t>(gi) * split_cost(pre, B, NC, W, X, X);
+  int64_t lo = 0, hi = X;   // the answer lies in [lo, hi]; hi satisfies the test
+  while (lo < hi) {
+    const int64_t span = hi - lo;
+    const int64_t probe = lo + span * lane / 32;
+    const bool hit = split_cost(pre, B, NC, W, probe, X) * NG >= target;
+    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+    if (bal & 1u) {
+      hi = lo;
+    } else if (bal == 0u) {
+      lo = lo + span * 31 / 32 + 1;
+    } else {
+      const int k = __ffs(bal) - 1;
+      const int64_t h = lo + span * k / 32;
+      lo = lo + span * (k - 1) / 32 + 1;
+      hi = h;
+    }
+  }
+  return hi;
 }
 
 // bf16x2 -> f16x2 with a flag for values beyond the f16 range.
@@ -102,24 +222,29 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, bool& fine) {
 }  // namespace
 
 // Shared-memory layout (bytes from the 1024-aligned base), host and device:
-//   off_buf   2 x kMtcBuf          the two block buffers in the MMA layout
-//   off_q     P buffers            2 (block parity) x NPT (hi / lo) x R_pad x 128 B
-//   off_stage raw page slots       nstage x (16 x 576 x esz), as the TMA box lands
+//   off_buf   3 x kMtcBuf          the block buffers in the MMA layout
+//   off_q     P buffers            2 (block parity) x R_pad x 128 B
+//   off_stage raw page slots       fp8: nstage x 16 x 576 bytes, as the TMA box lands
+//   off_qring Q staging ring       q_slots x R_pad rows x 208 B (a 192-byte slice of each row)
 //   off_bar   barriers
-//   off_xchg  softmax exchange     alpha [2][128] f32, flags [2][4] u32, row stats [128] float2
+//   off_xchg  softmax exchange     alpha [4][32] f32, flags [4][4] u32, row factors [32] f32,
+//                                  row outputs [32] pointers
 //   off_prefix sequence metadata
 template <bool FP8, int RP>
 __global__ void __launch_bounds__(kMtcThreads, 1)
-    pa_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
+    pa_mla_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_box,
+                     const SplitParams p) {
   constexpr int ESZ = FP8 ? 1 : 2;
   constexpr uint32_t kRawPage = kPage * kMtcDqk * ESZ;   // one TMA box: [9 blocks][16 rows][64 x esz B]
   constexpr uint32_t kRawBlock = 16u * 64u * ESZ;
-  constexpr int NPT = FP8 ? 1 : 2;                       // P terms
+  constexpr int NPT = 1;                                 // P terms
   constexpr uint32_t kPbuf = static_cast<uint32_t>(RP) * 128u;
+  constexpr int NSB = RP == 16 ? 2 : 1;                  // S buffers
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_scan[kMtcThreads / 32 + 1];
   __shared__ int s_total;
   __shared__ uint32_t s_tmem;
+  __shared__ int64_t s_split[2];
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -137,36 +262,55 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (nstage + s); };
   const uint32_t xb = bar0 + 8u * (2 * nstage);
-  auto cfull_bar = [&](int x) { return xb + 8u * x; };          // block buffer x converted (4 converter warps)
-  auto bfree_bar = [&](int x) { return xb + 8u * (2 + x); };    // block buffer x read by both MMAs (commit)
-  auto pfull_bar = [&](int x) { return xb + 8u * (4 + x); };    // P buffer x written (4 softmax warps)
-  auto pfree_bar = [&](int x) { return xb + 8u * (6 + x); };    // P V of the block in P buffer x done (commit)
-  const uint32_t sfull_bar = xb + 8u * 8;                       // S of a block in tensor memory (commit)
-  const uint32_t sfree_bar = xb + 8u * 9;                       // S read, block statistics published (4 warps)
-  const uint32_t qfull_bar = xb + 8u * 10;                      // a segment's Q in tensor memory (4 warps)
-  const uint32_t ebar = xb + 8u * 11;                           // a segment's row statistics published (4 warps)
-  const uint32_t ofree_bar = xb + 8u * 12;                      // O read by a segment's epilogue (4 warps)
-  const uint32_t drain_bar = xb + 8u * 13;
-  const uint32_t drain2_bar = xb + 8u * 14;
-  float* const x_alpha = reinterpret_cast<float*>(gbase + p.off_xchg);              // [2][128]
-  uint32_t* const x_flag = reinterpret_cast<uint32_t*>(gbase + p.off_xchg + 1024);  // [2][4]
-  float2* const x_stat = reinterpret_cast<float2*>(gbase + p.off_xchg + 1280);      // [128] (m, l)
+  // block buffer x (blocks b with b % 3 == x, phase b / 3): filled (fp8: 4
+  // converter warps; bf16: 5 producer warps and their bytes); read by both
+  // MMAs (commit)
+  auto cfull_bar = [&](int x) { return xb + 8u * x; };
+  auto bfree_bar = [&](int x) { return xb + 8u * (3 + x); };
+  // P buffer x (blocks b with b % 2 == x): written (4 softmax warps); P V of
+  // the block done (commit)
+  auto pfull_bar = [&](int x) { return xb + 8u * (6 + x); };
+  auto pfree_bar = [&](int x) { return xb + 8u * (8 + x); };
+  // per S buffer x (blocks b with b % NSB == x, phase b / NSB): S in tensor
+  // memory (commit); S read and the block's statistics published (4 warps)
+  auto sfull_bar = [&](int x) { return xb + 8u * (10 + x); };
+  auto sfree_bar = [&](int x) { return xb + 8u * (12 + x); };
+  const uint32_t qfull_bar = xb + 8u * 14;                      // a segment's Q in tensor memory (its stager)
+  const uint32_t ebar = xb + 8u * 15;                           // a segment's row statistics published (4 warps)
+  const uint32_t ofree_bar = xb + 8u * 16;                      // O read by a segment's epilogue (4 warps)
+  const uint32_t drain_bar = xb + 8u * 17;
+  const uint32_t drain2_bar = xb + 8u * 18;
+  auto qbar = [&](int x) { return xb + 8u * (19 + x); };       // Q ring slot x landed (32 lanes)
+  const uint32_t qst0 = base + p.off_qring;
+  const uint32_t qslot = static_cast<uint32_t>(RP) * kMtcQrow;
+  // the softmax exchange, by block b % 4: a buffer is rewritten four blocks
+  // later, after every softmax warp has passed block b + 2 (two S buffers) or
+  // b + 1 (one), and so finished block b
+  float* const x_alpha = reinterpret_cast<float*>(gbase + p.off_xchg);              // [4][32]
+  uint32_t* const x_flag = reinterpret_cast<uint32_t*>(gbase + p.off_xchg + 2048);  // [4][4]
+  float* const x_fac = reinterpret_cast<float*>(gbase + p.off_xchg + 2304);         // [32] output factor of a row
+  uint16_t** const x_dst = reinterpret_cast<uint16_t**>(gbase + p.off_xchg + 2432);  // [32] output row of a row
 
   if (tid == 0) {
-    prefetch_tensormap(&tmap);
+    prefetch_tensormap(FP8 ? &tmap : &tmap_box);
     for (int s = 0; s < nstage; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kMtcConverters);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(cfull_bar(x), kMtcConverters);
+    for (int x = 0; x < kMtcNbuf; ++x) {
+      mbar_init(cfull_bar(x), FP8 ? kMtcConverters : kMtcBoxProducers);
       mbar_init(bfree_bar(x), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(pfull_bar(x), 4);
       mbar_init(pfree_bar(x), 1);
     }
-    mbar_init(sfull_bar, 1);
-    mbar_init(sfree_bar, 4);
-    mbar_init(qfull_bar, 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(sfull_bar(x), 1);
+      mbar_init(sfree_bar(x), 4);
+    }
+    mbar_init(qfull_bar, 1);
+    for (int x = 0; x < p.q_slots; ++x) mbar_init(qbar(x), 32);
     mbar_init(ebar, 4);
     mbar_init(ofree_bar, 4);
     mbar_init(drain_bar, 1);
@@ -187,11 +331,34 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
   grid_launch_dependents();
   const int g = blockIdx.x;
   if (g >= NG || X == 0) return;
-  const int64_t start = static_cast<int64_t>(g) * X / NG;
-  const int64_t end = static_cast<int64_t>(g + 1) * X / NG;
+  const int64_t W = p.seg_cost;
+  const int64_t Ctot = split_cost(s_pre, B, NC, W, X, X);
+  if (warp < 2) {
+    const int64_t sp = split_point(s_pre, B, NC, W, X, NG, g + warp, lane);
+    if (lane == 0) s_split[warp] = sp;
+  }
+  __syncthreads();
+  const int64_t start = s_split[0];
+  const int64_t end = s_split[1];
   const int64_t count = end - start;
   if (count <= 0) return;
 
+  if (warp == kMtcSoftmax0) {
+    // the Q rows of this CTA's first segments start towards L2 while tensor
+    // memory is set up (a later staging then waits on L2, not on HBM)
+    int64_t x = start;
+    for (int sg = 0; sg < 4 && x < end; ++sg) {
+      const Cursor cs = locate(s_pre, B, NC, x);
+      const SeqInfo s0 = seq_info(p, s_len, s_qsl, cs.i, false, 0);
+      if (lane < G * s0.qn) {
+        const uint16_t* const src = p.q + static_cast<int64_t>(s0.t0 + lane / G) * p.q_stride_t +
+                                    static_cast<int64_t>(cs.c * G + lane % G) * kMtcDqk;
+#pragma unroll
+        for (int k = 0; k < kMtcDqk * 2 / 128; ++k) prefetch_l2(src + 64 * k);
+      }
+      x += cs.n - cs.j;
+    }
+  }
   if (warp == kMtcQkWarp) tmem_alloc(smem_addr(&s_tmem), kMtcCols);
   tc_fence_before();
   __syncthreads();
@@ -199,10 +366,61 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
   const uint32_t tbase = warp_uniform(s_tmem);
   const uint32_t buf0 = base + p.off_buf;
   const uint32_t pbuf0 = base + p.off_q;
-  const uint32_t ring0 = base + p.off_stage;
+  const uint32_t ring0 = base + p.off_stage;   // raw page slots
 
-  if (warp == kMtcProducer) {
-    // ============================ producer =================================
+  if (!FP8 && (warp == 0 || warp == 3 || warp >= kMtcSoftmax0 + 4)) {
+    // ==================== bf16: box producers ==============================
+    // Box x of a block (page x / 9, column block x % 9) goes to producer warp
+    // x % 5, lane x / 5; each warp announces its own bytes on the block's full
+    // barrier, then its lanes issue their boxes.
+    const int pw = box_producer_index(warp);
+    BlockWalker wk(s_pre, B, NC, start, count, kMtcBlockPages);
+    BlockTableCache btc;
+    int b = 0;
+    bool ok = true;
+    while (wk.more()) {
+      const TcBlock t = wk.next(s_pre, B, NC);
+      const int x = b % kMtcNbuf;
+      // buffer x was last read by the MMAs of block b - 3 (its previous phase,
+      // block b - 6, seen at block b - 3)
+      if (b >= kMtcNbuf && !mtc_wait(bfree_bar(x), static_cast<uint32_t>(b / kMtcNbuf - 1) & 1u, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      int phys[kMtcBlockPages];
+#pragma unroll
+      for (int pg = 0; pg < kMtcBlockPages; ++pg) {
+        phys[pg] = 0;
+        if (pg < t.np) {
+          Cursor pc;
+          pc.i = t.i;
+          pc.c = t.c;
+          pc.j = t.j0 + pg;
+          pc.n = t.n;
+          phys[pg] = btc.lookup(p, pc, s_pre, s_len, s_qsl, B, NC, 0, lane);
+          if ((phys[pg] < 0 || phys[pg] >= p.num_pages) && lane == 0 && pw == 0) atomicOr(p.err, kErrPageRange);
+        }
+      }
+      const int nbox = t.np * kMtcCb;
+      const int mine = nbox > pw ? (nbox - pw + kMtcBoxProducers - 1) / kMtcBoxProducers : 0;
+      if (lane == 0) mbar_arrive_expect_tx(cfull_bar(x), static_cast<uint32_t>(mine) * kMtcTile);
+      __syncwarp();
+      const int bx = kMtcBoxProducers * lane + pw;
+      if (bx < nbox) {
+        const int pg = bx / kMtcCb, cb = bx - pg * kMtcCb;
+        int ph = phys[0];
+#pragma unroll
+        for (int q = 1; q < kMtcBlockPages; ++q) ph = pg == q ? phys[q] : ph;
+        // an out-of-range page id reads zeros (TMA fills outside the tensor)
+        tma_load_4d(buf0 + static_cast<uint32_t>(x) * kMtcBuf + static_cast<uint32_t>(cb) * kMtcCbStride +
+                        static_cast<uint32_t>(pg) * kMtcTile,
+                    &tmap_box, 0, 0, cb, ph, cfull_bar(x));
+      }
+      ++b;
+    }
+    if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
+  } else if (FP8 && warp == kMtcProducer) {
+    // ==================== fp8: page producer ===============================
     Cursor cu = locate(s_pre, B, NC, start);
     BlockTableCache btc;
     int stage = 0;
@@ -226,77 +444,79 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
         ++round;
       }
     }
-  } else if (warp == 3 || warp >= kMtcSoftmax0 + 4) {
-    // ============================ converters ===============================
+  } else if (FP8 && (warp == 3 || warp >= kMtcSoftmax0 + 4)) {
+    // ==================== fp8: converters ==================================
+    // A page is split into 16-byte source chunks dealt over the 128 converter
+    // threads.
+    constexpr int kChunks = kMtcCb * 16 * 4;   // 16-byte source chunks of an fp8 page
+    constexpr int kPer = (kChunks + 127) / 128;
     const int ct = converter_index(warp) * 32 + lane;   // 0..127
     BlockWalker wk(s_pre, B, NC, start, count, kMtcBlockPages);
-    int b = 0;
+    int b = 0, stage = 0;
+    uint32_t round = 0;
     bool ok = true;
     while (wk.more() && ok) {
       const TcBlock t = wk.next(s_pre, B, NC);
-      // buffer b % 2 was last read by the MMAs of block b - 2 (this warp saw
-      // the completion of block b - 4's, the previous phase, at block b - 2)
-      if (b >= 2 && !mtc_wait(bfree_bar(b & 1), static_cast<uint32_t>((b >> 1) - 1) & 1u, p.wait_ns)) {
+      const int xbuf = b % kMtcNbuf;
+      // buffer xbuf was last read by the MMAs of block b - 3 (this warp saw
+      // the completion of block b - 6's, the previous phase, at block b - 3)
+      if (b >= kMtcNbuf && !mtc_wait(bfree_bar(xbuf), static_cast<uint32_t>(b / kMtcNbuf - 1) & 1u, p.wait_ns)) {
         ok = false;
         break;
       }
-      const uint32_t dst0 = buf0 + static_cast<uint32_t>(b & 1) * kMtcBuf;
+      uint8_t* const dst0 = gbase + p.off_buf + static_cast<uint32_t>(xbuf) * kMtcBuf;
       const int L = s_len[t.i];
+#pragma unroll 1
       for (int pg = 0; pg < t.np; ++pg) {
-        const int64_t kk = t.k0 + pg;
-        const int stage = static_cast<int>(kk % nstage);
-        const uint32_t rnd = static_cast<uint32_t>(kk / nstage);
-        if (!mtc_wait(full_bar(stage), rnd & 1u, p.wait_ns)) {
+        if (!mtc_wait(full_bar(stage), round & 1u, p.wait_ns)) {
           ok = false;
           break;
         }
-        const uint32_t src = ring0 + static_cast<uint32_t>(stage) * kRawPage;
+        const uint8_t* const src = gbase + p.off_stage + static_cast<uint32_t>(stage) * kRawPage;
+        uint8_t* const dst = dst0 + static_cast<uint32_t>(pg) * kMtcTile;
         const int vt = L - kPage * (t.j0 + pg);   // rows of this page inside the sequence
-        const uint32_t dst = dst0 + static_cast<uint32_t>(pg) * kMtcTile;
-        if constexpr (FP8) {
-          // 16 codes (a 64-byte-swizzled chunk) -> 16 f16 values (two chunks of
-          // the 128-byte-swizzled MMA row)
-          for (int x = ct; x < kMtcCb * 16 * 4; x += 128) {
+        uint4 v[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {   // all loads first, then all stores
+          const int x = ct + 128 * i;
+          const int cb = x >> 6, r = (x >> 2) & 15, c = x & 3;
+          v[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (x < kChunks && r < vt) v[i] = *reinterpret_cast<const uint4*>(src + cb * kRawBlock + swz<64>(r, c));
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int x = ct + 128 * i;
+          if (x < kChunks) {
+            // 16 codes (a 64-byte-swizzled chunk) -> 16 f16 values (two chunks of
+            // the 128-byte-swizzled MMA row); exact
             const int cb = x >> 6, r = (x >> 2) & 15, c = x & 3;
-            uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-            if (r < vt) {
-              const uint4 v = lds128(src + cb * kRawBlock + swz<64>(r, c));
-              o0.x = e4m3x2_to_f16x2(v.x);
-              o0.y = e4m3x2_to_f16x2(v.x >> 16);
-              o0.z = e4m3x2_to_f16x2(v.y);
-              o0.w = e4m3x2_to_f16x2(v.y >> 16);
-              o1.x = e4m3x2_to_f16x2(v.z);
-              o1.y = e4m3x2_to_f16x2(v.z >> 16);
-              o1.z = e4m3x2_to_f16x2(v.w);
-              o1.w = e4m3x2_to_f16x2(v.w >> 16);
-            }
-            const uint32_t d = dst + static_cast<uint32_t>(cb) * kMtcCbStride;
-            sts128(d + swz<128>(r, 2 * c), o0);
-            sts128(d + swz<128>(r, 2 * c + 1), o1);
-          }
-        } else {
-          // a raw column block is already one 128-byte-swizzled 16 x 128 B tile
-          for (int x = ct; x < kMtcCb * 16 * 8; x += 128) {
-            const int cb = x >> 7, r = (x >> 3) & 15, c = x & 7;
-            const uint32_t off = swz<128>(r, c);
-            const uint4 v = r < vt ? lds128(src + cb * kRawBlock + off) : make_uint4(0u, 0u, 0u, 0u);
-            sts128(dst + static_cast<uint32_t>(cb) * kMtcCbStride + off, v);
+            uint8_t* const d = dst + cb * kMtcCbStride;
+            const uint4 w = v[i];
+            *reinterpret_cast<uint4*>(d + swz<128>(r, 2 * c)) =
+                make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
+                           e4m3x2_to_f16x2(w.y >> 16));
+            *reinterpret_cast<uint4*>(d + swz<128>(r, 2 * c + 1)) =
+                make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
+                           e4m3x2_to_f16x2(w.w >> 16));
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(stage));
+        if (++stage == nstage) {
+          stage = 0;
+          ++round;
+        }
       }
       if (!ok) break;
       fence_proxy_async_smem();   // the tensor cores read what these generic stores wrote
       __syncwarp();
-      if (lane == 0) mbar_arrive(cfull_bar(b & 1));
+      if (lane == 0) mbar_arrive(cfull_bar(xbuf));
       ++b;
     }
     if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
   } else if (warp == kMtcQkWarp) {
     // ============================ Q K^T issuer =============================
     const uint32_t idesc0 = mtc_idesc(128, 16, !FP8, false, false) & ~(0x3Fu << 17);
-    const uint32_t tS = tbase + kMtcTmemS;
     const uint32_t tQ = tbase + kMtcTmemQ;
     BlockWalker wk(s_pre, B, NC, start, count, kMtcBlockPages);
     int b = 0, seg = -1;
@@ -304,26 +524,27 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
     while (wk.more()) {
       const TcBlock t = wk.next(s_pre, B, NC);
       if (t.first) ++seg;
-      // converted rows of the block; the single S buffer read by the softmax
-      // (phase b - 1, after phase b - 2 seen at the previous block); at a
+      // converted rows of the block; its S buffer read by the softmax at block
+      // b - NSB (that buffer's previous phase seen at block b - 2 NSB); at a
       // segment's first block its Q (every segment's phase seen in order)
-      if (!mtc_wait(cfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u, p.wait_ns) ||
-          (b >= 1 && !mtc_wait(sfree_bar, static_cast<uint32_t>(b - 1) & 1u, p.wait_ns)) ||
+      if (!mtc_wait(cfull_bar(b % kMtcNbuf), static_cast<uint32_t>(b / kMtcNbuf) & 1u, p.wait_ns) ||
+          (b >= NSB && !mtc_wait(sfree_bar(b % NSB), static_cast<uint32_t>(b / NSB - 1) & 1u, p.wait_ns)) ||
           (t.first && !mtc_wait(qfull_bar, static_cast<uint32_t>(seg) & 1u, p.wait_ns))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t kb = warp_uniform(buf0 + static_cast<uint32_t>(b & 1) * kMtcBuf);
+      const uint32_t kb = warp_uniform(buf0 + static_cast<uint32_t>(b % kMtcNbuf) * kMtcBuf);
       const uint64_t kd = umma_sdesc_sw128(kb, 16u, 1024u);
       const uint32_t idesc = warp_uniform(idesc0 | (static_cast<uint32_t>(2 * t.np) << 17));   // N = 16 np
+      const uint32_t tS = warp_uniform(tbase + mtc_tmem_s<RP>(b % NSB));
       if (lane == 0) {
-#pragma unroll 4
-        for (int s = 0; s < kMtcQsteps; ++s) {
-          const uint32_t koff = static_cast<uint32_t>(s >> 2) * kMtcCbStride + static_cast<uint32_t>(s & 3) * 32u;
-          umma_ts(tS, tQ + 8u * s, kd + (koff >> 4), idesc, s > 0);
-        }
-        umma_commit(sfull_bar);
+        // k-step s: features 16 s .. +15 = 32-byte slice (s % 4) of column block s / 4
+#pragma unroll
+        for (int s = 0; s < kMtcQsteps; ++s)
+          umma_ts(tS, tQ + 8u * s, kd + ((static_cast<uint32_t>(s >> 2) * kMtcCbStride + (s & 3) * 32u) >> 4), idesc,
+                  s > 0);
+        umma_commit(sfull_bar(b % NSB));
       }
       __syncwarp();
       ++b;
@@ -345,33 +566,52 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
       // here too so the stores are visible to this warp's MMAs; at a
       // segment's first block, the previous segment's epilogue done with O
       if (!mtc_wait(pfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u, p.wait_ns) ||
-          !mtc_wait(cfull_bar(b & 1), static_cast<uint32_t>(b >> 1) & 1u, p.wait_ns) ||
+          !mtc_wait(cfull_bar(b % kMtcNbuf), static_cast<uint32_t>(b / kMtcNbuf) & 1u, p.wait_ns) ||
           (t.first && seg >= 1 && !mtc_wait(ofree_bar, static_cast<uint32_t>(seg - 1) & 1u, p.wait_ns))) {
         ok = false;
         break;
       }
+      const uint32_t vb0 = warp_uniform(buf0 + static_cast<uint32_t>(b % kMtcNbuf) * kMtcBuf);
+      if constexpr (!FP8) {
+        // Value rows past the context in the unit's last page: zero them so
+        // that whatever the pool holds there cannot reach O through 0 * NaN
+        // (Q K^T of this block, which also reads them, is complete: P exists).
+        if (t.j0 + t.np == t.n) {
+          const int vt = s_len[t.i] - kPage * (t.n - 1);
+          if (vt < kPage) {
+            uint8_t* const vg = gbase + (vb0 - base) + static_cast<uint32_t>(t.np - 1) * kMtcTile;
+            const int nbytes = (kPage - vt) * 128;
+            for (int cb = 0; cb < kMtcDv / 64; ++cb)
+              for (int o = lane * 16; o < nbytes; o += 32 * 16)
+                *reinterpret_cast<uint4*>(vg + cb * kMtcCbStride + vt * 128 + o) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+      }
       tc_fence_after();
-      const uint32_t vb0 = warp_uniform(buf0 + static_cast<uint32_t>(b & 1) * kMtcBuf);
       const uint32_t pb = warp_uniform(pbuf0 + static_cast<uint32_t>(b & 1) * NPT * kPbuf);
+      // V^T block vb of page pg: value columns 128 vb .. +127 (column blocks
+      // 2 vb, 2 vb + 1, kMtcCbStride apart) over the page's 16 keys (two 8-key
+      // groups, 1024 B apart); P^T: the page's 32-byte slice of the P rows
+      const uint64_t ad0 = umma_sdesc_sw128(vb0, kMtcCbStride, 1024u);
+      const uint64_t bd0 = umma_sdesc_sw128(pb, 16u, 1024u);
+      const uint32_t tO = tbase + kMtcTmemO;
+      const bool first = t.first;
+      const int np = t.np;
       if (lane == 0) {
-        for (int pg = 0; pg < t.np; ++pg) {
 #pragma unroll
-          for (int vb = 0; vb < kMtcDv / 128; ++vb) {
-            // V^T block vb: value columns 128 vb .. +127 (column blocks 2 vb, 2 vb + 1,
-            // kMtcCbStride apart) over the page's 16 keys (two 8-key groups, 1024 B apart)
-            const uint64_t ad = umma_sdesc_sw128(vb0 + static_cast<uint32_t>(2 * vb) * kMtcCbStride +
-                                                     static_cast<uint32_t>(pg) * kMtcTile,
-                                                 kMtcCbStride, 1024u);
-            const uint32_t tO = tbase + kMtcTmemO + static_cast<uint32_t>(vb * RP);
+        for (int pg = 0; pg < kMtcBlockPages; ++pg) {
+          if (pg < np) {
 #pragma unroll
-            for (int h = 0; h < NPT; ++h) {
-              const uint64_t bd = umma_sdesc_sw128(pb + static_cast<uint32_t>(h) * kPbuf + 32u * pg, 16u, 1024u);
-              umma_ss(tO, ad, bd, idesc, !(t.first && pg == 0 && h == 0));
-            }
+            for (int vb = 0; vb < kMtcDv / 128; ++vb)
+              umma_ss(tO + static_cast<uint32_t>(vb * RP),
+                      ad0 + ((static_cast<uint32_t>(2 * vb) * kMtcCbStride + static_cast<uint32_t>(pg) * kMtcTile) >> 4),
+                      bd0 + static_cast<uint32_t>(2 * pg), idesc, !(first && pg == 0));
           }
         }
         umma_commit(pfree_bar(b & 1));
-        umma_commit(bfree_bar(b & 1));
+        umma_commit(bfree_bar(b % kMtcNbuf));
       }
       __syncwarp();
       ++b;
@@ -382,89 +622,174 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
     if (!mtc_wait(drain2_bar, 0u, p.wait_ns) && lane == 0) atomicOr(p.err, kErrTimeout);
   } else {
     // ============================ softmax ==================================
+    // Segment s keeps its Q rows, and so its S rows, in tensor-memory lane
+    // quarter s % 2.  The softmax warp of that quarter owns the rows; the warp
+    // of the other quarter meanwhile stages the next segment's Q into its own
+    // lanes (rows the running Q K^T products compute but nothing reads).  Q
+    // goes through a ring of shared-memory slots, one 96-feature slice of
+    // every row a slot, filled by asynchronous copies a block ahead of their
+    // use, so the staging rarely waits on a load.  Every warp owns 32 value columns of O^T (its
+    // lanes) for the rescale and the epilogue.
     const int q4 = warp & 3;                 // tensor-memory lane quarter of this warp
-    const int rho = 32 * q4 + lane;          // query row = lane of S and Q
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    const uint32_t tS = tbase + lane_off + kMtcTmemS;
     const uint32_t tQ = tbase + lane_off + kMtcTmemQ;
     const uint32_t tO = tbase + lane_off + kMtcTmemO;
     const float c = p.scale_log2;
+    const int QR = p.q_slots;                // slots of the Q ring
     BlockWalker wk(s_pre, B, NC, start, count, kMtcBlockPages);
     int b = 0, seg = -1;
     SeqInfo si = {0, 0, 0, 0};
-    bool row_ok = false, fine = true;
+    bool act = false, row_ok = false, wact = false, fine = true;
     int lim = 0, seg_j0 = 0, seg_c = 0;
     int64_t seg_k0 = 0;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, lr = 0.f;   // row max, row sum, row sum of the rounded weights
     bool ok = true;
 
-    // Row rho of the segment starting at block t into tensor memory (the A
-    // operand of Q K^T; fp8 caches: f16 with a range check), zeros past R.
-    auto stage_q = [&](const TcBlock& t) {
-      const SeqInfo s2 = seq_info(p, s_len, s_qsl, t.i, false, 0);
-      const bool have = rho < G * s2.qn;
-      const uint4* src = nullptr;
-      if (have)
-        src = reinterpret_cast<const uint4*>(p.q + static_cast<int64_t>(s2.t0 + rho / G) * p.q_stride_t +
-                                             static_cast<int64_t>(t.c * G + rho % G) * kMtcDqk);
-#pragma unroll 1
-      for (int k = 0; k < kMtcDqk / 32; ++k) {   // 16 columns (32 features) at a time
+    // Staging of segment qj's Q by this warp: slices issued and written.
+    int qj = -1, q_iss = kMtcQslices, q_done = kMtcQslices;
+    const uint16_t* q_src = nullptr;         // this lane's Q row (null past the rows)
+    auto q_begin = [&](int i, int cc, int j) {
+      const SeqInfo s2 = seq_info(p, s_len, s_qsl, i, false, 0);
+      const int R2 = G * s2.qn;
+      qj = j;
+      q_iss = 0;
+      q_done = 0;
+      q_src = lane < R2 ? p.q + static_cast<int64_t>(s2.t0 + lane / G) * p.q_stride_t +
+                              static_cast<int64_t>(cc * G + lane % G) * kMtcDqk
+                        : nullptr;
+    };
+    // slice q_iss of this lane's row into its ring slot: 12 copies of 16 bytes
+    // and an arrival on the slot's barrier once they land (every lane arrives);
+    // slices of all stagings are numbered in order, and so are a slot's phases
+    auto q_issue = [&]() {
+      const int gs = kMtcQslices * qj + q_iss;
+      const int x = gs % QR;
+      const uint32_t dst = qst0 + static_cast<uint32_t>(x) * qslot + static_cast<uint32_t>(lane) * kMtcQrow;
+      if (q_src != nullptr) {
+        const uint16_t* const src = q_src + kMtcQsliceBytes / 2 * q_iss;
+#pragma unroll
+        for (int u = 0; u < static_cast<int>(kMtcQsliceBytes / 16); ++u) cp_async16(dst + 16u * u, src + 8 * u);
+      }
+      cp_async_arrive(qbar(x));
+      ++q_iss;
+    };
+    // has slice q_done landed in every lane (no waiting)?
+    auto q_ready = [&]() -> bool {
+      const int gs = kMtcQslices * qj + q_done;
+      return __all_sync(0xffffffffu, mbar_test(qbar(gs % QR), static_cast<uint32_t>(gs / QR) & 1u));
+    };
+    // slice q_done, landed, into this warp's lanes of tensor memory (each lane
+    // reads back the row it copied; fp8 caches: f16 with a range check); the
+    // last one announces the Q
+    auto q_write = [&]() -> bool {
+      const int gs = kMtcQslices * qj + q_done;
+      const int x = gs % QR;
+      if (!mtc_wait(qbar(x), static_cast<uint32_t>(gs / QR) & 1u, p.wait_ns)) return false;
+      // lanes past the rows read row 0 and keep zeros, so the warp stays
+      // converged for the tensor-memory stores
+      const bool have = q_src != nullptr;
+      const uint32_t row = qst0 + static_cast<uint32_t>(x) * qslot + (have ? static_cast<uint32_t>(lane) * kMtcQrow : 0u);
+#pragma unroll
+      for (int gq = 0; gq < kMtcQsliceBytes / 64; ++gq) {   // 16 tensor-memory columns at a time
         uint32_t w[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 v = have ? src[4 * k + u] : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * u] = v.x;
-          w[4 * u + 1] = v.y;
-          w[4 * u + 2] = v.z;
-          w[4 * u + 3] = v.w;
+          const uint4 v = lds128(row + 64u * gq + 16u * u);
+          w[4 * u] = have ? v.x : 0u;
+          w[4 * u + 1] = have ? v.y : 0u;
+          w[4 * u + 2] = have ? v.z : 0u;
+          w[4 * u + 3] = have ? v.w : 0u;
         }
         if constexpr (FP8) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = bf16x2_to_f16x2(w[e], fine);
         }
-        tmem_st16(tQ + 16u * k, w);
+        __syncwarp();
+        tmem_st16(tQ + static_cast<uint32_t>(16 * (kMtcQsliceBytes / 64 * q_done + gq)), w);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qfull_bar);
+      if (++q_done == kMtcQslices) {
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qfull_bar);
+      }
+      return true;
+    };
+    // the rest of the staging, waiting on each slice
+    auto q_finish = [&]() -> bool {
+      while (q_done < kMtcQslices) {
+        while (q_iss < kMtcQslices && q_iss - q_done < QR) q_issue();
+        if (!q_write()) return false;
+      }
+      return true;
     };
 
     while (wk.more()) {
       const TcBlock t = wk.next(s_pre, B, NC);
       if (t.first) {
         ++seg;
-        if (seg == 0) stage_q(t);
-        si = seq_info(p, s_len, s_qsl, t.i, rho == 0, 0);
-        row_ok = rho < G * si.qn;
-        lim = si.L - si.qn + (row_ok ? rho / G : 0);
+        act = q4 == (seg & 1);
+        if (seg == 0 && q4 == 0) {
+          q_begin(t.i, t.c, 0);
+          if (!q_finish()) {
+            ok = false;
+            break;
+          }
+        }
+        if (q4 == ((seg + 1) & 1) && t.k0 + (t.n - t.j0) < count) {
+          // This warp stages the next segment's Q during this one, once this
+          // segment's own staging is complete: the two share the ring (its
+          // slots and their barriers).  This segment's phase of the Q barrier
+          // is the last one before the phase this warp completes itself.
+          if (!mtc_wait(qfull_bar, static_cast<uint32_t>(seg) & 1u, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const Cursor nc = locate(s_pre, B, NC, start + t.k0 + (t.n - t.j0));
+          q_begin(nc.i, nc.c, seg + 1);
+        }
+        si = seq_info(p, s_len, s_qsl, t.i, q4 == 0 && lane == 0, 0);
+        row_ok = act && lane < G * si.qn;
+        wact = __any_sync(0xffffffffu, row_ok);
+        lim = si.L - si.qn + (row_ok ? lane / G : 0);
         seg_j0 = t.j0;
         seg_k0 = t.k0;
         seg_c = t.c;
         m = -INFINITY;
         l = 0.f;
-        if (seg_j0 == 0 && rho == 0) {
+        lr = 0.f;
+        if (seg_j0 == 0 && q4 == 0 && lane == 0) {
           // This CTA holds the unit's first page: describe the unit for the merge.
+          // the CTA holding the unit's last page, by the split's cost prefix
           const int64_t a = static_cast<int64_t>(NC) * s_pre[t.i] + static_cast<int64_t>(t.c) * t.n;
-          const int last_cta = static_cast<int>(((a + t.n) * NG - 1) / X);
+          const int64_t own = split_cost(s_pre, B, NC, W, a + t.n - 1, X) * NG / Ctot;
+          const int last_cta = static_cast<int>(own < NG - 1 ? own : NG - 1);
           p.ws_unit[static_cast<int64_t>(t.i) * NC + t.c] =
               make_int4(g, (last_cta - g + 1) | (t.k0 != 0 ? (1 << 30) : 0), si.t0, si.qn);
         }
       }
-      // ---- S row of the block (every phase of S seen in order) ----------------
-      if (!mtc_wait(sfull_bar, static_cast<uint32_t>(b) & 1u, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[4][16];
-      {
-        uint32_t r[4][16];
+      // the staging of the next segment's Q advances at every block
+      const bool staging = qj == seg + 1 && q_done < kMtcQslices;
+      if (staging)
+        while (q_iss < kMtcQslices && q_iss - q_done < QR) q_issue();
+      // ---- S row of the block (every phase of its S buffer seen in order) ------
+      const int sx = b % NSB;
+      const uint32_t tS = tbase + lane_off + mtc_tmem_s<RP>(sx);
+      // A warp with no query row in this segment skips the S row, the maximum
+      // and the exponentials; it keeps every barrier step.
+      float sv[kMtcBlockPages][16];
+      if (wact) {
+        if (!mtc_wait(sfull_bar(sx), static_cast<uint32_t>(b / NSB) & 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[kMtcBlockPages][16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld16(tS + 16u * k, r[k]);
+        for (int k = 0; k < kMtcBlockPages; ++k) tmem_ld16(tS + 16u * k, r[k]);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kMtcBlockPages; ++k)
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[k][e] = __uint_as_float(r[k][e]);
       }
@@ -472,18 +797,18 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
       // folded into the exponent) -------------------------------------------------
       const int tb = kPage * t.j0;
       const bool interior = t.np == kMtcBlockPages && c > 0.f && tb + kMtcBlockPages * kPage <= si.L - si.qn + 1;
-      float mb;
-      {
-        float mx[64];
+      float mb = -INFINITY;
+      if (wact) {
+        float mx[16 * kMtcBlockPages];
         if (interior) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < kMtcBlockPages; ++k)
 #pragma unroll
             for (int e = 0; e < 16; ++e) mx[16 * k + e] = sv[k][e];
-          mb = Max3Tree<64>::run(mx) * c;
+          mb = Max3Tree<16 * kMtcBlockPages>::run(mx) * c;
         } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < kMtcBlockPages; ++k)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int tok = tb + 16 * k + e;
@@ -492,7 +817,7 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
               sv[k][e] = x;
               mx[16 * k + e] = x;
             }
-          mb = Max3Tree<64>::run(mx);
+          mb = Max3Tree<16 * kMtcBlockPages>::run(mx);
         }
       }
       if (!row_ok) mb = -INFINITY;
@@ -502,22 +827,23 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
       if (grow) {
         alpha = fast_exp2(m - m_new);        // 0 when m = -inf
         l *= alpha;
+        lr *= alpha;
         m = m_new;
       }
-      // publish: this row's O factor and whether this warp needs an O rescale
+      // publish: the rows' O factors and whether this warp needs an O rescale
       // (a segment's first block has no O history: its P V overwrites O)
-      x_alpha[(b & 1) * 128 + rho] = alpha;
+      const int xq = b & 3;
+      if (act) x_alpha[xq * 32 + lane] = alpha;
       const bool need = __any_sync(0xffffffffu, grow && !t.first && row_ok);
-      if (lane == 0) x_flag[(b & 1) * 4 + q4] = need ? 1u : 0u;
+      if (lane == 0) x_flag[xq * 4 + q4] = need ? 1u : 0u;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sfree_bar);
-      if (!mtc_wait(sfree_bar, static_cast<uint32_t>(b) & 1u, p.wait_ns)) {
+      if (lane == 0) mbar_arrive(sfree_bar(sx));
+      if (!mtc_wait(sfree_bar(sx), static_cast<uint32_t>(b / NSB) & 1u, p.wait_ns)) {
         ok = false;
         break;
       }
-      const bool any = (x_flag[(b & 1) * 4 + 0] | x_flag[(b & 1) * 4 + 1] | x_flag[(b & 1) * 4 + 2] |
-                        x_flag[(b & 1) * 4 + 3]) != 0u;
+      const bool any = (x_flag[xq * 4 + 0] | x_flag[xq * 4 + 1] | x_flag[xq * 4 + 2] | x_flag[xq * 4 + 3]) != 0u;
       if (any) {
         // ---- lazy O rescale: O must hold P V of block b - 1 first (this warp
         // saw block b - 3's completion, the previous phase, at block b - 1) ----
@@ -526,19 +852,17 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
           break;
         }
         tc_fence_after();
-        const float* al = x_alpha + (b & 1) * 128;
+        const float* al = x_alpha + xq * 32;
 #pragma unroll 1
-        for (int vb = 0; vb < kMtcDv / 128; ++vb) {
+        for (int vh = 0; vh < kMtcDv / 128 * (RP / 16); ++vh) {   // 16 columns of O^T at a time
+          uint32_t r[16];
+          const uint32_t ta = tO + static_cast<uint32_t>(16 * vh);
+          const float* const a16 = al + 16 * (vh % (RP / 16));
+          tmem_ld16(ta, r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < RP / 16; ++h) {
-            uint32_t r[16];
-            const uint32_t ta = tO + static_cast<uint32_t>(vb * RP + 16 * h);
-            tmem_ld16(ta, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * al[16 * h + e]);
-            tmem_st16(ta, r);
-          }
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a16[e]);
+          tmem_st16(ta, r);
         }
         tmem_wait_st();
       }
@@ -548,16 +872,16 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
         ok = false;
         break;
       }
-      {
+      if (wact) {
         const float mneg = m == -INFINITY ? 0.f : -m;
         const float mult = interior ? c : 1.f;   // masked scores are already scaled
         const uint64_t mult2 = f2_pack(mult, mult), mneg2 = f2_pack(mneg, mneg);
-        uint64_t lsum2 = f2_pack(0.f, 0.f);
+        uint64_t lsum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
         const uint32_t prow = pbuf0 + static_cast<uint32_t>(b & 1) * NPT * kPbuf +
-                              static_cast<uint32_t>(rho >> 3) * 1024u + static_cast<uint32_t>(rho & 7) * 128u;
+                              static_cast<uint32_t>(lane >> 3) * 1024u + static_cast<uint32_t>(lane & 7) * 128u;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {       // 8 keys (one 16-byte chunk of the P row) at a time
-          uint32_t w[4], wl[4];
+        for (int ch = 0; ch < 2 * kMtcBlockPages; ++ch) {   // 8 keys (one 16-byte chunk of the P row) at a time
+          uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = ch >> 1, i0 = 8 * (ch & 1) + 2 * e;
@@ -566,36 +890,48 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
             float a0 = fast_exp2(x0), a1 = fast_exp2(x1);
             if (!row_ok) a0 = a1 = 0.f;
             lsum2 = fadd2(lsum2, f2_pack(a0, a1));
+            w[e] = FP8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+            // a second row sum adds the weights as the P V product sees them
+            // (rounded): O divided by it stays a weighted mean of V rows
+            float r0, r1;
             if constexpr (FP8) {
-              w[e] = pack_f16(a0, a1);
+              f16x2_unpack(w[e], r0, r1);
             } else {
-              w[e] = pack_bf16(a0, a1);
-              float r0, r1;   // exact residues a - bf16(a), rounded once below
-              f2_unpack(ffma2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), f2_pack(-1.f, -1.f), f2_pack(a0, a1)), r0, r1);
-              wl[e] = pack_bf16(r0, r1);
+              r0 = bf16_lo(w[e]);
+              r1 = bf16_hi(w[e]);
             }
+            rsum2 = fadd2(rsum2, f2_pack(r0, r1));
           }
-          if (rho < RP) {
-            const uint32_t off = static_cast<uint32_t>((ch ^ (rho & 7)) << 4);
+          if (lane < RP) {
+            const uint32_t off = static_cast<uint32_t>((ch ^ (lane & 7)) << 4);
             sts128(prow + off, make_uint4(w[0], w[1], w[2], w[3]));
-            if constexpr (!FP8) sts128(prow + kPbuf + off, make_uint4(wl[0], wl[1], wl[2], wl[3]));
           }
         }
         float s0, s1;
         f2_unpack(lsum2, s0, s1);
         l += s0 + s1;
+        f2_unpack(rsum2, s0, s1);
+        lr += s0 + s1;
       }
       fence_proxy_async_smem();   // the P V MMA reads what these stores wrote
       __syncwarp();
       if (lane == 0) mbar_arrive(pfull_bar(b & 1));
+      if (staging) {
+        // the slices that have landed (in order), then more copies
+        while (q_done < q_iss && q_ready())
+          if (!q_write()) {
+            ok = false;
+            break;
+          }
+        if (!ok) break;
+        while (q_iss < kMtcQslices && q_iss - q_done < QR) q_issue();
+      }
 
       if (t.last) {
-        // Every Q K^T of this segment is complete (S of its last block was read
-        // above): the next segment's Q goes in now.
-        if (wk.more()) {
-          BlockWalker peek = wk;
-          const TcBlock nt = peek.next(s_pre, B, NC);
-          stage_q(nt);
+        // the next segment's Q complete before this one's epilogue
+        if (qj == seg + 1 && !q_finish()) {
+          ok = false;
+          break;
         }
         // O complete once P V of this block is done (previous phase, block
         // b - 2, seen above)
@@ -603,7 +939,28 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
           ok = false;
           break;
         }
-        x_stat[rho] = make_float2(m, l);
+        const bool complete = (seg_j0 == 0) && (t.j0 + t.np == t.n);
+        const int R = G * si.qn;
+        const int which = (seg_k0 == 0) ? 0 : 1;
+        const int64_t rowbase = static_cast<int64_t>(2 * g + which) * p.R_max;
+        if (act && lane < RP) {
+          // this row's output factor and destination, once per row: the store
+          // loop below is then a multiply and a store per element
+          float f = 0.f;
+          uint16_t* dst = nullptr;
+          if (row_ok) {
+            if (complete) {
+              f = lr > 0.f ? p.v_scale / lr : 0.f;
+              dst = p.out + static_cast<int64_t>(si.t0 + lane / G) * p.out_stride_t +
+                    static_cast<int64_t>(seg_c * G + lane % G) * p.out_stride_h;
+            } else {
+              f = lr > 0.f ? 1.f / lr : 0.f;
+              dst = reinterpret_cast<uint16_t*>(p.ws_o) + (rowbase + lane) * kMtcDv;
+            }
+          }
+          x_fac[lane] = f;
+          x_dst[lane] = dst;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(ebar);
         if (!mtc_wait(ebar, static_cast<uint32_t>(seg) & 1u, p.wait_ns)) {
@@ -611,47 +968,40 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
           break;
         }
         tc_fence_after();
-        const bool complete = (seg_j0 == 0) && (t.j0 + t.np == t.n);
-        const int R = G * si.qn;
-        const int which = (seg_k0 == 0) ? 0 : 1;
-        const int64_t rowbase = static_cast<int64_t>(2 * g + which) * p.R_max;
 #pragma unroll 1
         for (int vb = 0; vb < kMtcDv / 128; ++vb) {
-          const int col = 128 * vb + rho;   // this thread's value column (its lane of O^T)
+          const int col = 128 * vb + 32 * q4 + lane;   // this thread's value column (its lane of O^T)
 #pragma unroll
           for (int h = 0; h < RP / 16; ++h) {
             uint32_t r[16];
             tmem_ld16(tO + static_cast<uint32_t>(vb * RP + 16 * h), r);
+            // the rows' factors and destinations are read before any store (a
+            // store may not be moved above a later read it could alias)
+            float f[16];
+            uint16_t* d[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              f[e] = x_fac[16 * h + e];
+              d[e] = x_dst[16 * h + e];
+            }
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int rr = 16 * h + e;
-              if (rr >= R) continue;
-              const float2 st = x_stat[rr];
-              const float o = __uint_as_float(r[e]);
-              if (complete) {
-                const float inv = st.y > 0.f ? p.v_scale / st.y : 0.f;
-                const int tok = si.t0 + rr / G;
-                const int hq = seg_c * G + rr % G;
-                p.out[static_cast<int64_t>(tok) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h + col] =
-                    static_cast<uint16_t>(pack_bf16(o * inv, 0.f) & 0xFFFFu);
-              } else {
-                const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
-                reinterpret_cast<uint16_t*>(p.ws_o)[(rowbase + rr) * kMtcDv + col] =
-                    static_cast<uint16_t>(pack_f16(o * inv, 0.f) & 0xFFFFu);
-              }
+              if (16 * h + e >= R) continue;
+              const float o = __uint_as_float(r[e]) * f[e];
+              d[e][col] = static_cast<uint16_t>((complete ? pack_bf16(o, 0.f) : pack_f16(o, 0.f)) & 0xFFFFu);
             }
           }
         }
         if (row_ok) {
-          const int tok = si.t0 + rho / G;
-          const int hq = seg_c * G + rho % G;
+          const int tok = si.t0 + lane / G;
+          const int hq = seg_c * G + lane % G;
           if (complete) {
             if (p.lse != nullptr)
               p.lse[static_cast<int64_t>(tok) * p.lse_stride_t + static_cast<int64_t>(hq) * p.lse_stride_h] =
                   l > 0.f ? (m + fast_log2(l)) * 0.69314718055994530942f : -INFINITY;
           } else {
-            p.ws_ml[rowbase + rho] = make_float2(m, l);
+            p.ws_ml[rowbase + lane] = make_float2(m, l);
           }
         }
         tc_fence_before();
@@ -671,8 +1021,8 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
 }
 
 template <bool FP8, int RP>
-static cudaError_t launch_mla_tc_one(const CUtensorMap& tm, const SplitParams& p, int grid, int smem, bool pdl,
-                                     cudaStream_t stream) {
+static cudaError_t launch_mla_tc_one(const CUtensorMap& tm, const CUtensorMap& tb, const SplitParams& p, int grid,
+                                     int smem, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kMtcThreads, 1, 1);
@@ -683,17 +1033,17 @@ static cudaError_t launch_mla_tc_one(const CUtensorMap& tm, const SplitParams& p
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, pa_mla_tc_kernel<FP8, RP>, tm, p);
+  return cudaLaunchKernelEx(&cfg, pa_mla_tc_kernel<FP8, RP>, tm, tb, p);
 }
 
 int mla_tc_threads() { return kMtcThreads; }
 
-cudaError_t launch_mla_tc(bool fp8, int rpad, const CUtensorMap& tm, const SplitParams& p, int grid, int smem,
-                          bool pdl, cudaStream_t stream) {
-  if (rpad == 16) return fp8 ? launch_mla_tc_one<true, 16>(tm, p, grid, smem, pdl, stream)
-                             : launch_mla_tc_one<false, 16>(tm, p, grid, smem, pdl, stream);
-  if (rpad == 32) return fp8 ? launch_mla_tc_one<true, 32>(tm, p, grid, smem, pdl, stream)
-                             : launch_mla_tc_one<false, 32>(tm, p, grid, smem, pdl, stream);
+cudaError_t launch_mla_tc(bool fp8, int rpad, const CUtensorMap& tm, const CUtensorMap& tb, const SplitParams& p,
+                          int grid, int smem, bool pdl, cudaStream_t stream) {
+  if (rpad == 16) return fp8 ? launch_mla_tc_one<true, 16>(tm, tb, p, grid, smem, pdl, stream)
+                             : launch_mla_tc_one<false, 16>(tm, tb, p, grid, smem, pdl, stream);
+  if (rpad == 32) return fp8 ? launch_mla_tc_one<true, 32>(tm, tb, p, grid, smem, pdl, stream)
+                             : launch_mla_tc_one<false, 32>(tm, tb, p, grid, smem, pdl, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -289,6 +289,8 @@ def _mla_call(lib, a, scale=0.07):
     (lambda a: a.update(opts=binding.make_options(heads_per_cta=2)), binding.PA_ERR_UNSUPPORTED),
     (lambda a: a.update(opts=binding.make_options(use_tcgen05=3)), binding.PA_ERR_INVALID_ARG),
     (lambda a: a.update(opts=binding.make_options(test_starve_cta=1)), binding.PA_ERR_UNSUPPORTED),
+    (lambda a: a.update(opts=binding.make_options(use_tcgen05=2, segment_cost_pages=(1 << 20) + 1)),
+     binding.PA_ERR_INVALID_ARG),
     (lambda a: a.update(opts=binding.make_options(wait_limit_us=-1)), binding.PA_ERR_INVALID_ARG),
     (lambda a: a.update(lse=torch.zeros(3, 8, dtype=torch.float32)), binding.PA_ERR_INVALID_ARG),
 ])
@@ -339,3 +341,15 @@ def test_wait_limit_and_starve_options_checked_on_the_host(lib):
     if not torch.cuda.is_available():
         # valid values pass every host check; the call then fails at device set-up
         assert _opt_call(lib, binding.make_options(wait_limit_us=1000, test_starve_cta=3)) == binding.PA_ERR_CUDA
+
+
+def test_options_struct_matches_the_header():
+    """The binding's pa_options_t mirrors the header's fields, in order."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                            "paged_attn.h")).read()
+    body = hdr[hdr.index("typedef struct pa_options_t {"):hdr.index("} pa_options_t;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"\b(\w+);", body)
+    assert names == [n for n, _ in binding.PaOptions._fields_]

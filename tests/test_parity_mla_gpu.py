@@ -5,8 +5,9 @@ Tolerances (max absolute error): out 1e-2 for bf16 caches, 2e-2 for fp8
 caches; lse 1e-3.  Small cases are compared in full; the full-size MLA
 workloads on every row against the plain-C oracle and on sampled sequences
 against the NumPy oracle, in the launch configuration the benchmark times.
-The main cases run on both split kernels: the mma.sync kernel (the default)
-and the tensor-memory (tcgen05) kernel (use_tcgen05 = 2)."""
+The main cases run on both split kernels: the mma.sync kernel (use_tcgen05 =
+1) and the tensor-memory (tcgen05) kernel (use_tcgen05 = 2); the planner's
+default picks one of them."""
 import numpy as np
 import pytest
 import torch
@@ -33,7 +34,7 @@ def _rows_of(w, seqs):
     return np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seqs])
 
 
-KERNELS = {"tc": 2, "mma": 0}
+KERNELS = {"tc": 2, "mma": 1}
 
 
 def _opts(kernel, **kw):
@@ -83,7 +84,10 @@ def test_mla_page_boundaries_and_ragged_tails(kv, kernel):
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_mla_plan_variants(kv):
     code = binding.PA_FP8_E4M3 if kv == "fp8" else binding.PA_BF16
-    assert binding.paged_attn_mla_plan(32, 16, code, 4)["variant"] == 2
+    # default: the tensor-memory kernel for fp8 caches or more than 16 rows a unit
+    assert binding.paged_attn_mla_plan(32, 16, code, 1)["variant"] == (3 if kv == "fp8" else 2)
+    assert binding.paged_attn_mla_plan(32, 16, code, 4)["variant"] == 3
+    assert binding.paged_attn_mla_plan(32, 16, code, 4, options=_opts("mma"))["variant"] == 2
     assert binding.paged_attn_mla_plan(32, 16, code, 4, options=_opts("tc"))["variant"] == 3
 
 
@@ -106,6 +110,20 @@ def test_mla_forced_split_counts_exercise_the_merge(num_ctas, kv, Hq, qlens, ker
                              device="cuda")
     ref = oracle.run_mla_workload(w)
     check(w, ref=ref, options=_opts(kernel, num_ctas=num_ctas, min_pages_per_cta=1))
+
+
+# The tensor-memory kernel's work split charges every unit a CTA starts
+# segment_cost_pages pages: an equal page split (< 0), small and large charges,
+# one so large that CTAs between units get no pages at all; with few and many
+# CTAs, so that units span several CTAs and CTAs span several units.
+@pytest.mark.parametrize("num_ctas", [5, 152])
+@pytest.mark.parametrize("seg_cost", [-1, 3, 40, 100000])
+@pytest.mark.parametrize("kv,Hq,qlens", [("bf16", 16, (1,)), ("fp8", 16, (4,))])
+def test_mla_tc_segment_cost_split(seg_cost, num_ctas, kv, Hq, qlens):
+    w = wl.make_mla_workload(_spec(kv=kv, Hq=Hq, qlens=qlens, seq_lens=(3, 50, 300, 17, 1000, 1, 64, 700),
+                                   seed=abs(seg_cost) % 97 + num_ctas), device="cuda")
+    ref = oracle.run_mla_workload(w)
+    check(w, ref=ref, options=_opts("tc", num_ctas=num_ctas, min_pages_per_cta=1, segment_cost_pages=seg_cost))
 
 
 @pytest.mark.parametrize("kernel", ["tc", "mma"])
