@@ -268,7 +268,7 @@ int make_plan(int B, int Hq, int Hkv, int D, int kv_dtype, int max_qlen, const p
     p.stage_bytes = static_cast<uint32_t>(2 * p.block_pages) * p.kv_bytes;
     p.q_slot_bytes = 0;
     const uint32_t tc_bar_bytes = static_cast<uint32_t>(align_up(8u * (2 * kMaxStages + 40), 1024));
-    const uint32_t tc_xchg_bytes = 4096;   // softmax warps' partial maxima and sums
+    const uint32_t tc_xchg_bytes = 8192;   // softmax warps' (max, sum, rounded sum) of a row, [2][2][128] float4
     const uint32_t tc_prefix_bytes = static_cast<uint32_t>(align_up(4u * (3 * B + 2), 16));
     const int64_t room = smem_optin - (1024 + static_cast<int64_t>(tc_bar_bytes) + tc_xchg_bytes + tc_prefix_bytes);
     p.nstage = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / p.stage_bytes)) : 0;

@@ -66,10 +66,11 @@ constexpr uint32_t kMtcCbStride = kMtcBlockPages * kMtcTile;
 constexpr uint32_t kMtcBuf = kMtcCb * kMtcCbStride;   // one block's rows in the MMA layout (54 KB)
 constexpr int kMtcThreads = 352;
 constexpr int kMtcProducer = 0, kMtcQkWarp = 1, kMtcPvWarp = 2, kMtcSoftmax0 = 4;
+constexpr int kMtcTmemUsers = 6;                   // warps 1, 2, 4..7 (named barrier 1 at set-up)
 constexpr int kMtcConverters = 4;                 // fp8: warps 3, 8, 9, 10
 constexpr int kMtcBoxProducers = 5;               // bf16: warps 0, 3, 8, 9, 10
 constexpr uint32_t kMtcCols = 512;
-constexpr uint32_t kMtcTmemO = 0, kMtcTmemQ = 192;   // S: see mtc_tmem_s
+constexpr uint32_t kMtcTmemO = 0, kMtcTmemQ = 176;   // S: see mtc_tmem_s
 constexpr int kMtcQsteps = kMtcDqk / 16;          // k-steps of Q K^T
 // Q staging ring: a slot holds one 96-feature slice (192 B) of every row, rows
 // 208 B apart (odd multiple of 16 B: the 16-byte reads of 8 lanes hit
@@ -82,12 +83,13 @@ static_assert(kMtcQsliceBytes % 64 == 0, "a slice is whole groups of 16 tensor-m
 __device__ __forceinline__ int converter_index(int warp) { return warp == 3 ? 0 : warp - 7; }
 __device__ __forceinline__ int box_producer_index(int warp) { return warp == 0 ? 0 : (warp == 3 ? 1 : warp - 6); }
 
-// S buffers: two when a unit has at most 16 rows (O^T then needs only 64
-// columns), so Q K^T of the next block runs while the softmax reads this one;
-// one for 32 rows.  Tensor-memory column of S buffer x.
+// Tensor memory (512 columns): O^T at 0 (4 x R_pad columns), Q at 176 (288
+// columns), two S buffers of 48 columns (Q K^T of the next block runs while
+// the softmax reads this one): at 64 and 128 for 16-row units, at 128 and
+// 464 for 32-row units.  Tensor-memory column of S buffer x.
 template <int RP>
 __device__ __forceinline__ constexpr uint32_t mtc_tmem_s(int x) {
-  return RP == 16 ? 64u + 64u * static_cast<uint32_t>(x) : 128u;
+  return RP == 16 ? 64u + 64u * static_cast<uint32_t>(x) : (x == 0 ? 128u : 464u);
 }
 
 // Instruction descriptor of kind::f16 (fp32 accumulator): A and B both bf16 or
@@ -188,28 +190,27 @@ __device__ __forceinline__ int64_t split_cost(const int32_t* pre, int B, int NC,
   return x + W * (static_cast<int64_t>(NC) * cu.i + cu.c);
 }
 
-// First position x in [0, X] whose cost prefix reaches gi / NG of the total
-// (a 32-way search by one warp; every lane returns it).
-__device__ int64_t split_point(const int32_t* pre, int B, int NC, int64_t W, int64_t X, int NG, int gi, int lane) {
-  const int64_t target = static_cast<int64_t>(gi) * split_cost(pre, B, NC, W, X, X);
-  int64_t lo = 0, hi = X;   // the answer lies in [lo, hi]; hi satisfies the test
+// First position x in [0, X] whose cost prefix reaches gi / NG of the total:
+// the first sequence whose last position reaches it (a binary search over
+// the sequences), then the head chunk and page by arithmetic (inside a
+// sequence of n pages the prefix runs over chunks of n pages, W apart).
+__device__ int64_t split_point(const int32_t* pre, int B, int NC, int64_t W, int64_t X, int NG, int gi) {
+  const int64_t total = X + W * (static_cast<int64_t>(NC) * B - 1);
+  const int64_t tau = (static_cast<int64_t>(gi) * total + NG - 1) / NG;   // cost prefix >= tau
+  int lo = 0, hi = B;
   while (lo < hi) {
-    const int64_t span = hi - lo;
-    const int64_t probe = lo + span * lane / 32;
-    const bool hit = split_cost(pre, B, NC, W, probe, X) * NG >= target;
-    const unsigned bal = __ballot_sync(0xffffffffu, hit);
-    if (bal & 1u) {
-      hi = lo;
-    } else if (bal == 0u) {
-      lo = lo + span * 31 / 32 + 1;
-    } else {
-      const int k = __ffs(bal) - 1;
-      const int64_t h = lo + span * k / 32;
-      lo = lo + span * (k - 1) / 32 + 1;
-      hi = h;
-    }
+    const int mid = (lo + hi) >> 1;
+    const int64_t last = static_cast<int64_t>(NC) * pre[mid + 1] - 1 + W * (static_cast<int64_t>(NC) * mid + NC - 1);
+    if (last >= tau) hi = mid; else lo = mid + 1;
   }
-  return hi;
+  if (lo == B) return X;
+  const int64_t n = pre[lo + 1] - pre[lo];
+  const int64_t s0 = static_cast<int64_t>(NC) * pre[lo];
+  if (n == 0) return s0;
+  const int64_t d = tau - (s0 + W * NC * lo);
+  if (d <= 0) return s0;
+  const int64_t c = d / (n + W), r = d - c * (n + W);
+  return r < n ? s0 + c * n + r : s0 + (c + 1) * n;
 }
 
 // bf16x2 -> f16x2 with a flag for values beyond the f16 range.
@@ -239,7 +240,13 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
   constexpr uint32_t kRawBlock = 16u * 64u * ESZ;
   constexpr int NPT = 1;                                 // P terms
   constexpr uint32_t kPbuf = static_cast<uint32_t>(RP) * 128u;
-  constexpr int NSB = RP == 16 ? 2 : 1;                  // S buffers
+  constexpr int NSB = 2;                                 // S buffers
+  constexpr uint32_t kS = 16u * kMtcBlockPages;          // columns of an S buffer
+  static_assert(kMtcTmemO + 4u * RP <= mtc_tmem_s<RP>(0) && mtc_tmem_s<RP>(0) + kS <= kMtcTmemQ &&
+                    (RP == 32 || mtc_tmem_s<RP>(1) + kS <= kMtcTmemQ) &&
+                    kMtcTmemQ + kMtcDqk / 2 <= kMtcCols && (RP == 16 || (kMtcTmemQ + kMtcDqk / 2 <= mtc_tmem_s<RP>(1) &&
+                                                                          mtc_tmem_s<RP>(1) + kS <= kMtcCols)),
+                "tensor-memory regions overlap");
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_scan[kMtcThreads / 32 + 1];
   __shared__ int s_total;
@@ -333,10 +340,7 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
   if (g >= NG || X == 0) return;
   const int64_t W = p.seg_cost;
   const int64_t Ctot = split_cost(s_pre, B, NC, W, X, X);
-  if (warp < 2) {
-    const int64_t sp = split_point(s_pre, B, NC, W, X, NG, g + warp, lane);
-    if (lane == 0) s_split[warp] = sp;
-  }
+  if (tid < 2) s_split[tid] = split_point(s_pre, B, NC, W, X, NG, g + tid);
   __syncthreads();
   const int64_t start = s_split[0];
   const int64_t end = s_split[1];
@@ -359,11 +363,24 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
       x += cs.n - cs.j;
     }
   }
-  if (warp == kMtcQkWarp) tmem_alloc(smem_addr(&s_tmem), kMtcCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = warp_uniform(s_tmem);
+  // fp8: only the tensor-memory users (Q K^T and P V issuers, softmax warps)
+  // wait for the allocation, so the page producer and the converters start
+  // at once (measured faster); bf16: the whole CTA waits (measured faster:
+  // an earlier flood of box loads delays the first Q).
+  const bool tmem_user = !FP8 || warp == kMtcQkWarp || warp == kMtcPvWarp ||
+                         (warp >= kMtcSoftmax0 && warp < kMtcSoftmax0 + 4);
+  uint32_t tbase = 0;
+  if (tmem_user) {
+    if (warp == kMtcQkWarp) tmem_alloc(smem_addr(&s_tmem), kMtcCols);
+    tc_fence_before();
+    if constexpr (FP8) {
+      asm volatile("bar.sync 1, %0;" ::"n"(kMtcTmemUsers * 32) : "memory");
+    } else {
+      __syncthreads();
+    }
+    tc_fence_after();
+    tbase = warp_uniform(s_tmem);
+  }
   const uint32_t buf0 = base + p.off_buf;
   const uint32_t pbuf0 = base + p.off_q;
   const uint32_t ring0 = base + p.off_stage;   // raw page slots
@@ -729,9 +746,20 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
       if (t.first) {
         ++seg;
         act = q4 == (seg & 1);
-        if (seg == 0 && q4 == 0) {
+        if (seg == 0) {
+          // the first segment's Q, into quarter 0; with a slot for every slice
+          // the four warps issue the copies together, then warp 4 writes them
           q_begin(t.i, t.c, 0);
-          if (!q_finish()) {
+          if (QR >= kMtcQslices) {
+            for (int k = q4; k < kMtcQslices; k += 4) {
+              q_iss = k;
+              q_issue();
+            }
+            q_iss = kMtcQslices;
+          }
+          if (q4 != 0) {
+            q_done = kMtcQslices;
+          } else if (!q_finish()) {
             ok = false;
             break;
           }

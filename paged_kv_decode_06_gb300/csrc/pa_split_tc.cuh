@@ -23,7 +23,7 @@
 //   warp 3    Q K^T issuer (one lane) and owner of the TMEM allocation:
 //               S[b%2]  = Q[s%2] K_b^T     (TS-MMA, Q read from TMEM, N = 16 * pages)
 //   warp 2    P V issuer (one lane):
-//               O      += (P_hi + P_lo)[b%2] V_b   (TS-MMA, P read from TMEM, N = D)
+//               O      += P[b%2] V_b   (TS-MMA, P read from TMEM, N = D)
 //             Two issuers, because one lane issues a tcgen05.mma every ~60
 //             cycles at best and a single issuer interleaving both streams
 //             (S of block b+1 between P V of blocks b-1 and b) set the pace;
@@ -33,17 +33,20 @@
 //             with the group's own running max, sum and O accumulator.  Per
 //             block: load S, mask (causal run, context tail, sliding window),
 //             update the running max, rescale O in TMEM only when the max grew
-//             by more than 2^8 (lazy rescale), write P over the block's S as two
-//             bf16 terms P_hi = bf16(P), P_lo = bf16(P - P_hi), so P V carries P
-//             to about 16 bits instead of bf16's 8 (a row dominated by one or two
-//             keys would otherwise lose up to 2^-9 |v| to P's rounding).  At a
-//             segment's end the two threads of a row exchange (max, sum), each
-//             combines half of the two O accumulators and writes out / lse or the
-//             partials.  They also store each segment's Q rows into one of two
-//             TMEM slots.
+//             by more than 2^8 (lazy rescale), write P over the block's S in
+//             bf16 and keep two row sums: of the weights (for the lse and the
+//             merge) and of the weights as rounded into P, which normalises O
+//             (O divided by it is a weighted mean of V rows, so P's rounding
+//             perturbs the weights without leaving their sum: a row dominated
+//             by one key keeps that key's V row).  At a segment's end the two
+//             threads of a row exchange (max, sum, rounded sum), each combines
+//             half of the two O accumulators and writes out / lse or the
+//             partials (O rescaled by sum / rounded sum, so the merge's
+//             O / sum is the same weighted mean).  They also store each
+//             segment's Q rows into one of two TMEM slots.
 // TMEM columns: O_0 [0,128) O_1 [128,256) S/P of group 0 [256,320) and of
-//               group 1 [320,384) (S fp32, 16 columns per page; P_hi at +8 per
-//               page, P_lo at +32 + 8 per page) Q0 [384,448) Q1 [448,512).
+//               group 1 [320,384) (S fp32, 16 columns per page; bf16 P over it,
+//               8 columns per page) Q0 [384,448) Q1 [448,512).
 // Shared memory holds only the ring (6 stages of 4 pages at D = 128) and
 // metadata: Q lives in TMEM, as the A operand of a TS-MMA.
 // Every wait is bounded (kErrTimeout); the CTA drains its MMAs before it frees
@@ -96,8 +99,7 @@ constexpr int kTcMaxBlockPages = 4;
 constexpr uint32_t kTcCols = 512;
 constexpr uint32_t kTmemO = 0;     // + 128 * group: fp32 O of softmax group g, D columns
 constexpr uint32_t kTmemSP = 256;  // + 64 * group: fp32 S of the group's block, 16 columns per page;
-constexpr uint32_t kTmemPhi = 0;   //   P overwrites it: bf16 P at + 8 * page,
-constexpr uint32_t kTmemPlo = 32;  //   bf16 rounding residue at + 32 + 8 * page
+constexpr uint32_t kTmemPhi = 0;   //   P overwrites it: bf16 P at + 8 * page
 constexpr uint32_t kTmemQ = 384;   // + 64 * (segment % 2): bf16 Q, D / 2 columns
 constexpr uint32_t kTcBox = 2048;  // one page of one 64-column half: 16 rows x 128 bytes
 constexpr uint32_t kTcHalf = kTcMaxBlockPages * kTcBox;   // one 64-column half of a stage's K or V
@@ -398,14 +400,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t vd0 = umma_sdesc_sw128(sb + TG::NH * half_stride, half_stride, 1024u);
       const uint32_t tO = warp_uniform(tbase + kTmemO + 128u * static_cast<uint32_t>(b & 1));
       const uint32_t tP = warp_uniform(tbase + kTmemSP + 64u * static_cast<uint32_t>(b & 1) + kTmemPhi);
-      const uint32_t tPlo = tP + (kTmemPlo - kTmemPhi);
       if (lane == 0) {
 #pragma unroll
         for (int pg = 0; pg < kTcMaxBlockPages; ++pg) {
           if (pg < t.np) {
             const uint64_t vd = vd0 + static_cast<uint64_t>((pg * kTcBox) >> 4);
             umma_ts(tO, tP + 8u * pg, vd, idesc_o, !(ofirst && pg == 0));
-            umma_ts(tO, tPlo + 8u * pg, vd, idesc_o, true);
           }
         }
         umma_commit(odone_bar(b & 1));
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q4 = warp & 3;               // TMEM lane quarter this warp may access
     const int rho = 32 * q4 + lane;        // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    float2* const xstat = reinterpret_cast<float2*>(gbase + p.off_xchg);   // [segment % 2][group][128] (max, sum)
+    float4* const xstat = reinterpret_cast<float4*>(gbase + p.off_xchg);   // [segment % 2][group][128] (max, sum, rounded sum)
     constexpr int HD = D / 2;              // O columns each group's thread writes out
     constexpr int NP4 = kTcMaxBlockPages;
     BlockWalker wk(s_pre, B, NC, start, count, kTcMaxBlockPages);
@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int lim = 0, seg_j0 = 0;
     int64_t seg_k0 = 0;
     float m = -INFINITY, l = 0.f;          // this group's running max (log2 units) and sum of the row
+    float lr = 0.f;                        // the sum of the weights as rounded into P (O's normaliser)
     bool ok = true;
 
     // This thread's half (by group) of row rho of the segment starting at
@@ -490,6 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         seg_k0 = t.k0;
         m = -INFINITY;
         l = 0.f;
+        lr = 0.f;
         if (seg_j0 == 0 && rho == 0 && gi == 0) {
           // This CTA holds the unit's first page: describe the unit for the merge.
           const int64_t a = static_cast<int64_t>(NC) * s_pre[t.i] + static_cast<int64_t>(t.c) * t.n;
@@ -504,6 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // piece holding the unit's first page.
           m = p.sinks[t.c * G + rho % G] * 1.4426950408889634f;
           l = 1.f;
+          lr = 1.f;                          // the sink's weight, exact (it is not in P)
         }
       }
       if ((b & 1) == gi) {
@@ -565,7 +568,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (b - b0 < 2) {
           // the group's first block of the segment: O has no history yet
           if (grow) {
-            l *= fast_exp2(m - m_new);       // only a sink carries weight here
+            const float a = fast_exp2(m - m_new);   // only a sink carries weight here
+            l *= a;
+            lr *= a;
             m = m_new;
           }
         } else if (__any_sync(0xffffffffu, grow)) {
@@ -589,10 +594,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_wait_st();
           if (grow) {
             l *= alpha;
+            lr *= alpha;
             m = m_new;
           }
         }
-        // ---- P (bf16 hi + lo) over the block's S ------------------------------
+        // ---- P (bf16) over the block's S -----------------------------------------
         // This thread has read its whole S row above; P V of the group's
         // previous block read P from these columns before Q K^T of this block
         // was issued into them.
@@ -602,15 +608,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float mneg = m == -INFINITY ? 0.f : -m;
           const float mult = interior ? c : 1.f;   // masked scores are already scaled
           const uint32_t tP = tSP + kTmemPhi;
-          const uint32_t tPlo = tSP + kTmemPlo;
           // pairs of scores through packed fp32 arithmetic: exponent argument
-          // (one FMA for two), residue a - bf16(a) (one FMA for two), running sum
+          // (one FMA for two) and two running sums, of the weights and of the
+          // weights as rounded into P (O divided by the second stays a
+          // weighted mean of V rows; the first gives the lse)
           const uint64_t mult2 = f2_pack(mult, mult), mneg2 = f2_pack(mneg, mneg);
-          const uint64_t minus1 = f2_pack(-1.f, -1.f);
-          uint64_t lsum2 = f2_pack(0.f, 0.f);
+          uint64_t lsum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < NP4; ++k) {
-            uint32_t w[8], wl[8];
+            uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               float x0, x1;
@@ -618,19 +624,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float a0 = fast_exp2(x0);
               const float a1 = fast_exp2(x1);
               w[e] = pack_bf16(a0, a1);
-              const uint64_t a2 = f2_pack(a0, a1);
-              float r0, r1;   // exact residues a - bf16(a), rounded once below
-              f2_unpack(ffma2(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), minus1, a2), r0, r1);
-              wl[e] = pack_bf16(r0, r1);
-              lsum2 = fadd2(lsum2, a2);
+              lsum2 = fadd2(lsum2, f2_pack(a0, a1));
+              rsum2 = fadd2(rsum2, f2_pack(bf16_lo(w[e]), bf16_hi(w[e])));
             }
             tmem_st8(tP + 8u * k, w);
-            tmem_st8(tPlo + 8u * k, wl);
           }
           {
             float s0, s1;
             f2_unpack(lsum2, s0, s1);
             l += s0 + s1;
+            f2_unpack(rsum2, s0, s1);
+            lr += s0 + s1;
           }
           tmem_wait_st();
         }
@@ -648,21 +652,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           stage_q(nt, (seg + 1) & 1);
         }
         // the other group's (max, sum) of the row
-        xstat[(seg & 1) * 256 + gi * 128 + rho] = make_float2(m, l);
+        xstat[(seg & 1) * 256 + gi * 128 + rho] = make_float4(m, l, lr, 0.f);
         __syncwarp();
         if (lane == 0) mbar_arrive(xstat_bar(q4));
         if (!warp_wait(xstat_bar(q4), static_cast<uint32_t>(seg) & 1u, p.wait_ns)) {
           ok = false;
           break;
         }
-        const float2 other = xstat[(seg & 1) * 256 + (gi ^ 1) * 128 + rho];
+        const float4 other = xstat[(seg & 1) * 256 + (gi ^ 1) * 128 + rho];
         // group 0's and group 1's statistics
-        const float m0 = gi == 0 ? m : other.x, l0 = gi == 0 ? l : other.y;
-        const float m1 = gi == 0 ? other.x : m, l1 = gi == 0 ? other.y : l;
+        const float m0 = gi == 0 ? m : other.x, l0 = gi == 0 ? l : other.y, r0 = gi == 0 ? lr : other.z;
+        const float m1 = gi == 0 ? other.x : m, l1 = gi == 0 ? other.y : l, r1 = gi == 0 ? other.z : lr;
         const float mt = fmaxf(m0, m1);
         const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mt);
         const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mt);
-        const float lt = l0 * a0 + l1 * a1;
+        const float lt = l0 * a0 + l1 * a1;    // the row's sum (lse, merge weights)
+        const float lrt = r0 * a0 + r1 * a1;   // O's normaliser
         // Each group's last block of the segment: b and b - 1 (this block is
         // the segment's last); a group with no block in it has no O to read.
         const int bl0 = (b & 1) == 0 ? b : b - 1;
@@ -679,7 +684,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t tO1 = tO0 + 128u;
         const int tok = si.t0 + rho / G;
         const int hq = t.c * G + rho % G;
-        const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
+        const float inv = lrt > 0.f ? p.v_scale / lrt : 0.f;
+        // a piece's O goes to the merge scaled so that O / lt is O's weighted mean
+        const float pscale = lrt > 0.f ? lt / lrt : 0.f;
         uint16_t* orow =
             p.out + static_cast<int64_t>(tok) * p.out_stride_t + static_cast<int64_t>(hq) * p.out_stride_h + HD * gi;
         const int which = (seg_k0 == 0) ? 0 : 1;
@@ -713,7 +720,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
 #pragma unroll
               for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4*>(wrow + 16 * ch + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                *reinterpret_cast<float4*>(wrow + 16 * ch + e) =
+                    make_float4(o[e] * pscale, o[e + 1] * pscale, o[e + 2] * pscale, o[e + 3] * pscale);
             }
           }
         }
