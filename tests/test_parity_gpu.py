@@ -310,3 +310,33 @@ def test_batch_of_512_sequences(kv, qlens):
     w = wl.make_workload(_spec(kv=kv, G=4, Hkv=8, qlens=qlens, seq_lens=lens, seed=513), device="cuda")
     seqs = sorted(set(rng.choice(512, size=16, replace=False).tolist()) | {0, 255, 256, 511})
     check(w, seqs=seqs)
+
+
+# A sequence with an empty context (seq_len 0) owns no page: its rows come out
+# as zeros with lse = -inf and the call reports status bit 1, while the other
+# sequences (cut across CTAs, so merged) still match the oracle; with a forced
+# split count and with every sequence empty.
+@pytest.mark.parametrize("num_ctas", [0, 3])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_empty_context_rows_are_zero_and_reported(kv, num_ctas):
+    w = wl.make_workload(_spec(kv=kv, seq_lens=(40, 17, 300, 5)), device="cuda")
+    ref = oracle.run_workload(w)
+    w.seq_lens = w.seq_lens.copy()
+    w.seq_lens[1] = 0
+    opts = binding.make_options(num_ctas=num_ctas, min_pages_per_cta=1) if num_ctas else None
+    out, lse = binding.decode_workload(w, options=opts)
+    torch.cuda.synchronize()
+    status = binding.paged_attn_device_status(clear=True)
+    assert status & binding.STATUS_SEQ_LEN
+    rows = _rows_of(w, [0, 2, 3])
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    assert np.abs(o[rows] - ref[0][rows]).max() <= TOL_OUT[kv]
+    assert np.abs(l[rows] - ref[1][rows]).max() <= TOL_LSE
+    empty = _rows_of(w, [1])
+    assert (o[empty] == 0).all() and np.isneginf(l[empty]).all()
+    w.seq_lens[:] = 0
+    out, lse = binding.decode_workload(w, options=opts)
+    torch.cuda.synchronize()
+    assert binding.paged_attn_device_status(clear=True) & binding.STATUS_SEQ_LEN
+    assert (out.float().cpu().numpy() == 0).all() and np.isneginf(lse.cpu().numpy()).all()
