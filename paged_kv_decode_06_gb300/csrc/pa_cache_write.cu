@@ -3,7 +3,8 @@
 // with slot s >= 0 stores its key and value rows of all KV heads at page s / 16,
 // slot s % 16 of the paged caches.  bf16 caches take the rows as they are; fp8
 // caches take e4m3fn codes of x / scale (a cached value reads back as code *
-// scale): one IEEE fp32 division, round to nearest even, saturating to +-448.
+// scale): the IEEE fp32 quotient (round to nearest even; see div_by2), then
+// e4m3 round to nearest even, saturating to +-448.
 //
 // One thread moves 8 consecutive features (16 bytes of bf16 input) of one
 // (token, head) row; a grid of one wave of resident blocks strides over all
@@ -21,13 +22,64 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   return r;
 }
 
-// Four e4m3fn code pairs of eight bf16 values (one 16-byte chunk) divided by s:
-// every quotient an IEEE round-to-nearest fp32 division.
-__device__ __forceinline__ uint2 e4m3x8_div(const uint4 v, float s) {
+// Division by a scale that stays fixed over many values: the IEEE
+// round-to-nearest quotient x / s formed from the correctly rounded reciprocal
+// r = 1/s by Markstein's correction step (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990; also Muller et al., "Handbook of Floating-Point
+// Arithmetic", division with a fused multiply-add): q0 = x r rounded, the
+// remainder x - q0 s exact by one FMA, and q0 + (x - q0 s) r rounded once.
+// Kept from q0: a zero quotient (its sign: the correction's sum of zeros
+// would be +0) and |q0| >= 1024 or NaN (the e4m3 code saturates at 448 either
+// way, and an infinite q0 would make the remainder NaN).  Outside
+// 2^-64 <= |s| <= 2^64 the plain IEEE division is used.  Checked equal to
+// __fdiv_rn (quotients on [2^-20, 1000] and e4m3 codes everywhere) over every
+// fp32 x, for every scale amax / 448 of a positive finite bf16 amax and 10000
+// random scales (and, for a set of scales, by tests/test_cache_write_div_gpu.py).
+struct ScaleDiv {
+  float s, r;
+  bool fast;
+};
+
+__device__ __forceinline__ ScaleDiv scale_div(float s) {
+  ScaleDiv d;
+  d.s = s;
+  d.r = __frcp_rn(s);
+  d.fast = fabsf(s) >= 5.421010862427522e-20f && fabsf(s) <= 1.8446744073709552e+19f;   // 2^-64 .. 2^64
+  return d;
+}
+
+// (a, b) / s on the fast path, two at a time (packed f32x2 arithmetic, each
+// half rounded as its scalar form would be).
+__device__ __forceinline__ void div_by2(const ScaleDiv& d, float a, float b, float& qa, float& qb) {
+  const uint64_t x = f2_pack(a, b);
+  const uint64_t r2 = f2_pack(d.r, d.r), ns2 = f2_pack(-d.s, -d.s);
+  const uint64_t q0 = fmul2(x, r2);
+  const uint64_t q1 = ffma2(ffma2(q0, ns2, x), r2, q0);
+  float a0, b0, a1, b1;
+  f2_unpack(q0, a0, b0);
+  f2_unpack(q1, a1, b1);
+  qa = (a0 == 0.f || !(fabsf(a0) < 1024.f)) ? a0 : a1;
+  qb = (b0 == 0.f || !(fabsf(b0) < 1024.f)) ? b0 : b1;
+}
+
+// Four e4m3fn code pairs of eight bf16 values (one 16-byte chunk) divided by
+// the scale: every quotient the IEEE round-to-nearest fp32 division.
+__device__ __forceinline__ uint2 e4m3x8_div(const uint4 v, const ScaleDiv& d) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t q[4];
+  if (d.fast) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) q[e] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[e]), s), __fdiv_rn(bf16_hi(w[e]), s));
+    for (int e = 0; e < 4; ++e) {
+      float lo, hi;
+      div_by2(d, bf16_lo(w[e]), bf16_hi(w[e]), lo, hi);
+      q[e] = e4m3x2_from_f32(lo, hi);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      q[e] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[e]), d.s), __fdiv_rn(bf16_hi(w[e]), d.s));
+  }
   return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
 }
 
@@ -49,6 +101,7 @@ __global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWritePar
   const bool narrow = total <= 0xFFFFFFFFll;
   const int64_t num_slots = static_cast<int64_t>(p.num_pages) * kPage;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const ScaleDiv dk = scale_div(p.k_scale), dv = scale_div(p.v_scale);
   for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total; i0 += U * stride) {
     int64_t t[U];
     int h[U], d0[U], slot[U];
@@ -84,7 +137,7 @@ __global__ void __launch_bounds__(256) pa_cache_write_kernel(const CacheWritePar
                                  static_cast<int64_t>(h[u]) * (tensor ? p.vc_stride_head : p.kc_stride_head) + d0[u];
         if constexpr (FP8) {
           *reinterpret_cast<uint2*>((tensor ? p.v_cache : p.k_cache) + dst_elem) =
-              e4m3x8_div(x[u][tensor], tensor ? p.v_scale : p.k_scale);
+              e4m3x8_div(x[u][tensor], tensor ? dv : dk);
         } else {
           *reinterpret_cast<uint4*>((tensor ? p.v_cache : p.k_cache) + dst_elem * 2) = x[u][tensor];
         }
@@ -174,6 +227,7 @@ __global__ void __launch_bounds__(256) pa_cache_write_tok_kernel(const CacheWrit
       // quotients), so no broadcast is needed; an all-zero row's scale is 0
       const float sc[2] = {__fdiv_rn(__uint_as_float(m[u] << 16), 448.f),
                            __fdiv_rn(__uint_as_float(m[u] & 0xFFFF0000u), 448.f)};
+      const ScaleDiv ds[2] = {scale_div(sc[0]), scale_div(sc[1])};
 #pragma unroll
       for (int tensor = 0; tensor < 2; ++tensor) {
         uint8_t* row = (tensor ? p.v_cache : p.k_cache) + page * (tensor ? p.vc_stride_page : p.kc_stride_page) +
@@ -185,7 +239,7 @@ __global__ void __launch_bounds__(256) pa_cache_write_tok_kernel(const CacheWrit
           if (d0 >= p.head_dim) continue;
           // an all-zero row (its elements +0 or -0) stores the code 0x00 throughout
           *reinterpret_cast<uint2*>(row + d0) =
-              sc[tensor] > 0.f ? e4m3x8_div(x[u][k][tensor], sc[tensor]) : make_uint2(0u, 0u);
+              sc[tensor] > 0.f ? e4m3x8_div(x[u][k][tensor], ds[tensor]) : make_uint2(0u, 0u);
         }
       }
       // the row's two scales: lane c0 = 0 stores K's and c0 = 1 V's (one lane
