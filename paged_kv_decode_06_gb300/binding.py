@@ -162,8 +162,15 @@ def _check(lib, status: int):
                              lib.paged_attn_error_string(status).decode())
 
 
+# The current stream's raw handle without building a torch.cuda.Stream object
+# (about 0.2 us a call instead of 3); the public route where torch lacks it.
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
+        if _RAW_STREAM is not None:
+            return int(_RAW_STREAM(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream)
 

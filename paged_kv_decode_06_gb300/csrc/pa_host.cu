@@ -311,6 +311,58 @@ int check_tensor(const pa_tensor_t* t, const char* name, int ndim, bool allow_nu
   return PA_OK;
 }
 
+// cuTensorMapEncodeTiled through a small memo: a map depends only on its
+// arguments (address, geometry, layout), and a decode loop passes the same
+// ones every step, so repeated encodes are copies of the stored map.  Caller
+// holds g_mu.
+struct MapKey {
+  const void* ptr;
+  uint64_t dims[4];
+  uint64_t strides[3];
+  uint32_t box[4];
+  int32_t dtype, rank, swizzle;
+};
+struct MapMemo {
+  bool used;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapMemo = 16;
+MapMemo g_map_memo[kMapMemo];
+int g_map_next = 0;
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* ptr, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.ptr = ptr;
+  for (int d = 0; d < rank && d < 4; ++d) {
+    k.dims[d] = dims[d];
+    k.box[d] = box[d];
+    if (d + 1 < rank) k.strides[d] = strides[d];
+  }
+  k.dtype = static_cast<int32_t>(dtype);
+  k.rank = rank;
+  k.swizzle = static_cast<int32_t>(swizzle);
+  for (int i = 0; i < kMapMemo; ++i)
+    if (g_map_memo[i].used && std::memcmp(&g_map_memo[i].key, &k, sizeof(k)) == 0) {
+      *map = g_map_memo[i].map;
+      return CUDA_SUCCESS;
+    }
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), ptr, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS && rank <= 4) {
+    MapMemo& m = g_map_memo[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapMemo;
+    m.used = true;
+    m.key = k;
+    m.map = *map;
+  }
+  return r;
+}
+
 // TMA map over a cache [NB, 16, Hkv, D] with dimensions ordered (d, slot, head,
 // page): one box is RB bytes of the row x 16 slots x HC heads, which lands in
 // shared memory head-major, 16 swizzled rows per head.
@@ -323,11 +375,9 @@ int encode_cache_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int D, int
                            static_cast<cuuint64_t>(t->stride[0]) * esz};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(rb / esz), static_cast<cuuint32_t>(kPageSize),
                        static_cast<cuuint32_t>(HC), 1u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUresult r = g_encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                              t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = encode_tiled(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                                  t->data, dims, strides, box,
+                                  rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for a KV cache", r);
   return PA_OK;
 }
@@ -766,11 +816,9 @@ int encode_mla_map(CUtensorMap* map, const pa_tensor_t* t, int esz, int64_t NB, 
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->stride[1]) * esz, static_cast<cuuint64_t>(64 * esz),
                            static_cast<cuuint64_t>(t->stride[0]) * esz};
   cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(kPageSize), static_cast<cuuint32_t>(box_blocks), 1u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUresult r = g_encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                              t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              esz == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = encode_tiled(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                                  t->data, dims, strides, box,
+                                  esz == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for the latent cache", r);
   return PA_OK;
 }

@@ -340,3 +340,28 @@ def test_empty_context_rows_are_zero_and_reported(kv, num_ctas):
     torch.cuda.synchronize()
     assert binding.paged_attn_device_status(clear=True) & binding.STATUS_SEQ_LEN
     assert (out.float().cpu().numpy() == 0).all() and np.isneginf(lse.cpu().numpy()).all()
+
+
+def test_calls_run_on_the_current_stream_and_reuse_tensor_maps():
+    """With no stream argument the call is enqueued on torch's current stream
+    (the binding reads its raw handle), inside a stream context as well; the
+    same call repeated (tensor maps then come from the library's memo) and the
+    same caches after a second workload's maps were encoded give the oracle's
+    results."""
+    assert binding._stream_handle(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert binding._stream_handle(None) == s.cuda_stream
+    w = wl.make_workload(wl.CONFIGS["tiny"], device="cuda")
+    w2 = wl.make_workload(wl.CONFIGS["tiny"], device="cuda", seed=wl.CONFIGS["tiny"].seed + 5)
+    ref = oracle.run_workload(w)
+    check(w, ref=ref)
+    with torch.cuda.stream(s):
+        out, lse = binding.decode_workload(w)
+    s.synchronize()
+    assert binding.paged_attn_device_status(clear=True) == 0
+    o1, l1 = binding.decode_workload(w)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o1) and torch.equal(lse, l1)
+    check(w2)
+    check(w, ref=ref)
