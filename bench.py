@@ -720,7 +720,9 @@ def _per_config_entry(r, args, world):
     return {"us_per_step": ln["us_per_step"], "kv_gbs": ln["value"], "frac": ln["frac_of_hbm_peak"],
             "split_kernel_us": roof["split_kernel_us_mean"], "split_kernel_frac": roof["frac"],
             "traffic": roof["traffic"], "kernel": roof["kernel"], "kv_bytes_per_step": r["step_bytes"],
-            "e2e_gbs": ln["e2e"]["value"], "e2e_schedule": ln["e2e"]["schedule"], "timed_windows": r["repeats"], "clocks": ln["clocks"],
+            "e2e_gbs": ln["e2e"]["value"], "e2e_schedule": ln["e2e"]["schedule"],
+            "e2e_pipelined_gbs": ln["e2e"]["pipelined_value"], "e2e_serial_gbs": ln["e2e"]["serial_value"],
+            "timed_windows": r["repeats"], "clocks": ln["clocks"],
             "device_status": r["status"], "dtype": ln["dtype"]}
 
 
