@@ -380,12 +380,14 @@ def _timed_passes(step, ev_opts_for, pools, args, world, local, dev):
     return max_over_ranks(ms, world, device=dev), split_ms, direct_ms, clk.summary(), repeats
 
 
-def _packed_e2e(base, works, out, lse, dev, call, args):
+def _packed_e2e(base, works, out, lse, dev, prepare, args):
     """End to end through the public API: every step copies its inputs (q,
     block table, lengths, query starts) from pinned host memory and reads out /
     lse back; each direction is one copy of one packed buffer whose views are the
-    tensors the call takes.  call(k, q, bt, sl, qsl, out, lse) makes step k's API
-    call on the device views.
+    tensors the call takes.  prepare(pool, q, bt, sl, qsl, out, lse) returns the
+    binding's prepared call (arguments marshalled once, as a serving loop with
+    static buffers holds it) of pool `pool` on those device views; step k runs
+    pool k % pools's call.
 
     Two schedules, both with every step's copies inside the timed region:
     pipelined, as a serving loop runs them (the copy in of step k + 1 and the
@@ -420,9 +422,14 @@ def _packed_e2e(base, works, out, lse, dev, call, args):
         h_ins.append(h_in)
     pools = len(works)
 
+    calls = {}
+    for pidx in range(pools):
+        for x in range(2):
+            v, ov = d_views[x], d_oviews[x]
+            calls[(pidx, x)] = prepare(pidx, v[0], v[1], v[2], v[3] if has_qsl else None, ov[0], ov[1])
+
     def api_call(k, x):
-        v, ov = d_views[x], d_oviews[x]
-        call(k, v[0], v[1], v[2], v[3] if has_qsl else None, ov[0], ov[1])
+        calls[(k % pools, x)]()
 
     comp = torch.cuda.current_stream()
     s_in = torch.cuda.Stream(device=dev)
@@ -575,12 +582,12 @@ def measure_decode(spec, args, world, local, dev, window=0, sinks=False, tc=0):
         step, lambda pidx, ea, eb: pool_options(works[pidx], split_start_event=ea, split_stop_event=eb), pools, args,
         world, local, dev)
 
-    def e2e_call(k, q, bt_, sl_, qsl_, out_, lse_):
-        w = works[k % pools]
-        binding.paged_attn_decode(q, w.k_cache, w.v_cache, bt_, sl_, qsl_, mq, spec.scale, spec.k_scale,
-                                  spec.v_scale, out=out_, lse=lse_, options=pool_opts[k % pools])
+    def e2e_prepare(pidx, q, bt_, sl_, qsl_, out_, lse_):
+        w = works[pidx]
+        return binding.prepare_decode(q, w.k_cache, w.v_cache, bt_, sl_, qsl_, mq, spec.scale, spec.k_scale,
+                                      spec.v_scale, out=out_, lse=lse_, options=pool_opts[pidx])
 
-    e2e_ms, e2e_serial_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
+    e2e_ms, e2e_serial_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_prepare, args)
     status = binding.paged_attn_device_status(clear=True)
     plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                                    binding.kv_dtype_code(spec.kv_dtype), mq,
@@ -632,12 +639,12 @@ def measure_mla(spec, args, world, local, dev, tc=0):
 
     ms, split_ms, direct_ms, clocks, repeats = _timed_passes(step, ev_opts_for, pools, args, world, local, dev)
 
-    def e2e_call(k, q, bt_, sl_, qsl_, out_, lse_):
-        w = works[k % pools]
-        binding.paged_attn_mla_decode(q, w.kv_cache, bt_, sl_, qsl_, mq, spec.scale, spec.kv_scale, out=out_,
-                                      lse=lse_, options=kopts)
+    def e2e_prepare(pidx, q, bt_, sl_, qsl_, out_, lse_):
+        w = works[pidx]
+        return binding.prepare_mla_decode(q, w.kv_cache, bt_, sl_, qsl_, mq, spec.scale, spec.kv_scale, out=out_,
+                                          lse=lse_, options=kopts)
 
-    e2e_ms, e2e_serial_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_call, args)
+    e2e_ms, e2e_serial_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_prepare, args)
     status = binding.paged_attn_device_status(clear=True)
     plan = binding.paged_attn_mla_plan(spec.num_seqs, spec.num_q_heads, binding.kv_dtype_code(spec.kv_dtype), mq,
                                        options=binding.make_options(use_tcgen05=tc))
@@ -695,7 +702,8 @@ def _line(r, args, world, window=0, sinks=False, tc=0):
                 "serial_value": r["step_bytes"] / (r["e2e_serial_ms"] * 1e-3) / 1e9,
                 "serial_ms_per_step": r["e2e_serial_ms"],
                 "note": "per step: one copy of the packed inputs from pinned host memory, the API call from "
-                        "Python, one copy of the packed out / lse back, in two schedules: pipelined (the copies "
+                        "Python (a prepared call: arguments marshalled once, the buffers refreshed in place), "
+                        "one copy of the packed out / lse back, in two schedules: pipelined (the copies "
                         "of steps k + 1 and k - 1 on their own streams while step k computes, device buffers "
                         "double-buffered) and serial (copy in, call, copy out in order on one stream); value is "
                         "the faster (short steps are bound by the host's per-call work, which the pipelined "

@@ -390,6 +390,66 @@ def paged_attn_mla_decode(q, kv_cache, block_tables, seq_lens, query_start_loc=N
     return out, lse
 
 
+class PreparedCall:
+    """One decode (or MLA decode) call with its arguments marshalled once, for
+    a serving loop that reuses the same tensors every step and refreshes
+    their contents in place (new q rows, block tables, lengths), as CUDA-graph
+    static buffers are used.  ``call(stream=None)`` enqueues the C entry point
+    with the stored descriptors on ``stream`` (None: torch's current stream)
+    and returns (out, lse).  The tensors are kept referenced by the object;
+    their addresses, shapes and strides must not change while it is used."""
+
+    def __init__(self, fn, tensors, scalars, out, lse, options):
+        self._lib = load()
+        self._fn = fn
+        self._keep = (tensors, out, lse, options)
+        self._descs = [_new_desc(t) for t in tensors] + [_new_desc(out), _new_desc(lse)]
+        n_in = len(tensors)
+        refs = [ctypes.byref(d) for d in self._descs]
+        head = refs[:n_in] + list(scalars) + refs[n_in:]
+        if options is not None:
+            head.append(ctypes.byref(options))
+        self._args = tuple(head)
+        self.out, self.lse = out, lse
+
+    def __call__(self, stream=None):
+        st = self._fn(*self._args, _stream_handle(stream))
+        if st != PA_OK:
+            _check(self._lib, st)
+        return self.out, self.lse
+
+
+def prepare_decode(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc=None, max_query_len=1, scale=None,
+                   k_scale=1.0, v_scale=1.0, out=None, lse=None, options=None, want_lse=True) -> PreparedCall:
+    """``paged_attn_decode`` with its arguments marshalled once (see PreparedCall)."""
+    lib = load()
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    scalars = (ctypes.c_int32(int(max_query_len)), ctypes.c_float(float(scale)), ctypes.c_float(float(k_scale)),
+               ctypes.c_float(float(v_scale)))
+    fn = lib.paged_attn_decode if options is None else lib.paged_attn_decode_ex
+    return PreparedCall(fn, (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc), scalars, out, lse, options)
+
+
+def prepare_mla_decode(q, kv_cache, block_tables, seq_lens, query_start_loc=None, max_query_len=1, scale=None,
+                       kv_scale=1.0, out=None, lse=None, options=None, want_lse=True) -> PreparedCall:
+    """``paged_attn_mla_decode`` with its arguments marshalled once (see PreparedCall)."""
+    lib = load()
+    if scale is None:
+        scale = 192 ** -0.5
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    scalars = (ctypes.c_int32(int(max_query_len)), ctypes.c_float(float(scale)), ctypes.c_float(float(kv_scale)))
+    fn = lib.paged_attn_mla_decode if options is None else lib.paged_attn_mla_decode_ex
+    return PreparedCall(fn, (q, kv_cache, block_tables, seq_lens, query_start_loc), scalars, out, lse, options)
+
+
 def paged_attn_mla_plan(num_seqs, num_q_heads, kv_dtype=PA_BF16, max_query_len=1, options=None) -> dict:
     lib = load()
     plan = PaPlan()

@@ -365,3 +365,32 @@ def test_calls_run_on_the_current_stream_and_reuse_tensor_maps():
     assert torch.equal(out, o1) and torch.equal(lse, l1)
     check(w2)
     check(w, ref=ref)
+
+
+def test_prepared_call_follows_buffers_refreshed_in_place():
+    """A prepared call (arguments marshalled once) over static buffers gives
+    the oracle's results for each batch copied into those buffers."""
+    spec = wl.CONFIGS["tiny"]
+    w1 = wl.make_workload(spec, device="cuda")
+    w2 = wl.make_workload(spec, device="cuda", seed=spec.seed + 11, content_seed=spec.seed + 12)
+    q = w1.q.clone()
+    bt = torch.from_numpy(w1.block_tables).cuda()
+    sl = torch.from_numpy(w1.seq_lens).cuda()
+    call = binding.prepare_decode(q, w1.k_cache, w1.v_cache, bt, sl, None, 1, spec.scale, spec.k_scale,
+                                  spec.v_scale)
+    for w in (w1, w2, w1):
+        q.copy_(w.q)
+        bt.copy_(torch.from_numpy(w.block_tables))
+        sl.copy_(torch.from_numpy(w.seq_lens))
+        # the second batch's pages live in its own caches: same shapes, other tensors
+        if w is w2:
+            call2 = binding.prepare_decode(q, w2.k_cache, w2.v_cache, bt, sl, None, 1, spec.scale, spec.k_scale,
+                                           spec.v_scale)
+            out, lse = call2()
+        else:
+            out, lse = call()
+        torch.cuda.synchronize()
+        assert binding.paged_attn_device_status(clear=True) == 0
+        ref_out, ref_lse = oracle.run_workload(w)
+        assert np.abs(out.float().cpu().numpy() - ref_out).max() <= TOL_OUT["bf16"]
+        assert np.abs(lse.cpu().numpy() - ref_lse).max() <= TOL_LSE
