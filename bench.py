@@ -393,8 +393,11 @@ def _packed_e2e(base, works, out, lse, dev, prepare, args):
     pipelined, as a serving loop runs them (the copy in of step k + 1 and the
     copy out of step k - 1 on their own streams while step k computes; device
     input and output buffers double-buffered, events order each buffer's
-    reuse), and serial (copy in, call, copy out on one stream).  Returns
-    (pipelined ms per step, serial ms per step, H2D bytes, D2H bytes)."""
+    reuse), and serial (copy in, call, copy out on one stream).  Afterwards a
+    few pipelined steps, each followed by a synchronize, have their copied-back
+    results compared bit for bit with the same call on the workload's own
+    device tensors.  Returns (pipelined ms per step, serial ms per step, H2D
+    bytes, D2H bytes, steps verified, all equal)."""
     import torch
     has_qsl = base.query_start_loc is not None
     in_parts = [(tuple(base.q.shape), base.q.dtype), (tuple(base.block_tables.shape), torch.int32),
@@ -402,7 +405,7 @@ def _packed_e2e(base, works, out, lse, dev, prepare, args):
     if has_qsl:
         in_parts.append((tuple(base.query_start_loc.shape), torch.int32))
     out_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
-    d_in, d_views, d_out, d_oviews, h_out = [], [], [], [], []
+    d_in, d_views, d_out, d_oviews, h_out, h_oviews = [], [], [], [], [], []
     for _ in range(2):
         b, v = _packed_views(in_parts, dev)
         d_in.append(b)
@@ -410,7 +413,9 @@ def _packed_e2e(base, works, out, lse, dev, prepare, args):
         b, v = _packed_views(out_parts, dev)
         d_out.append(b)
         d_oviews.append(v)
-        h_out.append(_packed_views(out_parts, "pinned")[0])
+        b, v = _packed_views(out_parts, "pinned")
+        h_out.append(b)
+        h_oviews.append(v)
     h_ins = []
     for w in works:
         h_in, hv = _packed_views(in_parts, "pinned")
@@ -481,7 +486,22 @@ def _packed_e2e(base, works, out, lse, dev, prepare, args):
 
     pipe_ms = timed(pipelined_step, True)
     serial_ms = timed(serial_step, False)
-    return pipe_ms, serial_ms, d_in[0].numel(), d_out[0].numel()
+
+    ref_bt = torch.from_numpy(base.block_tables).to(dev)
+    ref_sl = torch.from_numpy(base.seq_lens).to(dev)
+    ref_qsl = torch.from_numpy(base.query_start_loc).to(dev) if has_qsl else None
+    ref_out, ref_lse = torch.empty_like(out), torch.empty_like(lse)
+    nver = min(4, 2 * pools)
+    same = True
+    for k in range(nver):
+        pipelined_step(k)
+        comp.wait_stream(s_out)
+        torch.cuda.synchronize()
+        prepare(k % pools, works[k % pools].q, ref_bt, ref_sl, ref_qsl, ref_out, ref_lse)()
+        torch.cuda.synchronize()
+        x = k & 1
+        same = same and torch.equal(h_oviews[x][0], ref_out.cpu()) and torch.equal(h_oviews[x][1], ref_lse.cpu())
+    return pipe_ms, serial_ms, d_in[0].numel(), d_out[0].numel(), nver, same
 
 
 def run_reference(args, world, rank):
@@ -587,7 +607,7 @@ def measure_decode(spec, args, world, local, dev, window=0, sinks=False, tc=0):
         return binding.prepare_decode(q, w.k_cache, w.v_cache, bt_, sl_, qsl_, mq, spec.scale, spec.k_scale,
                                       spec.v_scale, out=out_, lse=lse_, options=pool_opts[pidx])
 
-    e2e_ms, e2e_serial_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_prepare, args)
+    e2e_ms, e2e_serial_ms, h2d, d2h, e2e_nver, e2e_same = _packed_e2e(base, works, out, lse, dev, e2e_prepare, args)
     status = binding.paged_attn_device_status(clear=True)
     plan = binding.paged_attn_plan(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                                    binding.kv_dtype_code(spec.kv_dtype), mq,
@@ -597,6 +617,7 @@ def measure_decode(spec, args, world, local, dev, window=0, sinks=False, tc=0):
     torch.cuda.empty_cache()
     return dict(spec=spec, step_bytes=step_bytes, pools=pools, ms=ms, split_ms=split_ms, direct_ms=direct_ms,
                 clocks=clocks, repeats=repeats, e2e_ms=e2e_ms, e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h,
+                e2e_nver=e2e_nver, e2e_same=e2e_same,
                 status=status, plan=plan,
                 kernel=kernel, traffic=_traffic_from_profiles(spec.name, kernel), flops=None)
 
@@ -644,7 +665,7 @@ def measure_mla(spec, args, world, local, dev, tc=0):
         return binding.prepare_mla_decode(q, w.kv_cache, bt_, sl_, qsl_, mq, spec.scale, spec.kv_scale, out=out_,
                                           lse=lse_, options=kopts)
 
-    e2e_ms, e2e_serial_ms, h2d, d2h = _packed_e2e(base, works, out, lse, dev, e2e_prepare, args)
+    e2e_ms, e2e_serial_ms, h2d, d2h, e2e_nver, e2e_same = _packed_e2e(base, works, out, lse, dev, e2e_prepare, args)
     status = binding.paged_attn_device_status(clear=True)
     plan = binding.paged_attn_mla_plan(spec.num_seqs, spec.num_q_heads, binding.kv_dtype_code(spec.kv_dtype), mq,
                                        options=binding.make_options(use_tcgen05=tc))
@@ -656,6 +677,7 @@ def measure_mla(spec, args, world, local, dev, tc=0):
     kernel = "pa_mla_tc_kernel" if plan["variant"] == 3 else "pa_mla_kernel"
     return dict(spec=spec, step_bytes=step_bytes, pools=pools, ms=ms, split_ms=split_ms, direct_ms=direct_ms,
                 clocks=clocks, repeats=repeats, e2e_ms=e2e_ms, e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h,
+                e2e_nver=e2e_nver, e2e_same=e2e_same,
                 status=status, plan=plan,
                 kernel=kernel, traffic=_traffic_from_profiles(spec.name, kernel), flops=flops)
 
@@ -701,6 +723,7 @@ def _line(r, args, world, window=0, sinks=False, tc=0):
                 "pipelined_value": r["step_bytes"] / (r["e2e_ms"] * 1e-3) / 1e9, "pipelined_ms_per_step": r["e2e_ms"],
                 "serial_value": r["step_bytes"] / (r["e2e_serial_ms"] * 1e-3) / 1e9,
                 "serial_ms_per_step": r["e2e_serial_ms"],
+                "verified_steps": r["e2e_nver"], "verified_equal_to_direct_call": r["e2e_same"],
                 "note": "per step: one copy of the packed inputs from pinned host memory, the API call from "
                         "Python (a prepared call: arguments marshalled once, the buffers refreshed in place), "
                         "one copy of the packed out / lse back, in two schedules: pipelined (the copies "
@@ -730,6 +753,7 @@ def _per_config_entry(r, args, world):
             "traffic": roof["traffic"], "kernel": roof["kernel"], "kv_bytes_per_step": r["step_bytes"],
             "e2e_gbs": ln["e2e"]["value"], "e2e_schedule": ln["e2e"]["schedule"],
             "e2e_pipelined_gbs": ln["e2e"]["pipelined_value"], "e2e_serial_gbs": ln["e2e"]["serial_value"],
+            "e2e_verified": ln["e2e"]["verified_equal_to_direct_call"],
             "timed_windows": r["repeats"], "clocks": ln["clocks"],
             "device_status": r["status"], "dtype": ln["dtype"]}
 
