@@ -919,16 +919,14 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
             if (!row_ok) a0 = a1 = 0.f;
             lsum2 = fadd2(lsum2, f2_pack(a0, a1));
             w[e] = FP8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
-            // a second row sum adds the weights as the P V product sees them
-            // (rounded): O divided by it stays a weighted mean of V rows
-            float r0, r1;
-            if constexpr (FP8) {
-              f16x2_unpack(w[e], r0, r1);
-            } else {
-              r0 = bf16_lo(w[e]);
-              r1 = bf16_hi(w[e]);
-            }
-            rsum2 = fadd2(rsum2, f2_pack(r0, r1));
+            // bf16 P: a second row sum adds the weights as the P V product sees
+            // them (rounded), so O divided by it stays a weighted mean of V rows
+            // (a bf16 weight is off by up to 2^-9 of itself, and a row dominated
+            // by one key would otherwise keep up to 2^-9 of that key's |v|).
+            // f16 P (fp8 caches) is off by at most 2^-11 of each weight, so O
+            // over the exact sum is within 2^-11 of the largest |v| of the mean:
+            // for e4m3 values (|code| <= 448) a quarter of a bf16 unit of them.
+            if constexpr (!FP8) rsum2 = fadd2(rsum2, f2_pack(bf16_lo(w[e]), bf16_hi(w[e])));
           }
           if (lane < RP) {
             const uint32_t off = static_cast<uint32_t>((ch ^ (lane & 7)) << 4);
@@ -938,8 +936,12 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
         float s0, s1;
         f2_unpack(lsum2, s0, s1);
         l += s0 + s1;
-        f2_unpack(rsum2, s0, s1);
-        lr += s0 + s1;
+        if constexpr (FP8) {
+          lr = l;
+        } else {
+          f2_unpack(rsum2, s0, s1);
+          lr += s0 + s1;
+        }
       }
       fence_proxy_async_smem();   // the P V MMA reads what these stores wrote
       __syncwarp();
