@@ -901,7 +901,9 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
         break;
       }
       if (wact) {
-        const float mneg = m == -INFINITY ? 0.f : -m;
+        // a row past the unit's rows gets zero weights through its exponent
+        // argument: its scores are finite (zero query rows; masked ones -inf)
+        const float mneg = row_ok ? (m == -INFINITY ? 0.f : -m) : -INFINITY;
         const float mult = interior ? c : 1.f;   // masked scores are already scaled
         const uint64_t mult2 = f2_pack(mult, mult), mneg2 = f2_pack(mneg, mneg);
         uint64_t lsum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
@@ -916,7 +918,6 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
             float x0, x1;
             f2_unpack(ffma2(f2_pack(sv[k][i0], sv[k][i0 + 1]), mult2, mneg2), x0, x1);
             float a0 = fast_exp2(x0), a1 = fast_exp2(x1);
-            if (!row_ok) a0 = a1 = 0.f;
             lsum2 = fadd2(lsum2, f2_pack(a0, a1));
             w[e] = FP8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
             // bf16 P: a second row sum adds the weights as the P V product sees
