@@ -871,7 +871,8 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
         ok = false;
         break;
       }
-      const bool any = (x_flag[xq * 4 + 0] | x_flag[xq * 4 + 1] | x_flag[xq * 4 + 2] | x_flag[xq * 4 + 3]) != 0u;
+      const uint4 fl = *reinterpret_cast<const uint4*>(x_flag + xq * 4);
+      const bool any = (fl.x | fl.y | fl.z | fl.w) != 0u;
       if (any) {
         // ---- lazy O rescale: O must hold P V of block b - 1 first (this warp
         // saw block b - 3's completion, the previous phase, at block b - 1) ----
@@ -944,7 +945,7 @@ __global__ void __launch_bounds__(kMtcThreads, 1)
           lr += s0 + s1;
         }
       }
-      fence_proxy_async_smem();   // the P V MMA reads what these stores wrote
+      if (wact) fence_proxy_async_smem();   // the P V MMA reads what these stores wrote
       __syncwarp();
       if (lane == 0) mbar_arrive(pfull_bar(b & 1));
       if (staging) {
