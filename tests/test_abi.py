@@ -353,3 +353,31 @@ def test_options_struct_matches_the_header():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     names = re.findall(r"\b(\w+);", body)
     assert names == [n for n, _ in binding.PaOptions._fields_]
+
+
+class _NullStream:
+    cuda_stream = 0
+
+
+def test_prepared_calls_reach_the_host_checks(lib):
+    """A prepared call passes its stored arguments in the entry point's order:
+    an argument error is reported by the library's host checks (no device
+    work), for decode and for MLA decode."""
+    a = _good_args()
+    call = binding.prepare_decode(a["q"].float(), a["k"], a["v"], a["bt"], a["sl"], None, 1, 0.1, 1.0, 1.0,
+                                  out=a["out"], lse=a["lse"])
+    with pytest.raises(binding.PagedAttnError) as e:
+        call(stream=_NullStream())
+    assert e.value.status == binding.PA_ERR_INVALID_ARG
+    assert "q" in binding.paged_attn_last_error_message()
+    call = binding.prepare_decode(a["q"], a["k"], a["v"], a["bt"], a["sl"], None, 2, 0.1, 1.0, 1.0,
+                                  out=a["out"], lse=a["lse"], options=binding.make_options())
+    with pytest.raises(binding.PagedAttnError) as e:
+        call(stream=_NullStream())
+    assert e.value.status == binding.PA_ERR_INVALID_ARG   # max_query_len 2 without query_start_loc
+    m = _mla_args()
+    call = binding.prepare_mla_decode(m["q"].float(), m["c"], m["bt"], m["sl"], None, 1, 0.07, 1.0,
+                                      out=m["out"], lse=m["lse"])
+    with pytest.raises(binding.PagedAttnError) as e:
+        call(stream=_NullStream())
+    assert e.value.status == binding.PA_ERR_INVALID_ARG
